@@ -1,0 +1,338 @@
+"""Plain fp64 CPU oracle for single-token GQA decode attention.
+
+TEST INFRASTRUCTURE.  This module is the reference that the CUDA library is
+checked against.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import it.  It shares no code with the CUDA
+path (no kernels, headers, helpers, tables or pre/post-processing); both are
+fed the same seeded inputs by a separate generator module.
+
+What is computed (the decode-attention definition that the source pages build
+their kernels around; none of the pages writes it as an equation):
+for sequence b, query head h and its KV head g = h // G (G = Hq / Hkv, the G
+query heads of one KV head are consecutive), over the L_b cached tokens t,
+
+    s_t   = scale * sum_d q[b,h,d] * k[b,t,g,d]
+    out   = sum_t exp(s_t - M) v[b,t,g,:] / sum_t exp(s_t - M),   M = max_t s_t
+
+in float64 from the exactly widened bf16 inputs, then rounded once to bf16
+(round to nearest, ties to even).
+
+Split-KV (AstrAI commit 988e013 "csrc", split-KV items; "perf(qwen3.8):
+split the flash-decode KV range across warp-groups", section "Mechanism"):
+a piece of the token range yields unnormalised partials (acc, m, l) with
+m = max over the piece, acc = sum exp(s - m) v, l = sum exp(s - m); pieces
+are merged by the log-sum-exp rescale in ascending piece order.  The
+partition of the token range into pieces is this library's own rule (the
+pages only give caps on the split count); ``split_pieces`` states it.
+
+Paged caches (AstrAI commit 69fecaf "csrc/tests", paged decode items): token
+t of sequence b is row t % page_size of physical page page_table[b, t // page_size].
+
+Every function here is pinned by tests/test_oracle.py against closed forms,
+invariants, a high-precision brute force and torch's scaled_dot_product_attention.
+"""
+from __future__ import annotations
+
+import math
+from typing import Iterable, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+__all__ = [
+    "widen_bf16",
+    "round_to_bf16",
+    "attend",
+    "attend_partial",
+    "merge_partials",
+    "gather_paged",
+    "decode_contig",
+    "decode_paged",
+    "decode_rows",
+    "head_groups",
+    "split_pieces",
+    "decode_partials",
+    "combine_partials",
+    "BLOCK_TOKENS",
+    "MAX_GROUP_ROWS",
+]
+
+# Token granularity of the split rule: piece boundaries fall on multiples of
+# 16 tokens of a sequence.
+BLOCK_TOKENS = 16
+# At most 8 query heads share one pass over a KV head's tokens; larger groups
+# are cut into ceil(G / 8) equal-sized sub-groups, each a separate pass.
+MAX_GROUP_ROWS = 8
+
+
+# ---------------------------------------------------------------- bf16 bits
+
+def widen_bf16(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> float64, exactly (a bf16 is the top half of a float32)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """float64 -> bf16 bit patterns, one rounding: nearest, ties to even.
+
+    bf16 has an 8-bit significand (7 stored bits) and float32's exponent range.
+    Normal numbers are rounded to 8 significant bits; below 2**-126 the grid is
+    the subnormal spacing 2**-133; results of magnitude >= 2**128 after rounding
+    overflow to infinity.  NaN maps to the canonical quiet NaN.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint16)
+    flat = x.reshape(-1)
+    res = out.reshape(-1)
+    nan = np.isnan(flat)
+    sign = np.signbit(flat)
+    a = np.abs(np.where(nan, 0.0, flat))
+    mant, expo = np.frexp(a)                       # a = mant * 2**expo, mant in [0.5, 1)
+    normal = expo - 1 >= -126
+    # significand as an integer in [128, 256]: a = n * 2**(expo - 8)
+    n_norm = np.rint(np.ldexp(mant, 8))
+    v_norm = np.ldexp(n_norm, expo - 8)
+    v_sub = np.ldexp(np.rint(np.ldexp(a, 133)), -133)
+    v = np.where(normal, v_norm, v_sub)
+    v = np.where(v >= 2.0 ** 128, np.inf, v)
+    v32 = np.where(sign, -v, v).astype(np.float32)  # exact: v is on the bf16 grid
+    bits = (v32.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    bits[nan] = 0x7FC0
+    res[:] = bits
+    return out
+
+
+# ------------------------------------------------------------ the definition
+
+def attend(q_rows: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> np.ndarray:
+    """softmax(q K^T * scale) V for each query row, in float64.
+
+    q_rows [n, D], K [L, D], V [L, D] (float64).  Returns [n, D] float64.
+    L == 0 gives zeros (an empty context has nothing to attend to).
+    """
+    n, D = q_rows.shape
+    if K.shape[0] == 0:
+        return np.zeros((n, D), dtype=np.float64)
+    s = (q_rows @ K.T) * float(scale)              # [n, L]
+    M = s.max(axis=1, keepdims=True)
+    w = np.exp(s - M)
+    return (w @ V) / w.sum(axis=1, keepdims=True)
+
+
+def attend_partial(q_rows: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float):
+    """Unnormalised partials over one piece of the context.
+
+    Returns (acc [n, D], m [n], l [n]) with m = max_t s_t,
+    acc = sum_t exp(s_t - m) V_t, l = sum_t exp(s_t - m).
+    An empty piece gives (0, -inf, 0).
+    """
+    n, D = q_rows.shape
+    if K.shape[0] == 0:
+        return np.zeros((n, D)), np.full(n, -np.inf), np.zeros(n)
+    s = (q_rows @ K.T) * float(scale)
+    m = s.max(axis=1)
+    w = np.exp(s - m[:, None])
+    return w @ V, m, w.sum(axis=1)
+
+
+def merge_partials(parts: Sequence[Tuple[np.ndarray, np.ndarray, np.ndarray]]) -> np.ndarray:
+    """Log-sum-exp merge of partials, in the order given.
+
+    M = max_j m_j over pieces with l_j > 0; w_j = exp(m_j - M);
+    out = sum_j w_j acc_j / sum_j w_j l_j.  Pieces with l_j == 0 are skipped;
+    if every piece is empty the result is zero.
+    """
+    acc0 = parts[0][0]
+    n, D = acc0.shape
+    out = np.zeros((n, D))
+    for r in range(n):
+        live = [(a[r], m[r], l[r]) for (a, m, l) in parts if l[r] > 0]
+        if not live:
+            continue
+        M = max(m for (_, m, _) in live)
+        num = np.zeros(D)
+        den = 0.0
+        for a, m, l in live:
+            w = math.exp(m - M)
+            num += w * a
+            den += w * l
+        out[r] = num / den
+    return out
+
+
+# --------------------------------------------------------------- KV access
+
+def head_groups(G: int) -> List[Tuple[int, int]]:
+    """Sub-groups of the G query heads of one KV head: [(first, count)].
+
+    ceil(G / 8) groups of ceil(G / ngroups) heads; the last may be shorter.
+    """
+    ng = -(-G // MAX_GROUP_ROWS)
+    gr = -(-G // ng)
+    return [(j * gr, min(gr, G - j * gr)) for j in range(ng) if j * gr < G]
+
+
+def gather_paged(pool: np.ndarray, page_table: np.ndarray, b: int, L: int, page_size: int) -> np.ndarray:
+    """Logical token rows [L, Hkv, D] of sequence b from a paged pool, one token at a time."""
+    rows = [pool[page_table[b, t // page_size], t % page_size] for t in range(L)]
+    if not rows:
+        return pool[:0, 0]
+    return np.stack(rows)
+
+
+def _kv_rows(inp: dict, b: int, L: int):
+    """(K, V) for sequence b as bf16 bits [L, Hkv, D]."""
+    if "k" in inp:
+        return inp["k"][b, :L], inp["v"][b, :L]
+    ps = int(inp["page_size"])
+    return (gather_paged(inp["k_pool"], inp["page_table"], b, L, ps),
+            gather_paged(inp["v_pool"], inp["page_table"], b, L, ps))
+
+
+def decode_rows(inp: dict, pairs: Iterable[Tuple[int, int]], scale: Optional[float] = None) -> np.ndarray:
+    """fp64 outputs for selected (b, query head) pairs only.  Returns [n, D]."""
+    q = inp["q"]
+    Hq = q.shape[1]
+    Hkv = (inp["k"] if "k" in inp else inp["k_pool"]).shape[2]
+    G = Hq // Hkv
+    scale = inp["scale"] if scale is None else scale
+    res = []
+    cache = {}
+    for b, h in pairs:
+        L = int(inp["seq_lens"][b])
+        if b not in cache:
+            cache = {b: _kv_rows(inp, b, L)}
+        Kb, Vb = cache[b]
+        g = h // G
+        res.append(attend(widen_bf16(q[b, h])[None], widen_bf16(Kb[:, g]), widen_bf16(Vb[:, g]), scale)[0])
+    return np.stack(res) if res else np.zeros((0, q.shape[2]))
+
+
+def decode_contig(q, k, v, seq_lens, scale) -> np.ndarray:
+    """Contiguous cache k, v [B, max_ctx, Hkv, D] (bf16 bits).  Returns fp64 [B, Hq, D]."""
+    inp = {"q": q, "k": k, "v": v, "seq_lens": seq_lens, "scale": scale}
+    return _decode_all(inp)
+
+
+def decode_paged(q, k_pool, v_pool, page_table, seq_lens, page_size, scale) -> np.ndarray:
+    """Paged cache pools [num_pages, page_size, Hkv, D] + page_table [B, max_pages].  fp64 [B, Hq, D]."""
+    inp = {"q": q, "k_pool": k_pool, "v_pool": v_pool, "page_table": page_table,
+           "seq_lens": seq_lens, "page_size": page_size, "scale": scale}
+    return _decode_all(inp)
+
+
+def _decode_all(inp: dict) -> np.ndarray:
+    q = inp["q"]
+    B, Hq, D = q.shape
+    Hkv = (inp["k"] if "k" in inp else inp["k_pool"]).shape[2]
+    G = Hq // Hkv
+    out = np.zeros((B, Hq, D))
+    for b in range(B):
+        L = int(inp["seq_lens"][b])
+        Kb, Vb = _kv_rows(inp, b, L)
+        for g in range(Hkv):
+            Kg, Vg = widen_bf16(Kb[:, g]), widen_bf16(Vb[:, g])
+            out[b, g * G:(g + 1) * G] = attend(widen_bf16(q[b, g * G:(g + 1) * G]), Kg, Vg, inp["scale"])
+    return out
+
+
+# ------------------------------------------------------------ split rule
+
+def split_pieces(seq_lens: Sequence[int], Hkv: int, G: int, num_splits: int):
+    """The partition of every (sequence, KV-head sub-group) token range into pieces.
+
+    Work units are 16-token blocks; sequence b has n_b = ceil(L_b / 16) of them.
+    A segment is one (b, KV head h, head sub-group j); with U = Hkv * len(head_groups(G))
+    sub-group slots u = h * ngroups + j, segment (b, u) occupies blocks
+    [U * P_b + u * n_b, U * P_b + (u + 1) * n_b) of one global block line,
+    where P_b = n_0 + ... + n_{b-1}.  NB = U * P_B blocks in total.
+
+    num_splits == 1: every segment is one piece.
+    num_splits >= 2: the block line is cut into R = (num_splits - 1) * U ranges of
+    q = max(1, ceil(NB / R)) blocks; range r = [r q, (r + 1) q).  A segment's pieces
+    are its non-empty intersections with the ranges, in order; piece index
+    j = r - floor(start / q).  This never gives a segment more than num_splits pieces.
+
+    Returns a list of dicts {b, u, h, group (first, count), piece, t0, t1, npieces}.
+    """
+    groups = head_groups(G)
+    ng = len(groups)
+    U = Hkv * ng
+    lens = [int(x) for x in seq_lens]
+    nblk = [-(-L // BLOCK_TOKENS) for L in lens]
+    out = []
+    if num_splits == 1:
+        for b, L in enumerate(lens):
+            for u in range(U):
+                if L > 0:
+                    out.append(dict(b=b, u=u, h=u // ng, group=groups[u % ng], piece=0,
+                                    t0=0, t1=L, npieces=1))
+        return out
+    P = [0]
+    for n in nblk:
+        P.append(P[-1] + n)
+    NB = U * P[-1]
+    R = (num_splits - 1) * U
+    q = max(1, -(-NB // R))
+    for b, L in enumerate(lens):
+        for u in range(U):
+            start = U * P[b] + u * nblk[b]
+            end = start + nblk[b]
+            if nblk[b] == 0:
+                continue
+            r_first, r_last = start // q, (end - 1) // q
+            for r in range(r_first, r_last + 1):
+                x0, x1 = max(start, r * q), min(end, (r + 1) * q)
+                out.append(dict(b=b, u=u, h=u // ng, group=groups[u % ng], piece=r - r_first,
+                                t0=(x0 - start) * BLOCK_TOKENS,
+                                t1=min((x1 - start) * BLOCK_TOKENS, L),
+                                npieces=r_last - r_first + 1))
+    return out
+
+
+def decode_partials(inp: dict, num_splits: int):
+    """fp64 partials of every piece, laid out as the library's partial buffers.
+
+    Returns (part_acc [B, Hq, S, D], part_ml [B, Hq, S, 2], npieces [B, Hq]).
+    Slots that no piece fills are NaN.
+    """
+    q = inp["q"]
+    B, Hq, D = q.shape
+    Hkv = (inp["k"] if "k" in inp else inp["k_pool"]).shape[2]
+    G = Hq // Hkv
+    S = num_splits
+    acc = np.full((B, Hq, S, D), np.nan)
+    ml = np.full((B, Hq, S, 2), np.nan)
+    npieces = np.zeros((B, Hq), dtype=np.int64)
+    cache = {}
+    for pc in split_pieces(inp["seq_lens"], Hkv, G, S):
+        b, h = pc["b"], pc["h"]
+        if b not in cache:
+            cache = {b: _kv_rows(inp, b, int(inp["seq_lens"][b]))}
+        Kb, Vb = cache[b]
+        first, count = pc["group"]
+        heads = slice(h * G + first, h * G + first + count)
+        a, m, l = attend_partial(widen_bf16(q[b, heads]),
+                                 widen_bf16(Kb[pc["t0"]:pc["t1"], h]),
+                                 widen_bf16(Vb[pc["t0"]:pc["t1"], h]), inp["scale"])
+        acc[b, heads, pc["piece"]] = a
+        ml[b, heads, pc["piece"], 0] = m
+        ml[b, heads, pc["piece"], 1] = l
+        npieces[b, heads] = pc["npieces"]
+    return acc, ml, npieces
+
+
+def combine_partials(part_acc: np.ndarray, part_ml: np.ndarray) -> np.ndarray:
+    """The stand-alone merge: all S slots of each (b, h), skipping slots with l == 0.
+
+    part_acc [B, Hq, S, D], part_ml [B, Hq, S, 2] = (m, l).  Returns fp64 [B, Hq, D].
+    """
+    B, Hq, S, D = part_acc.shape
+    out = np.zeros((B, Hq, D))
+    for b in range(B):
+        for h in range(Hq):
+            parts = [(part_acc[b, h, j][None].astype(np.float64),
+                      np.array([float(part_ml[b, h, j, 0])]),
+                      np.array([float(part_ml[b, h, j, 1])])) for j in range(S)]
+            out[b, h] = merge_partials(parts)[0]
+    return out

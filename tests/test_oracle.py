@@ -1,0 +1,448 @@
+"""Pins for the CPU oracle: closed forms, invariants, brute force and a library routine.
+
+Each check is chosen so that a plausible mistake in the oracle (a dropped
+normalisation, a wrong sign in the exponent, the wrong query-head -> KV-head
+map, K and V swapped, a wrong page index, a wrong piece boundary, double
+rounding to bf16) fails at least one of them; ``test_planted_mistakes_are_caught``
+plants such mistakes in the oracle and checks that.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import decode_attention as od
+from gqa_split_kv_gb300.workloads import Workload, contig_to_paged, f32_to_bf16_bits, make_inputs
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def _rand_bits(rng, shape, std=1.0):
+    return f32_to_bf16_bits((rng.standard_normal(shape) * std).astype(np.float32))
+
+
+def _contig_case(rng, B, Hq, Hkv, D, ctx, lens=None, kstd=1.0):
+    q = _rand_bits(rng, (B, Hq, D))
+    k = _rand_bits(rng, (B, ctx, Hkv, D), kstd)
+    v = _rand_bits(rng, (B, ctx, Hkv, D))
+    seq = np.full(B, ctx, np.int32) if lens is None else np.asarray(lens, np.int32)
+    return dict(q=q, k=k, v=v, seq_lens=seq, scale=float(np.float32(1 / math.sqrt(D))))
+
+
+# ------------------------------------------------------------ bf16 rounding
+
+def _pos_finite_bf16():
+    bits = np.arange(0x0000, 0x7F80, dtype=np.uint16)  # +0 .. largest finite
+    return bits, od.widen_bf16(bits)
+
+
+def test_round_to_bf16_fixes_every_grid_point():
+    bits, vals = _pos_finite_bf16()
+    assert np.array_equal(od.round_to_bf16(vals), bits)
+    assert np.array_equal(od.round_to_bf16(-vals), bits | np.uint16(0x8000))
+
+
+def test_round_to_bf16_midpoints_ties_to_even_and_nearest():
+    bits, vals = _pos_finite_bf16()
+    lo, hi = vals[:-1], vals[1:]
+    mid = (lo + hi) / 2  # exact in fp64
+    even = np.where(bits[:-1] % 2 == 0, bits[:-1], bits[1:])
+    assert np.array_equal(od.round_to_bf16(mid), even)
+    above = np.nextafter(mid, np.inf)
+    below = np.nextafter(mid, -np.inf)
+    assert np.array_equal(od.round_to_bf16(above), bits[1:])
+    assert np.array_equal(od.round_to_bf16(below), bits[:-1])
+    # past the largest finite value: the midpoint to 2**128 rounds to infinity
+    top = float(vals[-1])
+    assert od.round_to_bf16(np.array([top + 2.0 ** 119]))[0] == 0x7F80
+    assert od.round_to_bf16(np.array([np.nextafter(top + 2.0 ** 119, 0)]))[0] == 0x7F7F
+
+
+def test_round_to_bf16_matches_torch_on_float32_values():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(7)
+    x = np.concatenate([rng.standard_normal(200000) * 10.0 ** rng.integers(-30, 30, 200000),
+                        (od.widen_bf16(np.arange(1, 0x7F7F, 97, dtype=np.uint16)) * (1 + 2.0 ** -8))])
+    x32 = x.astype(np.float32)
+    want = torch.from_numpy(x32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(od.round_to_bf16(x32.astype(np.float64)), want)
+
+
+# ---------------------------------------------------------- closed forms
+
+@pytest.mark.parametrize("D,Hq,Hkv", [(32, 4, 1), (64, 8, 2), (128, 32, 8), (256, 24, 4)])
+def test_single_key_returns_its_value_row(D, Hq, Hkv):
+    rng = np.random.default_rng(D)
+    inp = _contig_case(rng, 2, Hq, Hkv, D, ctx=5, lens=[1, 1])
+    out = od.round_to_bf16(od.decode_contig(**inp))
+    G = Hq // Hkv
+    for b in range(2):
+        for h in range(Hq):
+            assert np.array_equal(out[b, h], inp["v"][b, 0, h // G])
+
+
+def test_identical_keys_give_mean_of_values():
+    rng = np.random.default_rng(3)
+    inp = _contig_case(rng, 1, 6, 1, 64, ctx=37)
+    inp["k"][:] = inp["k"][:, :1]
+    out = od.decode_contig(**inp)
+    mean = od.widen_bf16(inp["v"][0, :, 0]).mean(axis=0)
+    assert np.allclose(out[0], mean[None], rtol=0, atol=1e-12)
+
+
+def test_zero_scale_gives_mean_of_values():
+    rng = np.random.default_rng(4)
+    inp = _contig_case(rng, 2, 8, 2, 32, ctx=19, lens=[19, 7])
+    inp["scale"] = 0.0
+    out = od.decode_contig(**inp)
+    for b, L in enumerate([19, 7]):
+        for h in range(8):
+            mean = od.widen_bf16(inp["v"][b, :L, h // 4]).mean(axis=0)
+            assert np.allclose(out[b, h], mean, rtol=0, atol=1e-12)
+
+
+def test_empty_sequence_gives_zeros():
+    rng = np.random.default_rng(5)
+    inp = _contig_case(rng, 2, 4, 2, 32, ctx=8, lens=[0, 8])
+    out = od.decode_contig(**inp)
+    assert np.all(out[0] == 0)
+    assert np.any(out[1] != 0)
+
+
+def test_hand_worked_example():
+    """Two keys, scores (1, 0) for head 0 and (0, 0) for head 1 -> weights e/(e+1), 1/(e+1) and 1/2, 1/2."""
+    one, zero = 0x3F80, 0x0000
+    q = np.array([[[one, zero], [zero, zero]]], np.uint16)          # heads 0 and 1, D=2
+    k = np.array([[[[one, zero]], [[zero, one]]]], np.uint16)        # tokens 0 and 1, one KV head
+    v = f32_to_bf16_bits(np.array([[[[2.0, -1.0]], [[4.0, 3.0]]]], np.float32))
+    out = od.decode_contig(q, k, v, np.array([2], np.int32), 1.0)
+    e = math.e
+    assert np.allclose(out[0, 0], [(2 * e + 4) / (e + 1), (-e + 3) / (e + 1)], atol=1e-15)
+    assert np.allclose(out[0, 1], [3.0, 1.0], atol=1e-15)
+
+
+# --------------------------------------------------------- brute force
+
+def test_matches_high_precision_brute_force():
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 40
+    rng = np.random.default_rng(11)
+    for trial in range(6):
+        B, Hkv, G, D = 2, 2, 1 + trial % 3, 2 + trial % 3
+        lens = [1 + (trial * 3) % 8, 8]
+        inp = _contig_case(rng, B, G * Hkv, Hkv, D, ctx=8, lens=lens, kstd=3.0)
+        inp["scale"] = 0.37
+        out = od.decode_contig(**inp)
+        qf = od.widen_bf16(inp["q"])
+        kf = od.widen_bf16(inp["k"])
+        vf = od.widen_bf16(inp["v"])
+        for b in range(B):
+            for h in range(G * Hkv):
+                g = h // G
+                w = [mpmath.exp(mpmath.mpf(0.37) * mpmath.fsum(mpmath.mpf(qf[b, h, d]) * mpmath.mpf(kf[b, t, g, d])
+                                                            for d in range(D))) for t in range(lens[b])]
+                den = mpmath.fsum(w)
+                for d in range(D):
+                    ref = mpmath.fsum(w[t] * mpmath.mpf(vf[b, t, g, d]) for t in range(lens[b])) / den
+                    assert abs(float(ref) - out[b, h, d]) <= 1e-12 * max(1.0, abs(float(ref)))
+
+
+def test_outlier_scores_stay_finite_and_exact():
+    """Scores of magnitude ~100 (keys x20): the max subtraction keeps exp finite."""
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 60
+    rng = np.random.default_rng(12)
+    inp = _contig_case(rng, 1, 2, 1, 16, ctx=12, kstd=20.0)
+    inp["scale"] = 1.0
+    out = od.decode_contig(**inp)
+    assert np.all(np.isfinite(out))
+    qf, kf, vf = (od.widen_bf16(inp[n]) for n in ("q", "k", "v"))
+    for h in range(2):
+        s = [mpmath.fsum(mpmath.mpf(qf[0, h, d]) * mpmath.mpf(kf[0, t, 0, d]) for d in range(16)) for t in range(12)]
+        w = [mpmath.exp(x) for x in s]
+        for d in range(16):
+            ref = mpmath.fsum(w[t] * mpmath.mpf(vf[0, t, 0, d]) for t in range(12)) / mpmath.fsum(w)
+            assert abs(float(ref) - out[0, h, d]) <= 1e-12 * max(1.0, abs(float(ref)))
+
+
+# ------------------------------------------------------- library routine
+
+@pytest.mark.parametrize("G,Hkv,D", [(1, 4, 64), (4, 2, 64), (6, 4, 256), (8, 8, 128), (12, 2, 32)])
+def test_matches_torch_sdpa_float64(G, Hkv, D):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(G * 100 + D)
+    lens = [33, 70, 1]
+    inp = _contig_case(rng, 3, G * Hkv, Hkv, D, ctx=70, lens=lens)
+    out = od.decode_contig(**inp)
+    for b, L in enumerate(lens):
+        q = torch.from_numpy(od.widen_bf16(inp["q"][b]))[None, :, None, :]                 # [1,Hq,1,D]
+        k = torch.from_numpy(od.widen_bf16(inp["k"][b, :L])).permute(1, 0, 2)[None]        # [1,Hkv,L,D]
+        v = torch.from_numpy(od.widen_bf16(inp["v"][b, :L])).permute(1, 0, 2)[None]
+        k = k.repeat_interleave(G, dim=1)
+        v = v.repeat_interleave(G, dim=1)
+        ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, scale=inp["scale"])[0, :, 0].numpy()
+        assert np.allclose(out[b], ref, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------ invariants
+
+def test_paged_matches_contiguous_and_ignores_page_order():
+    rng = np.random.default_rng(21)
+    lens = [1, 16, 17, 100, 63]
+    inp = _contig_case(rng, 5, 8, 2, 64, ctx=100, lens=lens)
+    ref = od.decode_contig(**inp)
+    for ps, spare in [(16, 0), (32, 3), (1, 2), (64, 1)]:
+        kp, vp, table = contig_to_paged(inp["k"], inp["v"], inp["seq_lens"], ps, rng, spare)
+        got = od.decode_paged(inp["q"], kp, vp, table, inp["seq_lens"], ps, inp["scale"])
+        assert np.array_equal(got, ref)
+        # shuffle the physical pages again: same logical data, same bits out
+        perm = rng.permutation(kp.shape[0])
+        inv = np.argsort(perm)
+        table2 = np.where(table >= 0, inv[np.maximum(table, 0)], -1).astype(np.int32)
+        got2 = od.decode_paged(inp["q"], kp[perm], vp[perm], table2, inp["seq_lens"], ps, inp["scale"])
+        assert np.array_equal(od.round_to_bf16(got2), od.round_to_bf16(ref))
+
+
+def test_joint_token_permutation_invariance():
+    rng = np.random.default_rng(22)
+    inp = _contig_case(rng, 1, 8, 2, 128, ctx=90)
+    ref = od.decode_contig(**inp)
+    perm = rng.permutation(90)
+    inp2 = dict(inp, k=inp["k"][:, perm], v=inp["v"][:, perm])
+    assert np.allclose(od.decode_contig(**inp2), ref, rtol=0, atol=1e-12)
+
+
+def test_linear_in_values():
+    rng = np.random.default_rng(23)
+    inp = _contig_case(rng, 2, 4, 1, 32, ctx=40, lens=[40, 9])
+    v2 = _rand_bits(rng, inp["v"].shape)
+    a = od.decode_contig(**inp)
+    b = od.decode_contig(**dict(inp, v=v2))
+    # v + v2 is not on the bf16 grid; the definition is linear in the widened values
+    qf = inp["q"]
+    both = np.zeros_like(a)
+    for bb, L in enumerate([40, 9]):
+        for h in range(4):
+            K = od.widen_bf16(inp["k"][bb, :L, 0])
+            V = od.widen_bf16(inp["v"][bb, :L, 0]) + od.widen_bf16(v2[bb, :L, 0])
+            both[bb, h] = od.attend(od.widen_bf16(qf[bb, h])[None], K, V, inp["scale"])[0]
+    assert np.allclose(both, a + b, rtol=0, atol=1e-12)
+
+
+def test_single_group_is_per_head_attention():
+    """G=1: every query head reads its own KV head (multi-head attention)."""
+    rng = np.random.default_rng(24)
+    inp = _contig_case(rng, 1, 4, 4, 64, ctx=30)
+    out = od.decode_contig(**inp)
+    for h in range(4):
+        ref = od.attend(od.widen_bf16(inp["q"][0, h])[None], od.widen_bf16(inp["k"][0, :, h]),
+                        od.widen_bf16(inp["v"][0, :, h]), inp["scale"])[0]
+        assert np.array_equal(out[0, h], ref)
+
+
+# ------------------------------------------------------------ split rule
+
+def _check_plan(lens, Hkv, G, S):
+    pieces = od.split_pieces(lens, Hkv, G, S)
+    ng = len(od.head_groups(G))
+    by_seg = {}
+    for p in pieces:
+        by_seg.setdefault((p["b"], p["u"]), []).append(p)
+    for b, L in enumerate(lens):
+        for u in range(Hkv * ng):
+            ps = by_seg.get((b, u), [])
+            if L == 0:
+                assert not ps
+                continue
+            assert 1 <= len(ps) <= S
+            assert [p["piece"] for p in ps] == list(range(len(ps)))
+            assert all(p["npieces"] == len(ps) for p in ps)
+            assert ps[0]["t0"] == 0 and ps[-1]["t1"] == L
+            for a, c in zip(ps, ps[1:]):
+                assert a["t1"] == c["t0"] and a["t1"] % 16 == 0
+            assert all(p["t0"] < p["t1"] for p in ps)
+    return pieces
+
+
+def test_split_rule_partitions_every_segment():
+    rng = np.random.default_rng(31)
+    for trial in range(200):
+        B = int(rng.integers(1, 6))
+        lens = rng.integers(0, 300, size=B).tolist()
+        Hkv = int(rng.integers(1, 5))
+        G = int(rng.integers(1, 18))
+        S = int(rng.integers(1, 12))
+        _check_plan(lens, Hkv, G, S)
+
+
+def test_split_rule_matches_block_by_block_brute_force():
+    """Re-derive the pieces by walking every 16-token block through its range."""
+    rng = np.random.default_rng(32)
+    for trial in range(100):
+        B = int(rng.integers(1, 5))
+        lens = rng.integers(0, 200, size=B).tolist()
+        Hkv, G, S = int(rng.integers(1, 4)), int(rng.integers(1, 10)), int(rng.integers(2, 9))
+        ng = -(-G // 8)
+        U = Hkv * ng
+        line = []  # one entry per block: (b, u, block index in segment)
+        for b, L in enumerate(lens):
+            n = -(-L // 16)
+            for u in range(U):
+                line += [(b, u, i) for i in range(n)]
+        R = (S - 1) * U
+        q = max(1, -(-len(line) // R))
+        want = {}
+        for x, (b, u, i) in enumerate(line):
+            want.setdefault((b, u, x // q), []).append(i)
+        got = {}
+        for p in od.split_pieces(lens, Hkv, G, S):
+            got[(p["b"], p["u"], p["t0"], p["t1"])] = True
+        want_pieces = set()
+        for (b, u, r), blocks in want.items():
+            want_pieces.add((b, u, blocks[0] * 16, min((blocks[-1] + 1) * 16, lens[b])))
+        assert set(got) == want_pieces
+
+
+def test_merge_of_partials_equals_unsplit():
+    rng = np.random.default_rng(33)
+    lens = [5, 130, 64, 1000]
+    inp = _contig_case(rng, 4, 12, 2, 64, ctx=1000, lens=lens)
+    ref = od.decode_contig(**inp)
+    for S in (1, 2, 3, 5, 17, 39):
+        acc, ml, npc = od.decode_partials(inp, S)
+        assert npc.max() <= S
+        for b in range(4):
+            for h in range(12):
+                n = npc[b, h]
+                parts = [(acc[b, h, j][None], ml[b, h, j, :1], ml[b, h, j, 1:]) for j in range(n)]
+                got = od.merge_partials(parts)[0]
+                assert np.allclose(got, ref[b, h], rtol=0, atol=1e-12), (S, b, h)
+
+
+def test_partials_follow_their_definition():
+    """acc / l of one piece is attention over that piece alone; m is the piece's max score."""
+    rng = np.random.default_rng(34)
+    inp = _contig_case(rng, 1, 4, 1, 32, ctx=200)
+    acc, ml, npc = od.decode_partials(inp, 4)
+    pieces = od.split_pieces([200], 1, 4, 4)
+    qf, kf, vf = (od.widen_bf16(inp[n]) for n in ("q", "k", "v"))
+    for p in pieces:
+        for h in range(4):
+            K, V = kf[0, p["t0"]:p["t1"], 0], vf[0, p["t0"]:p["t1"], 0]
+            s = K @ qf[0, h] * inp["scale"]
+            assert ml[0, h, p["piece"], 0] == s.max()
+            assert np.allclose(acc[0, h, p["piece"]] / ml[0, h, p["piece"], 1],
+                               od.attend(qf[0, h][None], K, V, inp["scale"])[0], atol=1e-13)
+
+
+def test_combine_skips_empty_slots():
+    rng = np.random.default_rng(35)
+    inp = _contig_case(rng, 2, 4, 1, 32, ctx=300, lens=[300, 40])
+    acc, ml, npc = od.decode_partials(inp, 6)
+    acc = np.nan_to_num(acc, nan=0.0)
+    ml[..., 0] = np.where(np.isnan(ml[..., 0]), -np.inf, ml[..., 0])
+    ml[..., 1] = np.nan_to_num(ml[..., 1], nan=0.0)
+    out = od.combine_partials(acc, ml)
+    assert np.allclose(out, od.decode_contig(**inp), rtol=0, atol=1e-12)
+
+
+def test_groups_larger_than_eight_are_split_evenly():
+    assert od.head_groups(8) == [(0, 8)]
+    assert od.head_groups(12) == [(0, 6), (6, 6)]
+    assert od.head_groups(9) == [(0, 5), (5, 4)]
+    assert od.head_groups(17) == [(0, 6), (6, 6), (12, 5)]
+
+
+# --------------------------------------------------- planted mistakes
+
+def _pins(monkey_od):
+    """A small battery of the checks above, run against a (possibly mutated) oracle."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(99)
+    inp = _contig_case(rng, 2, 6, 2, 16, ctx=24, lens=[24, 11], kstd=2.0)
+    out = monkey_od.decode_contig(**inp)
+    for b, L in enumerate([24, 11]):
+        q = torch.from_numpy(od.widen_bf16(inp["q"][b]))[None, :, None, :]
+        k = torch.from_numpy(od.widen_bf16(inp["k"][b, :L])).permute(1, 0, 2)[None].repeat_interleave(3, 1)
+        v = torch.from_numpy(od.widen_bf16(inp["v"][b, :L])).permute(1, 0, 2)[None].repeat_interleave(3, 1)
+        ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, scale=inp["scale"])[0, :, 0].numpy()
+        if not np.allclose(out[b], ref, rtol=0, atol=1e-12):
+            return False
+    acc, ml, npc = monkey_od.decode_partials(inp, 5)
+    for b in range(2):
+        for h in range(6):
+            parts = [(acc[b, h, j][None], ml[b, h, j, :1], ml[b, h, j, 1:]) for j in range(npc[b, h])]
+            if not np.allclose(monkey_od.merge_partials(parts)[0], out[b, h], atol=1e-12):
+                return False
+    return True
+
+
+def test_planted_mistakes_are_caught(monkeypatch):
+    assert _pins(od)
+    good_attend, good_partial, good_merge = od.attend, od.attend_partial, od.merge_partials
+
+    def no_norm(q, K, V, scale):
+        s = (q @ K.T) * scale
+        return np.exp(s - s.max(1, keepdims=True)) @ V
+
+    def wrong_sign(q, K, V, scale):
+        s = -(q @ K.T) * scale
+        w = np.exp(s - s.max(1, keepdims=True))
+        return (w @ V) / w.sum(1, keepdims=True)
+
+    def swapped_kv(q, K, V, scale):
+        return good_attend(q, V, K, scale)
+
+    def scale_twice(q, K, V, scale):
+        return good_attend(q, K, V, scale * scale)
+
+    def merge_without_rescale(parts):
+        out = np.zeros_like(parts[0][0])
+        num = sum(a for a, m, l in parts)
+        den = sum(l for a, m, l in parts)
+        return num / den[:, None]
+
+    def partial_off_by_one(q, K, V, scale):
+        return good_partial(q, K[:-1] if len(K) > 1 else K, V[:-1] if len(V) > 1 else V, scale)
+
+    for name, fn in [("attend", no_norm), ("attend", wrong_sign), ("attend", swapped_kv),
+                     ("attend", scale_twice), ("merge_partials", merge_without_rescale),
+                     ("attend_partial", partial_off_by_one)]:
+        with monkeypatch.context() as m:
+            m.setattr(od, name, fn)
+            assert not _pins(od), f"planted mistake in {name} ({fn.__name__}) went unnoticed"
+
+    # wrong query-head -> KV-head map (h % Hkv instead of h // G)
+    def decode_all_modmap(inp):
+        q = inp["q"]
+        B, Hq, D = q.shape
+        Hkv = inp["k"].shape[2]
+        out = np.zeros((B, Hq, D))
+        for b in range(B):
+            L = int(inp["seq_lens"][b])
+            for h in range(Hq):
+                out[b, h] = od.attend(od.widen_bf16(q[b, h])[None], od.widen_bf16(inp["k"][b, :L, h % Hkv]),
+                                      od.widen_bf16(inp["v"][b, :L, h % Hkv]), inp["scale"])[0]
+        return out
+
+    with monkeypatch.context() as m:
+        m.setattr(od, "_decode_all", decode_all_modmap)
+        assert not _pins(od)
+
+
+# ------------------------------------------------------ generator sanity
+
+def test_generator_workloads_have_the_stated_structure():
+    wl = Workload("t", B=8, Hq=16, Hkv=4, D=32, max_ctx=256, layout="paged", page_size=16,
+                  lens="uniform", lens_lo=10, lens_hi=256, seed=5)
+    inp = make_inputs(wl)
+    lens = inp["seq_lens"]
+    assert lens.min() >= 10 and lens.max() <= 256
+    used = inp["page_table"][inp["page_table"] >= 0]
+    assert sorted(used.tolist()) == list(range(inp["k_pool"].shape[0]))
+    wl2 = Workload("o", B=1, Hq=8, Hkv=2, D=64, max_ctx=5000, outlier_frac=0.001, seed=6)
+    inp2 = make_inputs(wl2)
+    assert len(inp2["outlier_pos"]) == 5
+    big = np.abs(od.widen_bf16(inp2["k"][0])).max(axis=(1, 2))
+    assert np.all(big[inp2["outlier_pos"]] > 8.0)
