@@ -1,0 +1,172 @@
+"""Thin Python binding of libdecode_attn.so (argument marshalling only).
+
+Every step of the attention runs in the library's CUDA kernels; this module
+only checks tensor shapes and dtypes, allocates outputs and partial buffers
+with PyTorch when the caller does not pass them, and forwards raw device
+pointers and the current CUDA stream through the C ABI of
+``include/decode_attn.h``.  There is no fallback: if the library is missing
+or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from .build import LIB
+
+__all__ = [
+    "load",
+    "DecodeAttnError",
+    "num_splits",
+    "decode_attn_contig",
+    "decode_attn_paged",
+    "decode_combine",
+    "device_error",
+    "STATUS",
+]
+
+STATUS = {0: "DA_OK", 1: "DA_ERR_INVALID_ARG", 2: "DA_ERR_UNSUPPORTED", 3: "DA_ERR_WORKSPACE",
+          4: "DA_ERR_CUDA", 5: "DA_ERR_TIMEOUT"}
+
+_lib = None
+
+
+class DecodeAttnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+        self.status = status
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the library (built in-tree by gqa_split_kv_gb300.build); raises if it is absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is not built; run gqa_split_kv_gb300.build.build() (needs nvcc)")
+    lib = ctypes.CDLL(p)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.decode_num_splits.argtypes = [i, i, i, i, i]
+    lib.decode_num_splits.restype = i
+    lib.decode_attn_contig.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, vp, vp]
+    lib.decode_attn_contig.restype = i
+    lib.decode_attn_paged.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, vp, vp, vp]
+    lib.decode_attn_paged.restype = i
+    lib.decode_combine.argtypes = [vp, vp, i, i, i, i, vp, vp]
+    lib.decode_combine.restype = i
+    lib.decode_status_string.argtypes = [i]
+    lib.decode_status_string.restype = ctypes.c_char_p
+    lib.decode_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+    lib.decode_device_error.restype = i
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise DecodeAttnError(fn, status)
+
+
+def _need(t, name, dtype, ndim):
+    import torch
+    if t.dtype != dtype or t.dim() != ndim or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor with {ndim} dims, "
+                         f"got {tuple(t.shape)} {t.dtype} on {t.device}")
+
+
+def num_splits(batch: int, num_kv_heads: int, max_seq_len: int, head_dim: int, num_sms: int = 0) -> int:
+    s = load().decode_num_splits(batch, num_kv_heads, max_seq_len, head_dim, num_sms)
+    if s < 0:
+        raise DecodeAttnError("decode_num_splits", -s)
+    return s
+
+
+def _workspace(B, Hq, D, S, part_acc, part_ml, device):
+    import torch
+    if S >= 2:
+        if part_acc is None:
+            part_acc = torch.empty((B, Hq, S, D), dtype=torch.float32, device=device)
+        if part_ml is None:
+            part_ml = torch.empty((B, Hq, S, 2), dtype=torch.float32, device=device)
+    return part_acc, part_ml
+
+
+def decode_attn_contig(q, k, v, seq_lens=None, scale: Optional[float] = None, splits: Optional[int] = None,
+                       part_acc=None, part_ml=None, out=None, stream=None):
+    """q [B,Hq,D], k/v [B,max_ctx,Hkv,D] bf16; seq_lens int32 [B] or None.  Returns out [B,Hq,D] bf16."""
+    import torch
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 4)
+    _need(v, "v", torch.bfloat16, 4)
+    B, Hq, D = q.shape
+    _, ctx, Hkv, _ = k.shape
+    if seq_lens is not None:
+        _need(seq_lens, "seq_lens", torch.int32, 1)
+    scale = D ** -0.5 if scale is None else float(scale)
+    S = num_splits(B, Hkv, ctx, D) if splits is None else int(splits)
+    part_acc, part_ml = _workspace(B, Hq, D, S, part_acc, part_ml, q.device)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    st = load().decode_attn_contig(_ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), B, Hq, Hkv, D, ctx, scale, S,
+                                   _ptr(part_acc), _ptr(part_ml), _ptr(out), _stream(stream))
+    _check("decode_attn_contig", st)
+    return out
+
+
+def decode_attn_paged(q, k_pool, v_pool, page_table, seq_lens, max_seq_len: int, scale: Optional[float] = None,
+                      splits: Optional[int] = None, part_acc=None, part_ml=None, out=None, stream=None):
+    """q [B,Hq,D]; pools [num_pages,page_size,Hkv,D] bf16; page_table int32 [B,max_pages]; seq_lens int32 [B]."""
+    import torch
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pool, "k_pool", torch.bfloat16, 4)
+    _need(v_pool, "v_pool", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, Hq, D = q.shape
+    num_pages, ps, Hkv, _ = k_pool.shape
+    max_pages = page_table.shape[1]
+    scale = D ** -0.5 if scale is None else float(scale)
+    S = num_splits(B, Hkv, max_seq_len, D) if splits is None else int(splits)
+    part_acc, part_ml = _workspace(B, Hq, D, S, part_acc, part_ml, q.device)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    st = load().decode_attn_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(seq_lens), B, Hq, Hkv,
+                                  D, ps, max_pages, num_pages, int(max_seq_len), scale, S, _ptr(part_acc),
+                                  _ptr(part_ml), _ptr(out), _stream(stream))
+    _check("decode_attn_paged", st)
+    return out
+
+
+def decode_combine(part_acc, part_ml, out=None, stream=None):
+    """part_acc [B,Hq,S,D], part_ml [B,Hq,S,2] fp32 -> out [B,Hq,D] bf16."""
+    import torch
+    _need(part_acc, "part_acc", torch.float32, 4)
+    _need(part_ml, "part_ml", torch.float32, 4)
+    B, Hq, S, D = part_acc.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=part_acc.device)
+    st = load().decode_combine(_ptr(part_acc), _ptr(part_ml), B, Hq, D, S, _ptr(out), _stream(stream))
+    _check("decode_combine", st)
+    return out
+
+
+def device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error word."""
+    flags = ctypes.c_uint(0)
+    st = load().decode_device_error(_stream(stream), ctypes.byref(flags))
+    if st not in (0, 5):
+        raise DecodeAttnError("decode_device_error", st)
+    return int(flags.value)

@@ -1,0 +1,452 @@
+// C-ABI entry points of the decode-attention library (declared in include/decode_attn.h).
+//
+// Host side of every call: validate the arguments, build the TMA tensor maps of
+// the caller's K/V/Q buffers, enqueue the persistent split kernel and, when the
+// plan has partial slots, the combine kernel as a programmatic dependent launch
+// (its CTAs are scheduled while the split kernel drains and wait on the device
+// for its completion, so no host round trip or launch gap separates them).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/decode_attn.h"
+#include "combine_kernel.cuh"
+#include "split_kernel.cuh"
+
+namespace da {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per bounded wait
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::mutex g_mu;
+EncodeTiledFn g_encode = nullptr;
+int g_num_sms[kMaxDevices] = {0};
+int g_smem_optin[kMaxDevices] = {0};
+
+int current_device(int* dev) { return cudaGetDevice(dev) == cudaSuccess ? DA_OK : DA_ERR_CUDA; }
+
+int device_info(int dev, int* sms, int* smem_optin) {
+  if (dev < 0 || dev >= kMaxDevices) return DA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_num_sms[dev] == 0) {
+    int s = 0, m = 0;
+    if (cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&m, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return DA_ERR_CUDA;
+    }
+    g_num_sms[dev] = s;
+    g_smem_optin[dev] = m;
+  }
+  *sms = g_num_sms[dev];
+  *smem_optin = g_smem_optin[dev];
+  return DA_OK;
+}
+
+int get_encoder(EncodeTiledFn* fn) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || p == nullptr) {
+      cudaGetLastError();
+      return DA_ERR_CUDA;
+    }
+    g_encode = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  *fn = g_encode;
+  return DA_OK;
+}
+
+// Tiled bf16 map; dims/box innermost first, strides in bytes for dims 1..rank-1.
+int encode_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+               const cuuint32_t* box, int head_dim) {
+  EncodeTiledFn enc;
+  if (int st = get_encoder(&enc)) return st;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUtensorMapSwizzle swz = head_dim >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DA_OK : DA_ERR_INVALID_ARG;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int sub_width(int D) { return D >= 64 ? 64 : 32; }
+
+// Query heads of one KV head are processed in ceil(G / 8) equal sub-groups.
+void head_groups(int G, int* ng, int* gr) {
+  *ng = (G + 7) / 8;
+  *gr = (G + *ng - 1) / *ng;
+}
+
+struct Launch {
+  int B, Hq, Hkv, D, max_len, S;
+  float scale;
+  const void* q;
+  const int* seq_lens;
+  const int* page_table;
+  int page_size, max_pages;
+  float* part_acc;
+  float* part_ml;
+  void* out;
+  cudaStream_t stream;
+  bool paged;
+};
+
+template <int D, bool PAGED>
+int launch_split(const SplitParams& prm, int grid, int smem, int dev, cudaStream_t st) {
+  static bool attr_done[kMaxDevices] = {false};
+  auto kern = split_kernel<D, PAGED>;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!attr_done[dev]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess) {
+        cudaGetLastError();
+        return DA_ERR_UNSUPPORTED;
+      }
+      attr_done[dev] = true;
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(SplitGeo<D>::NTHREADS);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  if (cudaLaunchKernelEx(&cfg, kern, prm) != cudaSuccess) {
+    cudaGetLastError();
+    return DA_ERR_CUDA;
+  }
+  return DA_OK;
+}
+
+template <int D>
+int launch_combine(const CombineParams& prm, int dev, cudaStream_t st, bool dependent) {
+  static bool attr_done[kMaxDevices] = {false};
+  auto kern = combine_kernel<D>;
+  const int smem = prm.planned ? (2 * prm.B + 1) * 4 : 0;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!attr_done[dev]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess) {
+        cudaGetLastError();
+        return DA_ERR_UNSUPPORTED;
+      }
+      attr_done[dev] = true;
+    }
+  }
+  const long long rows = (long long)prm.B * prm.Hq;
+  const long long grid = (rows + CombineGeo<D>::RPC - 1) / CombineGeo<D>::RPC;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(CombineGeo<D>::NTHREADS);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cfg.attrs = dependent ? attr : nullptr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, kern, prm) != cudaSuccess) {
+    cudaGetLastError();
+    return DA_ERR_CUDA;
+  }
+  return DA_OK;
+}
+
+template <int D>
+int run_decode(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, int dev, int sms) {
+  using Gm = SplitGeo<D>;
+  int ng, gr;
+  head_groups(a.Hq / a.Hkv, &ng, &gr);
+  SplitParams prm;
+  std::memset(&prm, 0, sizeof(prm));
+  prm.tm_k = tk;
+  prm.tm_v = tv;
+  {
+    const int SW = sub_width(D);
+    const cuuint64_t dims[4] = {(cuuint64_t)SW, (cuuint64_t)(D / SW), (cuuint64_t)a.Hq, (cuuint64_t)a.B};
+    const cuuint64_t strides[3] = {(cuuint64_t)SW * 2, (cuuint64_t)D * 2, (cuuint64_t)a.Hq * D * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)SW, 1, (cuuint32_t)gr, 1};
+    if (int st = encode_map(&prm.tm_q, a.q, 4, dims, strides, box, D)) return st;
+  }
+  prm.seq_lens = a.seq_lens;
+  prm.page_table = a.page_table;
+  prm.part_acc = a.part_acc;
+  prm.part_ml = a.part_ml;
+  prm.out = reinterpret_cast<__nv_bfloat16*>(a.out);
+  prm.B = a.B;
+  prm.Hq = a.Hq;
+  prm.G = a.Hq / a.Hkv;
+  prm.ng = ng;
+  prm.gr = gr;
+  prm.U = a.Hkv * ng;
+  prm.max_len = a.max_len;
+  prm.page_size = a.page_size;
+  prm.max_pages = a.max_pages;
+  prm.S = a.S;
+  prm.scale_log2 = a.scale * 1.4426950408889634f;
+  prm.timeout_ns = kWaitTimeoutNs;
+
+  // one persistent CTA per SM, never more CTAs than ranges or blocks of work
+  const long long nblk_max = (a.max_len + kBlockTokens - 1) / kBlockTokens;
+  long long ranges = a.S == 1 ? (long long)a.B * prm.U : (long long)(a.S - 1) * prm.U;
+  const long long work = (long long)a.B * prm.U * (nblk_max > 0 ? nblk_max : 1);
+  if (ranges > work) ranges = work;
+  const int grid = (int)(ranges < sms ? ranges : sms);
+  const int smem = Gm::smem_bytes(a.B);
+  if (int st = (a.paged ? launch_split<D, true>(prm, grid, smem, dev, a.stream)
+                        : launch_split<D, false>(prm, grid, smem, dev, a.stream)))
+    return st;
+  if (a.S == 1) return DA_OK;
+  CombineParams cp;
+  cp.part_acc = a.part_acc;
+  cp.part_ml = a.part_ml;
+  cp.out = prm.out;
+  cp.seq_lens = a.seq_lens;
+  cp.B = a.B;
+  cp.Hq = a.Hq;
+  cp.S = a.S;
+  cp.planned = 1;
+  cp.G = prm.G;
+  cp.U = prm.U;
+  cp.ng = ng;
+  cp.gr = gr;
+  cp.max_len = a.max_len;
+  return launch_combine<D>(cp, dev, a.stream, true);
+}
+
+int check_common(const void* q, const void* out, int B, int Hq, int Hkv, int D, float scale, int S,
+                 const float* part_acc, const float* part_ml) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return DA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return DA_ERR_INVALID_ARG;
+  if (S < 1 || S > DA_MAX_SPLITS) return DA_ERR_INVALID_ARG;
+  if (D != 32 && D != 64 && D != 128 && D != 256) return DA_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 64) return DA_ERR_UNSUPPORTED;
+  if (B == 0) return DA_OK;
+  if (!q || !out) return DA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16)) return DA_ERR_INVALID_ARG;
+  if (S >= 2) {
+    if (!part_acc || !part_ml) return DA_ERR_WORKSPACE;
+    if (!aligned(part_acc, 16) || !aligned(part_ml, 8)) return DA_ERR_INVALID_ARG;
+  }
+  return DA_OK;
+}
+
+int dispatch(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, int dev, int sms, int smem_optin) {
+  int need = 0;
+  switch (a.D) {
+    case 32: need = SplitGeo<32>::smem_bytes(a.B); break;
+    case 64: need = SplitGeo<64>::smem_bytes(a.B); break;
+    case 128: need = SplitGeo<128>::smem_bytes(a.B); break;
+    default: need = SplitGeo<256>::smem_bytes(a.B); break;
+  }
+  if (need > smem_optin || need > 227 * 1024) return DA_ERR_UNSUPPORTED;
+  switch (a.D) {
+    case 32: return run_decode<32>(a, tk, tv, dev, sms);
+    case 64: return run_decode<64>(a, tk, tv, dev, sms);
+    case 128: return run_decode<128>(a, tk, tv, dev, sms);
+    default: return run_decode<256>(a, tk, tv, dev, sms);
+  }
+}
+
+int zero_output(void* out, int B, int Hq, int D, cudaStream_t st) {
+  if (cudaMemsetAsync(out, 0, (size_t)B * Hq * D * 2, st) != cudaSuccess) {
+    cudaGetLastError();
+    return DA_ERR_CUDA;
+  }
+  return DA_OK;
+}
+
+}  // namespace
+}  // namespace da
+
+using namespace da;
+
+extern "C" int decode_num_splits(int batch, int num_kv_heads, int max_seq_len, int head_dim, int num_sms) {
+  if (batch < 0 || num_kv_heads <= 0 || max_seq_len < 0 || head_dim <= 0) return -DA_ERR_INVALID_ARG;
+  if (num_sms <= 0) {
+    int dev, smem;
+    if (current_device(&dev) || device_info(dev, &num_sms, &smem)) return -DA_ERR_CUDA;
+  }
+  const long long nblk = ((long long)max_seq_len + kBlockTokens - 1) / kBlockTokens;
+  if (nblk <= 1) return 1;
+  long long S = (num_sms + num_kv_heads - 1) / num_kv_heads + 1;
+  if (S > nblk) S = nblk;
+  if (S > DA_MAX_SPLITS) S = DA_MAX_SPLITS;
+  if (S < 2) S = 2;
+  return (int)S;
+}
+
+extern "C" int decode_attn_contig(const void* q, const void* k, const void* v, const int* seq_lens, int batch,
+                                  int num_q_heads, int num_kv_heads, int head_dim, int max_ctx, float scale,
+                                  int num_splits, float* part_acc, float* part_ml, void* out, void* stream) {
+  const int B = batch, Hq = num_q_heads, Hkv = num_kv_heads, D = head_dim, S = num_splits;
+  if (int st = check_common(q, out, B, Hq, Hkv, D, scale, S, part_acc, part_ml)) return st;
+  if (max_ctx < 0) return DA_ERR_INVALID_ARG;
+  if (B == 0) return DA_OK;
+  if (max_ctx > 0 && (!k || !v || !aligned(k, 16) || !aligned(v, 16))) return DA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (max_ctx == 0) return zero_output(out, B, Hq, D, st);
+  int dev, sms, smem_optin;
+  if (current_device(&dev) || device_info(dev, &sms, &smem_optin)) return DA_ERR_CUDA;
+
+  const int SW = sub_width(D);
+  const cuuint64_t row = (cuuint64_t)Hkv * D * 2;
+  const cuuint64_t dims[5] = {(cuuint64_t)SW, (cuuint64_t)(D / SW), (cuuint64_t)Hkv, (cuuint64_t)max_ctx,
+                              (cuuint64_t)B};
+  const cuuint64_t strides[4] = {(cuuint64_t)SW * 2, (cuuint64_t)D * 2, row, row * (cuuint64_t)max_ctx};
+  const cuuint32_t box[5] = {(cuuint32_t)SW, 1, 1, (cuuint32_t)SplitGeo<32>::T, 1};
+  CUtensorMap tk, tv;
+  if (int e = encode_map(&tk, k, 5, dims, strides, box, D)) return e;
+  if (int e = encode_map(&tv, v, 5, dims, strides, box, D)) return e;
+
+  Launch a;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.max_len = max_ctx;
+  a.S = S;
+  a.scale = scale;
+  a.q = q;
+  a.seq_lens = seq_lens;
+  a.page_table = nullptr;
+  a.page_size = 0;
+  a.max_pages = 0;
+  a.part_acc = part_acc;
+  a.part_ml = part_ml;
+  a.out = out;
+  a.stream = st;
+  a.paged = false;
+  return dispatch(a, tk, tv, dev, sms, smem_optin);
+}
+
+extern "C" int decode_attn_paged(const void* q, const void* k_pool, const void* v_pool, const int* page_table,
+                                 const int* seq_lens, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int page_size, int max_pages_per_seq, int num_pages, int max_seq_len, float scale,
+                                 int num_splits, float* part_acc, float* part_ml, void* out, void* stream) {
+  const int B = batch, Hq = num_q_heads, Hkv = num_kv_heads, D = head_dim, S = num_splits;
+  if (int st = check_common(q, out, B, Hq, Hkv, D, scale, S, part_acc, part_ml)) return st;
+  if (page_size <= 0 || max_pages_per_seq < 0 || num_pages < 0 || max_seq_len < 0) return DA_ERR_INVALID_ARG;
+  if (page_size % 16 != 0) return DA_ERR_UNSUPPORTED;
+  if (B == 0) return DA_OK;
+  if (!seq_lens) return DA_ERR_INVALID_ARG;
+  long long cap = (long long)max_pages_per_seq * page_size;
+  if (cap > max_seq_len) cap = max_seq_len;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cap == 0 || num_pages == 0) return zero_output(out, B, Hq, D, st);
+  if (cap > 0x7fffffffLL) return DA_ERR_UNSUPPORTED;
+  if (!k_pool || !v_pool || !page_table || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(page_table, 4))
+    return DA_ERR_INVALID_ARG;
+  int dev, sms, smem_optin;
+  if (current_device(&dev) || device_info(dev, &sms, &smem_optin)) return DA_ERR_CUDA;
+
+  const int SW = sub_width(D);
+  const cuuint64_t row = (cuuint64_t)Hkv * D * 2;
+  const cuuint64_t dims[5] = {(cuuint64_t)SW, (cuuint64_t)(D / SW), (cuuint64_t)Hkv, (cuuint64_t)page_size,
+                              (cuuint64_t)num_pages};
+  const cuuint64_t strides[4] = {(cuuint64_t)SW * 2, (cuuint64_t)D * 2, row, row * (cuuint64_t)page_size};
+  const cuuint32_t box[5] = {(cuuint32_t)SW, 1, 1, 16, 1};
+  CUtensorMap tk, tv;
+  if (int e = encode_map(&tk, k_pool, 5, dims, strides, box, D)) return e;
+  if (int e = encode_map(&tv, v_pool, 5, dims, strides, box, D)) return e;
+
+  Launch a;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.max_len = (int)cap;
+  a.S = S;
+  a.scale = scale;
+  a.q = q;
+  a.seq_lens = seq_lens;
+  a.page_table = page_table;
+  a.page_size = page_size;
+  a.max_pages = max_pages_per_seq;
+  a.part_acc = part_acc;
+  a.part_ml = part_ml;
+  a.out = out;
+  a.stream = st;
+  a.paged = true;
+  return dispatch(a, tk, tv, dev, sms, smem_optin);
+}
+
+extern "C" int decode_combine(const float* part_acc, const float* part_ml, int batch, int num_q_heads,
+                              int head_dim, int num_splits, void* out, void* stream) {
+  const int B = batch, Hq = num_q_heads, D = head_dim, S = num_splits;
+  if (B < 0 || Hq <= 0 || S < 1 || S > DA_MAX_SPLITS) return DA_ERR_INVALID_ARG;
+  if (D != 32 && D != 64 && D != 128 && D != 256) return DA_ERR_UNSUPPORTED;
+  if (B == 0) return DA_OK;
+  if (!part_acc || !part_ml || !out) return DA_ERR_INVALID_ARG;
+  if (!aligned(part_acc, 16) || !aligned(part_ml, 8) || !aligned(out, 16)) return DA_ERR_INVALID_ARG;
+  int dev;
+  if (current_device(&dev) || dev >= kMaxDevices) return DA_ERR_CUDA;
+  CombineParams cp;
+  std::memset(&cp, 0, sizeof(cp));
+  cp.part_acc = part_acc;
+  cp.part_ml = part_ml;
+  cp.out = reinterpret_cast<__nv_bfloat16*>(out);
+  cp.B = B;
+  cp.Hq = Hq;
+  cp.S = S;
+  cp.planned = 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  switch (D) {
+    case 32: return launch_combine<32>(cp, dev, st, false);
+    case 64: return launch_combine<64>(cp, dev, st, false);
+    case 128: return launch_combine<128>(cp, dev, st, false);
+    default: return launch_combine<256>(cp, dev, st, false);
+  }
+}
+
+extern "C" const char* decode_status_string(int status) {
+  switch (status) {
+    case DA_OK: return "DA_OK";
+    case DA_ERR_INVALID_ARG: return "DA_ERR_INVALID_ARG";
+    case DA_ERR_UNSUPPORTED: return "DA_ERR_UNSUPPORTED";
+    case DA_ERR_WORKSPACE: return "DA_ERR_WORKSPACE";
+    case DA_ERR_CUDA: return "DA_ERR_CUDA";
+    case DA_ERR_TIMEOUT: return "DA_ERR_TIMEOUT";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int decode_device_error(void* stream, unsigned int* flags) {
+  if (!flags) return DA_ERR_INVALID_ARG;
+  *flags = 0;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return DA_ERR_CUDA;
+  }
+  unsigned int w = 0;
+  if (cudaMemcpyFromSymbol(&w, g_error_word, sizeof(w)) != cudaSuccess) {
+    cudaGetLastError();
+    return DA_ERR_CUDA;
+  }
+  if (w) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) {
+      cudaGetLastError();
+      return DA_ERR_CUDA;
+    }
+  }
+  *flags = w;
+  return w ? DA_ERR_TIMEOUT : DA_OK;
+}

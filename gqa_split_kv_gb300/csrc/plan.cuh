@@ -1,0 +1,176 @@
+// Device-side split plan: the partition of every (sequence, KV-head sub-group)
+// token range into pieces, one contiguous range of 16-token blocks per CTA.
+//
+// The pages choose one split count for all sequences and cap it by the tile
+// count (AstrAI commit 988e013 "csrc", split-KV items).  This library instead
+// lays all segments end to end on one line of 16-token blocks and cuts the line
+// into equal ranges, so a persistent grid stays balanced for any mix of lengths.
+//
+//   n_b  = ceil(L_b / 16)                     blocks of sequence b
+//   P_b  = n_0 + ... + n_{b-1}                (prefix, P_B = total)
+//   U    = Hkv * ceil(G / 8)                  sub-group slots per sequence
+//   segment (b, u) = blocks [U P_b + u n_b, U P_b + (u + 1) n_b)
+//   S >= 2: q = max(1, ceil(U P_B / ((S - 1) U))), range r = [r q, (r + 1) q)
+//   S == 1: range r = segment (r / U, r % U), whole.
+#pragma once
+
+#include <cstdint>
+
+namespace da {
+
+constexpr int kBlockTokens = 16;
+
+struct Plan {
+  long long NB;      // blocks on the line
+  long long q;       // blocks per range (S >= 2)
+  long long ranges;  // ranges that hold work
+  int U;             // sub-group slots per sequence
+  int S;             // partial slots per (b, h)
+};
+
+struct Piece {
+  int b, u;      // sequence, sub-group slot
+  int t0, t1;    // token range [t0, t1) within the sequence
+  int j;         // piece index within the segment (partial slot)
+  int npieces;   // pieces of this segment
+};
+
+// lens[b] = clamp(seq_lens[b] or max_len, 0, max_len); P[0..B] = block prefix.
+// Called by every thread of the block (contains __syncthreads).
+__device__ __forceinline__ void build_plan_arrays(const int* __restrict__ seq_lens, int B, int max_len, int* lens,
+                                                  int* P) {
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    int L = seq_lens ? __ldg(seq_lens + b) : max_len;
+    L = L < 0 ? 0 : (L > max_len ? max_len : L);
+    lens[b] = L;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = (B + 31) / 32;
+    const int b0 = lane * per;
+    const int b1 = min(B, b0 + per);
+    int s = 0;
+    for (int b = b0; b < b1; ++b) s += (lens[b] + kBlockTokens - 1) / kBlockTokens;
+    int incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - s;
+    for (int b = b0; b < b1; ++b) {
+      P[b] = run;
+      run += (lens[b] + kBlockTokens - 1) / kBlockTokens;
+    }
+    if (lane == 31) P[B] = incl;
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ Plan make_plan(int B, int U, int S, const int* P) {
+  Plan pl;
+  pl.U = U;
+  pl.S = S;
+  pl.NB = (long long)U * P[B];
+  if (S == 1) {
+    pl.q = 0;
+    pl.ranges = (long long)B * U;
+  } else {
+    const long long R = (long long)(S - 1) * U;
+    pl.q = (pl.NB + R - 1) / R;
+    if (pl.q < 1) pl.q = 1;
+    pl.ranges = (pl.NB + pl.q - 1) / pl.q;
+  }
+  return pl;
+}
+
+// Number of pieces of segment (b, u) under plan pl (S >= 2).
+__device__ __forceinline__ int segment_pieces(const Plan& pl, const int* lens, const int* P, int b, int u) {
+  const int nb = (lens[b] + kBlockTokens - 1) / kBlockTokens;
+  if (nb == 0) return 0;
+  const long long s0 = (long long)pl.U * P[b] + (long long)u * nb;
+  const long long s1 = s0 + nb;
+  return (int)((s1 - 1) / pl.q - s0 / pl.q + 1);
+}
+
+// S >= 2: the piece that starts at block x of range r (x < xe = end of range).
+// Returns the block where the next piece of the range starts.
+__device__ __forceinline__ long long piece_at(const Plan& pl, const int* lens, const int* P, int B, long long x,
+                                              long long xe, long long r, Piece& pc) {
+  // sequence b: the last with U * P[b] <= x (sequences with no blocks are skipped
+  // because the following non-empty one shares their prefix value)
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((long long)pl.U * P[mid] <= x)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int b = lo;
+  const int nb = (lens[b] + kBlockTokens - 1) / kBlockTokens;
+  const long long base = (long long)pl.U * P[b];
+  const int u = (int)((x - base) / nb);
+  const long long s0 = base + (long long)u * nb;
+  const long long s1 = s0 + nb;
+  const long long pe = xe < s1 ? xe : s1;
+  pc.b = b;
+  pc.u = u;
+  pc.t0 = (int)(x - s0) * kBlockTokens;
+  pc.t1 = min((int)(pe - s0) * kBlockTokens, lens[b]);
+  pc.j = (int)(r - s0 / pl.q);
+  pc.npieces = (int)((s1 - 1) / pl.q - s0 / pl.q + 1);
+  return pe;
+}
+
+// Walks the pieces of the ranges blockIdx.x, blockIdx.x + gridDim.x, ...
+struct PieceWalker {
+  long long r;       // range being walked
+  long long x, xe;   // S >= 2: next block and end of range r
+  bool started;
+
+  __device__ __forceinline__ void init() {
+    r = blockIdx.x;
+    started = false;
+    x = xe = 0;
+  }
+
+  // Next piece in walk order; false when the CTA's work is done.  With
+  // skip_empty, segments of empty sequences (S == 1 only) are skipped.
+  __device__ __forceinline__ bool next(const Plan& pl, const int* lens, const int* P, int B, bool skip_empty,
+                                       Piece& pc) {
+    if (pl.S == 1) {
+      while (true) {
+        if (started) r += gridDim.x;
+        started = true;
+        if (r >= pl.ranges) return false;
+        pc.b = (int)(r / pl.U);
+        pc.u = (int)(r % pl.U);
+        pc.t0 = 0;
+        pc.t1 = lens[pc.b];
+        pc.j = 0;
+        pc.npieces = 1;
+        if (!(skip_empty && pc.t1 == 0)) return true;
+      }
+    }
+    while (true) {
+      if (!started) {
+        started = true;
+        if (r >= pl.ranges) return false;
+        x = r * pl.q;
+        xe = x + pl.q < pl.NB ? x + pl.q : pl.NB;
+      }
+      if (x < xe) {
+        x = piece_at(pl, lens, P, B, x, xe, r, pc);
+        return true;
+      }
+      r += gridDim.x;
+      if (r >= pl.ranges) return false;
+      x = r * pl.q;
+      xe = x + pl.q < pl.NB ? x + pl.q : pl.NB;
+    }
+  }
+};
+
+}  // namespace da

@@ -1,0 +1,468 @@
+// Split-KV decode kernel: one persistent CTA per SM walks its ranges of the
+// block line; for every piece it streams the K/V tiles of one (sequence, KV head)
+// through a TMA-fed shared-memory ring and runs the G query heads of the KV head
+// over them with head-packed bf16 tensor-core MMAs and an fp32 online softmax.
+//
+// Roles (warp-specialised):
+//   warp W (producer): one elected lane waits for a free stage, posts the byte
+//     count and issues the TMA tile copies (K, V and, for the first tile of a
+//     piece, the query rows).  Paged caches: the lanes resolve one page-table
+//     entry per 16-token block, prefetched LA tiles ahead with cp.async.
+//   warps 0..W-1 (consumers): warp w owns tokens [16 w, 16 w + 16) of every tile.
+//
+// Prior art on the pages: the two-stage cp.async ring of "perf(dspark): overlap
+// KV staging with compute via cp.async" (section "Summary"); the per-warp-group
+// KV stripes with their own (m, l, acc) folded in ascending order of
+// "perf(qwen3.8): split the flash-decode KV range across warp-groups" (section
+// "Mechanism"); MMA head packing, XOR swizzle and one page lookup per tile of
+// AstrAI commits 988e013 and 69fecaf.  Here the ring is filled by the Blackwell
+// tensor-memory accelerator (cp.async.bulk.tensor, 128-byte swizzle), the stage
+// count is sized for the 227 KB of shared memory per CTA, and tiles are
+// released through mbarriers instead of CTA-wide barriers.
+//
+// Head packing: the MMA tile is 16 rows; query heads fill rows 0..7 and rows
+// 8..15 carry the bf16 low part of the probabilities, so P = hi + lo reaches
+// the fp32 accumulator with ~2^-17 relative error at no extra MMA.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "plan.cuh"
+#include "ptx.cuh"
+
+namespace da {
+
+// Device error word (bit 0: a bounded wait ran out).  The library is one
+// translation unit, so the definition lives here; the host reads and clears it
+// through decode_device_error().
+__device__ unsigned int g_error_word = 0;
+
+struct SplitParams {
+  CUtensorMap tm_k;  // K cache / pool
+  CUtensorMap tm_v;  // V cache / pool
+  CUtensorMap tm_q;  // Q [B, Hq, D]
+  const int* seq_lens;
+  const int* page_table;
+  float* part_acc;
+  float* part_ml;
+  __nv_bfloat16* out;
+  int B, Hq, G, U, ng, gr;
+  int max_len;       // lengths are clamped to [0, max_len]
+  int page_size, max_pages;
+  int S;
+  float scale_log2;  // scale * log2(e)
+  unsigned long long timeout_ns;
+};
+
+template <int D>
+struct SplitGeo {
+  static constexpr int T = 64;                 // tokens per tile
+  static constexpr int W = 4;                  // consumer warps, 16 tokens each
+  static constexpr int NTHREADS = (W + 1) * 32;
+  static constexpr int SUBW = D >= 64 ? 64 : 32;    // elements per swizzle row
+  static constexpr int NSUB = D / SUBW;             // swizzle rows per token
+  static constexpr int ROWB = SUBW * 2;             // 128 or 64 bytes
+  static constexpr int CPR = SUBW / 8;              // 16-byte chunks per swizzle row
+  static constexpr int STAGES = D == 32 ? 8 : D == 64 ? 6 : D == 128 ? 4 : 2;
+  static constexpr int SUB_BYTES = T * ROWB;        // one swizzle column of a tile
+  static constexpr int KV_BYTES = T * D * 2;        // one tensor, one stage
+  static constexpr int Q_SUB_BYTES = 8 * ROWB;
+  static constexpr int Q_BYTES = 8 * D * 2;
+  static constexpr int RING = 4;                    // page-entry ring slots
+  static constexpr int LA = 2;                      // page-entry prefetch distance (tiles)
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
+  static constexpr int OFF_Q = OFF_V + STAGES * KV_BYTES;
+  static constexpr int OFF_FACC = OFF_Q + STAGES * Q_BYTES;
+  static constexpr int OFF_FML = OFF_FACC + W * 8 * D * 4;
+  static constexpr int OFF_BAR = OFF_FML + W * 8 * 2 * 4;
+  static constexpr int OFF_PG = OFF_BAR + 2 * STAGES * 8;
+  static constexpr int OFF_MISC = OFF_PG + RING * 32 * 4;
+  static constexpr int OFF_PLAN = OFF_MISC + 16;
+  static constexpr int smem_bytes(int B) { return OFF_PLAN + (2 * B + 1) * 4 + 1024; }
+  static_assert(T == 16 * W, "each consumer warp owns 16 tokens of a tile");
+  static_assert(T / 16 <= 32, "one producer lane per 16-token block");
+};
+
+template <int ROWB>
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  const uint32_t off = (uint32_t)(row * ROWB + chunk * 16);
+  return ROWB == 128 ? off ^ (((off >> 7) & 7u) << 4) : off ^ (((off >> 7) & 3u) << 4);
+}
+
+// Bounded mbarrier wait.  Gives up after timeout_ns: sets the device error word
+// and the CTA's abort flag, after which every later wait returns at once, so
+// all warps still reach the same named barriers and the CTA exits.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             unsigned long long timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  if (*abort_flag) return false;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      atomicOr(&g_error_word, 1u);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Piece + tile cursor used by the producer (pieces without tokens are skipped).
+struct TileCursor {
+  PieceWalker walk;
+  Piece pc;
+  int t;
+  bool valid;
+
+  __device__ __forceinline__ void init(const Plan& pl, const int* lens, const int* P, int B) {
+    walk.init();
+    valid = walk.next(pl, lens, P, B, true, pc);
+    t = pc.t0;
+  }
+  __device__ __forceinline__ void advance(const Plan& pl, const int* lens, const int* P, int B, int T) {
+    t += T;
+    if (t >= pc.t1) {
+      valid = walk.next(pl, lens, P, B, true, pc);
+      t = pc.t0;
+    }
+  }
+};
+
+template <int D, bool PAGED>
+__device__ __forceinline__ void split_producer(const SplitParams& p, const Plan& pl, const int* lens, const int* P,
+                                               uint8_t* smem, uint32_t sbase, volatile int* abort_flag) {
+  using Gm = SplitGeo<D>;
+  const int lane = threadIdx.x & 31;
+  const uint32_t bar_full = sbase + Gm::OFF_BAR;
+  const uint32_t bar_empty = bar_full + Gm::STAGES * 8;
+  const uint32_t pg_ring = sbase + Gm::OFF_PG;
+  const int* pg_ring_ptr = reinterpret_cast<const int*>(smem + Gm::OFF_PG);
+
+  TileCursor cur;
+  cur.init(pl, lens, P, p.B);
+  TileCursor look = cur;
+
+  // prologue of the page-entry prefetch: tiles 0 .. LA-1
+  if (PAGED) {
+#pragma unroll
+    for (int k = 0; k < Gm::LA; ++k) {
+      if (look.valid) {
+        const int nblk = min(Gm::T, look.pc.t1 - look.t + 15) / 16;
+        if (lane < nblk) {
+          const int tok = look.t + 16 * lane;
+          cp_async_4(pg_ring + (uint32_t)((k % Gm::RING) * 32 + lane) * 4,
+                     p.page_table + (size_t)look.pc.b * p.max_pages + tok / p.page_size);
+        }
+        look.advance(pl, lens, P, p.B, Gm::T);
+      }
+      cp_async_commit();
+    }
+  }
+
+  long long n = 0;  // tiles issued
+  while (cur.valid) {
+    const int stage = (int)(n % Gm::STAGES);
+    const uint32_t parity = (uint32_t)((n / Gm::STAGES) & 1);
+    const Piece& pc = cur.pc;
+    const int h = pc.u / p.ng;
+    const int first_head = h * p.G + (pc.u % p.ng) * p.gr;
+    const bool first_tile = cur.t == pc.t0;
+    const int ntok = min(Gm::T, pc.t1 - cur.t);
+    const int nblk = (ntok + 15) / 16;
+
+    int page = 0;
+    if (PAGED) {
+      if (look.valid) {
+        const int lblk = min(Gm::T, look.pc.t1 - look.t + 15) / 16;
+        if (lane < lblk) {
+          const int tok = look.t + 16 * lane;
+          cp_async_4(pg_ring + (uint32_t)(((n + Gm::LA) % Gm::RING) * 32 + lane) * 4,
+                     p.page_table + (size_t)look.pc.b * p.max_pages + tok / p.page_size);
+        }
+        look.advance(pl, lens, P, p.B, Gm::T);
+      }
+      cp_async_commit();
+      cp_async_wait<Gm::LA>();
+      __syncwarp();
+      if (lane < nblk) page = pg_ring_ptr[(n % Gm::RING) * 32 + lane];
+    }
+
+    // wait until the consumers have released this stage (first pass: free)
+    bool ok = true;
+    if (lane == 0) ok = wait_bounded(bar_empty + stage * 8, parity ^ 1u, abort_flag, p.timeout_ns);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (!ok) break;
+
+    const uint32_t full = bar_full + stage * 8;
+    const uint32_t kdst = sbase + Gm::OFF_K + stage * Gm::KV_BYTES;
+    const uint32_t vdst = sbase + Gm::OFF_V + stage * Gm::KV_BYTES;
+    const uint32_t qdst = sbase + Gm::OFF_Q + stage * Gm::Q_BYTES;
+    const uint32_t qbytes = first_tile ? (uint32_t)(Gm::NSUB * p.gr * Gm::ROWB) : 0u;
+    const uint32_t kvbytes = PAGED ? (uint32_t)(nblk * 16 * D * 2) : (uint32_t)Gm::KV_BYTES;
+    if (lane == 0) mbar_arrive_expect_tx(full, 2u * kvbytes + qbytes);
+    __syncwarp();
+    if (PAGED) {
+      if (lane < nblk) {
+        const int tok = cur.t + 16 * lane;
+        const int row0 = tok % p.page_size;
+#pragma unroll
+        for (int sub = 0; sub < Gm::NSUB; ++sub) {
+          const uint32_t off = (uint32_t)(sub * Gm::SUB_BYTES + lane * 16 * Gm::ROWB);
+          tma_load_5d(kdst + off, &p.tm_k, full, 0, sub, h, row0, page);
+          tma_load_5d(vdst + off, &p.tm_v, full, 0, sub, h, row0, page);
+        }
+      }
+    } else if (lane == 0) {
+#pragma unroll
+      for (int sub = 0; sub < Gm::NSUB; ++sub) {
+        tma_load_5d(kdst + sub * Gm::SUB_BYTES, &p.tm_k, full, 0, sub, h, cur.t, pc.b);
+        tma_load_5d(vdst + sub * Gm::SUB_BYTES, &p.tm_v, full, 0, sub, h, cur.t, pc.b);
+      }
+    }
+    if (first_tile && lane == 0) {
+#pragma unroll
+      for (int sub = 0; sub < Gm::NSUB; ++sub)
+        tma_load_4d(qdst + sub * Gm::Q_SUB_BYTES, &p.tm_q, full, 0, sub, first_head, pc.b);
+    }
+    ++n;
+    cur.advance(pl, lens, P, p.B, Gm::T);
+  }
+  if (PAGED) cp_async_wait<0>();
+
+  // After an abort, let the copies already issued land before the CTA exits.
+  if (*abort_flag && lane == 0) {
+    for (long long k = n > Gm::STAGES ? n - Gm::STAGES : 0; k < n; ++k) {
+      const uint32_t full = bar_full + (uint32_t)(k % Gm::STAGES) * 8;
+      const uint32_t par = (uint32_t)((k / Gm::STAGES) & 1);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(full, par) && globaltimer_ns() - t0 < p.timeout_ns) {
+      }
+    }
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan& pl, const int* lens, const int* P,
+                                               uint8_t* smem, uint32_t sbase, volatile int* abort_flag) {
+  using Gm = SplitGeo<D>;
+  constexpr int KCH = D / 16;  // k-chunks of the QK^T product
+  constexpr int NB8 = D / 8;   // 8-column blocks of the PV product
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;  // MMA row (query head within the group)
+  const int i4 = lane & 3;
+  const uint32_t bar_full = sbase + Gm::OFF_BAR;
+  const uint32_t bar_empty = bar_full + Gm::STAGES * 8;
+  float* facc = reinterpret_cast<float*>(smem + Gm::OFF_FACC);
+  float* fml = reinterpret_cast<float*>(smem + Gm::OFF_FML);
+  const float kNegInf = -__int_as_float(0x7f800000);
+
+  // ldmatrix lane -> (row, chunk) patterns
+  const int k_row = 16 * warp + (lane & 7) + ((lane >> 4) << 3);
+  const int k_chk = (lane >> 3) & 1;
+  const int v_row = 16 * warp + (lane & 7) + (((lane >> 3) & 1) << 3);
+  const int v_chk = lane >> 4;
+
+  PieceWalker walk;
+  walk.init();
+  Piece pc;
+  long long n = 0;  // tiles consumed
+  while (walk.next(pl, lens, P, p.B, false, pc)) {
+    uint32_t qa[KCH][2];
+    float acc[NB8][4];
+#pragma unroll
+    for (int c = 0; c < NB8; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
+    float m_run = kNegInf, l_run = 0.f;
+    const int h = pc.u / p.ng;
+    const int first_head = h * p.G + (pc.u % p.ng) * p.gr;
+    const int nrows = min(p.gr, p.G - (pc.u % p.ng) * p.gr);
+
+    for (int t = pc.t0; t < pc.t1; t += Gm::T) {
+      const int stage = (int)(n % Gm::STAGES);
+      const uint32_t parity = (uint32_t)((n / Gm::STAGES) & 1);
+      wait_bounded(bar_full + stage * 8, parity, abort_flag, p.timeout_ns);
+      if (t == pc.t0) {
+        const uint32_t qst = sbase + Gm::OFF_Q + stage * Gm::Q_BYTES;
+#pragma unroll
+        for (int jq = 0; jq < D / 32; ++jq) {
+          const int c = 4 * jq + (lane >> 3);
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4(qst + (c / Gm::CPR) * Gm::Q_SUB_BYTES + swz<Gm::ROWB>(lane & 7, c % Gm::CPR), r0, r1, r2, r3);
+          qa[2 * jq][0] = r0;
+          qa[2 * jq][1] = r1;
+          qa[2 * jq + 1][0] = r2;
+          qa[2 * jq + 1][1] = r3;
+        }
+        if (g >= nrows) {
+#pragma unroll
+          for (int c = 0; c < KCH; ++c) qa[c][0] = qa[c][1] = 0u;
+        }
+      }
+      const int tok0 = t + 16 * warp;
+      if (tok0 < pc.t1) {
+        const uint32_t kst = sbase + Gm::OFF_K + stage * Gm::KV_BYTES;
+        const uint32_t vst = sbase + Gm::OFF_V + stage * Gm::KV_BYTES;
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < KCH; ++kk) {
+          const int c = 2 * kk + k_chk;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kst + (c / Gm::CPR) * Gm::SUB_BYTES + swz<Gm::ROWB>(k_row, c % Gm::CPR), b0, b1, b2, b3);
+          mma_bf16_16816(s0, qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+          mma_bf16_16816(s1, qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
+        }
+        float x0 = s0[0] * p.scale_log2, x1 = s0[1] * p.scale_log2;
+        float x2 = s1[0] * p.scale_log2, x3 = s1[1] * p.scale_log2;
+        const bool tail = tok0 + 16 > pc.t1;
+        uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
+        if (tail) {
+          const int ta = tok0 + 2 * i4, tb = tok0 + 8 + 2 * i4;
+          x0 = ta < pc.t1 ? x0 : kNegInf;
+          x1 = ta + 1 < pc.t1 ? x1 : kNegInf;
+          x2 = tb < pc.t1 ? x2 : kNegInf;
+          x3 = tb + 1 < pc.t1 ? x3 : kNegInf;
+          vm_lo = (ta < pc.t1 ? 0x0000ffffu : 0u) | (ta + 1 < pc.t1 ? 0xffff0000u : 0u);
+          vm_hi = (tb < pc.t1 ? 0x0000ffffu : 0u) | (tb + 1 < pc.t1 ? 0xffff0000u : 0u);
+        }
+        float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run, mx);
+        const float alpha = exp2_approx(m_run - m_new);
+        const float p0 = exp2_approx(x0 - m_new), p1 = exp2_approx(x1 - m_new);
+        const float p2 = exp2_approx(x2 - m_new), p3 = exp2_approx(x3 - m_new);
+        l_run = l_run * alpha + ((p0 + p1) + (p2 + p3));
+        if (__any_sync(0xffffffffu, m_new != m_run)) {
+#pragma unroll
+          for (int c = 0; c < NB8; ++c) {
+            acc[c][0] *= alpha;
+            acc[c][1] *= alpha;
+            acc[c][2] *= alpha;
+            acc[c][3] *= alpha;
+          }
+        }
+        m_run = m_new;
+        // P = hi + lo in bf16: rows g (hi) and g + 8 (lo) of the A operand
+        const uint32_t ph0 = pack_bf16x2(p0, p1), ph1 = pack_bf16x2(p2, p3);
+        const uint32_t pl0 = pack_bf16x2(p0 - bf16lo_to_f32(ph0), p1 - bf16hi_to_f32(ph0));
+        const uint32_t pl1 = pack_bf16x2(p2 - bf16lo_to_f32(ph1), p3 - bf16hi_to_f32(ph1));
+#pragma unroll
+        for (int c2 = 0; c2 < NB8 / 2; ++c2) {
+          const int c = 2 * c2 + v_chk;
+          uint32_t v0, v1, v2, v3;
+          ldsm_x4_t(vst + (c / Gm::CPR) * Gm::SUB_BYTES + swz<Gm::ROWB>(v_row, c % Gm::CPR), v0, v1, v2, v3);
+          if (tail) {
+            v0 &= vm_lo;
+            v1 &= vm_hi;
+            v2 &= vm_lo;
+            v3 &= vm_hi;
+          }
+          mma_bf16_16816(acc[2 * c2], ph0, pl0, ph1, pl1, v0, v1);
+          mma_bf16_16816(acc[2 * c2 + 1], ph0, pl0, ph1, pl1, v2, v3);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + stage * 8);
+      ++n;
+    }
+
+    // ---- fold the W warps' (m, l, acc) in ascending warp order, then write
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    if (g < nrows) {
+      float* dst = facc + (warp * 8 + g) * D;
+#pragma unroll
+      for (int c = 0; c < NB8; ++c) {
+        *reinterpret_cast<float2*>(dst + 8 * c + 2 * i4) = make_float2(acc[c][0] + acc[c][2], acc[c][1] + acc[c][3]);
+      }
+      if (i4 == 0) {
+        fml[(warp * 8 + g) * 2 + 0] = m_run;
+        fml[(warp * 8 + g) * 2 + 1] = l_run;
+      }
+    }
+    named_bar_sync(1, Gm::W * 32);
+    const int tid = threadIdx.x;
+    const int total = nrows * (D / 2);
+    const bool direct = pc.npieces == 1;
+    for (int e = tid; e < total; e += Gm::W * 32) {
+      const int r = e / (D / 2);
+      const int d = 2 * (e % (D / 2));
+      float M = kNegInf;
+#pragma unroll
+      for (int w = 0; w < Gm::W; ++w) M = fmaxf(M, fml[(w * 8 + r) * 2]);
+      float a0 = 0.f, a1 = 0.f, L = 0.f;
+#pragma unroll
+      for (int w = 0; w < Gm::W; ++w) {
+        const float mw = fml[(w * 8 + r) * 2];
+        const float sc = mw == kNegInf ? 0.f : exp2_approx(mw - M);
+        const float2 v = *reinterpret_cast<const float2*>(facc + (w * 8 + r) * D + d);
+        a0 += sc * v.x;
+        a1 += sc * v.y;
+        L += sc * fml[(w * 8 + r) * 2 + 1];
+      }
+      const size_t row = (size_t)pc.b * p.Hq + first_head + r;
+      if (direct) {
+        const float o0 = L > 0.f ? a0 / L : 0.f;
+        const float o1 = L > 0.f ? a1 / L : 0.f;
+        *reinterpret_cast<uint32_t*>(p.out + row * D + d) = pack_bf16x2(o0, o1);
+      } else {
+        const size_t slot = row * p.S + pc.j;
+        *reinterpret_cast<float2*>(p.part_acc + slot * D + d) = make_float2(a0, a1);
+        if (d == 0) *reinterpret_cast<float2*>(p.part_ml + slot * 2) = make_float2(M * 0.69314718055994531f, L);
+      }
+    }
+    named_bar_sync(1, Gm::W * 32);
+  }
+}
+
+template <int D, bool PAGED>
+__global__ void __launch_bounds__(SplitGeo<D>::NTHREADS, 1) split_kernel(const __grid_constant__ SplitParams p) {
+  using Gm = SplitGeo<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw + pad;
+  int* lens = reinterpret_cast<int*>(smem + Gm::OFF_PLAN);
+  int* P = lens + p.B;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Gm::OFF_MISC);
+  const int warp = threadIdx.x >> 5;
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < Gm::STAGES; ++s) {
+      mbar_init(sbase + Gm::OFF_BAR + s * 8, 1);
+      mbar_init(sbase + Gm::OFF_BAR + (Gm::STAGES + s) * 8, Gm::W);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == Gm::W && (threadIdx.x & 31) == 0) {
+    prefetch_tensormap(&p.tm_k);
+    prefetch_tensormap(&p.tm_v);
+    prefetch_tensormap(&p.tm_q);
+  }
+  // The combine kernel may start launching now; it waits for this grid to finish.
+  pdl_launch_dependents();
+  build_plan_arrays(p.seq_lens, p.B, p.max_len, lens, P);
+  const Plan pl = make_plan(p.B, p.U, p.S, P);
+  if (warp == Gm::W)
+    split_producer<D, PAGED>(p, pl, lens, P, smem, sbase, abort_flag);
+  else
+    split_consumer<D>(p, pl, lens, P, smem, sbase, abort_flag);
+}
+
+}  // namespace da

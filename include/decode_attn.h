@@ -1,0 +1,149 @@
+/*
+ * decode_attn.h — C ABI of the split-KV GQA decode-attention library (GB300, sm_103a).
+ *
+ * One query token per sequence attends over that sequence's bf16 KV cache.  For
+ * sequence b, query head h and KV head g = h / G (G = Hq / Hkv; the G query heads
+ * of a KV head are consecutive), over the L_b cached tokens t:
+ *
+ *     s_t = scale * <q[b,h,:], k[b,t,g,:]>,   out[b,h,:] = sum_t softmax(s)_t * v[b,t,g,:]
+ *
+ * in fp32 on the GPU, rounded once to bf16.  The G query heads of a KV head share
+ * every K/V tile they read (head packing, AstrAI commit 988e013 "csrc", MMA decode
+ * items).  The token range of each (sequence, KV head) is cut into pieces processed
+ * by different CTAs; each piece leaves unnormalised partials (acc, m, l) and a
+ * log-sum-exp combine merges them (AstrAI commit 988e013, split-KV items; merge
+ * order as in "perf(qwen3.8): split the flash-decode KV range across warp-groups",
+ * section "Mechanism").  Paged caches are read through a page table (AstrAI commit
+ * 69fecaf "csrc/tests", paged decode items).
+ *
+ * Conventions shared by every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    allocates nothing, keeps no per-call state, never synchronises the stream and
+ *    enqueues its kernels on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *    of the current device.
+ *  - bf16 tensors are passed as `void*` (__nv_bfloat16 elements); fp32 as float*.
+ *  - q, k, v, k_pool, v_pool, out must be 16-byte aligned; part_acc and part_ml
+ *    16-byte and 8-byte aligned.
+ *  - Every argument is checked on the host first; a bad argument returns
+ *    DA_ERR_INVALID_ARG or DA_ERR_UNSUPPORTED and launches nothing.  A launch
+ *    failure returns DA_ERR_CUDA (the CUDA error is cleared).
+ *  - Supported: head_dim in {32, 64, 128, 256}; Hq % Hkv == 0; 1 <= G <= 64;
+ *    1 <= num_splits <= DA_MAX_SPLITS; page_size a multiple of 16.
+ *  - Device waits are bounded: a kernel that waits too long sets a device error
+ *    word and returns; decode_device_error() reads it.
+ *
+ * The split plan.  Work is counted in 16-token blocks, n_b = ceil(L_b / 16).
+ * The query heads of one KV head are processed in ceil(G / 8) equal sub-groups
+ * (one pass over the KV head each); U = Hkv * ceil(G / 8) sub-group slots.
+ * Segment (b, u) covers blocks [U*P_b + u*n_b, U*P_b + (u+1)*n_b) of one global
+ * block line, P_b = n_0 + ... + n_{b-1}, NB = U * P_B blocks in all.
+ *   num_splits == 1: every segment is computed whole and written directly.
+ *   num_splits >= 2: the line is cut into R = (num_splits - 1) * U ranges of
+ *     q = max(1, ceil(NB / R)) blocks; each range is one CTA's work; the pieces of
+ *     a segment are its intersections with the ranges (index j = r - floor(start/q)),
+ *     at most num_splits of them.  A segment with one piece is written directly;
+ *     one with several leaves partials in slots j = 0..pieces-1 and is merged by
+ *     the combine kernel; an empty sequence (L_b == 0) gets a zero output.
+ */
+#ifndef DECODE_ATTN_H
+#define DECODE_ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DA_OK = 0,
+  DA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, negative size, Hq % Hkv != 0, ... */
+  DA_ERR_UNSUPPORTED = 2,  /* head_dim, page_size, group size or batch outside the built kernels */
+  DA_ERR_WORKSPACE = 3,    /* num_splits >= 2 but part_acc / part_ml missing */
+  DA_ERR_CUDA = 4,         /* a CUDA call or launch failed (error cleared) */
+  DA_ERR_TIMEOUT = 5       /* a kernel gave up on a bounded wait (see decode_device_error) */
+} da_status;
+
+#define DA_MAX_SPLITS 1024
+
+/*
+ * decode_num_splits — the split count for a decode shape (host only, pure).
+ *
+ * The pages choose a split count that fills the device, capped by the tile count
+ * (AstrAI commit 988e013, split-KV items; AstrAI commit 69fecaf, planner items).
+ * Here it is the number of partial slots that lets every CTA of the persistent
+ * grid own one range: S = ceil(C / num_kv_heads) + 1 with C = num_sms (one CTA per
+ * SM), capped by ceil(max_seq_len / 16) and DA_MAX_SPLITS; S = 1 when
+ * max_seq_len <= 16.  batch is accepted for interface stability and does not
+ * change the result.  num_sms <= 0 queries the current device.
+ * Returns S >= 1, or -DA_ERR_INVALID_ARG / -DA_ERR_CUDA.
+ */
+int decode_num_splits(int batch, int num_kv_heads, int max_seq_len, int head_dim, int num_sms);
+
+/*
+ * decode_attn_contig — decode attention over a contiguous cache.
+ *
+ *  q        bf16 [batch, num_q_heads, head_dim]
+ *  k, v     bf16 [batch, max_ctx, num_kv_heads, head_dim]  (token-major rows)
+ *  seq_lens int32 [batch] on the device, or NULL (every sequence has max_ctx tokens);
+ *           values are clamped to [0, max_ctx]
+ *  scale    finite float multiplying q.k (applied in fp32 after the dot product)
+ *  num_splits, part_acc float [batch, num_q_heads, num_splits, head_dim],
+ *           part_ml float [batch, num_q_heads, num_splits, 2] = (m, l) with m in
+ *           natural-log units of the scaled score: caller-owned scratch, unused
+ *           (may be NULL) when num_splits == 1.  Slots the plan does not use are not
+ *           written.
+ *  out      bf16 [batch, num_q_heads, head_dim]
+ *  stream   cudaStream_t
+ * Enqueues the split kernel and, when num_splits >= 2, the combine kernel.
+ */
+int decode_attn_contig(const void* q, const void* k, const void* v, const int* seq_lens,
+                       int batch, int num_q_heads, int num_kv_heads, int head_dim, int max_ctx,
+                       float scale, int num_splits, float* part_acc, float* part_ml,
+                       void* out, void* stream);
+
+/*
+ * decode_attn_paged — decode attention over a paged cache.
+ *
+ *  k_pool, v_pool bf16 [num_pages, page_size, num_kv_heads, head_dim]
+ *  page_table     int32 [batch, max_pages_per_seq] on the device: token t of
+ *                 sequence b is row t % page_size of page page_table[b, t / page_size].
+ *                 Entries past ceil(L_b / page_size) are never read.  Entries that
+ *                 are read must lie in [0, num_pages).
+ *  seq_lens       int32 [batch] on the device (required); clamped to
+ *                 [0, min(max_seq_len, max_pages_per_seq * page_size)]
+ *  Other arguments as for decode_attn_contig.  Each 16-token block is fetched from
+ *  its page with one tile copy, so page_size must be a multiple of 16.
+ */
+int decode_attn_paged(const void* q, const void* k_pool, const void* v_pool,
+                      const int* page_table, const int* seq_lens,
+                      int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                      int page_size, int max_pages_per_seq, int num_pages, int max_seq_len,
+                      float scale, int num_splits, float* part_acc, float* part_ml,
+                      void* out, void* stream);
+
+/*
+ * decode_combine — stand-alone log-sum-exp merge of split partials.
+ *
+ * For each (b, h): M = max over slots j < num_splits with l_j > 0 of m_j,
+ * w_j = exp(m_j - M), out = sum_j w_j acc_j / sum_j w_j l_j, summed in ascending j;
+ * slots with l_j == 0 are skipped and a row with no live slot is written as zeros
+ * ("perf(qwen3.8): split the flash-decode KV range across warp-groups", section
+ * "Mechanism"; AstrAI commit 988e013, combine kernel).  Every slot is read, so
+ * unused slots must hold l == 0.  Layouts as in decode_attn_contig.
+ */
+int decode_combine(const float* part_acc, const float* part_ml, int batch, int num_q_heads,
+                   int head_dim, int num_splits, void* out, void* stream);
+
+/* Human-readable name of a da_status value (static string). */
+const char* decode_status_string(int status);
+
+/*
+ * decode_device_error — synchronise `stream`, then read and clear the device error
+ * word of the current device.  *flags receives the word (0 = no kernel gave up on a
+ * wait).  Returns DA_OK, DA_ERR_TIMEOUT when flags != 0, or DA_ERR_CUDA.
+ */
+int decode_device_error(void* stream, unsigned int* flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DECODE_ATTN_H */

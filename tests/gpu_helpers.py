@@ -1,0 +1,101 @@
+"""Shared helpers of the GPU parity tests: move seeded inputs to the device,
+call the library through its C ABI, and compare with the CPU oracle.
+
+Tolerances (decode-attention output is bf16, partials fp32):
+  output:   |gpu - ref| <= 2e-2 + 2e-2 * |ref| elementwise, ref the unrounded fp64 oracle
+  partials: m  |dm| <= 1e-4 * max(1, |m|);  l  |dl| <= 1e-4 * l;
+            acc  max|d acc| <= 1e-4 * max|acc_ref| over each (b, h, piece) row
+"""
+import numpy as np
+import torch
+
+import oracle
+from gqa_split_kv_gb300 import binding
+from gqa_split_kv_gb300.workloads import bf16_bits_to_f32
+
+OUT_ATOL = 2e-2
+OUT_RTOL = 2e-2
+PART_RTOL = 1e-4
+
+
+def dev_bf16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def dev_i32(x: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.int32)).cuda()
+
+
+def host_bits(t: torch.Tensor) -> np.ndarray:
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def num_splits_for(inp: dict) -> int:
+    q = inp["q"]
+    Hkv = (inp["k"] if "k" in inp else inp["k_pool"]).shape[2]
+    max_len = inp["k"].shape[1] if "k" in inp else inp["page_table"].shape[1] * inp["page_size"]
+    return binding.num_splits(q.shape[0], Hkv, max_len, q.shape[2])
+
+
+def run(inp: dict, S: int = None, lens_null: bool = False, dev_inputs: dict = None, max_seq_len: int = None):
+    """One library call on inp; returns (out bits, part_acc, part_ml, S) as numpy."""
+    if S is None:
+        S = num_splits_for(inp)
+    d = dev_inputs if dev_inputs is not None else to_device(inp)
+    B, Hq, D = inp["q"].shape
+    acc = torch.full((B, Hq, max(S, 1), D), float("nan"), dtype=torch.float32, device="cuda")
+    ml = torch.full((B, Hq, max(S, 1), 2), float("nan"), dtype=torch.float32, device="cuda")
+    out = torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    if "k" in inp:
+        binding.decode_attn_contig(d["q"], d["k"], d["v"], None if lens_null else d["seq_lens"], scale=inp["scale"],
+                                   splits=S, part_acc=acc, part_ml=ml, out=out)
+    else:
+        msl = max_seq_len if max_seq_len is not None else inp["page_table"].shape[1] * inp["page_size"]
+        binding.decode_attn_paged(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["seq_lens"], msl,
+                                  scale=inp["scale"], splits=S, part_acc=acc, part_ml=ml, out=out)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0, "a kernel gave up on a bounded wait"
+    return host_bits(out), acc.cpu().numpy(), ml.cpu().numpy(), S
+
+
+def to_device(inp: dict) -> dict:
+    d = {"q": dev_bf16(inp["q"]), "seq_lens": dev_i32(inp["seq_lens"])}
+    if "k" in inp:
+        d["k"] = dev_bf16(inp["k"])
+        d["v"] = dev_bf16(inp["v"])
+    else:
+        d["k_pool"] = dev_bf16(inp["k_pool"])
+        d["v_pool"] = dev_bf16(inp["v_pool"])
+        d["page_table"] = dev_i32(inp["page_table"])
+    return d
+
+
+def check_out(out_bits: np.ndarray, ref: np.ndarray, what: str = ""):
+    got = bf16_bits_to_f32(out_bits).astype(np.float64)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    bad = err > OUT_ATOL + OUT_RTOL * np.abs(ref)
+    assert not bad.any(), (f"{what}: {bad.sum()} outputs out of tolerance, max abs err {err.max():.3e} "
+                           f"at {np.unravel_index(err.argmax(), err.shape)}")
+    return float(err.max())
+
+
+def check_partials(acc: np.ndarray, ml: np.ndarray, ref_acc: np.ndarray, ref_ml: np.ndarray, npieces: np.ndarray,
+                   what: str = ""):
+    """Compare every slot j < npieces of rows that have >= 2 pieces."""
+    B, Hq, S, D = ref_acc.shape
+    checked = 0
+    for b in range(B):
+        for h in range(Hq):
+            n = int(npieces[b, h])
+            if n < 2:
+                continue
+            for j in range(n):
+                m_ref, l_ref = ref_ml[b, h, j]
+                m_got, l_got = ml[b, h, j]
+                assert abs(m_got - m_ref) <= PART_RTOL * max(1.0, abs(m_ref)), (what, b, h, j, m_got, m_ref)
+                assert abs(l_got - l_ref) <= PART_RTOL * l_ref, (what, b, h, j, l_got, l_ref)
+                da = np.abs(acc[b, h, j].astype(np.float64) - ref_acc[b, h, j]).max()
+                assert da <= PART_RTOL * np.abs(ref_acc[b, h, j]).max(), (what, b, h, j, da)
+                checked += 1
+    return checked

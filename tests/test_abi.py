@@ -1,0 +1,125 @@
+"""C ABI checks that need no GPU: the library loads, exports every declared
+symbol, the host planner's values, and argument validation (every rejected
+call returns its status before touching CUDA)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gqa_split_kv_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def clib():
+    build_mod.build()
+    from gqa_split_kv_gb300 import binding
+    return binding.load()
+
+
+def declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", src, flags=re.M)
+    return names
+
+
+def test_every_declared_symbol_is_exported(clib):
+    names = declared_functions()
+    assert {"decode_num_splits", "decode_attn_contig", "decode_attn_paged", "decode_combine"} <= set(names)
+    for n in names:
+        assert hasattr(clib, n), n
+
+
+def test_status_strings(clib):
+    assert clib.decode_status_string(0) == b"DA_OK"
+    assert clib.decode_status_string(3) == b"DA_ERR_WORKSPACE"
+    assert clib.decode_status_string(99) == b"unknown status"
+
+
+@pytest.mark.parametrize("args,want", [
+    ((1, 4, 4096, 256, 152), 39),     # GQA-6 ctx 4096: 38 ranges per KV head fill 152 SMs
+    ((1, 8, 65536, 128, 152), 20),
+    ((16, 8, 8192, 128, 152), 20),
+    ((64, 8, 32768, 128, 152), 20),
+    ((1, 2, 512, 64, 152), 32),       # capped by the 32 blocks of 16 tokens
+    ((1, 2, 16, 64, 152), 1),         # one block: nothing to split
+    ((1, 2, 17, 64, 152), 2),
+    ((4, 1, 10 ** 6, 128, 2000), 1024),
+])
+def test_num_splits_values(clib, args, want):
+    assert clib.decode_num_splits(*args) == want
+
+
+def test_num_splits_rejects_bad_shapes(clib):
+    assert clib.decode_num_splits(1, 0, 100, 64, 152) == -1
+    assert clib.decode_num_splits(-1, 2, 100, 64, 152) == -1
+    assert clib.decode_num_splits(1, 2, -5, 64, 152) == -1
+
+
+A = 0x10000  # a fake 16-byte-aligned address: never dereferenced by rejected calls
+
+
+def contig(clib, q=A, k=A, v=A, lens=None, B=1, Hq=8, Hkv=2, D=64, ctx=64, scale=0.125, S=2, pa=A, pm=A, out=A):
+    return clib.decode_attn_contig(q, k, v, lens, B, Hq, Hkv, D, ctx, scale, S, pa, pm, out, None)
+
+
+def paged(clib, ps=16, lens=A, table=A, D=64, S=2, maxp=4, npages=4, maxlen=64, pa=A, pm=A):
+    return clib.decode_attn_paged(A, A, A, table, lens, 1, 8, 2, D, ps, maxp, npages, maxlen, 0.125, S, pa, pm, A,
+                                  None)
+
+
+def test_contig_argument_errors(clib):
+    assert contig(clib, Hq=6, Hkv=4) == 1                 # Hq % Hkv
+    assert contig(clib, D=48) == 2                        # head_dim not built
+    assert contig(clib, D=512) == 2
+    assert contig(clib, Hq=130, Hkv=2) == 2               # G > 64
+    assert contig(clib, S=0) == 1
+    assert contig(clib, S=1025) == 1
+    assert contig(clib, pa=None) == 3                     # partial slots missing
+    assert contig(clib, pm=None) == 3
+    assert contig(clib, q=A + 2) == 1                     # misaligned
+    assert contig(clib, out=A + 8) == 1
+    assert contig(clib, k=A + 4) == 1
+    assert contig(clib, pa=A + 4) == 1
+    assert contig(clib, pm=A + 4) == 1
+    assert contig(clib, q=None) == 1
+    assert contig(clib, k=None) == 1
+    assert contig(clib, scale=float("inf")) == 1
+    assert contig(clib, scale=float("nan")) == 1
+    assert contig(clib, ctx=-1) == 1
+    assert contig(clib, B=-1) == 1
+    assert contig(clib, Hkv=0) == 1
+    assert contig(clib, B=0) == 0                         # empty batch: nothing to do
+
+
+def test_paged_argument_errors(clib):
+    assert paged(clib, ps=24) == 2                        # page size not a multiple of 16
+    assert paged(clib, ps=8) == 2
+    assert paged(clib, ps=0) == 1
+    assert paged(clib, lens=None) == 1                    # seq_lens required
+    assert paged(clib, table=None) == 1
+    assert paged(clib, table=A + 2) == 1
+    assert paged(clib, D=100) == 2
+    assert paged(clib, pa=None) == 3
+    assert paged(clib, maxp=-1) == 1
+    assert paged(clib, maxlen=-3) == 1
+
+
+def test_combine_argument_errors(clib):
+    assert clib.decode_combine(A, A, 1, 8, 48, 4, A, None) == 2
+    assert clib.decode_combine(A, A, 1, 8, 64, 0, A, None) == 1
+    assert clib.decode_combine(None, A, 1, 8, 64, 4, A, None) == 1
+    assert clib.decode_combine(A, A, 1, 8, 64, 4, None, None) == 1
+    assert clib.decode_combine(A + 4, A, 1, 8, 64, 4, A, None) == 1
+    assert clib.decode_combine(A, A, 0, 8, 64, 4, A, None) == 0
+
+
+def test_device_error_rejects_null(clib):
+    assert clib.decode_device_error(None, None) == 1

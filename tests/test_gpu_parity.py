@@ -1,0 +1,154 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, element by
+element, on seeded inputs spanning several tiles, ragged tails and every
+supported head_dim / group size, plus the bitwise determinism and
+paged-vs-contiguous identities the split plan guarantees."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from gqa_split_kv_gb300.workloads import Workload, contig_to_paged, f32_to_bf16_bits, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from gpu_helpers import check_out, check_partials, run, to_device  # noqa: E402
+
+RAGGED = [1, 15, 16, 17, 100, 300, 777]
+
+
+def contig_case(seed, B, Hq, Hkv, D, ctx, lens=None, kstd=1.0):
+    rng = np.random.default_rng(seed)
+    q = f32_to_bf16_bits(rng.standard_normal((B, Hq, D), dtype=np.float32))
+    k = f32_to_bf16_bits(rng.standard_normal((B, ctx, Hkv, D), dtype=np.float32) * np.float32(kstd))
+    v = f32_to_bf16_bits(rng.standard_normal((B, ctx, Hkv, D), dtype=np.float32))
+    seq = np.full(B, ctx, np.int32) if lens is None else np.asarray(lens, np.int32)
+    return dict(q=q, k=k, v=v, seq_lens=seq, scale=float(np.float32(1 / math.sqrt(D))))
+
+
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (24, 4), (16, 2), (4, 4), (24, 2)])
+def test_contig_matches_oracle(D, Hq, Hkv):
+    inp = contig_case(D * 1000 + Hq, len(RAGGED), Hq, Hkv, D, ctx=max(RAGGED), lens=RAGGED)
+    ref = oracle.decode_contig(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["scale"])
+    for S in (None, 1, 5):
+        out, acc, ml, S_used = run(inp, S)
+        check_out(out, ref, f"D={D} G={Hq // Hkv} S={S_used}")
+        if S_used >= 2:
+            ra, rm, npc = oracle.decode_partials(inp, S_used)
+            assert check_partials(acc, ml, ra, rm, npc, f"D={D} S={S_used}") > 0
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("ps", [16, 32, 64])
+def test_paged_matches_oracle_and_contiguous_bitwise(D, ps):
+    inp = contig_case(7 * D + ps, len(RAGGED), 32, 8, D, ctx=max(RAGGED), lens=RAGGED)
+    rng = np.random.default_rng(ps)
+    kp, vp, table = contig_to_paged(inp["k"], inp["v"], inp["seq_lens"], ps, rng, spare_pages=3)
+    pin = dict(q=inp["q"], k_pool=kp, v_pool=vp, page_table=table, seq_lens=inp["seq_lens"], page_size=ps,
+               scale=inp["scale"])
+    ref = oracle.decode_paged(inp["q"], kp, vp, table, inp["seq_lens"], ps, inp["scale"])
+    for S in (None, 1, 4):
+        out_c, acc_c, ml_c, S_used = run(inp, S)
+        out_p, acc_p, ml_p, _ = run(pin, S_used, max_seq_len=max(RAGGED))
+        check_out(out_p, ref, f"paged D={D} ps={ps} S={S_used}")
+        # same tokens, same plan, same order: identical bits
+        assert np.array_equal(out_p, out_c)
+        if S_used >= 2:
+            ra, rm, npc = oracle.decode_partials(pin, S_used)
+            check_partials(acc_p, ml_p, ra, rm, npc, "paged")
+            used = ~np.isnan(ml_c[..., 1])
+            assert np.array_equal(acc_p[used], acc_c[used]) and np.array_equal(ml_p[used], ml_c[used])
+
+
+def test_page_table_permutation_gives_identical_bits():
+    inp = contig_case(5, 5, 16, 2, 128, ctx=700, lens=[700, 333, 64, 1, 519])
+    rng = np.random.default_rng(1)
+    outs = []
+    for trial in range(3):
+        kp, vp, table = contig_to_paged(inp["k"], inp["v"], inp["seq_lens"], 16, rng, spare_pages=trial * 5)
+        pin = dict(q=inp["q"], k_pool=kp, v_pool=vp, page_table=table, seq_lens=inp["seq_lens"], page_size=16,
+                   scale=inp["scale"])
+        outs.append(run(pin, 6, max_seq_len=700)[0])
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+@pytest.mark.parametrize("G", [9, 12, 16, 64])
+def test_large_groups(G):
+    inp = contig_case(G, 2, 2 * G, 2, 64, ctx=300, lens=[300, 77])
+    ref = oracle.decode_contig(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["scale"])
+    for S in (None, 1, 3):
+        out, acc, ml, S_used = run(inp, S)
+        check_out(out, ref, f"G={G}")
+        if S_used >= 2:
+            ra, rm, npc = oracle.decode_partials(inp, S_used)
+            check_partials(acc, ml, ra, rm, npc, f"G={G}")
+
+
+def test_deterministic_across_runs():
+    inp = contig_case(9, 3, 32, 8, 128, ctx=2000, lens=[2000, 1500, 37])
+    d = to_device(inp)
+    first = run(inp, None, dev_inputs=d)
+    for _ in range(2):
+        again = run(inp, None, dev_inputs=d)
+        assert np.array_equal(first[0], again[0])
+        assert np.array_equal(first[1], again[1], equal_nan=True)
+        assert np.array_equal(first[2], again[2], equal_nan=True)
+
+
+def test_null_seq_lens_means_full_context():
+    inp = contig_case(10, 2, 8, 2, 64, ctx=200)
+    ref = oracle.decode_contig(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["scale"])
+    out, *_ = run(inp, None, lens_null=True)
+    check_out(out, ref, "null seq_lens")
+
+
+def test_empty_and_single_token_sequences():
+    inp = contig_case(11, 4, 8, 2, 128, ctx=100, lens=[0, 1, 0, 100])
+    ref = oracle.decode_contig(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["scale"])
+    for S in (1, 2, 7):
+        out, *_ = run(inp, S)
+        check_out(out, ref, f"empty S={S}")
+        assert np.all(out[0] == 0) and np.all(out[2] == 0)
+        assert np.array_equal(out[1], inp["v"][1, 0][np.arange(8) // 4])  # one key: its V row
+
+
+def test_lengths_beyond_the_cache_are_clamped():
+    inp = contig_case(12, 2, 8, 2, 64, ctx=64, lens=[64, 64])
+    inp_big = dict(inp, seq_lens=np.array([1000, -5], np.int32))
+    ref = oracle.decode_contig(inp["q"], inp["k"], inp["v"], np.array([64, 0], np.int32), inp["scale"])
+    out, *_ = run(inp_big, 3)
+    check_out(out, ref, "clamped")
+
+
+def test_outlier_keys_small():
+    wl = Workload("o", B=1, Hq=32, Hkv=8, D=128, max_ctx=4096, outlier_frac=0.001, seed=77)
+    inp = make_inputs(wl)
+    ref = oracle.decode_contig(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["scale"])
+    out, acc, ml, S = run(inp, None)
+    check_out(out, ref, "outliers")
+    ra, rm, npc = oracle.decode_partials(inp, S)
+    assert check_partials(acc, ml, ra, rm, npc, "outliers") > 0
+
+
+def test_combine_alone_matches_oracle_merge():
+    rng = np.random.default_rng(13)
+    inp = contig_case(13, 3, 8, 2, 64, ctx=900, lens=[900, 40, 0])
+    S = 6
+    ra, rm, npc = oracle.decode_partials(inp, S)
+    acc = np.nan_to_num(ra, nan=0.0).astype(np.float32)
+    ml = rm.copy()
+    ml[..., 0] = np.where(np.isnan(ml[..., 0]), -np.inf, ml[..., 0])
+    ml[..., 1] = np.nan_to_num(ml[..., 1], nan=0.0)
+    ml = ml.astype(np.float32)
+    want = oracle.combine_partials(acc.astype(np.float64), ml.astype(np.float64))
+    from gqa_split_kv_gb300 import binding
+    out = binding.decode_combine(torch.from_numpy(acc).cuda(), torch.from_numpy(ml).cuda())
+    torch.cuda.synchronize()
+    from gpu_helpers import host_bits
+    check_out(host_bits(out), want, "combine")
+    assert np.all(host_bits(out)[2] == 0)
