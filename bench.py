@@ -1,0 +1,426 @@
+#!/usr/bin/env python
+"""Benchmark of split-KV GQA decode attention on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--suite]
+
+One step = one decode-attention call (split kernel + log-sum-exp combine) over
+the GQA-6 long-context workload: B=1, Hq=24, Hkv=4 (G=6), head_dim 256,
+ctx 4096 tokens, contiguous bf16 cache, seeded N(0,1) inputs.  Inputs are
+resident in HBM; L2 is flushed before every step (a write of a buffer larger
+than L2, then a read of another, so no dirty lines are left to write back),
+outside the step's CUDA-event pair.  The value is achieved GB/s of algorithmic
+bytes (K/V + Q + partials read + seq_lens); µs/call is reported beside it.
+
+--impl reference times the fp64 CPU oracle on the host cores (bounded sample
+per step).  --suite also measures every other workload (one JSON line each).
+Under torchrun each rank runs an independent replica (no collective on the
+data path); the value is the total over ranks divided by the slowest rank.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn µs/call and achieved HBM GB/s vs GB300 peak (1 GPU)"
+HEADLINE = "gqa6_contig_b1_hq24_hkv4_d256_ctx4096"
+# Published time per call of the pages' fa_split_gqa_kernel on this exact workload
+# (RTX 5090, "perf(dspark): overlap KV staging with compute via cp.async",
+# section "Why there was still headroom").
+PAGES_US_PER_CALL = {HEADLINE: 1110.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--suite", action="store_true", help="also measure every other workload")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-child", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def kernel_source_hash() -> str:
+    csrc = os.path.join(ROOT, "gqa_split_kv_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    want = kernel_source_hash()
+    for line in open(p):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload and parts[1] == want:
+            return int(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.1)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                rows.append(f)
+        os.unlink(self.path)
+        mhz = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------ CPU baseline
+
+def cpu_child(workload: str, seconds: float):
+    """Runs in a subprocess with the BLAS thread count fixed: times the oracle."""
+    import numpy as np  # noqa: F401
+
+    import oracle
+    from gqa_split_kv_gb300.accounting import traffic_bytes
+    from gqa_split_kv_gb300.workloads import WORKLOADS, make_inputs
+
+    wl = WORKLOADS[workload]
+    inp = make_inputs(wl)
+    G = wl.Hq // wl.Hkv
+    # sample unit: all G query heads of one (sequence, KV head) over its full context
+    groups = [(b, g) for b in range(wl.B) for g in range(wl.Hkv)]
+    done_bytes, n = 0, 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds or n == 0:
+        b, g = groups[n % len(groups)]
+        oracle.decode_rows(inp, [(b, g * G + i) for i in range(G)])
+        L = int(inp["seq_lens"][b])
+        done_bytes += 2 * wl.D * 2 * L + G * wl.D * 2
+        n += 1
+    dt = time.perf_counter() - t0
+    print(json.dumps({"gbs": done_bytes / dt / 1e9, "units": n, "seconds": dt}))
+
+
+def run_cpu_baseline(workload: str, seconds: float) -> dict:
+    cores = os.cpu_count() or 1
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(cores)
+    res = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child", workload, "--cpu-seconds",
+                          str(seconds)], capture_output=True, text=True, env=env, cwd=ROOT)
+    line = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    if res.returncode != 0 or not line:
+        return {"value": None, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                "sample": f"failed: {res.stderr[-300:]}"}
+    d = json.loads(line[-1])
+    return {"value": round(d["gbs"], 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{d['units']} units of one (sequence, KV head) with its G query heads over the full "
+                      f"context, {d['seconds']:.1f} s, fp64 numpy oracle, BLAS threads = {cores}"}
+
+
+# ------------------------------------------------------------ our arm
+
+def measure(wl, inp, steps: int, warmup: int, flush_bytes: int, dist=None, sampler=None, e2e_steps: int = 0):
+    import numpy as np
+    import torch
+
+    from gqa_split_kv_gb300 import binding
+    from gqa_split_kv_gb300.accounting import traffic_bytes
+
+    dev = torch.cuda.current_device()
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+    paged = "k_pool" in inp
+    q = to_dev(inp["q"])
+    lens = torch.from_numpy(inp["seq_lens"]).cuda()
+    if paged:
+        kc, vc = to_dev(inp["k_pool"]), to_dev(inp["v_pool"])
+        table = torch.from_numpy(inp["page_table"]).cuda()
+        max_len = wl.max_ctx
+    else:
+        kc, vc = to_dev(inp["k"]), to_dev(inp["v"])
+        table = None
+        max_len = wl.max_ctx
+    S = binding.num_splits(wl.B, wl.Hkv, max_len, wl.D)
+    out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.bfloat16, device="cuda")
+    pa = torch.empty((wl.B, wl.Hq, S, wl.D), dtype=torch.float32, device="cuda") if S > 1 else None
+    pm = torch.empty((wl.B, wl.Hq, S, 2), dtype=torch.float32, device="cuda") if S > 1 else None
+    flush = torch.empty(flush_bytes, dtype=torch.uint8, device="cuda")
+    flush_src = torch.empty(flush_bytes // 4, dtype=torch.float32, device="cuda").zero_()
+    stream = torch.cuda.current_stream()
+
+    def flush_l2():
+        # write a buffer larger than L2, then read another: L2 ends up holding only
+        # clean, unrelated lines, so the timed call pays no write-back of the flush
+        flush.zero_()
+        torch.sum(flush_src)
+
+    def call(qq=q, kk=kc, vv=vc, ll=lens, oo=out):
+        if paged:
+            binding.decode_attn_paged(qq, kk, vv, table, ll, max_len, scale=wl.scale, splits=S, part_acc=pa,
+                                      part_ml=pm, out=oo)
+        else:
+            binding.decode_attn_contig(qq, kk, vv, ll, scale=wl.scale, splits=S, part_acc=pa, part_ml=pm, out=oo)
+
+    for _ in range(warmup):
+        flush_l2()
+        call()
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    for i in range(steps):
+        flush_l2()
+        ev0[i].record(stream)
+        call()
+        ev1[i].record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        clocks = sampler.stop()
+    else:
+        clocks = None
+    if dist is not None:
+        dist.barrier()
+    times = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]  # ms
+    assert binding.device_error() == 0
+    tb = traffic_bytes(wl.B, wl.Hq, wl.Hkv, wl.D, inp["seq_lens"], S, wl.page_size if paged else None)
+    res = {"S": S, "times_ms": times, "bytes": tb, "clocks": clocks, "launches_per_step": 1 if S == 1 else 2}
+
+    if e2e_steps > 0:
+        # end to end through the public call: pinned host inputs -> device, call, output -> host
+        host = {"q": torch.from_numpy(np.ascontiguousarray(inp["q"]).view(np.int16)).pin_memory(),
+                "lens": torch.from_numpy(inp["seq_lens"]).pin_memory()}
+        host["k"] = torch.from_numpy(np.ascontiguousarray(inp["k_pool" if paged else "k"]).view(np.int16)).pin_memory()
+        host["v"] = torch.from_numpy(np.ascontiguousarray(inp["v_pool" if paged else "v"]).view(np.int16)).pin_memory()
+        out_h = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.int16).pin_memory()
+        qi, ki, vi = q.view(torch.int16), kc.view(torch.int16), vc.view(torch.int16)
+        h2d = sum(t.numel() * t.element_size() for t in (host["q"], host["k"], host["v"], host["lens"]))
+        d2h = out_h.numel() * 2
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        for it in range(2):
+            n = 3 if it == 0 else e2e_steps
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(n):
+                qi.copy_(host["q"], non_blocking=True)
+                ki.copy_(host["k"], non_blocking=True)
+                vi.copy_(host["v"], non_blocking=True)
+                lens.copy_(host["lens"], non_blocking=True)
+                call()
+                out_h.copy_(out.view(torch.int16), non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize()
+        res["e2e_ms"] = e0.elapsed_time(e1) / e2e_steps
+        res["h2d"] = h2d
+        res["d2h"] = d2h
+    del flush, flush_src
+    return res
+
+
+def ours(args):
+    import torch
+
+    from gqa_split_kv_gb300.workloads import WORKLOADS, make_inputs
+    import gqa_split_kv_gb300
+
+    ws, rank, local = dist_env()
+    dist = None
+    if ws > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    else:
+        torch.cuda.set_device(0)
+    gqa_split_kv_gb300.load()
+    peaks = measured_peaks()
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    flush_bytes = max(4 * l2, 256 << 20)
+    wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl)
+    vis = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    phys = vis[local] if local < len(vis) else str(local)
+    sampler = ClockSampler(phys) if rank == 0 else None
+    r = measure(wl, inp, args.steps, args.warmup, flush_bytes, dist=dist, sampler=sampler,
+                e2e_steps=max(3, min(args.steps, 200)))
+    total_ms = sum(r["times_ms"])
+    if dist is not None:
+        t = torch.tensor([total_ms, r["e2e_ms"]], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+    else:
+        e2e_ms = r["e2e_ms"]
+    K = args.steps
+    alg = r["bytes"]["algorithmic"]
+    value = ws * alg * K / (total_ms / 1e3) / 1e9
+    per = sorted(r["times_ms"])
+    us_med = 1e3 * per[len(per) // 2]
+    achieved = alg / (total_ms / K / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / K, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": (round(PAGES_US_PER_CALL[wl.name] / (1e3 * total_ms / K), 2)
+                        if wl.name in PAGES_US_PER_CALL else None),
+        "vs_baseline_basis": "pages' fa_split_gqa_kernel 1.11 ms/call on RTX 5090, same workload (µs ratio)",
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "head_dim": wl.D,
+                   "ctx": wl.max_ctx, "layout": wl.layout, "num_splits": r["S"], "accum": "fp32",
+                   "l2": f"flushed before every step ({flush_bytes >> 20} MiB write + {flush_bytes >> 20} MiB read, "
+                         "outside the timed pair)",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "us_per_call": {"mean": round(1e3 * total_ms / K, 3), "median": round(us_med, 3),
+                        "p10": round(1e3 * per[len(per) // 10], 3), "p90": round(1e3 * per[9 * len(per) // 10], 3)},
+        "bytes_per_call": r["bytes"],
+        "roofline": {"bound": "hbm", "kernel": "split_kernel + combine_kernel (one call, events around both)",
+                     "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
+                     "traffic": ncu_traffic(wl.name)},
+        "e2e": {"value": round(ws * alg / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": r["launches_per_step"] * K,
+        "clocks": r["clocks"],
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = run_cpu_baseline(wl.name, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if args.suite and rank == 0:
+        for name, other in WORKLOADS.items():
+            if name == wl.name:
+                continue
+            oi = make_inputs(other)
+            rr = measure(other, oi, 50, 5, flush_bytes)
+            t = sorted(rr["times_ms"])
+            med = t[len(t) // 2]
+            a = rr["bytes"]["algorithmic"] / (med / 1e3) / 1e9
+            print(json.dumps({"suite": name, "us_per_call_median": round(1e3 * med, 3),
+                              "achieved_gbs": round(a, 1), "frac_of_peak": round(a / peaks["hbm_gbs"], 4),
+                              "strict_gbs": round(rr["bytes"]["strict"] / (med / 1e3) / 1e9, 1),
+                              "num_splits": rr["S"], "bytes": rr["bytes"]}), flush=True)
+            del oi
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def reference(args):
+    """The reference arm: the fp64 CPU oracle, one bounded sample per step."""
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    import numpy as np  # noqa: F401
+
+    import oracle
+    from gqa_split_kv_gb300.workloads import WORKLOADS, make_inputs
+
+    wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl)
+    G = wl.Hq // wl.Hkv
+    groups = [(b, g) for b in range(wl.B) for g in range(wl.Hkv)]
+
+    def step(i):
+        b, g = groups[i % len(groups)]
+        oracle.decode_rows(inp, [(b, g * G + j) for j in range(G)])
+        return 2 * wl.D * 2 * int(inp["seq_lens"][b]) + G * wl.D * 2
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    nbytes = sum(step(i) for i in range(args.steps))
+    dt = time.perf_counter() - t0
+    v = nbytes / dt / 1e9
+    cores = os.cpu_count() or 1
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "head_dim": wl.D, "ctx": wl.max_ctx,
+                   "layout": wl.layout},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": "per step: all G query heads of one (sequence, KV head) over its full context"},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.cpu_child:
+        cpu_child(args.cpu_child, args.cpu_seconds)
+        return
+    if args.impl == "reference":
+        reference(args)
+    else:
+        ours(args)
+
+
+if __name__ == "__main__":
+    main()

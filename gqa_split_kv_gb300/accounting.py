@@ -1,0 +1,68 @@
+"""Algorithmic byte counts of one decode-attention call (for GB/s and rooflines).
+
+The bytes a call must move at minimum, by tensor:
+  kv        = 2 * D * 2 B * Hkv * sum_b L_b        (every cached K and V row once)
+  q         = B * Hq * D * 2 B
+  out       = B * Hq * D * 2 B
+  partials  = per (b, h) with n >= 2 pieces: n * (D + 2) * 4 B, written once by the
+              split kernel and read once by the combine
+  page_table= 4 B * sum_b ceil(L_b / page_size)    (paged caches)
+  seq_lens  = 4 B * B
+
+"algorithmic" = kv + q + partials read + page_table + seq_lens (what the combine
+and split kernels must read); "strict" = kv + q + out.  The piece count per
+segment restates the library's split rule (see include/decode_attn.h) for
+counting only.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import numpy as np
+
+BLOCK = 16
+
+
+def _groups(G: int):
+    ng = -(-G // 8)
+    gr = -(-G // ng)
+    return ng, gr
+
+
+def piece_counts(seq_lens, Hkv: int, G: int, S: int) -> np.ndarray:
+    """Pieces of every segment, shape [B, Hkv * ceil(G/8)]."""
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    ng, _ = _groups(G)
+    U = Hkv * ng
+    nblk = (lens + BLOCK - 1) // BLOCK
+    B = len(lens)
+    if S == 1:
+        return np.where(nblk[:, None] > 0, 1, 0) * np.ones((B, U), dtype=np.int64)
+    P = np.concatenate([[0], np.cumsum(nblk)])
+    NB = U * int(P[-1])
+    R = (S - 1) * U
+    q = max(1, -(-NB // R))
+    s0 = U * P[:-1, None] + np.arange(U)[None, :] * nblk[:, None]
+    s1 = s0 + nblk[:, None]
+    n = (s1 - 1) // q - s0 // q + 1
+    return np.where(nblk[:, None] > 0, n, 0)
+
+
+def traffic_bytes(B: int, Hq: int, Hkv: int, D: int, seq_lens, S: int, page_size: Optional[int] = None) -> dict:
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    G = Hq // Hkv
+    ng, gr = _groups(G)
+    kv = 2 * D * 2 * Hkv * int(lens.sum())
+    q = B * Hq * D * 2
+    out = B * Hq * D * 2
+    n = piece_counts(lens, Hkv, G, S)                      # [B, U]
+    # heads per sub-group slot u = h * ng + j
+    heads = np.array([min(gr, G - (u % ng) * gr) for u in range(Hkv * ng)])
+    part_rows = int(((n >= 2) * n * heads[None, :]).sum())
+    partials = part_rows * (D + 2) * 4
+    pt = 0 if page_size is None else 4 * int(((lens + page_size - 1) // page_size).sum())
+    sl = 4 * B
+    return {"kv": kv, "q": q, "out": out, "partials_read": partials, "partials_written": partials,
+            "page_table": pt, "seq_lens": sl,
+            "algorithmic": kv + q + partials + pt + sl, "strict": kv + q + out}

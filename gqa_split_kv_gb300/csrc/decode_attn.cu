@@ -136,10 +136,11 @@ int launch_split(const SplitParams& prm, int grid, int smem, int dev, cudaStream
 }
 
 template <int D>
-int launch_combine(const CombineParams& prm, int dev, cudaStream_t st, bool dependent) {
+int launch_combine(const CombineParams& prm, int dev, int sms, cudaStream_t st, bool dependent) {
   static bool attr_done[kMaxDevices] = {false};
   auto kern = combine_kernel<D>;
-  const int smem = prm.planned ? (2 * prm.B + 1) * 4 : 0;
+  const int smem = CombineGeo<D>::smem_bytes(prm.B, prm.S, prm.planned != 0);
+  if (smem > 227 * 1024) return DA_ERR_UNSUPPORTED;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!attr_done[dev]) {
@@ -150,8 +151,10 @@ int launch_combine(const CombineParams& prm, int dev, cudaStream_t st, bool depe
       attr_done[dev] = true;
     }
   }
+  // grid-strided over rows: a few CTAs per SM, each builds the plan once
   const long long rows = (long long)prm.B * prm.Hq;
-  const long long grid = (rows + CombineGeo<D>::RPC - 1) / CombineGeo<D>::RPC;
+  const long long cap = 4LL * (sms > 0 ? sms : 1);
+  const long long grid = rows < cap ? rows : cap;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -228,7 +231,7 @@ int run_decode(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, in
   cp.ng = ng;
   cp.gr = gr;
   cp.max_len = a.max_len;
-  return launch_combine<D>(cp, dev, a.stream, true);
+  return launch_combine<D>(cp, dev, sms, a.stream, true);
 }
 
 int check_common(const void* q, const void* out, int B, int Hq, int Hkv, int D, float scale, int S,
@@ -396,8 +399,8 @@ extern "C" int decode_combine(const float* part_acc, const float* part_ml, int b
   if (B == 0) return DA_OK;
   if (!part_acc || !part_ml || !out) return DA_ERR_INVALID_ARG;
   if (!aligned(part_acc, 16) || !aligned(part_ml, 8) || !aligned(out, 16)) return DA_ERR_INVALID_ARG;
-  int dev;
-  if (current_device(&dev) || dev >= kMaxDevices) return DA_ERR_CUDA;
+  int dev, sms, smem_optin;
+  if (current_device(&dev) || device_info(dev, &sms, &smem_optin)) return DA_ERR_CUDA;
   CombineParams cp;
   std::memset(&cp, 0, sizeof(cp));
   cp.part_acc = part_acc;
@@ -409,10 +412,10 @@ extern "C" int decode_combine(const float* part_acc, const float* part_ml, int b
   cp.planned = 0;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   switch (D) {
-    case 32: return launch_combine<32>(cp, dev, st, false);
-    case 64: return launch_combine<64>(cp, dev, st, false);
-    case 128: return launch_combine<128>(cp, dev, st, false);
-    default: return launch_combine<256>(cp, dev, st, false);
+    case 32: return launch_combine<32>(cp, dev, sms, st, false);
+    case 64: return launch_combine<64>(cp, dev, sms, st, false);
+    case 128: return launch_combine<128>(cp, dev, sms, st, false);
+    default: return launch_combine<256>(cp, dev, sms, st, false);
   }
 }
 

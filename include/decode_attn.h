@@ -123,8 +123,9 @@ int decode_attn_paged(const void* q, const void* k_pool, const void* v_pool,
  * decode_combine — stand-alone log-sum-exp merge of split partials.
  *
  * For each (b, h): M = max over slots j < num_splits with l_j > 0 of m_j,
- * w_j = exp(m_j - M), out = sum_j w_j acc_j / sum_j w_j l_j, summed in ascending j;
- * slots with l_j == 0 are skipped and a row with no live slot is written as zeros
+ * w_j = exp(m_j - M), out = sum_j w_j acc_j / sum_j w_j l_j, summed in a fixed
+ * order (bitwise reproducible); slots with l_j == 0 are skipped and a row with no
+ * live slot is written as zeros
  * ("perf(qwen3.8): split the flash-decode KV range across warp-groups", section
  * "Mechanism"; AstrAI commit 988e013, combine kernel).  Every slot is read, so
  * unused slots must hold l == 0.  Layouts as in decode_attn_contig.
