@@ -453,3 +453,67 @@ extern "C" int decode_device_error(void* stream, unsigned int* flags) {
   *flags = w;
   return w ? DA_ERR_TIMEOUT : DA_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of decode_attn_contig.
+//
+// Some callers cannot hand this library any device workspace: a runtime that
+// owns a fixed device-memory budget and passes its plugins nothing but input
+// and output buffers, or a serving loop that must not call cudaMalloc (which
+// can synchronise the device) between steps.  For them the split partials live
+// in the file-scope array below instead of caller buffers.  Every GPU that
+// loads this library holds the array (8 MiB) until the process exits.
+//
+// Host code may not use the array's name as a device address (on the host it
+// names a shadow variable), so its device address is looked up once per device
+// with cudaGetSymbolAddress, with that device current, by the first call on it.
+// All calls share the array: two calls that overlap on the GPU (different
+// streams or threads) race on it.  Nothing in it needs to start at zero; every
+// slot the combine reads is written by the split kernel of the same call.
+// ---------------------------------------------------------------------------
+
+namespace da {
+namespace {
+constexpr size_t kNoAllocScratchFloats = (size_t)2 << 20;  // 8 MiB of fp32 partials
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevices] = {nullptr};
+}  // namespace
+}  // namespace da
+
+static __device__ __align__(256) float g_noalloc_scratch[da::kNoAllocScratchFloats];
+
+extern "C" int decode_attn_contig_noalloc(const void* q, const void* k, const void* v, const int* seq_lens,
+                                          int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                          int max_ctx, float scale, void* out, void* stream) {
+  const int B = batch, Hq = num_q_heads, Hkv = num_kv_heads, D = head_dim;
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_ctx < 0) return DA_ERR_INVALID_ARG;
+  if (D != 32 && D != 64 && D != 128 && D != 256) return DA_ERR_UNSUPPORTED;
+  if (B == 0) return DA_OK;
+  int dev, sms, smem_optin;
+  if (current_device(&dev) || device_info(dev, &sms, &smem_optin)) return DA_ERR_CUDA;
+  const int S = decode_num_splits(B, Hkv, max_ctx, D, sms);
+  if (S < 1) return DA_ERR_INVALID_ARG;
+  float* acc = nullptr;
+  float* ml = nullptr;
+  if (S >= 2) {
+    const size_t acc_floats = ((size_t)B * Hq * S * D + 63) / 64 * 64;  // keep part_ml 256-byte aligned
+    const size_t ml_floats = (size_t)B * Hq * S * 2;
+    if (acc_floats + ml_floats > kNoAllocScratchFloats) return DA_ERR_WORKSPACE;
+    float* base = nullptr;
+    {
+      std::lock_guard<std::mutex> lk(g_noalloc_mu);
+      if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+          cudaGetLastError();
+          return DA_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = static_cast<float*>(p);
+      }
+      base = g_noalloc_ptr[dev];
+    }
+    acc = base;
+    ml = base + acc_floats;
+  }
+  return decode_attn_contig(q, k, v, seq_lens, B, Hq, Hkv, D, max_ctx, scale, S, acc, ml, out, stream);
+}

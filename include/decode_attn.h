@@ -133,6 +133,27 @@ int decode_attn_paged(const void* q, const void* k_pool, const void* v_pool,
 int decode_combine(const float* part_acc, const float* part_ml, int batch, int num_q_heads,
                    int head_dim, int num_splits, void* out, void* stream);
 
+/*
+ * decode_attn_contig_noalloc — decode_attn_contig for callers that cannot allocate.
+ *
+ * The paper has no counterpart: this entry point exists for callers that may not
+ * allocate device memory or hold any workspace (a runtime with a fixed device
+ * budget that gives its plugins only input and output buffers, or a serving loop
+ * that must not call cudaMalloc between steps).  Arguments are those of
+ * decode_attn_contig without num_splits, part_acc and part_ml: the split count is
+ * decode_num_splits(batch, num_kv_heads, max_ctx, head_dim, <SMs of the device>)
+ * and the partials live in an 8 MiB array inside the library (every GPU that loads
+ * the library holds it until exit).  Shapes whose partials need more than
+ * 8 MiB (batch * num_q_heads * S * (head_dim + 2) * 4 bytes, plus alignment)
+ * return DA_ERR_WORKSPACE and launch nothing.  The first call on a device looks
+ * up the array's device address (no allocation); make that first call before any
+ * stream capture.  Calls share the array: calls that overlap on the GPU race.
+ * Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+int decode_attn_contig_noalloc(const void* q, const void* k, const void* v, const int* seq_lens,
+                               int batch, int num_q_heads, int num_kv_heads, int head_dim, int max_ctx,
+                               float scale, void* out, void* stream);
+
 /* Human-readable name of a da_status value (static string). */
 const char* decode_status_string(int status);
 
