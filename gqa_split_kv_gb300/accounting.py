@@ -42,7 +42,7 @@ def piece_counts(seq_lens, Hkv: int, G: int, S: int) -> np.ndarray:
     P = np.concatenate([[0], np.cumsum(nblk)])
     NB = U * int(P[-1])
     R = (S - 1) * U
-    q = max(1, -(-NB // R))
+    q = max(4, -(-max(1, -(-NB // R)) // 4) * 4)
     s0 = U * P[:-1, None] + np.arange(U)[None, :] * nblk[:, None]
     s1 = s0 + nblk[:, None]
     n = (s1 - 1) // q - s0 // q + 1

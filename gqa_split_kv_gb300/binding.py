@@ -23,6 +23,7 @@ __all__ = [
     "decode_attn_paged",
     "decode_combine",
     "device_error",
+    "counters_len",
     "STATUS",
 ]
 
@@ -50,9 +51,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.decode_num_splits.argtypes = [i, i, i, i, i]
     lib.decode_num_splits.restype = i
-    lib.decode_attn_contig.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, vp, vp]
+    lib.decode_attn_contig.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, vp, vp, vp]
     lib.decode_attn_contig.restype = i
-    lib.decode_attn_paged.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, vp, vp, vp]
+    lib.decode_attn_paged.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, vp, vp, vp, vp]
     lib.decode_attn_paged.restype = i
     lib.decode_combine.argtypes = [vp, vp, i, i, i, i, vp, vp]
     lib.decode_combine.restype = i
@@ -94,18 +95,26 @@ def num_splits(batch: int, num_kv_heads: int, max_seq_len: int, head_dim: int, n
     return s
 
 
-def _workspace(B, Hq, D, S, part_acc, part_ml, device):
+def counters_len(batch: int, num_q_heads: int, num_kv_heads: int) -> int:
+    """Entries of the per-segment counter array: batch * Hkv * ceil(G / 8)."""
+    G = num_q_heads // num_kv_heads
+    return batch * num_kv_heads * ((G + 7) // 8)
+
+
+def _workspace(B, Hq, Hkv, D, S, part_acc, part_ml, seg_counters, device):
     import torch
     if S >= 2:
         if part_acc is None:
             part_acc = torch.empty((B, Hq, S, D), dtype=torch.float32, device=device)
         if part_ml is None:
             part_ml = torch.empty((B, Hq, S, 2), dtype=torch.float32, device=device)
-    return part_acc, part_ml
+        if seg_counters is None:
+            seg_counters = torch.zeros(counters_len(B, Hq, Hkv), dtype=torch.int64, device=device)
+    return part_acc, part_ml, seg_counters
 
 
 def decode_attn_contig(q, k, v, seq_lens=None, scale: Optional[float] = None, splits: Optional[int] = None,
-                       part_acc=None, part_ml=None, out=None, stream=None):
+                       part_acc=None, part_ml=None, seg_counters=None, out=None, stream=None):
     """q [B,Hq,D], k/v [B,max_ctx,Hkv,D] bf16; seq_lens int32 [B] or None.  Returns out [B,Hq,D] bf16."""
     import torch
     _need(q, "q", torch.bfloat16, 3)
@@ -117,17 +126,18 @@ def decode_attn_contig(q, k, v, seq_lens=None, scale: Optional[float] = None, sp
         _need(seq_lens, "seq_lens", torch.int32, 1)
     scale = D ** -0.5 if scale is None else float(scale)
     S = num_splits(B, Hkv, ctx, D) if splits is None else int(splits)
-    part_acc, part_ml = _workspace(B, Hq, D, S, part_acc, part_ml, q.device)
+    part_acc, part_ml, seg_counters = _workspace(B, Hq, Hkv, D, S, part_acc, part_ml, seg_counters, q.device)
     if out is None:
         out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
     st = load().decode_attn_contig(_ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), B, Hq, Hkv, D, ctx, scale, S,
-                                   _ptr(part_acc), _ptr(part_ml), _ptr(out), _stream(stream))
+                                   _ptr(part_acc), _ptr(part_ml), _ptr(seg_counters), _ptr(out), _stream(stream))
     _check("decode_attn_contig", st)
     return out
 
 
 def decode_attn_paged(q, k_pool, v_pool, page_table, seq_lens, max_seq_len: int, scale: Optional[float] = None,
-                      splits: Optional[int] = None, part_acc=None, part_ml=None, out=None, stream=None):
+                      splits: Optional[int] = None, part_acc=None, part_ml=None, seg_counters=None, out=None,
+                      stream=None):
     """q [B,Hq,D]; pools [num_pages,page_size,Hkv,D] bf16; page_table int32 [B,max_pages]; seq_lens int32 [B]."""
     import torch
     _need(q, "q", torch.bfloat16, 3)
@@ -140,12 +150,12 @@ def decode_attn_paged(q, k_pool, v_pool, page_table, seq_lens, max_seq_len: int,
     max_pages = page_table.shape[1]
     scale = D ** -0.5 if scale is None else float(scale)
     S = num_splits(B, Hkv, max_seq_len, D) if splits is None else int(splits)
-    part_acc, part_ml = _workspace(B, Hq, D, S, part_acc, part_ml, q.device)
+    part_acc, part_ml, seg_counters = _workspace(B, Hq, Hkv, D, S, part_acc, part_ml, seg_counters, q.device)
     if out is None:
         out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
     st = load().decode_attn_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(seq_lens), B, Hq, Hkv,
                                   D, ps, max_pages, num_pages, int(max_seq_len), scale, S, _ptr(part_acc),
-                                  _ptr(part_ml), _ptr(out), _stream(stream))
+                                  _ptr(part_ml), _ptr(seg_counters), _ptr(out), _stream(stream))
     _check("decode_attn_paged", st)
     return out
 

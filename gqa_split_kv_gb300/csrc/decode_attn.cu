@@ -1,10 +1,11 @@
 // C-ABI entry points of the decode-attention library (declared in include/decode_attn.h).
 //
 // Host side of every call: validate the arguments, build the TMA tensor maps of
-// the caller's K/V/Q buffers, enqueue the persistent split kernel and, when the
-// plan has partial slots, the combine kernel as a programmatic dependent launch
-// (its CTAs are scheduled while the split kernel drains and wait on the device
-// for its completion, so no host round trip or launch gap separates them).
+// the caller's K/V/Q buffers and enqueue the persistent split kernel, which also
+// merges segments cut into at most 8 pieces.  When the plan allows longer
+// segments, the combine kernel follows as a programmatic dependent launch (its
+// CTAs start while the split kernel drains and wait on the device for it) and
+// merges those.  decode_combine runs the stand-alone merge.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -12,6 +13,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/decode_attn.h"
@@ -30,6 +32,14 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 
 std::mutex g_mu;
 EncodeTiledFn g_encode = nullptr;
+std::atomic<unsigned int> g_epoch{0};
+
+// A fresh non-zero tag for the per-segment counters of one call.
+unsigned int next_epoch() {
+  unsigned int e = ++g_epoch;
+  while (e == 0) e = ++g_epoch;
+  return e;
+}
 int g_num_sms[kMaxDevices] = {0};
 int g_smem_optin[kMaxDevices] = {0};
 
@@ -87,6 +97,14 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int sub_width(int D) { return D >= 64 ? 64 : 32; }
 
+// tokens per tile of the split kernel for head_dim D (the TMA box height of a contiguous cache)
+int tile_tokens(int D) {
+  static_assert(SplitGeo<32>::T == 256 && SplitGeo<64>::T == 128 && SplitGeo<128>::T == 64 &&
+                    SplitGeo<256>::T == 64,
+                "host and device tile sizes must agree");
+  return D == 32 ? 256 : D == 64 ? 128 : 64;
+}
+
 // Query heads of one KV head are processed in ceil(G / 8) equal sub-groups.
 void head_groups(int G, int* ng, int* gr) {
   *ng = (G + 7) / 8;
@@ -102,6 +120,7 @@ struct Launch {
   int page_size, max_pages;
   float* part_acc;
   float* part_ml;
+  unsigned long long* seg_counters;
   void* out;
   cudaStream_t stream;
   bool paged;
@@ -114,7 +133,9 @@ int launch_split(const SplitParams& prm, int grid, int smem, int dev, cudaStream
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!attr_done[dev]) {
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess ||
+          cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
         cudaGetLastError();
         return DA_ERR_UNSUPPORTED;
       }
@@ -144,16 +165,20 @@ int launch_combine(const CombineParams& prm, int dev, int sms, cudaStream_t st, 
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!attr_done[dev]) {
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess ||
+          cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
         cudaGetLastError();
         return DA_ERR_UNSUPPORTED;
       }
       attr_done[dev] = true;
     }
   }
-  // grid-strided over rows: a few CTAs per SM, each builds the plan once
+  // grid-strided over rows; after the split kernel one CTA per SM, so every CTA
+  // fits beside a split CTA, starts early and has its plan ready when the split
+  // kernel completes; alone, a few CTAs per SM
   const long long rows = (long long)prm.B * prm.Hq;
-  const long long cap = 4LL * (sms > 0 ? sms : 1);
+  const long long cap = (dependent ? 1LL : 4LL) * (sms > 0 ? sms : 1);
   const long long grid = rows < cap ? rows : cap;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -192,7 +217,9 @@ int run_decode(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, in
   prm.page_table = a.page_table;
   prm.part_acc = a.part_acc;
   prm.part_ml = a.part_ml;
+  prm.seg_counters = a.seg_counters;
   prm.out = reinterpret_cast<__nv_bfloat16*>(a.out);
+  prm.epoch = next_epoch();
   prm.B = a.B;
   prm.Hq = a.Hq;
   prm.G = a.Hq / a.Hkv;
@@ -208,6 +235,8 @@ int run_decode(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, in
 
   // one persistent CTA per SM, never more CTAs than ranges or blocks of work
   const long long nblk_max = (a.max_len + kBlockTokens - 1) / kBlockTokens;
+  if ((long long)a.B * prm.U * nblk_max >= (1LL << 30) || (long long)a.B * a.Hq >= (1LL << 30))
+    return DA_ERR_UNSUPPORTED;  // the device plan counts blocks in 32 bits
   long long ranges = a.S == 1 ? (long long)a.B * prm.U : (long long)(a.S - 1) * prm.U;
   const long long work = (long long)a.B * prm.U * (nblk_max > 0 ? nblk_max : 1);
   if (ranges > work) ranges = work;
@@ -216,8 +245,9 @@ int run_decode(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, in
   if (int st = (a.paged ? launch_split<D, true>(prm, grid, smem, dev, a.stream)
                         : launch_split<D, false>(prm, grid, smem, dev, a.stream)))
     return st;
-  if (a.S == 1) return DA_OK;
+  if (a.S <= kFusedMergeMax) return DA_OK;  // every segment is merged inside the split kernel
   CombineParams cp;
+  std::memset(&cp, 0, sizeof(cp));
   cp.part_acc = a.part_acc;
   cp.part_ml = a.part_ml;
   cp.out = prm.out;
@@ -235,7 +265,7 @@ int run_decode(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, in
 }
 
 int check_common(const void* q, const void* out, int B, int Hq, int Hkv, int D, float scale, int S,
-                 const float* part_acc, const float* part_ml) {
+                 const float* part_acc, const float* part_ml, const unsigned long long* seg_counters) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return DA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return DA_ERR_INVALID_ARG;
   if (S < 1 || S > DA_MAX_SPLITS) return DA_ERR_INVALID_ARG;
@@ -245,8 +275,8 @@ int check_common(const void* q, const void* out, int B, int Hq, int Hkv, int D, 
   if (!q || !out) return DA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(out, 16)) return DA_ERR_INVALID_ARG;
   if (S >= 2) {
-    if (!part_acc || !part_ml) return DA_ERR_WORKSPACE;
-    if (!aligned(part_acc, 16) || !aligned(part_ml, 8)) return DA_ERR_INVALID_ARG;
+    if (!part_acc || !part_ml || !seg_counters) return DA_ERR_WORKSPACE;
+    if (!aligned(part_acc, 16) || !aligned(part_ml, 8) || !aligned(seg_counters, 8)) return DA_ERR_INVALID_ARG;
   }
   return DA_OK;
 }
@@ -298,9 +328,10 @@ extern "C" int decode_num_splits(int batch, int num_kv_heads, int max_seq_len, i
 
 extern "C" int decode_attn_contig(const void* q, const void* k, const void* v, const int* seq_lens, int batch,
                                   int num_q_heads, int num_kv_heads, int head_dim, int max_ctx, float scale,
-                                  int num_splits, float* part_acc, float* part_ml, void* out, void* stream) {
+                                  int num_splits, float* part_acc, float* part_ml,
+                                  unsigned long long* seg_counters, void* out, void* stream) {
   const int B = batch, Hq = num_q_heads, Hkv = num_kv_heads, D = head_dim, S = num_splits;
-  if (int st = check_common(q, out, B, Hq, Hkv, D, scale, S, part_acc, part_ml)) return st;
+  if (int st = check_common(q, out, B, Hq, Hkv, D, scale, S, part_acc, part_ml, seg_counters)) return st;
   if (max_ctx < 0) return DA_ERR_INVALID_ARG;
   if (B == 0) return DA_OK;
   if (max_ctx > 0 && (!k || !v || !aligned(k, 16) || !aligned(v, 16))) return DA_ERR_INVALID_ARG;
@@ -314,7 +345,7 @@ extern "C" int decode_attn_contig(const void* q, const void* k, const void* v, c
   const cuuint64_t dims[5] = {(cuuint64_t)SW, (cuuint64_t)(D / SW), (cuuint64_t)Hkv, (cuuint64_t)max_ctx,
                               (cuuint64_t)B};
   const cuuint64_t strides[4] = {(cuuint64_t)SW * 2, (cuuint64_t)D * 2, row, row * (cuuint64_t)max_ctx};
-  const cuuint32_t box[5] = {(cuuint32_t)SW, 1, 1, (cuuint32_t)SplitGeo<32>::T, 1};
+  const cuuint32_t box[5] = {(cuuint32_t)SW, 1, 1, (cuuint32_t)tile_tokens(D), 1};
   CUtensorMap tk, tv;
   if (int e = encode_map(&tk, k, 5, dims, strides, box, D)) return e;
   if (int e = encode_map(&tv, v, 5, dims, strides, box, D)) return e;
@@ -334,6 +365,7 @@ extern "C" int decode_attn_contig(const void* q, const void* k, const void* v, c
   a.max_pages = 0;
   a.part_acc = part_acc;
   a.part_ml = part_ml;
+  a.seg_counters = seg_counters;
   a.out = out;
   a.stream = st;
   a.paged = false;
@@ -343,9 +375,10 @@ extern "C" int decode_attn_contig(const void* q, const void* k, const void* v, c
 extern "C" int decode_attn_paged(const void* q, const void* k_pool, const void* v_pool, const int* page_table,
                                  const int* seq_lens, int batch, int num_q_heads, int num_kv_heads, int head_dim,
                                  int page_size, int max_pages_per_seq, int num_pages, int max_seq_len, float scale,
-                                 int num_splits, float* part_acc, float* part_ml, void* out, void* stream) {
+                                 int num_splits, float* part_acc, float* part_ml, unsigned long long* seg_counters,
+                                 void* out, void* stream) {
   const int B = batch, Hq = num_q_heads, Hkv = num_kv_heads, D = head_dim, S = num_splits;
-  if (int st = check_common(q, out, B, Hq, Hkv, D, scale, S, part_acc, part_ml)) return st;
+  if (int st = check_common(q, out, B, Hq, Hkv, D, scale, S, part_acc, part_ml, seg_counters)) return st;
   if (page_size <= 0 || max_pages_per_seq < 0 || num_pages < 0 || max_seq_len < 0) return DA_ERR_INVALID_ARG;
   if (page_size % 16 != 0) return DA_ERR_UNSUPPORTED;
   if (B == 0) return DA_OK;
@@ -385,6 +418,7 @@ extern "C" int decode_attn_paged(const void* q, const void* k_pool, const void* 
   a.max_pages = max_pages_per_seq;
   a.part_acc = part_acc;
   a.part_ml = part_ml;
+  a.seg_counters = seg_counters;
   a.out = out;
   a.stream = st;
   a.paged = true;
@@ -468,8 +502,9 @@ extern "C" int decode_device_error(void* stream, unsigned int* flags) {
 // names a shadow variable), so its device address is looked up once per device
 // with cudaGetSymbolAddress, with that device current, by the first call on it.
 // All calls share the array: two calls that overlap on the GPU (different
-// streams or threads) race on it.  Nothing in it needs to start at zero; every
-// slot the combine reads is written by the split kernel of the same call.
+// streams or threads) race on it.  Nothing in it needs to start at zero: every
+// partial slot a merge reads is written earlier in the same call, and the
+// per-segment counters carry a per-call tag, so stale values count as zero.
 // ---------------------------------------------------------------------------
 
 namespace da {
@@ -495,10 +530,12 @@ extern "C" int decode_attn_contig_noalloc(const void* q, const void* k, const vo
   if (S < 1) return DA_ERR_INVALID_ARG;
   float* acc = nullptr;
   float* ml = nullptr;
+  unsigned long long* ctr = nullptr;
   if (S >= 2) {
     const size_t acc_floats = ((size_t)B * Hq * S * D + 63) / 64 * 64;  // keep part_ml 256-byte aligned
-    const size_t ml_floats = (size_t)B * Hq * S * 2;
-    if (acc_floats + ml_floats > kNoAllocScratchFloats) return DA_ERR_WORKSPACE;
+    const size_t ml_floats = ((size_t)B * Hq * S * 2 + 63) / 64 * 64;
+    const size_t ctr_floats = (size_t)B * Hkv * ((Hq / Hkv + 7) / 8) * 2;  // one 8-byte counter per segment
+    if (acc_floats + ml_floats + ctr_floats > kNoAllocScratchFloats) return DA_ERR_WORKSPACE;
     float* base = nullptr;
     {
       std::lock_guard<std::mutex> lk(g_noalloc_mu);
@@ -514,6 +551,7 @@ extern "C" int decode_attn_contig_noalloc(const void* q, const void* k, const vo
     }
     acc = base;
     ml = base + acc_floats;
+    ctr = reinterpret_cast<unsigned long long*>(base + acc_floats + ml_floats);
   }
-  return decode_attn_contig(q, k, v, seq_lens, B, Hq, Hkv, D, max_ctx, scale, S, acc, ml, out, stream);
+  return decode_attn_contig(q, k, v, seq_lens, B, Hq, Hkv, D, max_ctx, scale, S, acc, ml, ctr, out, stream);
 }

@@ -10,7 +10,8 @@
 //   P_b  = n_0 + ... + n_{b-1}                (prefix, P_B = total)
 //   U    = Hkv * ceil(G / 8)                  sub-group slots per sequence
 //   segment (b, u) = blocks [U P_b + u n_b, U P_b + (u + 1) n_b)
-//   S >= 2: q = max(1, ceil(U P_B / ((S - 1) U))), range r = [r q, (r + 1) q)
+//   S >= 2: q = ceil(U P_B / ((S - 1) U)) rounded up to a multiple of 4 blocks
+//           (whole 64-token tiles), range r = [r q, (r + 1) q)
 //   S == 1: range r = segment (r / U, r % U), whole.
 #pragma once
 
@@ -19,11 +20,16 @@
 namespace da {
 
 constexpr int kBlockTokens = 16;
+constexpr int kRangeQuantum = 4;  // ranges are whole 64-token tiles
+// Segments cut into at most this many pieces are merged inside the split kernel
+// by the CTA that finishes the last piece; longer ones by the combine kernel.
+constexpr int kFusedMergeMax = 8;
 
+// Block counts are 32-bit: the host rejects problems with 2^30 blocks or more.
 struct Plan {
-  long long NB;      // blocks on the line
-  long long q;       // blocks per range (S >= 2)
-  long long ranges;  // ranges that hold work
+  int NB;      // blocks on the line
+  int q;       // blocks per range (S >= 2)
+  int ranges;  // ranges that hold work
   int U;             // sub-group slots per sequence
   int S;             // partial slots per (b, h)
 };
@@ -72,14 +78,15 @@ __device__ __forceinline__ Plan make_plan(int B, int U, int S, const int* P) {
   Plan pl;
   pl.U = U;
   pl.S = S;
-  pl.NB = (long long)U * P[B];
+  pl.NB = U * P[B];
   if (S == 1) {
     pl.q = 0;
-    pl.ranges = (long long)B * U;
+    pl.ranges = B * U;
   } else {
-    const long long R = (long long)(S - 1) * U;
+    const int R = (S - 1) * U;
     pl.q = (pl.NB + R - 1) / R;
-    if (pl.q < 1) pl.q = 1;
+    pl.q = (pl.q + kRangeQuantum - 1) / kRangeQuantum * kRangeQuantum;
+    if (pl.q < kRangeQuantum) pl.q = kRangeQuantum;
     pl.ranges = (pl.NB + pl.q - 1) / pl.q;
   }
   return pl;
@@ -89,45 +96,45 @@ __device__ __forceinline__ Plan make_plan(int B, int U, int S, const int* P) {
 __device__ __forceinline__ int segment_pieces(const Plan& pl, const int* lens, const int* P, int b, int u) {
   const int nb = (lens[b] + kBlockTokens - 1) / kBlockTokens;
   if (nb == 0) return 0;
-  const long long s0 = (long long)pl.U * P[b] + (long long)u * nb;
-  const long long s1 = s0 + nb;
-  return (int)((s1 - 1) / pl.q - s0 / pl.q + 1);
+  const int s0 = pl.U * P[b] + u * nb;
+  const int s1 = s0 + nb;
+  return (s1 - 1) / pl.q - s0 / pl.q + 1;
 }
 
 // S >= 2: the piece that starts at block x of range r (x < xe = end of range).
 // Returns the block where the next piece of the range starts.
-__device__ __forceinline__ long long piece_at(const Plan& pl, const int* lens, const int* P, int B, long long x,
-                                              long long xe, long long r, Piece& pc) {
+__device__ __forceinline__ int piece_at(const Plan& pl, const int* lens, const int* P, int B, int x, int xe, int r,
+                                        Piece& pc) {
   // sequence b: the last with U * P[b] <= x (sequences with no blocks are skipped
   // because the following non-empty one shares their prefix value)
   int lo = 0, hi = B - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if ((long long)pl.U * P[mid] <= x)
+    if (pl.U * P[mid] <= x)
       lo = mid;
     else
       hi = mid - 1;
   }
   const int b = lo;
   const int nb = (lens[b] + kBlockTokens - 1) / kBlockTokens;
-  const long long base = (long long)pl.U * P[b];
-  const int u = (int)((x - base) / nb);
-  const long long s0 = base + (long long)u * nb;
-  const long long s1 = s0 + nb;
-  const long long pe = xe < s1 ? xe : s1;
+  const int base = pl.U * P[b];
+  const int u = (x - base) / nb;
+  const int s0 = base + u * nb;
+  const int s1 = s0 + nb;
+  const int pe = xe < s1 ? xe : s1;
   pc.b = b;
   pc.u = u;
-  pc.t0 = (int)(x - s0) * kBlockTokens;
-  pc.t1 = min((int)(pe - s0) * kBlockTokens, lens[b]);
-  pc.j = (int)(r - s0 / pl.q);
-  pc.npieces = (int)((s1 - 1) / pl.q - s0 / pl.q + 1);
+  pc.t0 = (x - s0) * kBlockTokens;
+  pc.t1 = min((pe - s0) * kBlockTokens, lens[b]);
+  pc.j = r - s0 / pl.q;
+  pc.npieces = (s1 - 1) / pl.q - s0 / pl.q + 1;
   return pe;
 }
 
 // Walks the pieces of the ranges blockIdx.x, blockIdx.x + gridDim.x, ...
 struct PieceWalker {
-  long long r;       // range being walked
-  long long x, xe;   // S >= 2: next block and end of range r
+  int r;       // range being walked
+  int x, xe;   // S >= 2: next block and end of range r
   bool started;
 
   __device__ __forceinline__ void init() {
@@ -145,8 +152,8 @@ struct PieceWalker {
         if (started) r += gridDim.x;
         started = true;
         if (r >= pl.ranges) return false;
-        pc.b = (int)(r / pl.U);
-        pc.u = (int)(r % pl.U);
+        pc.b = r / pl.U;
+        pc.u = r % pl.U;
         pc.t0 = 0;
         pc.t1 = lens[pc.b];
         pc.j = 0;

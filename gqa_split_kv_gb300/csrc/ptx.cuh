@@ -114,12 +114,14 @@ __device__ __forceinline__ float exp2_approx(float x) {
   return y;
 }
 
-// ---------------------------------------------------------------- barriers / PDL
+// ---------------------------------------------------------------- barriers
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel in the stream start its
+// CTAs now / wait until the previous kernel has completed and flushed memory.
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

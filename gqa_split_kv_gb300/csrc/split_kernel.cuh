@@ -8,7 +8,8 @@
 //     count and issues the TMA tile copies (K, V and, for the first tile of a
 //     piece, the query rows).  Paged caches: the lanes resolve one page-table
 //     entry per 16-token block, prefetched LA tiles ahead with cp.async.
-//   warps 0..W-1 (consumers): warp w owns tokens [16 w, 16 w + 16) of every tile.
+//   warps 0..W-1 (consumers): warp w owns the 16-token sub-blocks w, w + W, ... of
+//     every tile.
 //
 // Prior art on the pages: the two-stage cp.async ring of "perf(dspark): overlap
 // KV staging with compute via cp.async" (section "Summary"); the per-warp-group
@@ -19,6 +20,11 @@
 // tensor-memory accelerator (cp.async.bulk.tensor, 128-byte swizzle), the stage
 // count is sized for the 227 KB of shared memory per CTA, and tiles are
 // released through mbarriers instead of CTA-wide barriers.
+//
+// A segment cut into at most 8 pieces is merged by the CTA that finishes its last
+// piece (log-sum-exp over the pieces' partials, ascending order), detected with
+// one per-segment counter.  Longer segments (long contexts over few heads) are
+// merged by the combine kernel, spread over many CTAs.
 //
 // Head packing: the MMA tile is 16 rows; query heads fill rows 0..7 and rows
 // 8..15 carry the bf16 low part of the probabilities, so P = hi + lo reaches
@@ -47,7 +53,9 @@ struct SplitParams {
   const int* page_table;
   float* part_acc;
   float* part_ml;
+  unsigned long long* seg_counters;  // one per segment (b, u): (epoch << 32) | pieces done
   __nv_bfloat16* out;
+  unsigned int epoch;                // tags this call's counter updates (never 0)
   int B, Hq, G, U, ng, gr;
   int max_len;       // lengths are clamped to [0, max_len]
   int page_size, max_pages;
@@ -58,32 +66,38 @@ struct SplitParams {
 
 template <int D>
 struct SplitGeo {
-  static constexpr int T = 64;                 // tokens per tile
-  static constexpr int W = 4;                  // consumer warps, 16 tokens each
+  // Tiles carry 32 KB (D <= 128) or 64 KB (D = 256) of K+V so the per-tile costs
+  // (barrier round trip, TMA issue) stay small against the bytes moved.
+  static constexpr int T = D == 32 ? 256 : D == 64 ? 128 : 64;  // tokens per tile
+  static constexpr int W = 4;                       // consumer warps
+  static constexpr int SB = T / 16;                 // 16-token sub-blocks per tile
+  static constexpr int SBW = SB / W;                // sub-blocks per warp: k = warp + W * i
   static constexpr int NTHREADS = (W + 1) * 32;
   static constexpr int SUBW = D >= 64 ? 64 : 32;    // elements per swizzle row
   static constexpr int NSUB = D / SUBW;             // swizzle rows per token
   static constexpr int ROWB = SUBW * 2;             // 128 or 64 bytes
   static constexpr int CPR = SUBW / 8;              // 16-byte chunks per swizzle row
-  static constexpr int STAGES = D == 32 ? 8 : D == 64 ? 6 : D == 128 ? 4 : 2;
+  static constexpr int STAGES = D == 256 ? 2 : D == 128 ? 4 : 5;
   static constexpr int SUB_BYTES = T * ROWB;        // one swizzle column of a tile
   static constexpr int KV_BYTES = T * D * 2;        // one tensor, one stage
   static constexpr int Q_SUB_BYTES = 8 * ROWB;
   static constexpr int Q_BYTES = 8 * D * 2;
-  static constexpr int RING = 4;                    // page-entry ring slots
-  static constexpr int LA = 2;                      // page-entry prefetch distance (tiles)
+  static constexpr int RING = 16;                   // page-entry ring slots
+  static constexpr int LA = 8;                      // page-entry prefetch distance (tiles)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_Q = OFF_V + STAGES * KV_BYTES;
   static constexpr int OFF_FACC = OFF_Q + STAGES * Q_BYTES;
   static constexpr int OFF_FML = OFF_FACC + W * 8 * D * 4;
-  static constexpr int OFF_BAR = OFF_FML + W * 8 * 2 * 4;
+  static constexpr int OFF_FSC = OFF_FML + W * 8 * 2 * 4;   // per-(warp, row) merge weights
+  static constexpr int OFF_FROW = OFF_FSC + W * 8 * 4;      // per-row (M, L, 1/L, -)
+  static constexpr int OFF_BAR = OFF_FROW + 8 * 4 * 4;
   static constexpr int OFF_PG = OFF_BAR + 2 * STAGES * 8;
   static constexpr int OFF_MISC = OFF_PG + RING * 32 * 4;
   static constexpr int OFF_PLAN = OFF_MISC + 16;
   static constexpr int smem_bytes(int B) { return OFF_PLAN + (2 * B + 1) * 4 + 1024; }
-  static_assert(T == 16 * W, "each consumer warp owns 16 tokens of a tile");
-  static_assert(T / 16 <= 32, "one producer lane per 16-token block");
+  static_assert(SB % W == 0 && SB <= 32, "whole sub-blocks per warp; one producer lane per block");
+  static_assert(RING >= LA + 2, "page ring must hold the prefetch window");
 };
 
 template <int ROWB>
@@ -172,10 +186,10 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
     }
   }
 
-  long long n = 0;  // tiles issued
+  int n = 0;  // tiles issued
+  int stage = 0;
+  uint32_t parity = 0;
   while (cur.valid) {
-    const int stage = (int)(n % Gm::STAGES);
-    const uint32_t parity = (uint32_t)((n / Gm::STAGES) & 1);
     const Piece& pc = cur.pc;
     const int h = pc.u / p.ng;
     const int first_head = h * p.G + (pc.u % p.ng) * p.gr;
@@ -238,19 +252,97 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
         tma_load_4d(qdst + sub * Gm::Q_SUB_BYTES, &p.tm_q, full, 0, sub, first_head, pc.b);
     }
     ++n;
+    if (++stage == Gm::STAGES) {
+      stage = 0;
+      parity ^= 1u;
+    }
     cur.advance(pl, lens, P, p.B, Gm::T);
   }
   if (PAGED) cp_async_wait<0>();
 
   // After an abort, let the copies already issued land before the CTA exits.
   if (*abort_flag && lane == 0) {
-    for (long long k = n > Gm::STAGES ? n - Gm::STAGES : 0; k < n; ++k) {
+    for (int k = n > Gm::STAGES ? n - Gm::STAGES : 0; k < n; ++k) {
       const uint32_t full = bar_full + (uint32_t)(k % Gm::STAGES) * 8;
       const uint32_t par = (uint32_t)((k / Gm::STAGES) & 1);
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(full, par) && globaltimer_ns() - t0 < p.timeout_ns) {
       }
     }
+  }
+}
+
+// Counts one finished piece of a segment; true for the piece that completes it.
+// The counter holds (epoch << 32) | count; a value from another call (another
+// epoch) counts as zero, so counters never need resetting.  Bounded retries.
+__device__ __forceinline__ bool claim_last_piece(unsigned long long* c, unsigned int epoch, int npieces) {
+  unsigned long long v = *reinterpret_cast<volatile unsigned long long*>(c);
+  for (int it = 0; it < (1 << 20); ++it) {
+    const unsigned int cnt = (unsigned int)(v >> 32) == epoch ? (unsigned int)v : 0u;
+    const unsigned long long nv = ((unsigned long long)epoch << 32) | (unsigned long long)(cnt + 1);
+    const unsigned long long prev = atomicCAS(c, v, nv);
+    if (prev == v) return (int)(cnt + 1) == npieces;
+    v = prev;
+  }
+  atomicOr(&g_error_word, 2u);
+  return false;
+}
+
+// Log-sum-exp merge of the n <= kFusedMergeMax partials of one segment into its
+// bf16 output rows, in ascending piece order (run by the CTA that finished the
+// segment's last piece; the 4 consumer warps, 128 threads).  Partials written by
+// other CTAs are read through L2 (ld.global.cg).
+template <int D>
+__device__ __forceinline__ void merge_segment(const SplitParams& p, int b, int first_head, int nrows, int n,
+                                              float* rowM) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const float kNegInf = -__int_as_float(0x7f800000);
+  for (int r = warp; r < nrows; r += 4) {
+    const float* ml = p.part_ml + ((size_t)b * p.Hq + first_head + r) * p.S * 2;
+    float M = kNegInf;
+    for (int j = lane; j < n; j += 32) M = fmaxf(M, __ldcg(ml + 2 * j));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (lane == 0) rowM[r] = M;
+  }
+  named_bar_sync(1, 128);
+  for (int e = tid; e < nrows * (D / 4); e += 128) {
+    const int r = e / (D / 4), c4 = e % (D / 4);
+    const size_t row = (size_t)b * p.Hq + first_head + r;
+    const float2* ml = reinterpret_cast<const float2*>(p.part_ml + row * p.S * 2);
+    const float4* acc = reinterpret_cast<const float4*>(p.part_acc + row * p.S * D) + c4;
+    const float M = rowM[r];
+    // n <= kFusedMergeMax: a column's loads are issued 4 at a time
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den = 0.f;
+#pragma unroll
+    for (int j0 = 0; j0 < kFusedMergeMax; j0 += 4) {
+      float2 v[4];
+      float4 a[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (j0 + u < n) {
+          v[u] = __ldcg(ml + j0 + u);
+          a[u] = __ldcg(acc + (size_t)(j0 + u) * (D / 4));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (j0 + u < n) {
+          const float w = exp2_approx((v[u].x - M) * 1.4426950408889634f);
+          num.x += w * a[u].x;
+          num.y += w * a[u].y;
+          num.z += w * a[u].z;
+          num.w += w * a[u].w;
+          den += w * v[u].y;
+        }
+      }
+    }
+    const float inv = 1.f / den;
+    uint2 o;
+    o.x = pack_bf16x2(num.x * inv, num.y * inv);
+    o.y = pack_bf16x2(num.z * inv, num.w * inv);
+    *reinterpret_cast<uint2*>(p.out + row * D + 4 * c4) = o;
   }
 }
 
@@ -271,15 +363,25 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
   const float kNegInf = -__int_as_float(0x7f800000);
 
   // ldmatrix lane -> (row, chunk) patterns
-  const int k_row = 16 * warp + (lane & 7) + ((lane >> 4) << 3);
+  const int k_row0 = (lane & 7) + ((lane >> 4) << 3);
   const int k_chk = (lane >> 3) & 1;
-  const int v_row = 16 * warp + (lane & 7) + (((lane >> 3) & 1) << 3);
+  const int v_row0 = (lane & 7) + (((lane >> 3) & 1) << 3);
   const int v_chk = lane >> 4;
+
+  if (p.S >= 2) {
+    // empty sequences have no pieces on the block line: write their zero outputs
+    for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+      if (lens[b] != 0) continue;
+      uint4* o = reinterpret_cast<uint4*>(p.out + (size_t)b * p.Hq * D);
+      for (int i = threadIdx.x; i < p.Hq * D / 8; i += Gm::W * 32) o[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
 
   PieceWalker walk;
   walk.init();
   Piece pc;
-  long long n = 0;  // tiles consumed
+  int stage = 0;  // ring position of the next tile to consume
+  uint32_t parity = 0;
   while (walk.next(pl, lens, P, p.B, false, pc)) {
     uint32_t qa[KCH][2];
     float acc[NB8][4];
@@ -291,8 +393,6 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
     const int nrows = min(p.gr, p.G - (pc.u % p.ng) * p.gr);
 
     for (int t = pc.t0; t < pc.t1; t += Gm::T) {
-      const int stage = (int)(n % Gm::STAGES);
-      const uint32_t parity = (uint32_t)((n / Gm::STAGES) & 1);
       wait_bounded(bar_full + stage * 8, parity, abort_flag, p.timeout_ns);
       if (t == pc.t0) {
         const uint32_t qst = sbase + Gm::OFF_Q + stage * Gm::Q_BYTES;
@@ -311,72 +411,81 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
           for (int c = 0; c < KCH; ++c) qa[c][0] = qa[c][1] = 0u;
         }
       }
-      const int tok0 = t + 16 * warp;
-      if (tok0 < pc.t1) {
-        const uint32_t kst = sbase + Gm::OFF_K + stage * Gm::KV_BYTES;
-        const uint32_t vst = sbase + Gm::OFF_V + stage * Gm::KV_BYTES;
-        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int sb = 0; sb < Gm::SBW; ++sb) {
+        const int kb = warp + Gm::W * sb;  // sub-block of the tile owned by this warp
+        const int tok0 = t + 16 * kb;
+        const int k_row = 16 * kb + k_row0;
+        const int v_row = 16 * kb + v_row0;
+        if (tok0 < pc.t1) {
+          const uint32_t kst = sbase + Gm::OFF_K + stage * Gm::KV_BYTES;
+          const uint32_t vst = sbase + Gm::OFF_V + stage * Gm::KV_BYTES;
+          float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int kk = 0; kk < KCH; ++kk) {
-          const int c = 2 * kk + k_chk;
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kst + (c / Gm::CPR) * Gm::SUB_BYTES + swz<Gm::ROWB>(k_row, c % Gm::CPR), b0, b1, b2, b3);
-          mma_bf16_16816(s0, qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
-          mma_bf16_16816(s1, qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
-        }
-        float x0 = s0[0] * p.scale_log2, x1 = s0[1] * p.scale_log2;
-        float x2 = s1[0] * p.scale_log2, x3 = s1[1] * p.scale_log2;
-        const bool tail = tok0 + 16 > pc.t1;
-        uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
-        if (tail) {
-          const int ta = tok0 + 2 * i4, tb = tok0 + 8 + 2 * i4;
-          x0 = ta < pc.t1 ? x0 : kNegInf;
-          x1 = ta + 1 < pc.t1 ? x1 : kNegInf;
-          x2 = tb < pc.t1 ? x2 : kNegInf;
-          x3 = tb + 1 < pc.t1 ? x3 : kNegInf;
-          vm_lo = (ta < pc.t1 ? 0x0000ffffu : 0u) | (ta + 1 < pc.t1 ? 0xffff0000u : 0u);
-          vm_hi = (tb < pc.t1 ? 0x0000ffffu : 0u) | (tb + 1 < pc.t1 ? 0xffff0000u : 0u);
-        }
-        float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run, mx);
-        const float alpha = exp2_approx(m_run - m_new);
-        const float p0 = exp2_approx(x0 - m_new), p1 = exp2_approx(x1 - m_new);
-        const float p2 = exp2_approx(x2 - m_new), p3 = exp2_approx(x3 - m_new);
-        l_run = l_run * alpha + ((p0 + p1) + (p2 + p3));
-        if (__any_sync(0xffffffffu, m_new != m_run)) {
-#pragma unroll
-          for (int c = 0; c < NB8; ++c) {
-            acc[c][0] *= alpha;
-            acc[c][1] *= alpha;
-            acc[c][2] *= alpha;
-            acc[c][3] *= alpha;
+          for (int kk = 0; kk < KCH; ++kk) {
+            const int c = 2 * kk + k_chk;
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kst + (c / Gm::CPR) * Gm::SUB_BYTES + swz<Gm::ROWB>(k_row, c % Gm::CPR), b0, b1, b2, b3);
+            mma_bf16_16816(s0, qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+            mma_bf16_16816(s1, qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
           }
-        }
-        m_run = m_new;
-        // P = hi + lo in bf16: rows g (hi) and g + 8 (lo) of the A operand
-        const uint32_t ph0 = pack_bf16x2(p0, p1), ph1 = pack_bf16x2(p2, p3);
-        const uint32_t pl0 = pack_bf16x2(p0 - bf16lo_to_f32(ph0), p1 - bf16hi_to_f32(ph0));
-        const uint32_t pl1 = pack_bf16x2(p2 - bf16lo_to_f32(ph1), p3 - bf16hi_to_f32(ph1));
-#pragma unroll
-        for (int c2 = 0; c2 < NB8 / 2; ++c2) {
-          const int c = 2 * c2 + v_chk;
-          uint32_t v0, v1, v2, v3;
-          ldsm_x4_t(vst + (c / Gm::CPR) * Gm::SUB_BYTES + swz<Gm::ROWB>(v_row, c % Gm::CPR), v0, v1, v2, v3);
+          float x0 = s0[0] * p.scale_log2, x1 = s0[1] * p.scale_log2;
+          float x2 = s1[0] * p.scale_log2, x3 = s1[1] * p.scale_log2;
+          const bool tail = tok0 + 16 > pc.t1;
+          uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
           if (tail) {
-            v0 &= vm_lo;
-            v1 &= vm_hi;
-            v2 &= vm_lo;
-            v3 &= vm_hi;
+            const int ta = tok0 + 2 * i4, tb = tok0 + 8 + 2 * i4;
+            x0 = ta < pc.t1 ? x0 : kNegInf;
+            x1 = ta + 1 < pc.t1 ? x1 : kNegInf;
+            x2 = tb < pc.t1 ? x2 : kNegInf;
+            x3 = tb + 1 < pc.t1 ? x3 : kNegInf;
+            vm_lo = (ta < pc.t1 ? 0x0000ffffu : 0u) | (ta + 1 < pc.t1 ? 0xffff0000u : 0u);
+            vm_hi = (tb < pc.t1 ? 0x0000ffffu : 0u) | (tb + 1 < pc.t1 ? 0xffff0000u : 0u);
           }
-          mma_bf16_16816(acc[2 * c2], ph0, pl0, ph1, pl1, v0, v1);
-          mma_bf16_16816(acc[2 * c2 + 1], ph0, pl0, ph1, pl1, v2, v3);
+          float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          const float m_new = fmaxf(m_run, mx);
+          const float alpha = exp2_approx(m_run - m_new);
+          const float p0 = exp2_approx(x0 - m_new), p1 = exp2_approx(x1 - m_new);
+          const float p2 = exp2_approx(x2 - m_new), p3 = exp2_approx(x3 - m_new);
+          l_run = l_run * alpha + ((p0 + p1) + (p2 + p3));
+          if (__any_sync(0xffffffffu, m_new != m_run)) {
+#pragma unroll
+            for (int c = 0; c < NB8; ++c) {
+              acc[c][0] *= alpha;
+              acc[c][1] *= alpha;
+              acc[c][2] *= alpha;
+              acc[c][3] *= alpha;
+            }
+          }
+          m_run = m_new;
+          // P = hi + lo in bf16: rows g (hi) and g + 8 (lo) of the A operand
+          const uint32_t ph0 = pack_bf16x2(p0, p1), ph1 = pack_bf16x2(p2, p3);
+          const uint32_t pl0 = pack_bf16x2(p0 - bf16lo_to_f32(ph0), p1 - bf16hi_to_f32(ph0));
+          const uint32_t pl1 = pack_bf16x2(p2 - bf16lo_to_f32(ph1), p3 - bf16hi_to_f32(ph1));
+#pragma unroll
+          for (int c2 = 0; c2 < NB8 / 2; ++c2) {
+            const int c = 2 * c2 + v_chk;
+            uint32_t v0, v1, v2, v3;
+            ldsm_x4_t(vst + (c / Gm::CPR) * Gm::SUB_BYTES + swz<Gm::ROWB>(v_row, c % Gm::CPR), v0, v1, v2, v3);
+            if (tail) {
+              v0 &= vm_lo;
+              v1 &= vm_hi;
+              v2 &= vm_lo;
+              v3 &= vm_hi;
+            }
+            mma_bf16_16816(acc[2 * c2], ph0, pl0, ph1, pl1, v0, v1);
+            mma_bf16_16816(acc[2 * c2 + 1], ph0, pl0, ph1, pl1, v2, v3);
+          }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + stage * 8);
-      ++n;
+      if (++stage == Gm::STAGES) {
+        stage = 0;
+        parity ^= 1u;
+      }
     }
 
     // ---- fold the W warps' (m, l, acc) in ascending warp order, then write
@@ -395,33 +504,60 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
     }
     named_bar_sync(1, Gm::W * 32);
     const int tid = threadIdx.x;
+    float* fsc = reinterpret_cast<float*>(smem + Gm::OFF_FSC);
+    float* frow = reinterpret_cast<float*>(smem + Gm::OFF_FROW);
+    if (tid < nrows) {  // one thread per row: the W warps' merge weights and the row's (M, L)
+      float M = kNegInf;
+#pragma unroll
+      for (int w = 0; w < Gm::W; ++w) M = fmaxf(M, fml[(w * 8 + tid) * 2]);
+      float L = 0.f;
+#pragma unroll
+      for (int w = 0; w < Gm::W; ++w) {
+        const float mw = fml[(w * 8 + tid) * 2];
+        const float sc = mw == kNegInf ? 0.f : exp2_approx(mw - M);
+        fsc[w * 8 + tid] = sc;
+        L += sc * fml[(w * 8 + tid) * 2 + 1];
+      }
+      frow[tid * 4 + 0] = M;
+      frow[tid * 4 + 1] = L;
+      frow[tid * 4 + 2] = L > 0.f ? 1.f / L : 0.f;
+    }
+    named_bar_sync(1, Gm::W * 32);
     const int total = nrows * (D / 2);
     const bool direct = pc.npieces == 1;
     for (int e = tid; e < total; e += Gm::W * 32) {
       const int r = e / (D / 2);
       const int d = 2 * (e % (D / 2));
-      float M = kNegInf;
-#pragma unroll
-      for (int w = 0; w < Gm::W; ++w) M = fmaxf(M, fml[(w * 8 + r) * 2]);
-      float a0 = 0.f, a1 = 0.f, L = 0.f;
+      float a0 = 0.f, a1 = 0.f;
 #pragma unroll
       for (int w = 0; w < Gm::W; ++w) {
-        const float mw = fml[(w * 8 + r) * 2];
-        const float sc = mw == kNegInf ? 0.f : exp2_approx(mw - M);
+        const float sc = fsc[w * 8 + r];
         const float2 v = *reinterpret_cast<const float2*>(facc + (w * 8 + r) * D + d);
         a0 += sc * v.x;
         a1 += sc * v.y;
-        L += sc * fml[(w * 8 + r) * 2 + 1];
       }
       const size_t row = (size_t)pc.b * p.Hq + first_head + r;
       if (direct) {
-        const float o0 = L > 0.f ? a0 / L : 0.f;
-        const float o1 = L > 0.f ? a1 / L : 0.f;
-        *reinterpret_cast<uint32_t*>(p.out + row * D + d) = pack_bf16x2(o0, o1);
+        const float inv = frow[r * 4 + 2];
+        *reinterpret_cast<uint32_t*>(p.out + row * D + d) = pack_bf16x2(a0 * inv, a1 * inv);
       } else {
         const size_t slot = row * p.S + pc.j;
         *reinterpret_cast<float2*>(p.part_acc + slot * D + d) = make_float2(a0, a1);
-        if (d == 0) *reinterpret_cast<float2*>(p.part_ml + slot * 2) = make_float2(M * 0.69314718055994531f, L);
+        if (d == 0)
+          *reinterpret_cast<float2*>(p.part_ml + slot * 2) =
+              make_float2(frow[r * 4] * 0.69314718055994531f, frow[r * 4 + 1]);
+      }
+    }
+    if (!direct && pc.npieces <= kFusedMergeMax) {
+      // publish this piece; the CTA that completes the segment merges it
+      __threadfence();
+      named_bar_sync(1, Gm::W * 32);
+      volatile int* last = reinterpret_cast<volatile int*>(smem + Gm::OFF_MISC) + 1;
+      if (tid == 0) *last = claim_last_piece(p.seg_counters + (size_t)pc.b * p.U + pc.u, p.epoch, pc.npieces);
+      named_bar_sync(1, Gm::W * 32);
+      if (*last) {
+        __threadfence();
+        merge_segment<D>(p, pc.b, first_head, nrows, pc.npieces, fsc);
       }
     }
     named_bar_sync(1, Gm::W * 32);
@@ -455,7 +591,8 @@ __global__ void __launch_bounds__(SplitGeo<D>::NTHREADS, 1) split_kernel(const _
     prefetch_tensormap(&p.tm_v);
     prefetch_tensormap(&p.tm_q);
   }
-  // The combine kernel may start launching now; it waits for this grid to finish.
+  // The combine kernel (launched only when a segment can have more than 8 pieces)
+  // may start now; it waits on the device for this grid to finish.
   pdl_launch_dependents();
   build_plan_arrays(p.seq_lens, p.B, p.max_len, lens, P);
   const Plan pl = make_plan(p.B, p.U, p.S, P);

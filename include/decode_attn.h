@@ -38,12 +38,16 @@
  * Segment (b, u) covers blocks [U*P_b + u*n_b, U*P_b + (u+1)*n_b) of one global
  * block line, P_b = n_0 + ... + n_{b-1}, NB = U * P_B blocks in all.
  *   num_splits == 1: every segment is computed whole and written directly.
- *   num_splits >= 2: the line is cut into R = (num_splits - 1) * U ranges of
- *     q = max(1, ceil(NB / R)) blocks; each range is one CTA's work; the pieces of
+ *   num_splits >= 2: the line is cut into ranges of q blocks, q = ceil(NB / R) with
+ *     R = (num_splits - 1) * U, rounded up to a multiple of 4 blocks (whole 64-token
+ *     tiles); each range is one CTA's work; the pieces of
  *     a segment are its intersections with the ranges (index j = r - floor(start/q)),
  *     at most num_splits of them.  A segment with one piece is written directly;
- *     one with several leaves partials in slots j = 0..pieces-1 and is merged by
- *     the combine kernel; an empty sequence (L_b == 0) gets a zero output.
+ *     one with several leaves partials in slots j = 0..pieces-1, which are merged
+ *     into the output by the CTA that finishes its last piece (found with the
+ *     segment's counter) when there are at most 8, else by a combine kernel that
+ *     follows as a programmatic dependent launch; an empty sequence (L_b == 0)
+ *     gets a zero output.
  */
 #ifndef DECODE_ATTN_H
 #define DECODE_ATTN_H
@@ -56,7 +60,7 @@ typedef enum {
   DA_OK = 0,
   DA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, negative size, Hq % Hkv != 0, ... */
   DA_ERR_UNSUPPORTED = 2,  /* head_dim, page_size, group size or batch outside the built kernels */
-  DA_ERR_WORKSPACE = 3,    /* num_splits >= 2 but part_acc / part_ml missing */
+  DA_ERR_WORKSPACE = 3,    /* num_splits >= 2 but part_acc / part_ml / seg_counters missing */
   DA_ERR_CUDA = 4,         /* a CUDA call or launch failed (error cleared) */
   DA_ERR_TIMEOUT = 5       /* a kernel gave up on a bounded wait (see decode_device_error) */
 } da_status;
@@ -90,14 +94,19 @@ int decode_num_splits(int batch, int num_kv_heads, int max_seq_len, int head_dim
  *           natural-log units of the scaled score: caller-owned scratch, unused
  *           (may be NULL) when num_splits == 1.  Slots the plan does not use are not
  *           written.
+ *  seg_counters  uint64 [batch * num_kv_heads * ceil(G / 8)]: caller-owned, zeroed
+ *           once before the first call and then reusable by every later call
+ *           (each call tags its updates, so no reset is needed, even after a
+ *           failed call); unused (may be NULL) when num_splits == 1.  Calls that
+ *           share partial buffers or counters must not overlap on the GPU.
  *  out      bf16 [batch, num_q_heads, head_dim]
  *  stream   cudaStream_t
- * Enqueues the split kernel and, when num_splits >= 2, the combine kernel.
+ * Enqueues the split kernel, and the combine kernel when num_splits > 8.
  */
 int decode_attn_contig(const void* q, const void* k, const void* v, const int* seq_lens,
                        int batch, int num_q_heads, int num_kv_heads, int head_dim, int max_ctx,
                        float scale, int num_splits, float* part_acc, float* part_ml,
-                       void* out, void* stream);
+                       unsigned long long* seg_counters, void* out, void* stream);
 
 /*
  * decode_attn_paged — decode attention over a paged cache.
@@ -117,7 +126,7 @@ int decode_attn_paged(const void* q, const void* k_pool, const void* v_pool,
                       int batch, int num_q_heads, int num_kv_heads, int head_dim,
                       int page_size, int max_pages_per_seq, int num_pages, int max_seq_len,
                       float scale, int num_splits, float* part_acc, float* part_ml,
-                      void* out, void* stream);
+                      unsigned long long* seg_counters, void* out, void* stream);
 
 /*
  * decode_combine — stand-alone log-sum-exp merge of split partials.
@@ -142,10 +151,10 @@ int decode_combine(const float* part_acc, const float* part_ml, int batch, int n
  * that must not call cudaMalloc between steps).  Arguments are those of
  * decode_attn_contig without num_splits, part_acc and part_ml: the split count is
  * decode_num_splits(batch, num_kv_heads, max_ctx, head_dim, <SMs of the device>)
- * and the partials live in an 8 MiB array inside the library (every GPU that loads
- * the library holds it until exit).  Shapes whose partials need more than
- * 8 MiB (batch * num_q_heads * S * (head_dim + 2) * 4 bytes, plus alignment)
- * return DA_ERR_WORKSPACE and launch nothing.  The first call on a device looks
+ * and the partials and segment counters live in an 8 MiB array inside the library
+ * (every GPU that loads the library holds it until exit).  Shapes that need more
+ * than 8 MiB (batch * num_q_heads * S * (head_dim + 2) * 4 bytes of partials plus
+ * 8 bytes per segment, plus alignment) return DA_ERR_WORKSPACE and launch nothing.  The first call on a device looks
  * up the array's device address (no allocation); make that first call before any
  * stream capture.  Calls share the array: calls that overlap on the GPU race.
  * Calls no cudaMalloc, cudaFree or allocating library routine.

@@ -248,8 +248,9 @@ def split_pieces(seq_lens: Sequence[int], Hkv: int, G: int, num_splits: int):
     where P_b = n_0 + ... + n_{b-1}.  NB = U * P_B blocks in total.
 
     num_splits == 1: every segment is one piece.
-    num_splits >= 2: the block line is cut into R = (num_splits - 1) * U ranges of
-    q = max(1, ceil(NB / R)) blocks; range r = [r q, (r + 1) q).  A segment's pieces
+    num_splits >= 2: the block line is cut into ranges of q blocks, q = ceil(NB / R)
+    with R = (num_splits - 1) * U, rounded up to a multiple of 4 blocks (ranges hold
+    whole 64-token tiles), at least 4; range r = [r q, (r + 1) q).  A segment's pieces
     are its non-empty intersections with the ranges, in order; piece index
     j = r - floor(start / q).  This never gives a segment more than num_splits pieces.
 
@@ -273,7 +274,7 @@ def split_pieces(seq_lens: Sequence[int], Hkv: int, G: int, num_splits: int):
         P.append(P[-1] + n)
     NB = U * P[-1]
     R = (num_splits - 1) * U
-    q = max(1, -(-NB // R))
+    q = max(4, -(-max(1, -(-NB // R)) // 4) * 4)
     for b, L in enumerate(lens):
         for u in range(U):
             start = U * P[b] + u * nblk[b]

@@ -37,7 +37,8 @@ def num_splits_for(inp: dict) -> int:
     return binding.num_splits(q.shape[0], Hkv, max_len, q.shape[2])
 
 
-def run(inp: dict, S: int = None, lens_null: bool = False, dev_inputs: dict = None, max_seq_len: int = None):
+def run(inp: dict, S: int = None, lens_null: bool = False, dev_inputs: dict = None, max_seq_len: int = None,
+        counters=None):
     """One library call on inp; returns (out bits, part_acc, part_ml, S) as numpy."""
     if S is None:
         S = num_splits_for(inp)
@@ -46,13 +47,16 @@ def run(inp: dict, S: int = None, lens_null: bool = False, dev_inputs: dict = No
     acc = torch.full((B, Hq, max(S, 1), D), float("nan"), dtype=torch.float32, device="cuda")
     ml = torch.full((B, Hq, max(S, 1), 2), float("nan"), dtype=torch.float32, device="cuda")
     out = torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    Hkv = (inp["k"] if "k" in inp else inp["k_pool"]).shape[2]
+    ctr = counters if counters is not None else torch.zeros(binding.counters_len(B, Hq, Hkv), dtype=torch.int64,
+                                                            device="cuda")
     if "k" in inp:
         binding.decode_attn_contig(d["q"], d["k"], d["v"], None if lens_null else d["seq_lens"], scale=inp["scale"],
-                                   splits=S, part_acc=acc, part_ml=ml, out=out)
+                                   splits=S, part_acc=acc, part_ml=ml, seg_counters=ctr, out=out)
     else:
         msl = max_seq_len if max_seq_len is not None else inp["page_table"].shape[1] * inp["page_size"]
         binding.decode_attn_paged(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["seq_lens"], msl,
-                                  scale=inp["scale"], splits=S, part_acc=acc, part_ml=ml, out=out)
+                                  scale=inp["scale"], splits=S, part_acc=acc, part_ml=ml, seg_counters=ctr, out=out)
     torch.cuda.synchronize()
     assert binding.device_error() == 0, "a kernel gave up on a bounded wait"
     return host_bits(out), acc.cpu().numpy(), ml.cpu().numpy(), S

@@ -66,13 +66,14 @@ def test_num_splits_rejects_bad_shapes(clib):
 A = 0x10000  # a fake 16-byte-aligned address: never dereferenced by rejected calls
 
 
-def contig(clib, q=A, k=A, v=A, lens=None, B=1, Hq=8, Hkv=2, D=64, ctx=64, scale=0.125, S=2, pa=A, pm=A, out=A):
-    return clib.decode_attn_contig(q, k, v, lens, B, Hq, Hkv, D, ctx, scale, S, pa, pm, out, None)
+def contig(clib, q=A, k=A, v=A, lens=None, B=1, Hq=8, Hkv=2, D=64, ctx=64, scale=0.125, S=2, pa=A, pm=A, ctr=A,
+           out=A):
+    return clib.decode_attn_contig(q, k, v, lens, B, Hq, Hkv, D, ctx, scale, S, pa, pm, ctr, out, None)
 
 
-def paged(clib, ps=16, lens=A, table=A, D=64, S=2, maxp=4, npages=4, maxlen=64, pa=A, pm=A):
-    return clib.decode_attn_paged(A, A, A, table, lens, 1, 8, 2, D, ps, maxp, npages, maxlen, 0.125, S, pa, pm, A,
-                                  None)
+def paged(clib, ps=16, lens=A, table=A, D=64, S=2, maxp=4, npages=4, maxlen=64, pa=A, pm=A, ctr=A):
+    return clib.decode_attn_paged(A, A, A, table, lens, 1, 8, 2, D, ps, maxp, npages, maxlen, 0.125, S, pa, pm, ctr,
+                                  A, None)
 
 
 def test_contig_argument_errors(clib):
@@ -84,6 +85,8 @@ def test_contig_argument_errors(clib):
     assert contig(clib, S=1025) == 1
     assert contig(clib, pa=None) == 3                     # partial slots missing
     assert contig(clib, pm=None) == 3
+    assert contig(clib, ctr=None) == 3
+    assert contig(clib, ctr=A + 4) == 1
     assert contig(clib, q=A + 2) == 1                     # misaligned
     assert contig(clib, out=A + 8) == 1
     assert contig(clib, k=A + 4) == 1
@@ -108,6 +111,7 @@ def test_paged_argument_errors(clib):
     assert paged(clib, table=A + 2) == 1
     assert paged(clib, D=100) == 2
     assert paged(clib, pa=None) == 3
+    assert paged(clib, ctr=None) == 3
     assert paged(clib, maxp=-1) == 1
     assert paged(clib, maxlen=-3) == 1
 

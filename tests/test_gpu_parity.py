@@ -152,3 +152,20 @@ def test_combine_alone_matches_oracle_merge():
     from gpu_helpers import host_bits
     check_out(host_bits(out), want, "combine")
     assert np.all(host_bits(out)[2] == 0)
+
+
+def test_counters_are_reused_without_reset():
+    """Segment counters are zeroed once; later calls (any shape) reuse them as they are."""
+    from gqa_split_kv_gb300 import binding
+    inp = contig_case(14, 3, 16, 4, 128, ctx=1500, lens=[1500, 900, 20])
+    ref = oracle.decode_contig(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["scale"])
+    ctr = torch.zeros(binding.counters_len(3, 16, 4), dtype=torch.int64, device="cuda")
+    first = run(inp, 9, counters=ctr)[0]
+    check_out(first, ref, "first")
+    other = contig_case(15, 2, 16, 4, 128, ctx=700, lens=[700, 300])  # another shape on the same counters
+    run(other, 5, counters=ctr)
+    for _ in range(2):
+        assert np.array_equal(run(inp, 9, counters=ctr)[0], first)
+    # counters left with arbitrary values by someone else
+    ctr.copy_(torch.randint(0, 2 ** 31, ctr.shape, device="cuda"))
+    assert np.array_equal(run(inp, 9, counters=ctr)[0], first)

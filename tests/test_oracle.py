@@ -291,7 +291,7 @@ def test_split_rule_matches_block_by_block_brute_force():
             for u in range(U):
                 line += [(b, u, i) for i in range(n)]
         R = (S - 1) * U
-        q = max(1, -(-len(line) // R))
+        q = max(4, -(-max(1, -(-len(line) // R)) // 4) * 4)
         want = {}
         for x, (b, u, i) in enumerate(line):
             want.setdefault((b, u, x // q), []).append(i)
@@ -360,9 +360,9 @@ def _pins(monkey_od):
     """A small battery of the checks above, run against a (possibly mutated) oracle."""
     torch = pytest.importorskip("torch")
     rng = np.random.default_rng(99)
-    inp = _contig_case(rng, 2, 6, 2, 16, ctx=24, lens=[24, 11], kstd=2.0)
+    inp = _contig_case(rng, 2, 6, 2, 16, ctx=200, lens=[200, 11], kstd=2.0)
     out = monkey_od.decode_contig(**inp)
-    for b, L in enumerate([24, 11]):
+    for b, L in enumerate([200, 11]):
         q = torch.from_numpy(od.widen_bf16(inp["q"][b]))[None, :, None, :]
         k = torch.from_numpy(od.widen_bf16(inp["k"][b, :L])).permute(1, 0, 2)[None].repeat_interleave(3, 1)
         v = torch.from_numpy(od.widen_bf16(inp["v"][b, :L])).permute(1, 0, 2)[None].repeat_interleave(3, 1)
@@ -370,6 +370,7 @@ def _pins(monkey_od):
         if not np.allclose(out[b], ref, rtol=0, atol=1e-12):
             return False
     acc, ml, npc = monkey_od.decode_partials(inp, 5)
+    assert npc.max() >= 2  # the merge must be exercised
     for b in range(2):
         for h in range(6):
             parts = [(acc[b, h, j][None], ml[b, h, j, :1], ml[b, h, j, 1:]) for j in range(npc[b, h])]
