@@ -47,10 +47,11 @@ struct CombineGeo {
   static constexpr int JL = NTHREADS / TPS;       // slot lanes
   static constexpr int KB = 4;                    // slot loads in flight per thread
   // shared: plan arrays (2B+1 ints) | weights (S floats) | lane sums (NTHREADS float4) | misc (32 floats)
-  //         | row list (1 + 2 NTHREADS ints)
+  //         | row list (1 + 2 CLS ints)
+  static constexpr int CLS = 128;                 // rows classified per round
   static int smem_bytes(int B, int S, bool planned) {
     return ((planned ? (2 * B + 1) * 4 : 0) + 15) / 16 * 16 + ((S * 4 + 15) / 16) * 16 + NTHREADS * 16 + 128 +
-           (1 + 2 * NTHREADS) * 4;
+           (1 + 2 * CLS) * 4;
   }
 };
 
@@ -77,12 +78,12 @@ __global__ void __launch_bounds__(512) combine_kernel(const CombineParams p) {
   const int jl = tid / Cg::TPS, c4 = tid % Cg::TPS;
   const float kNegInf = -__int_as_float(0x7f800000);
   const int rows = p.B * p.Hq;
-  int* todo = reinterpret_cast<int*>(red + 32);  // [0] count, [1..NTHREADS] (row, n) pairs packed
-  for (int base = blockIdx.x; base < rows; base += Cg::NTHREADS * gridDim.x) {
-    // each thread classifies one of this CTA's rows; rows to merge go to a list
+  int* todo = reinterpret_cast<int*>(red + 32);  // [0] count, then (row, n) pairs
+  for (int base = blockIdx.x; base < rows; base += Cg::CLS * gridDim.x) {
+    // CLS threads classify one of this CTA's rows each; rows to merge go to a list
     if (tid == 0) todo[0] = 0;
     __syncthreads();
-    {
+    if (tid < Cg::CLS) {
       const int row = base + tid * gridDim.x;
       if (row < rows) {
         int n = p.S;

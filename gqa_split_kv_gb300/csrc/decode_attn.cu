@@ -340,12 +340,14 @@ extern "C" int decode_attn_contig(const void* q, const void* k, const void* v, c
   int dev, sms, smem_optin;
   if (current_device(&dev) || device_info(dev, &sms, &smem_optin)) return DA_ERR_CUDA;
 
+  // dims (swizzle row, token, swizzle column, head, batch): one box fills every
+  // swizzle column of T tokens of one head, [D/SW][T][SW] in shared memory
   const int SW = sub_width(D);
   const cuuint64_t row = (cuuint64_t)Hkv * D * 2;
-  const cuuint64_t dims[5] = {(cuuint64_t)SW, (cuuint64_t)(D / SW), (cuuint64_t)Hkv, (cuuint64_t)max_ctx,
+  const cuuint64_t dims[5] = {(cuuint64_t)SW, (cuuint64_t)max_ctx, (cuuint64_t)(D / SW), (cuuint64_t)Hkv,
                               (cuuint64_t)B};
-  const cuuint64_t strides[4] = {(cuuint64_t)SW * 2, (cuuint64_t)D * 2, row, row * (cuuint64_t)max_ctx};
-  const cuuint32_t box[5] = {(cuuint32_t)SW, 1, 1, (cuuint32_t)tile_tokens(D), 1};
+  const cuuint64_t strides[4] = {row, (cuuint64_t)SW * 2, (cuuint64_t)D * 2, row * (cuuint64_t)max_ctx};
+  const cuuint32_t box[5] = {(cuuint32_t)SW, (cuuint32_t)tile_tokens(D), (cuuint32_t)(D / SW), 1, 1};
   CUtensorMap tk, tv;
   if (int e = encode_map(&tk, k, 5, dims, strides, box, D)) return e;
   if (int e = encode_map(&tv, v, 5, dims, strides, box, D)) return e;
@@ -393,12 +395,14 @@ extern "C" int decode_attn_paged(const void* q, const void* k_pool, const void* 
   int dev, sms, smem_optin;
   if (current_device(&dev) || device_info(dev, &sms, &smem_optin)) return DA_ERR_CUDA;
 
+  // dims (swizzle row, row in page, swizzle column, head, page): one box fills every
+  // swizzle column of a 16-token block, [D/SW][16][SW] in shared memory
   const int SW = sub_width(D);
   const cuuint64_t row = (cuuint64_t)Hkv * D * 2;
-  const cuuint64_t dims[5] = {(cuuint64_t)SW, (cuuint64_t)(D / SW), (cuuint64_t)Hkv, (cuuint64_t)page_size,
+  const cuuint64_t dims[5] = {(cuuint64_t)SW, (cuuint64_t)page_size, (cuuint64_t)(D / SW), (cuuint64_t)Hkv,
                               (cuuint64_t)num_pages};
-  const cuuint64_t strides[4] = {(cuuint64_t)SW * 2, (cuuint64_t)D * 2, row, row * (cuuint64_t)page_size};
-  const cuuint32_t box[5] = {(cuuint32_t)SW, 1, 1, 16, 1};
+  const cuuint64_t strides[4] = {row, (cuuint64_t)SW * 2, (cuuint64_t)D * 2, row * (cuuint64_t)page_size};
+  const cuuint32_t box[5] = {(cuuint32_t)SW, 16, (cuuint32_t)(D / SW), 1, 1};
   CUtensorMap tk, tv;
   if (int e = encode_map(&tk, k_pool, 5, dims, strides, box, D)) return e;
   if (int e = encode_map(&tv, v_pool, 5, dims, strides, box, D)) return e;

@@ -78,7 +78,11 @@ struct SplitGeo {
   static constexpr int ROWB = SUBW * 2;             // 128 or 64 bytes
   static constexpr int CPR = SUBW / 8;              // 16-byte chunks per swizzle row
   static constexpr int STAGES = D == 256 ? 2 : D == 128 ? 4 : 5;
-  static constexpr int SUB_BYTES = T * ROWB;        // one swizzle column of a tile
+  static constexpr int FD = D >= 128 ? 64 : D;  // fold scratch columns per pass
+  static constexpr int SUB_BYTES = T * ROWB;        // one swizzle column of a contiguous tile
+  // One TMA box fills all NSUB swizzle columns of its rows: a contiguous tile is
+  // [NSUB][T][SUBW]; a paged tile is block-major, [T/16][NSUB][16][SUBW].
+  static constexpr int BLK_BYTES = 16 * D * 2;      // one 16-token block of one tensor
   static constexpr int KV_BYTES = T * D * 2;        // one tensor, one stage
   static constexpr int Q_SUB_BYTES = 8 * ROWB;
   static constexpr int Q_BYTES = 8 * D * 2;
@@ -88,7 +92,7 @@ struct SplitGeo {
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_Q = OFF_V + STAGES * KV_BYTES;
   static constexpr int OFF_FACC = OFF_Q + STAGES * Q_BYTES;
-  static constexpr int OFF_FML = OFF_FACC + W * 8 * D * 4;
+  static constexpr int OFF_FML = OFF_FACC + W * 8 * FD * 4;
   static constexpr int OFF_FSC = OFF_FML + W * 8 * 2 * 4;   // per-(warp, row) merge weights
   static constexpr int OFF_FROW = OFF_FSC + W * 8 * 4;      // per-row (M, L, 1/L, -)
   static constexpr int OFF_BAR = OFF_FROW + 8 * 4 * 4;
@@ -98,6 +102,7 @@ struct SplitGeo {
   static constexpr int smem_bytes(int B) { return OFF_PLAN + (2 * B + 1) * 4 + 1024; }
   static_assert(SB % W == 0 && SB <= 32, "whole sub-blocks per warp; one producer lane per block");
   static_assert(RING >= LA + 2, "page ring must hold the prefetch window");
+  static_assert(smem_bytes(64) <= 227 * 1024, "shared memory budget");
 };
 
 template <int ROWB>
@@ -232,19 +237,13 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
       if (lane < nblk) {
         const int tok = cur.t + 16 * lane;
         const int row0 = tok % p.page_size;
-#pragma unroll
-        for (int sub = 0; sub < Gm::NSUB; ++sub) {
-          const uint32_t off = (uint32_t)(sub * Gm::SUB_BYTES + lane * 16 * Gm::ROWB);
-          tma_load_5d(kdst + off, &p.tm_k, full, 0, sub, h, row0, page);
-          tma_load_5d(vdst + off, &p.tm_v, full, 0, sub, h, row0, page);
-        }
+        const uint32_t off = (uint32_t)(lane * Gm::BLK_BYTES);
+        tma_load_5d(kdst + off, &p.tm_k, full, 0, row0, 0, h, page);
+        tma_load_5d(vdst + off, &p.tm_v, full, 0, row0, 0, h, page);
       }
     } else if (lane == 0) {
-#pragma unroll
-      for (int sub = 0; sub < Gm::NSUB; ++sub) {
-        tma_load_5d(kdst + sub * Gm::SUB_BYTES, &p.tm_k, full, 0, sub, h, cur.t, pc.b);
-        tma_load_5d(vdst + sub * Gm::SUB_BYTES, &p.tm_v, full, 0, sub, h, cur.t, pc.b);
-      }
+      tma_load_5d(kdst, &p.tm_k, full, 0, cur.t, 0, h, pc.b);
+      tma_load_5d(vdst, &p.tm_v, full, 0, cur.t, 0, h, pc.b);
     }
     if (first_tile && lane == 0) {
 #pragma unroll
@@ -346,7 +345,7 @@ __device__ __forceinline__ void merge_segment(const SplitParams& p, int b, int f
   }
 }
 
-template <int D>
+template <int D, bool PAGED>
 __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan& pl, const int* lens, const int* P,
                                                uint8_t* smem, uint32_t sbase, volatile int* abort_flag) {
   using Gm = SplitGeo<D>;
@@ -362,6 +361,9 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
   float* fml = reinterpret_cast<float*>(smem + Gm::OFF_FML);
   const float kNegInf = -__int_as_float(0x7f800000);
 
+  // shared-memory strides of a 16-token block and of a swizzle column (see SplitGeo)
+  constexpr int BLK_STRIDE = PAGED ? Gm::NSUB * 16 * Gm::ROWB : 16 * Gm::ROWB;
+  constexpr int COL_STRIDE = PAGED ? 16 * Gm::ROWB : Gm::SUB_BYTES;
   // ldmatrix lane -> (row, chunk) patterns
   const int k_row0 = (lane & 7) + ((lane >> 4) << 3);
   const int k_chk = (lane >> 3) & 1;
@@ -415,8 +417,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
       for (int sb = 0; sb < Gm::SBW; ++sb) {
         const int kb = warp + Gm::W * sb;  // sub-block of the tile owned by this warp
         const int tok0 = t + 16 * kb;
-        const int k_row = 16 * kb + k_row0;
-        const int v_row = 16 * kb + v_row0;
+        const uint32_t blk = (uint32_t)(kb * BLK_STRIDE);
         if (tok0 < pc.t1) {
           const uint32_t kst = sbase + Gm::OFF_K + stage * Gm::KV_BYTES;
           const uint32_t vst = sbase + Gm::OFF_V + stage * Gm::KV_BYTES;
@@ -425,7 +426,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
           for (int kk = 0; kk < KCH; ++kk) {
             const int c = 2 * kk + k_chk;
             uint32_t b0, b1, b2, b3;
-            ldsm_x4(kst + (c / Gm::CPR) * Gm::SUB_BYTES + swz<Gm::ROWB>(k_row, c % Gm::CPR), b0, b1, b2, b3);
+            ldsm_x4(kst + blk + (c / Gm::CPR) * COL_STRIDE + swz<Gm::ROWB>(k_row0, c % Gm::CPR), b0, b1, b2, b3);
             mma_bf16_16816(s0, qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
             mma_bf16_16816(s1, qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
           }
@@ -468,7 +469,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
           for (int c2 = 0; c2 < NB8 / 2; ++c2) {
             const int c = 2 * c2 + v_chk;
             uint32_t v0, v1, v2, v3;
-            ldsm_x4_t(vst + (c / Gm::CPR) * Gm::SUB_BYTES + swz<Gm::ROWB>(v_row, c % Gm::CPR), v0, v1, v2, v3);
+            ldsm_x4_t(vst + blk + (c / Gm::CPR) * COL_STRIDE + swz<Gm::ROWB>(v_row0, c % Gm::CPR), v0, v1, v2, v3);
             if (tail) {
               v0 &= vm_lo;
               v1 &= vm_hi;
@@ -488,65 +489,73 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
       }
     }
 
-    // ---- fold the W warps' (m, l, acc) in ascending warp order, then write
+    // ---- fold the W warps' (m, l, acc) in ascending warp order, then write.  The
+    // scratch holds FD columns per warp and row; wider heads fold in D / FD passes.
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-    if (g < nrows) {
-      float* dst = facc + (warp * 8 + g) * D;
-#pragma unroll
-      for (int c = 0; c < NB8; ++c) {
-        *reinterpret_cast<float2*>(dst + 8 * c + 2 * i4) = make_float2(acc[c][0] + acc[c][2], acc[c][1] + acc[c][3]);
-      }
-      if (i4 == 0) {
-        fml[(warp * 8 + g) * 2 + 0] = m_run;
-        fml[(warp * 8 + g) * 2 + 1] = l_run;
-      }
+    if (g < nrows && i4 == 0) {
+      fml[(warp * 8 + g) * 2 + 0] = m_run;
+      fml[(warp * 8 + g) * 2 + 1] = l_run;
     }
-    named_bar_sync(1, Gm::W * 32);
     const int tid = threadIdx.x;
     float* fsc = reinterpret_cast<float*>(smem + Gm::OFF_FSC);
     float* frow = reinterpret_cast<float*>(smem + Gm::OFF_FROW);
-    if (tid < nrows) {  // one thread per row: the W warps' merge weights and the row's (M, L)
-      float M = kNegInf;
-#pragma unroll
-      for (int w = 0; w < Gm::W; ++w) M = fmaxf(M, fml[(w * 8 + tid) * 2]);
-      float L = 0.f;
-#pragma unroll
-      for (int w = 0; w < Gm::W; ++w) {
-        const float mw = fml[(w * 8 + tid) * 2];
-        const float sc = mw == kNegInf ? 0.f : exp2_approx(mw - M);
-        fsc[w * 8 + tid] = sc;
-        L += sc * fml[(w * 8 + tid) * 2 + 1];
-      }
-      frow[tid * 4 + 0] = M;
-      frow[tid * 4 + 1] = L;
-      frow[tid * 4 + 2] = L > 0.f ? 1.f / L : 0.f;
-    }
-    named_bar_sync(1, Gm::W * 32);
-    const int total = nrows * (D / 2);
     const bool direct = pc.npieces == 1;
-    for (int e = tid; e < total; e += Gm::W * 32) {
-      const int r = e / (D / 2);
-      const int d = 2 * (e % (D / 2));
-      float a0 = 0.f, a1 = 0.f;
+    constexpr int FD = Gm::FD;
 #pragma unroll
-      for (int w = 0; w < Gm::W; ++w) {
-        const float sc = fsc[w * 8 + r];
-        const float2 v = *reinterpret_cast<const float2*>(facc + (w * 8 + r) * D + d);
-        a0 += sc * v.x;
-        a1 += sc * v.y;
+    for (int pass = 0; pass < D / FD; ++pass) {
+      if (g < nrows) {
+        float* dst = facc + (warp * 8 + g) * FD;
+#pragma unroll
+        for (int c = pass * (FD / 8); c < (pass + 1) * (FD / 8); ++c)
+          *reinterpret_cast<float2*>(dst + 8 * c - pass * FD + 2 * i4) =
+              make_float2(acc[c][0] + acc[c][2], acc[c][1] + acc[c][3]);
       }
-      const size_t row = (size_t)pc.b * p.Hq + first_head + r;
-      if (direct) {
-        const float inv = frow[r * 4 + 2];
-        *reinterpret_cast<uint32_t*>(p.out + row * D + d) = pack_bf16x2(a0 * inv, a1 * inv);
-      } else {
-        const size_t slot = row * p.S + pc.j;
-        *reinterpret_cast<float2*>(p.part_acc + slot * D + d) = make_float2(a0, a1);
-        if (d == 0)
-          *reinterpret_cast<float2*>(p.part_ml + slot * 2) =
-              make_float2(frow[r * 4] * 0.69314718055994531f, frow[r * 4 + 1]);
+      named_bar_sync(1, Gm::W * 32);
+      if (pass == 0) {
+        if (tid < nrows) {  // one thread per row: the W warps' merge weights and the row's (M, L)
+          float M = kNegInf;
+#pragma unroll
+          for (int w = 0; w < Gm::W; ++w) M = fmaxf(M, fml[(w * 8 + tid) * 2]);
+          float L = 0.f;
+#pragma unroll
+          for (int w = 0; w < Gm::W; ++w) {
+            const float mw = fml[(w * 8 + tid) * 2];
+            const float sc = mw == kNegInf ? 0.f : exp2_approx(mw - M);
+            fsc[w * 8 + tid] = sc;
+            L += sc * fml[(w * 8 + tid) * 2 + 1];
+          }
+          frow[tid * 4 + 0] = M;
+          frow[tid * 4 + 1] = L;
+          frow[tid * 4 + 2] = L > 0.f ? 1.f / L : 0.f;
+        }
+        named_bar_sync(1, Gm::W * 32);
       }
+      for (int e = tid; e < nrows * (FD / 2); e += Gm::W * 32) {
+        const int r = e / (FD / 2);
+        const int dl = 2 * (e % (FD / 2));
+        const int d = pass * FD + dl;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < Gm::W; ++w) {
+          const float sc = fsc[w * 8 + r];
+          const float2 v = *reinterpret_cast<const float2*>(facc + (w * 8 + r) * FD + dl);
+          a0 += sc * v.x;
+          a1 += sc * v.y;
+        }
+        const size_t row = (size_t)pc.b * p.Hq + first_head + r;
+        if (direct) {
+          const float inv = frow[r * 4 + 2];
+          *reinterpret_cast<uint32_t*>(p.out + row * D + d) = pack_bf16x2(a0 * inv, a1 * inv);
+        } else {
+          const size_t slot = row * p.S + pc.j;
+          *reinterpret_cast<float2*>(p.part_acc + slot * D + d) = make_float2(a0, a1);
+          if (d == 0)
+            *reinterpret_cast<float2*>(p.part_ml + slot * 2) =
+                make_float2(frow[r * 4] * 0.69314718055994531f, frow[r * 4 + 1]);
+        }
+      }
+      if (pass + 1 < D / FD) named_bar_sync(1, Gm::W * 32);  // scratch reused by the next pass
     }
     if (!direct && pc.npieces <= kFusedMergeMax) {
       // publish this piece; the CTA that completes the segment merges it
@@ -599,7 +608,7 @@ __global__ void __launch_bounds__(SplitGeo<D>::NTHREADS, 1) split_kernel(const _
   if (warp == Gm::W)
     split_producer<D, PAGED>(p, pl, lens, P, smem, sbase, abort_flag);
   else
-    split_consumer<D>(p, pl, lens, P, smem, sbase, abort_flag);
+    split_consumer<D, PAGED>(p, pl, lens, P, smem, sbase, abort_flag);
 }
 
 }  // namespace da
