@@ -5,8 +5,9 @@
 // flash-decode KV range across warp-groups", section "Mechanism"; the
 // partial/merge split of AstrAI commit 988e013 "csrc", split-KV items).
 //
-// The CTA's rows are classified one per thread; each row that needs merging is
-// then handled by the whole CTA, one at a time (grid-strided over rows).  All (m, l) of the row are
+// Work items are (row, 128-column chunk) pairs, grid-strided over CTAs; a CTA's
+// items are classified one per thread, and each item that needs merging is then
+// handled by the whole CTA, one at a time.  All (m, l) of the row are
 // loaded at once and reduced to M and the weights in shared memory; the slot x
 // column products are spread over the 512 threads (JL slot lanes x D/4 column
 // groups of 4), each thread keeping 8 loads in flight, so a row's loads overlap; the JL lane sums
@@ -43,25 +44,27 @@ struct CombineParams {
 template <int D>
 struct CombineGeo {
   static constexpr int NTHREADS = 512;
-  static constexpr int TPS = D / 4;               // threads per slot (4 columns each)
+  static constexpr int CW = D < 128 ? D : 128;    // columns per work item (a row has D / CW items)
+  static constexpr int NCH = D / CW;
+  static constexpr int TPS = CW / 4;              // threads per slot (4 columns each)
   static constexpr int JL = NTHREADS / TPS;       // slot lanes
   static constexpr int KB = 4;                    // slot loads in flight per thread
-  // shared: plan arrays (2B+1 ints) | weights (S floats) | lane sums (NTHREADS float4) | misc (32 floats)
+  // shared: plan arrays (2B+2 ints) | weights (S floats) | lane sums (NTHREADS float4) | misc (32 floats)
   //         | row list (1 + 2 CLS ints)
   static constexpr int CLS = 128;                 // rows classified per round
   static int smem_bytes(int B, int S, bool planned) {
-    return ((planned ? (2 * B + 1) * 4 : 0) + 15) / 16 * 16 + ((S * 4 + 15) / 16) * 16 + NTHREADS * 16 + 128 +
+    return ((planned ? (2 * B + 2) * 4 : 0) + 15) / 16 * 16 + ((S * 4 + 15) / 16) * 16 + NTHREADS * 16 + 128 +
            (1 + 2 * CLS) * 4;
   }
 };
 
 template <int D>
-__global__ void __launch_bounds__(512) combine_kernel(const CombineParams p) {
+__global__ void __maxnreg__(40) combine_kernel(const CombineParams p) {  // 512 threads; fits beside a split CTA
   using Cg = CombineGeo<D>;
   extern __shared__ __align__(16) uint8_t csm[];
   int* lens = reinterpret_cast<int*>(csm);
   int* P = lens + p.B;
-  const int plan_bytes = p.planned ? (2 * p.B + 1) * 4 : 0;
+  const int plan_bytes = p.planned ? (2 * p.B + 2) * 4 : 0;
   float* wts = reinterpret_cast<float*>(csm + ((plan_bytes + 15) / 16) * 16);
   float4* lane_sum = reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(wts) + ((p.S * 4 + 15) / 16) * 16);
   float* red = reinterpret_cast<float*>(lane_sum + Cg::NTHREADS);  // [17] den
@@ -77,15 +80,16 @@ __global__ void __launch_bounds__(512) combine_kernel(const CombineParams p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int jl = tid / Cg::TPS, c4 = tid % Cg::TPS;
   const float kNegInf = -__int_as_float(0x7f800000);
-  const int rows = p.B * p.Hq;
-  int* todo = reinterpret_cast<int*>(red + 32);  // [0] count, then (row, n) pairs
-  for (int base = blockIdx.x; base < rows; base += Cg::CLS * gridDim.x) {
-    // CLS threads classify one of this CTA's rows each; rows to merge go to a list
+  const int items = p.B * p.Hq * Cg::NCH;        // (row, column chunk) pairs
+  int* todo = reinterpret_cast<int*>(red + 32);  // [0] count, then (item, n) pairs
+  for (int base = blockIdx.x; base < items; base += Cg::CLS * gridDim.x) {
+    // CLS threads classify one of this CTA's items each; items to merge go to a list
     if (tid == 0) todo[0] = 0;
     __syncthreads();
     if (tid < Cg::CLS) {
-      const int row = base + tid * gridDim.x;
-      if (row < rows) {
+      const int item = base + tid * gridDim.x;
+      const int row = item / Cg::NCH;
+      if (item < items) {
         int n = p.S;
         if (p.planned) {
           const int b = row / p.Hq, h = row % p.Hq;
@@ -94,7 +98,7 @@ __global__ void __launch_bounds__(512) combine_kernel(const CombineParams p) {
         }
         if (!p.planned || n > kFusedMergeMax) {  // smaller segments were merged by the split kernel
           const int k = atomicAdd(&todo[0], 1);
-          todo[1 + 2 * k] = row;
+          todo[1 + 2 * k] = item;
           todo[2 + 2 * k] = n;
         }
       }
@@ -102,10 +106,12 @@ __global__ void __launch_bounds__(512) combine_kernel(const CombineParams p) {
     __syncthreads();
     const int count = todo[0];
     for (int it = 0; it < count; ++it) {
-      const int row = todo[1 + 2 * it];
+      const int item = todo[1 + 2 * it];
+      const int row = item / Cg::NCH;
+      const int col0 = (item % Cg::NCH) * Cg::CW;  // first column of this item
       const int n = todo[2 + 2 * it];
       const float* ml = p.part_ml + (size_t)row * p.S * 2;
-      const float4* acc = reinterpret_cast<const float4*>(p.part_acc + (size_t)row * p.S * D) + c4;
+      const float4* acc = reinterpret_cast<const float4*>(p.part_acc + (size_t)row * p.S * D + col0) + c4;
       // issue this thread's first KB slot loads before the weights are known
       float4 a[Cg::KB];
 #pragma unroll
@@ -170,7 +176,7 @@ __global__ void __launch_bounds__(512) combine_kernel(const CombineParams p) {
         uint2 o;
         o.x = pack_bf16x2(t.x * inv, t.y * inv);
         o.y = pack_bf16x2(t.z * inv, t.w * inv);
-        *reinterpret_cast<uint2*>(p.out + (size_t)row * D + 4 * c4) = o;
+        *reinterpret_cast<uint2*>(p.out + (size_t)row * D + col0 + 4 * c4) = o;
       }
       __syncthreads();
     }

@@ -147,8 +147,6 @@ int launch_split(const SplitParams& prm, int grid, int smem, int dev, cudaStream
   cfg.blockDim = dim3(SplitGeo<D>::NTHREADS);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = st;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
   if (cudaLaunchKernelEx(&cfg, kern, prm) != cudaSuccess) {
     cudaGetLastError();
     return DA_ERR_CUDA;
@@ -174,12 +172,12 @@ int launch_combine(const CombineParams& prm, int dev, int sms, cudaStream_t st, 
       attr_done[dev] = true;
     }
   }
-  // grid-strided over rows; after the split kernel one CTA per SM, so every CTA
+  // grid-strided over (row, column chunk) items; after the split kernel one CTA per SM, so every CTA
   // fits beside a split CTA, starts early and has its plan ready when the split
   // kernel completes; alone, a few CTAs per SM
-  const long long rows = (long long)prm.B * prm.Hq;
+  const long long items = (long long)prm.B * prm.Hq * CombineGeo<D>::NCH;
   const long long cap = (dependent ? 1LL : 4LL) * (sms > 0 ? sms : 1);
-  const long long grid = rows < cap ? rows : cap;
+  const long long grid = items < cap ? items : cap;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;

@@ -25,6 +25,7 @@ constexpr int kRangeQuantum = 4;  // ranges are whole 64-token tiles
 // by the CTA that finishes the last piece; longer ones by the combine kernel.
 constexpr int kFusedMergeMax = 8;
 
+
 // Block counts are 32-bit: the host rejects problems with 2^30 blocks or more.
 struct Plan {
   int NB;      // blocks on the line
@@ -41,7 +42,8 @@ struct Piece {
   int npieces;   // pieces of this segment
 };
 
-// lens[b] = clamp(seq_lens[b] or max_len, 0, max_len); P[0..B] = block prefix.
+// lens[b] = clamp(seq_lens[b] or max_len, 0, max_len); P[0..B] = block prefix;
+// P[B + 1] = the largest block count of one sequence.
 // Called by every thread of the block (contains __syncthreads).
 __device__ __forceinline__ void build_plan_arrays(const int* __restrict__ seq_lens, int B, int max_len, int* lens,
                                                   int* P) {
@@ -56,20 +58,28 @@ __device__ __forceinline__ void build_plan_arrays(const int* __restrict__ seq_le
     const int per = (B + 31) / 32;
     const int b0 = lane * per;
     const int b1 = min(B, b0 + per);
-    int s = 0;
-    for (int b = b0; b < b1; ++b) s += (lens[b] + kBlockTokens - 1) / kBlockTokens;
+    int s = 0, mx = 0;
+    for (int b = b0; b < b1; ++b) {
+      const int nb = (lens[b] + kBlockTokens - 1) / kBlockTokens;
+      s += nb;
+      mx = max(mx, nb);
+    }
     int incl = s;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int v = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += v;
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
     int run = incl - s;
     for (int b = b0; b < b1; ++b) {
       P[b] = run;
       run += (lens[b] + kBlockTokens - 1) / kBlockTokens;
     }
-    if (lane == 31) P[B] = incl;
+    if (lane == 31) {
+      P[B] = incl;
+      P[B + 1] = mx;
+    }
   }
   __syncthreads();
 }

@@ -72,13 +72,14 @@ struct SplitGeo {
   static constexpr int W = 4;                       // consumer warps
   static constexpr int SB = T / 16;                 // 16-token sub-blocks per tile
   static constexpr int SBW = SB / W;                // sub-blocks per warp: k = warp + W * i
+  static constexpr int NP = D <= 64 ? 2 : 1;        // sub-blocks per online-softmax step
   static constexpr int NTHREADS = (W + 1) * 32;
   static constexpr int SUBW = D >= 64 ? 64 : 32;    // elements per swizzle row
   static constexpr int NSUB = D / SUBW;             // swizzle rows per token
   static constexpr int ROWB = SUBW * 2;             // 128 or 64 bytes
   static constexpr int CPR = SUBW / 8;              // 16-byte chunks per swizzle row
   static constexpr int STAGES = D == 256 ? 2 : D == 128 ? 4 : 5;
-  static constexpr int FD = D >= 128 ? 64 : D;  // fold scratch columns per pass
+  static constexpr int FD = D;                      // fold scratch columns per pass (one pass)
   static constexpr int SUB_BYTES = T * ROWB;        // one swizzle column of a contiguous tile
   // One TMA box fills all NSUB swizzle columns of its rows: a contiguous tile is
   // [NSUB][T][SUBW]; a paged tile is block-major, [T/16][NSUB][16][SUBW].
@@ -99,8 +100,9 @@ struct SplitGeo {
   static constexpr int OFF_PG = OFF_BAR + 2 * STAGES * 8;
   static constexpr int OFF_MISC = OFF_PG + RING * 32 * 4;
   static constexpr int OFF_PLAN = OFF_MISC + 16;
-  static constexpr int smem_bytes(int B) { return OFF_PLAN + (2 * B + 1) * 4 + 1024; }
+  static constexpr int smem_bytes(int B) { return OFF_PLAN + (2 * B + 2) * 4 + 1024; }
   static_assert(SB % W == 0 && SB <= 32, "whole sub-blocks per warp; one producer lane per block");
+  static_assert(SBW % NP == 0, "softmax steps cover whole sub-blocks");
   static_assert(RING >= LA + 2, "page ring must hold the prefetch window");
   static_assert(smem_bytes(64) <= 227 * 1024, "shared memory budget");
 };
@@ -351,6 +353,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
   using Gm = SplitGeo<D>;
   constexpr int KCH = D / 16;  // k-chunks of the QK^T product
   constexpr int NB8 = D / 8;   // 8-column blocks of the PV product
+  constexpr int NP = Gm::NP;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;  // MMA row (query head within the group)
@@ -413,14 +416,20 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
           for (int c = 0; c < KCH; ++c) qa[c][0] = qa[c][1] = 0u;
         }
       }
+      const uint32_t kst = sbase + Gm::OFF_K + stage * Gm::KV_BYTES;
+      const uint32_t vst = sbase + Gm::OFF_V + stage * Gm::KV_BYTES;
 #pragma unroll 1
-      for (int sb = 0; sb < Gm::SBW; ++sb) {
-        const int kb = warp + Gm::W * sb;  // sub-block of the tile owned by this warp
-        const int tok0 = t + 16 * kb;
-        const uint32_t blk = (uint32_t)(kb * BLK_STRIDE);
-        if (tok0 < pc.t1) {
-          const uint32_t kst = sbase + Gm::OFF_K + stage * Gm::KV_BYTES;
-          const uint32_t vst = sbase + Gm::OFF_V + stage * Gm::KV_BYTES;
+      for (int sb = 0; sb < Gm::SBW; sb += NP) {
+        // NP sub-blocks of this warp share one online-softmax step
+        if (t + 16 * (warp + Gm::W * sb) >= pc.t1) break;  // later sub-blocks lie further out
+        float x[NP][4];
+        uint32_t vm_lo[NP], vm_hi[NP];
+        bool tail[NP];
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+          const int kb = warp + Gm::W * (sb + i);
+          const int tok0 = t + 16 * kb;
+          const uint32_t blk = (uint32_t)(kb * BLK_STRIDE);
           float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int kk = 0; kk < KCH; ++kk) {
@@ -430,51 +439,67 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
             mma_bf16_16816(s0, qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
             mma_bf16_16816(s1, qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
           }
-          float x0 = s0[0] * p.scale_log2, x1 = s0[1] * p.scale_log2;
-          float x2 = s1[0] * p.scale_log2, x3 = s1[1] * p.scale_log2;
-          const bool tail = tok0 + 16 > pc.t1;
-          uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
-          if (tail) {
+          x[i][0] = s0[0] * p.scale_log2;
+          x[i][1] = s0[1] * p.scale_log2;
+          x[i][2] = s1[0] * p.scale_log2;
+          x[i][3] = s1[1] * p.scale_log2;
+          // tokens at or past the piece end: score -inf, V row zeroed (its shared
+          // memory may hold anything, and 0 * NaN would poison the accumulator)
+          tail[i] = tok0 + 16 > pc.t1;
+          vm_lo[i] = vm_hi[i] = 0xffffffffu;
+          if (tail[i]) {
             const int ta = tok0 + 2 * i4, tb = tok0 + 8 + 2 * i4;
-            x0 = ta < pc.t1 ? x0 : kNegInf;
-            x1 = ta + 1 < pc.t1 ? x1 : kNegInf;
-            x2 = tb < pc.t1 ? x2 : kNegInf;
-            x3 = tb + 1 < pc.t1 ? x3 : kNegInf;
-            vm_lo = (ta < pc.t1 ? 0x0000ffffu : 0u) | (ta + 1 < pc.t1 ? 0xffff0000u : 0u);
-            vm_hi = (tb < pc.t1 ? 0x0000ffffu : 0u) | (tb + 1 < pc.t1 ? 0xffff0000u : 0u);
+            x[i][0] = ta < pc.t1 ? x[i][0] : kNegInf;
+            x[i][1] = ta + 1 < pc.t1 ? x[i][1] : kNegInf;
+            x[i][2] = tb < pc.t1 ? x[i][2] : kNegInf;
+            x[i][3] = tb + 1 < pc.t1 ? x[i][3] : kNegInf;
+            vm_lo[i] = (ta < pc.t1 ? 0x0000ffffu : 0u) | (ta + 1 < pc.t1 ? 0xffff0000u : 0u);
+            vm_hi[i] = (tb < pc.t1 ? 0x0000ffffu : 0u) | (tb + 1 < pc.t1 ? 0xffff0000u : 0u);
           }
-          float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          const float m_new = fmaxf(m_run, mx);
-          const float alpha = exp2_approx(m_run - m_new);
-          const float p0 = exp2_approx(x0 - m_new), p1 = exp2_approx(x1 - m_new);
-          const float p2 = exp2_approx(x2 - m_new), p3 = exp2_approx(x3 - m_new);
-          l_run = l_run * alpha + ((p0 + p1) + (p2 + p3));
-          if (__any_sync(0xffffffffu, m_new != m_run)) {
+        }
+        float mx = kNegInf;
 #pragma unroll
-            for (int c = 0; c < NB8; ++c) {
-              acc[c][0] *= alpha;
-              acc[c][1] *= alpha;
-              acc[c][2] *= alpha;
-              acc[c][3] *= alpha;
-            }
+        for (int i = 0; i < NP; ++i) mx = fmaxf(mx, fmaxf(fmaxf(x[i][0], x[i][1]), fmaxf(x[i][2], x[i][3])));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run, mx);
+        const float alpha = exp2_approx(m_run - m_new);
+        float pr[NP][4];
+        float psum = 0.f;
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) pr[i][k4] = exp2_approx(x[i][k4] - m_new);
+          psum += (pr[i][0] + pr[i][1]) + (pr[i][2] + pr[i][3]);
+        }
+        l_run = l_run * alpha + psum;
+        if (__any_sync(0xffffffffu, m_new != m_run)) {
+#pragma unroll
+          for (int c = 0; c < NB8; ++c) {
+            acc[c][0] *= alpha;
+            acc[c][1] *= alpha;
+            acc[c][2] *= alpha;
+            acc[c][3] *= alpha;
           }
-          m_run = m_new;
+        }
+        m_run = m_new;
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+          const uint32_t blk = (uint32_t)((warp + Gm::W * (sb + i)) * BLK_STRIDE);
           // P = hi + lo in bf16: rows g (hi) and g + 8 (lo) of the A operand
-          const uint32_t ph0 = pack_bf16x2(p0, p1), ph1 = pack_bf16x2(p2, p3);
-          const uint32_t pl0 = pack_bf16x2(p0 - bf16lo_to_f32(ph0), p1 - bf16hi_to_f32(ph0));
-          const uint32_t pl1 = pack_bf16x2(p2 - bf16lo_to_f32(ph1), p3 - bf16hi_to_f32(ph1));
+          const uint32_t ph0 = pack_bf16x2(pr[i][0], pr[i][1]), ph1 = pack_bf16x2(pr[i][2], pr[i][3]);
+          const uint32_t pl0 = pack_bf16x2(pr[i][0] - bf16lo_to_f32(ph0), pr[i][1] - bf16hi_to_f32(ph0));
+          const uint32_t pl1 = pack_bf16x2(pr[i][2] - bf16lo_to_f32(ph1), pr[i][3] - bf16hi_to_f32(ph1));
 #pragma unroll
           for (int c2 = 0; c2 < NB8 / 2; ++c2) {
             const int c = 2 * c2 + v_chk;
             uint32_t v0, v1, v2, v3;
             ldsm_x4_t(vst + blk + (c / Gm::CPR) * COL_STRIDE + swz<Gm::ROWB>(v_row0, c % Gm::CPR), v0, v1, v2, v3);
-            if (tail) {
-              v0 &= vm_lo;
-              v1 &= vm_hi;
-              v2 &= vm_lo;
-              v3 &= vm_hi;
+            if (tail[i]) {
+              v0 &= vm_lo[i];
+              v1 &= vm_hi[i];
+              v2 &= vm_lo[i];
+              v3 &= vm_hi[i];
             }
             mma_bf16_16816(acc[2 * c2], ph0, pl0, ph1, pl1, v0, v1);
             mma_bf16_16816(acc[2 * c2 + 1], ph0, pl0, ph1, pl1, v2, v3);
@@ -558,16 +583,18 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
       if (pass + 1 < D / FD) named_bar_sync(1, Gm::W * 32);  // scratch reused by the next pass
     }
     if (!direct && pc.npieces <= kFusedMergeMax) {
-      // publish this piece; the CTA that completes the segment merges it
-      __threadfence();
+      // publish this piece; the CTA that completes the segment merges it.  The
+      // barrier orders every consumer's partial stores before thread 0's gpu-scope
+      // fence, which releases them before the counter update.
       named_bar_sync(1, Gm::W * 32);
       volatile int* last = reinterpret_cast<volatile int*>(smem + Gm::OFF_MISC) + 1;
-      if (tid == 0) *last = claim_last_piece(p.seg_counters + (size_t)pc.b * p.U + pc.u, p.epoch, pc.npieces);
-      named_bar_sync(1, Gm::W * 32);
-      if (*last) {
+      if (tid == 0) {
         __threadfence();
-        merge_segment<D>(p, pc.b, first_head, nrows, pc.npieces, fsc);
+        *last = claim_last_piece(p.seg_counters + (size_t)pc.b * p.U + pc.u, p.epoch, pc.npieces);
+        if (*last) __threadfence();  // acquire: the other pieces' partials are read next
       }
+      named_bar_sync(1, Gm::W * 32);
+      if (*last) merge_segment<D>(p, pc.b, first_head, nrows, pc.npieces, fsc);
     }
     named_bar_sync(1, Gm::W * 32);
   }
