@@ -10,7 +10,7 @@
 // handled by the whole CTA, one at a time.  All (m, l) of the row are
 // loaded at once and reduced to M and the weights in shared memory; the slot x
 // column products are spread over the 512 threads (JL slot lanes x D/4 column
-// groups of 4), each thread keeping 8 loads in flight, so a row's loads overlap; the JL lane sums
+// groups of 4), each thread keeping KB loads in flight; the JL lane sums
 // are added in ascending lane order.  The summation order is fixed, so results
 // are bitwise reproducible.
 //
@@ -110,37 +110,32 @@ __global__ void __maxnreg__(40) combine_kernel(const CombineParams p) {  // 512 
       const int row = item / Cg::NCH;
       const int col0 = (item % Cg::NCH) * Cg::CW;  // first column of this item
       const int n = todo[2 + 2 * it];
-      const float* ml = p.part_ml + (size_t)row * p.S * 2;
+      const float2* ml = reinterpret_cast<const float2*>(p.part_ml + (size_t)row * p.S * 2);
       const float4* acc = reinterpret_cast<const float4*>(p.part_acc + (size_t)row * p.S * D + col0) + c4;
-      // issue this thread's first KB slot loads before the weights are known
+      // this thread's first KB slot loads go out first
       float4 a[Cg::KB];
 #pragma unroll
       for (int u = 0; u < Cg::KB; ++u) {
         const int j = jl + u * Cg::JL;
         a[u] = j < n ? acc[(size_t)j * (D / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      // warp 0: M over live slots, weights w_j = exp(m_j - M), den = sum_j w_j l_j (fixed shuffle tree)
-      if (warp == 0) {
-        float mloc = kNegInf;
-        for (int j = lane; j < n; j += 32) {
-          const float2 v = *reinterpret_cast<const float2*>(ml + 2 * j);
-          if (v.y > 0.f) mloc = fmaxf(mloc, v.x);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
-        float dloc = 0.f;
-        for (int j = lane; j < n; j += 32) {
-          const float2 v = *reinterpret_cast<const float2*>(ml + 2 * j);
-          const float w = v.y > 0.f ? expf(v.x - mloc) : 0.f;
-          wts[j] = w;
-          dloc += w * (v.y > 0.f ? v.y : 0.f);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) dloc += __shfl_xor_sync(0xffffffffu, dloc, o);
-        if (lane == 0) red[17] = dloc;
+      // every warp derives M and the denominator itself (same values in every warp:
+      // same loads, same butterfly order), so no barrier waits on them
+      float M = kNegInf;
+      for (int j = lane; j < n; j += 32) {
+        const float2 v = ml[j];
+        if (v.y > 0.f) M = fmaxf(M, v.x);
       }
-      __syncthreads();
-      // weighted column sums, slots strided over the JL lanes
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      float den = 0.f;
+      for (int j = lane; j < n; j += 32) {
+        const float2 v = ml[j];
+        if (v.y > 0.f) den += expf(v.x - M) * v.y;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+      // weighted column sums over this thread's slots (jl, jl + JL, ...)
       float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int j0 = jl; j0 < n; j0 += Cg::KB * Cg::JL) {
         if (j0 != jl) {
@@ -153,13 +148,18 @@ __global__ void __maxnreg__(40) combine_kernel(const CombineParams p) {  // 512 
 #pragma unroll
         for (int u = 0; u < Cg::KB; ++u) {
           const int j = j0 + u * Cg::JL;
-          const float w = j < n ? wts[j] : 0.f;
+          float w = 0.f;
+          if (j < n) {
+            const float2 v = ml[j];
+            w = v.y > 0.f ? expf(v.x - M) : 0.f;
+          }
           s.x += w * a[u].x;
           s.y += w * a[u].y;
           s.z += w * a[u].z;
           s.w += w * a[u].w;
         }
       }
+      if (tid == 0) red[17] = den;
       lane_sum[tid] = s;
       __syncthreads();
       if (jl == 0) {
