@@ -30,8 +30,12 @@ def _groups(G: int):
     return ng, gr
 
 
-def piece_counts(seq_lens, Hkv: int, G: int, S: int) -> np.ndarray:
-    """Pieces of every segment, shape [B, Hkv * ceil(G/8)]."""
+def piece_counts(seq_lens, Hkv: int, G: int, S: int, D: int) -> np.ndarray:
+    """Pieces of every segment, shape [B, Hkv * ceil(G/8)].
+
+    The library's split plan: segments lie end to end on one line, each taking
+    gap + n_b positions (gap = 2816 / D positions without blocks, then its
+    blocks); the line is cut into ranges of q positions."""
     lens = np.asarray(seq_lens, dtype=np.int64)
     ng, _ = _groups(G)
     U = Hkv * ng
@@ -39,11 +43,13 @@ def piece_counts(seq_lens, Hkv: int, G: int, S: int) -> np.ndarray:
     B = len(lens)
     if S == 1:
         return np.where(nblk[:, None] > 0, 1, 0) * np.ones((B, U), dtype=np.int64)
-    P = np.concatenate([[0], np.cumsum(nblk)])
+    gap = 2816 // D
+    w = np.where(nblk > 0, nblk + gap, 0)
+    P = np.concatenate([[0], np.cumsum(w)])
     NB = U * int(P[-1])
     R = (S - 1) * U
     q = max(4, -(-max(1, -(-NB // R)) // 4) * 4)
-    s0 = U * P[:-1, None] + np.arange(U)[None, :] * nblk[:, None]
+    s0 = U * P[:-1, None] + np.arange(U)[None, :] * w[:, None] + gap
     s1 = s0 + nblk[:, None]
     n = (s1 - 1) // q - s0 // q + 1
     return np.where(nblk[:, None] > 0, n, 0)
@@ -56,7 +62,7 @@ def traffic_bytes(B: int, Hq: int, Hkv: int, D: int, seq_lens, S: int, page_size
     kv = 2 * D * 2 * Hkv * int(lens.sum())
     q = B * Hq * D * 2
     out = B * Hq * D * 2
-    n = piece_counts(lens, Hkv, G, S)                      # [B, U]
+    n = piece_counts(lens, Hkv, G, S, D)                      # [B, U]
     # heads per sub-group slot u = h * ng + j
     heads = np.array([min(gr, G - (u % ng) * gr) for u in range(Hkv * ng)])
     part_rows = int(((n >= 2) * n * heads[None, :]).sum())

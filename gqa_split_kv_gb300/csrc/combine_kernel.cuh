@@ -72,8 +72,8 @@ __global__ void __maxnreg__(40) combine_kernel(const CombineParams p) {  // 512 
   Plan pl{};
   if (p.planned) {
     // seq_lens is not written by the split kernel: read it before waiting on it.
-    build_plan_arrays(p.seq_lens, p.B, p.max_len, lens, P);
-    pl = make_plan(p.B, p.U, p.S, P);
+    build_plan_arrays(p.seq_lens, p.B, p.max_len, plan_gap_blocks(D), lens, P);
+    pl = make_plan(p.B, p.U, p.S, plan_gap_blocks(D), P);
   }
   pdl_wait_primary();
 

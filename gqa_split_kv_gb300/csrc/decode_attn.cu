@@ -99,10 +99,12 @@ int sub_width(int D) { return D >= 64 ? 64 : 32; }
 
 // tokens per tile of the split kernel for head_dim D (the TMA box height of a contiguous cache)
 int tile_tokens(int D) {
-  static_assert(SplitGeo<32>::T == 256 && SplitGeo<64>::T == 128 && SplitGeo<128>::T == 64 &&
-                    SplitGeo<256>::T == 64,
-                "host and device tile sizes must agree");
-  return D == 32 ? 256 : D == 64 ? 128 : 64;
+  switch (D) {
+    case 32: return SplitGeo<32>::T;
+    case 64: return SplitGeo<64>::T;
+    case 128: return SplitGeo<128>::T;
+    default: return SplitGeo<256>::T;
+  }
 }
 
 // Query heads of one KV head are processed in ceil(G / 8) equal sub-groups.
@@ -233,8 +235,8 @@ int run_decode(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, in
 
   // one persistent CTA per SM, never more CTAs than ranges or blocks of work
   const long long nblk_max = (a.max_len + kBlockTokens - 1) / kBlockTokens;
-  if ((long long)a.B * prm.U * nblk_max >= (1LL << 30) || (long long)a.B * a.Hq >= (1LL << 30))
-    return DA_ERR_UNSUPPORTED;  // the device plan counts blocks in 32 bits
+  if ((long long)a.B * prm.U * (nblk_max + plan_gap_blocks(D)) >= (1LL << 30) || (long long)a.B * a.Hq >= (1LL << 30))
+    return DA_ERR_UNSUPPORTED;  // the device plan counts line positions in 32 bits
   long long ranges = a.S == 1 ? (long long)a.B * prm.U : (long long)(a.S - 1) * prm.U;
   const long long work = (long long)a.B * prm.U * (nblk_max > 0 ? nblk_max : 1);
   if (ranges > work) ranges = work;

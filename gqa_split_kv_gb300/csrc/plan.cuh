@@ -3,15 +3,23 @@
 //
 // The pages choose one split count for all sequences and cap it by the tile
 // count (AstrAI commit 988e013 "csrc", split-KV items).  This library instead
-// lays all segments end to end on one line of 16-token blocks and cuts the line
-// into equal ranges, so a persistent grid stays balanced for any mix of lengths.
+// lays all segments end to end on one weighted line and cuts the line into equal
+// ranges, so a persistent grid stays balanced for any mix of lengths.  Every
+// segment is preceded by a gap of c positions that stands for the fixed cost of
+// a piece (epilogue, partial tile, query load), so a range full of short
+// sequences holds fewer blocks than one inside a long sequence.
 //
 //   n_b  = ceil(L_b / 16)                     blocks of sequence b
-//   P_b  = n_0 + ... + n_{b-1}                (prefix, P_B = total)
+//   w_b  = n_b + c if n_b > 0, else 0         line positions of one segment
+//   c    = 2816 / head_dim                    (about 176 KB of K+V streaming)
+//   P_b  = w_0 + ... + w_{b-1}                (prefix, P_B = line length / U)
 //   U    = Hkv * ceil(G / 8)                  sub-group slots per sequence
-//   segment (b, u) = blocks [U P_b + u n_b, U P_b + (u + 1) n_b)
-//   S >= 2: q = ceil(U P_B / ((S - 1) U)) rounded up to a multiple of 4 blocks
-//           (whole 64-token tiles), range r = [r q, (r + 1) q)
+//   segment (b, u) = positions [s0, s0 + w_b), s0 = U P_b + u w_b; its blocks
+//                    sit at [s0 + c, s0 + c + n_b)
+//   S >= 2: q = ceil(U P_B / ((S - 1) U)) rounded up to a multiple of 4
+//           positions (at least 4), range r = [r q, (r + 1) q); a piece is the
+//           blocks of one segment inside one range (ranges that meet only a gap
+//           give none)
 //   S == 1: range r = segment (r / U, r % U), whole.
 #pragma once
 
@@ -25,14 +33,18 @@ constexpr int kRangeQuantum = 4;  // ranges are whole 64-token tiles
 // by the CTA that finishes the last piece; longer ones by the combine kernel.
 constexpr int kFusedMergeMax = 8;
 
+// Line positions charged to every segment for the fixed cost of a piece.
+__host__ __device__ constexpr int plan_gap_blocks(int head_dim) { return 2816 / head_dim; }
+
 
 // Block counts are 32-bit: the host rejects problems with 2^30 blocks or more.
 struct Plan {
-  int NB;      // blocks on the line
+  int NB;      // positions on the line (blocks and gaps)
   int q;       // blocks per range (S >= 2)
   int ranges;  // ranges that hold work
   int U;             // sub-group slots per sequence
   int S;             // partial slots per (b, h)
+  int gap;           // positions before each segment's blocks
 };
 
 struct Piece {
@@ -42,11 +54,12 @@ struct Piece {
   int npieces;   // pieces of this segment
 };
 
-// lens[b] = clamp(seq_lens[b] or max_len, 0, max_len); P[0..B] = block prefix;
-// P[B + 1] = the largest block count of one sequence.
-// Called by every thread of the block (contains __syncthreads).
-__device__ __forceinline__ void build_plan_arrays(const int* __restrict__ seq_lens, int B, int max_len, int* lens,
-                                                  int* P) {
+// lens[b] = clamp(seq_lens[b] or max_len, 0, max_len); P[0..B] = prefix of the
+// segment weights w_b = n_b + gap (0 for empty sequences); P[B + 1] = the largest
+// block count of one sequence.  Called by every thread of the block (contains
+// __syncthreads).
+__device__ __forceinline__ void build_plan_arrays(const int* __restrict__ seq_lens, int B, int max_len, int gap,
+                                                  int* lens, int* P) {
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
     int L = seq_lens ? __ldg(seq_lens + b) : max_len;
     L = L < 0 ? 0 : (L > max_len ? max_len : L);
@@ -61,7 +74,7 @@ __device__ __forceinline__ void build_plan_arrays(const int* __restrict__ seq_le
     int s = 0, mx = 0;
     for (int b = b0; b < b1; ++b) {
       const int nb = (lens[b] + kBlockTokens - 1) / kBlockTokens;
-      s += nb;
+      s += nb > 0 ? nb + gap : 0;
       mx = max(mx, nb);
     }
     int incl = s;
@@ -74,7 +87,8 @@ __device__ __forceinline__ void build_plan_arrays(const int* __restrict__ seq_le
     int run = incl - s;
     for (int b = b0; b < b1; ++b) {
       P[b] = run;
-      run += (lens[b] + kBlockTokens - 1) / kBlockTokens;
+      const int nb = (lens[b] + kBlockTokens - 1) / kBlockTokens;
+      run += nb > 0 ? nb + gap : 0;
     }
     if (lane == 31) {
       P[B] = incl;
@@ -84,10 +98,11 @@ __device__ __forceinline__ void build_plan_arrays(const int* __restrict__ seq_le
   __syncthreads();
 }
 
-__device__ __forceinline__ Plan make_plan(int B, int U, int S, const int* P) {
+__device__ __forceinline__ Plan make_plan(int B, int U, int S, int gap, const int* P) {
   Plan pl;
   pl.U = U;
   pl.S = S;
+  pl.gap = gap;
   pl.NB = U * P[B];
   if (S == 1) {
     pl.q = 0;
@@ -106,13 +121,13 @@ __device__ __forceinline__ Plan make_plan(int B, int U, int S, const int* P) {
 __device__ __forceinline__ int segment_pieces(const Plan& pl, const int* lens, const int* P, int b, int u) {
   const int nb = (lens[b] + kBlockTokens - 1) / kBlockTokens;
   if (nb == 0) return 0;
-  const int s0 = pl.U * P[b] + u * nb;
-  const int s1 = s0 + nb;
-  return (s1 - 1) / pl.q - s0 / pl.q + 1;
+  const int bs = pl.U * P[b] + u * (nb + pl.gap) + pl.gap;  // first block
+  return (bs + nb - 1) / pl.q - bs / pl.q + 1;
 }
 
-// S >= 2: the piece that starts at block x of range r (x < xe = end of range).
-// Returns the block where the next piece of the range starts.
+// S >= 2: the blocks of the segment at line position x that lie in [x, xe), the
+// rest of range r.  Returns the position where the next piece of the range
+// starts; pc.t0 == pc.t1 when [x, pe) holds only the segment's gap.
 __device__ __forceinline__ int piece_at(const Plan& pl, const int* lens, const int* P, int B, int x, int xe, int r,
                                         Piece& pc) {
   // sequence b: the last with U * P[b] <= x (sequences with no blocks are skipped
@@ -127,17 +142,19 @@ __device__ __forceinline__ int piece_at(const Plan& pl, const int* lens, const i
   }
   const int b = lo;
   const int nb = (lens[b] + kBlockTokens - 1) / kBlockTokens;
+  const int w = nb + pl.gap;
   const int base = pl.U * P[b];
-  const int u = (x - base) / nb;
-  const int s0 = base + u * nb;
-  const int s1 = s0 + nb;
-  const int pe = xe < s1 ? xe : s1;
+  const int u = (x - base) / w;
+  const int bs = base + u * w + pl.gap;  // first block of the segment
+  const int be = bs + nb;                // end of the segment
+  const int pe = xe < be ? xe : be;
+  const int x0 = x > bs ? x : bs;
   pc.b = b;
   pc.u = u;
-  pc.t0 = (x - s0) * kBlockTokens;
-  pc.t1 = min((pe - s0) * kBlockTokens, lens[b]);
-  pc.j = r - s0 / pl.q;
-  pc.npieces = (s1 - 1) / pl.q - s0 / pl.q + 1;
+  pc.t0 = (x0 - bs) * kBlockTokens;
+  pc.t1 = pe > x0 ? min((pe - bs) * kBlockTokens, lens[b]) : pc.t0;
+  pc.j = r - bs / pl.q;
+  pc.npieces = (be - 1) / pl.q - bs / pl.q + 1;
   return pe;
 }
 
@@ -180,7 +197,8 @@ struct PieceWalker {
       }
       if (x < xe) {
         x = piece_at(pl, lens, P, B, x, xe, r, pc);
-        return true;
+        if (pc.t1 > pc.t0) return true;
+        continue;  // only a gap: no piece
       }
       r += gridDim.x;
       if (r >= pl.ranges) return false;

@@ -66,19 +66,19 @@ struct SplitParams {
 
 template <int D>
 struct SplitGeo {
-  // Tiles carry 32 KB (D <= 128) or 64 KB (D = 256) of K+V so the per-tile costs
+  // Tiles carry 32 KB (D <= 64) or 64 KB (D >= 128) of K+V so the per-tile costs
   // (barrier round trip, TMA issue) stay small against the bytes moved.
-  static constexpr int T = D == 32 ? 256 : D == 64 ? 128 : 64;  // tokens per tile
+  static constexpr int T = D == 32 ? 256 : D <= 128 ? 128 : 64;  // tokens per tile
   static constexpr int W = 4;                       // consumer warps
   static constexpr int SB = T / 16;                 // 16-token sub-blocks per tile
   static constexpr int SBW = SB / W;                // sub-blocks per warp: k = warp + W * i
-  static constexpr int NP = D <= 64 ? 2 : 1;        // sub-blocks per online-softmax step
+  static constexpr int NP = D <= 128 ? 2 : 1;       // sub-blocks per online-softmax step
   static constexpr int NTHREADS = (W + 1) * 32;
   static constexpr int SUBW = D >= 64 ? 64 : 32;    // elements per swizzle row
   static constexpr int NSUB = D / SUBW;             // swizzle rows per token
   static constexpr int ROWB = SUBW * 2;             // 128 or 64 bytes
   static constexpr int CPR = SUBW / 8;              // 16-byte chunks per swizzle row
-  static constexpr int STAGES = D == 256 ? 2 : D == 128 ? 4 : 5;
+  static constexpr int STAGES = D == 256 ? 2 : D == 128 ? 3 : 5;
   static constexpr int FD = D;                      // fold scratch columns per pass (one pass)
   static constexpr int SUB_BYTES = T * ROWB;        // one swizzle column of a contiguous tile
   // One TMA box fills all NSUB swizzle columns of its rows: a contiguous tile is
@@ -430,14 +430,28 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
           const int kb = warp + Gm::W * (sb + i);
           const int tok0 = t + 16 * kb;
           const uint32_t blk = (uint32_t)(kb * BLK_STRIDE);
+          // even and odd k-chunks go to separate accumulators (two short dependency
+          // chains per 8-token half instead of one long one), added at the end
           float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+          float s2[4] = {0.f, 0.f, 0.f, 0.f}, s3[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int kk = 0; kk < KCH; ++kk) {
             const int c = 2 * kk + k_chk;
             uint32_t b0, b1, b2, b3;
             ldsm_x4(kst + blk + (c / Gm::CPR) * COL_STRIDE + swz<Gm::ROWB>(k_row0, c % Gm::CPR), b0, b1, b2, b3);
-            mma_bf16_16816(s0, qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
-            mma_bf16_16816(s1, qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
+            if (KCH >= 4 && (kk & 1)) {
+              mma_bf16_16816(s2, qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+              mma_bf16_16816(s3, qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
+            } else {
+              mma_bf16_16816(s0, qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+              mma_bf16_16816(s1, qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
+            }
+          }
+          if (KCH >= 4) {
+            s0[0] += s2[0];
+            s0[1] += s2[1];
+            s1[0] += s3[0];
+            s1[1] += s3[1];
           }
           x[i][0] = s0[0] * p.scale_log2;
           x[i][1] = s0[1] * p.scale_log2;
@@ -630,8 +644,8 @@ __global__ void __launch_bounds__(SplitGeo<D>::NTHREADS, 1) split_kernel(const _
   // The combine kernel (launched only when a segment can have more than 8 pieces)
   // may start now; it waits on the device for this grid to finish.
   pdl_launch_dependents();
-  build_plan_arrays(p.seq_lens, p.B, p.max_len, lens, P);
-  const Plan pl = make_plan(p.B, p.U, p.S, P);
+  build_plan_arrays(p.seq_lens, p.B, p.max_len, plan_gap_blocks(D), lens, P);
+  const Plan pl = make_plan(p.B, p.U, p.S, plan_gap_blocks(D), P);
   if (warp == Gm::W)
     split_producer<D, PAGED>(p, pl, lens, P, smem, sbase, abort_flag);
   else

@@ -35,13 +35,15 @@
  * The split plan.  Work is counted in 16-token blocks, n_b = ceil(L_b / 16).
  * The query heads of one KV head are processed in ceil(G / 8) equal sub-groups
  * (one pass over the KV head each); U = Hkv * ceil(G / 8) sub-group slots.
- * Segment (b, u) covers blocks [U*P_b + u*n_b, U*P_b + (u+1)*n_b) of one global
- * block line, P_b = n_0 + ... + n_{b-1}, NB = U * P_B blocks in all.
+ * The segments (b, u) lie end to end on one line in (b, u) order; a segment of a
+ * non-empty sequence takes w_b = c + n_b positions, c = 2816 / head_dim of them
+ * without blocks (they stand for the fixed cost of a piece) followed by its n_b
+ * blocks; P_b = w_0 + ... + w_{b-1}, NB = U * P_B positions in all.
  *   num_splits == 1: every segment is computed whole and written directly.
- *   num_splits >= 2: the line is cut into ranges of q blocks, q = ceil(NB / R) with
- *     R = (num_splits - 1) * U, rounded up to a multiple of 4 blocks (whole 64-token
- *     tiles); each range is one CTA's work; the pieces of
- *     a segment are its intersections with the ranges (index j = r - floor(start/q)),
+ *   num_splits >= 2: the line is cut into ranges of q positions, q = ceil(NB / R)
+ *     with R = (num_splits - 1) * U, rounded up to a multiple of 4 (at least 4);
+ *     each range is one CTA's work; the pieces of a segment are the non-empty sets
+ *     of its blocks that share a range (index j = r - range of its first block),
  *     at most num_splits of them.  A segment with one piece is written directly;
  *     one with several leaves partials in slots j = 0..pieces-1, which are merged
  *     into the output by the CTA that finishes its last piece (found with the

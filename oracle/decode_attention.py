@@ -49,6 +49,7 @@ __all__ = [
     "decode_paged",
     "decode_rows",
     "head_groups",
+    "piece_gap_blocks",
     "split_pieces",
     "decode_partials",
     "combine_partials",
@@ -238,21 +239,27 @@ def _decode_all(inp: dict) -> np.ndarray:
 
 # ------------------------------------------------------------ split rule
 
-def split_pieces(seq_lens: Sequence[int], Hkv: int, G: int, num_splits: int):
+def piece_gap_blocks(head_dim: int) -> int:
+    """Line positions charged to each segment for the fixed cost of one piece."""
+    return 2816 // head_dim
+
+
+def split_pieces(seq_lens: Sequence[int], Hkv: int, G: int, num_splits: int, gap: int = 0):
     """The partition of every (sequence, KV-head sub-group) token range into pieces.
 
     Work units are 16-token blocks; sequence b has n_b = ceil(L_b / 16) of them.
     A segment is one (b, KV head h, head sub-group j); with U = Hkv * len(head_groups(G))
-    sub-group slots u = h * ngroups + j, segment (b, u) occupies blocks
-    [U * P_b + u * n_b, U * P_b + (u + 1) * n_b) of one global block line,
-    where P_b = n_0 + ... + n_{b-1}.  NB = U * P_B blocks in total.
+    sub-group slots u = h * ngroups + j.  The segments lie end to end on one line,
+    in (b, u) order; segment (b, u) takes w_b = gap + n_b positions (none when the
+    sequence is empty): first `gap` positions that hold no block, then its n_b
+    blocks.  NB = U * (w_0 + ... + w_{B-1}) positions in total.
 
     num_splits == 1: every segment is one piece.
-    num_splits >= 2: the block line is cut into ranges of q blocks, q = ceil(NB / R)
-    with R = (num_splits - 1) * U, rounded up to a multiple of 4 blocks (ranges hold
-    whole 64-token tiles), at least 4; range r = [r q, (r + 1) q).  A segment's pieces
-    are its non-empty intersections with the ranges, in order; piece index
-    j = r - floor(start / q).  This never gives a segment more than num_splits pieces.
+    num_splits >= 2: the line is cut into ranges of q positions, q = ceil(NB / R)
+    with R = (num_splits - 1) * U, rounded up to a multiple of 4, at least 4;
+    range r = [r q, (r + 1) q).  A segment's pieces are the non-empty sets of its
+    blocks that share a range, in order; piece index j = r - (range of its first
+    block).  This never gives a segment more than num_splits pieces.
 
     Returns a list of dicts {b, u, h, group (first, count), piece, t0, t1, npieces}.
     """
@@ -269,18 +276,19 @@ def split_pieces(seq_lens: Sequence[int], Hkv: int, G: int, num_splits: int):
                     out.append(dict(b=b, u=u, h=u // ng, group=groups[u % ng], piece=0,
                                     t0=0, t1=L, npieces=1))
         return out
+    w = [gap + n if n > 0 else 0 for n in nblk]
     P = [0]
-    for n in nblk:
-        P.append(P[-1] + n)
+    for x in w:
+        P.append(P[-1] + x)
     NB = U * P[-1]
     R = (num_splits - 1) * U
     q = max(4, -(-max(1, -(-NB // R)) // 4) * 4)
     for b, L in enumerate(lens):
         for u in range(U):
-            start = U * P[b] + u * nblk[b]
-            end = start + nblk[b]
             if nblk[b] == 0:
                 continue
+            start = U * P[b] + u * w[b] + gap  # first block
+            end = start + nblk[b]
             r_first, r_last = start // q, (end - 1) // q
             for r in range(r_first, r_last + 1):
                 x0, x1 = max(start, r * q), min(end, (r + 1) * q)
@@ -306,7 +314,7 @@ def decode_partials(inp: dict, num_splits: int):
     ml = np.full((B, Hq, S, 2), np.nan)
     npieces = np.zeros((B, Hq), dtype=np.int64)
     cache = {}
-    for pc in split_pieces(inp["seq_lens"], Hkv, G, S):
+    for pc in split_pieces(inp["seq_lens"], Hkv, G, S, piece_gap_blocks(D)):
         b, h = pc["b"], pc["h"]
         if b not in cache:
             cache = {b: _kv_rows(inp, b, int(inp["seq_lens"][b]))}

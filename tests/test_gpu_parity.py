@@ -35,12 +35,14 @@ def contig_case(seed, B, Hq, Hkv, D, ctx, lens=None, kstd=1.0):
 def test_contig_matches_oracle(D, Hq, Hkv):
     inp = contig_case(D * 1000 + Hq, len(RAGGED), Hq, Hkv, D, ctx=max(RAGGED), lens=RAGGED)
     ref = oracle.decode_contig(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["scale"])
-    for S in (None, 1, 5):
+    checked = 0
+    for S in (None, 1, 5, 40):
         out, acc, ml, S_used = run(inp, S)
         check_out(out, ref, f"D={D} G={Hq // Hkv} S={S_used}")
         if S_used >= 2:
             ra, rm, npc = oracle.decode_partials(inp, S_used)
-            assert check_partials(acc, ml, ra, rm, npc, f"D={D} S={S_used}") > 0
+            checked += check_partials(acc, ml, ra, rm, npc, f"D={D} S={S_used}")
+    assert checked > 0  # some segment was cut into several pieces
 
 
 @pytest.mark.parametrize("D", [64, 128])

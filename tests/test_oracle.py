@@ -243,8 +243,8 @@ def test_single_group_is_per_head_attention():
 
 # ------------------------------------------------------------ split rule
 
-def _check_plan(lens, Hkv, G, S):
-    pieces = od.split_pieces(lens, Hkv, G, S)
+def _check_plan(lens, Hkv, G, S, gap=0):
+    pieces = od.split_pieces(lens, Hkv, G, S, gap)
     ng = len(od.head_groups(G))
     by_seg = {}
     for p in pieces:
@@ -273,30 +273,33 @@ def test_split_rule_partitions_every_segment():
         Hkv = int(rng.integers(1, 5))
         G = int(rng.integers(1, 18))
         S = int(rng.integers(1, 12))
-        _check_plan(lens, Hkv, G, S)
+        _check_plan(lens, Hkv, G, S, int(rng.choice([0, 1, 6, 12, 48])))
 
 
 def test_split_rule_matches_block_by_block_brute_force():
-    """Re-derive the pieces by walking every 16-token block through its range."""
+    """Re-derive the pieces by walking every line position (gap or block) through its range."""
     rng = np.random.default_rng(32)
-    for trial in range(100):
+    for trial in range(150):
         B = int(rng.integers(1, 5))
         lens = rng.integers(0, 200, size=B).tolist()
         Hkv, G, S = int(rng.integers(1, 4)), int(rng.integers(1, 10)), int(rng.integers(2, 9))
+        gap = int(rng.choice([0, 1, 3, 6, 12, 24]))
         ng = -(-G // 8)
         U = Hkv * ng
-        line = []  # one entry per block: (b, u, block index in segment)
+        line = []  # one entry per position: None (gap) or (b, u, block index in segment)
         for b, L in enumerate(lens):
             n = -(-L // 16)
             for u in range(U):
-                line += [(b, u, i) for i in range(n)]
+                if n:
+                    line += [None] * gap + [(b, u, i) for i in range(n)]
         R = (S - 1) * U
         q = max(4, -(-max(1, -(-len(line) // R)) // 4) * 4)
         want = {}
-        for x, (b, u, i) in enumerate(line):
-            want.setdefault((b, u, x // q), []).append(i)
+        for x, e in enumerate(line):
+            if e is not None:
+                want.setdefault((e[0], e[1], x // q), []).append(e[2])
         got = {}
-        for p in od.split_pieces(lens, Hkv, G, S):
+        for p in od.split_pieces(lens, Hkv, G, S, gap):
             got[(p["b"], p["u"], p["t0"], p["t1"])] = True
         want_pieces = set()
         for (b, u, r), blocks in want.items():
@@ -325,7 +328,7 @@ def test_partials_follow_their_definition():
     rng = np.random.default_rng(34)
     inp = _contig_case(rng, 1, 4, 1, 32, ctx=200)
     acc, ml, npc = od.decode_partials(inp, 4)
-    pieces = od.split_pieces([200], 1, 4, 4)
+    pieces = od.split_pieces([200], 1, 4, 4, od.piece_gap_blocks(32))
     qf, kf, vf = (od.widen_bf16(inp[n]) for n in ("q", "k", "v"))
     for p in pieces:
         for h in range(4):
