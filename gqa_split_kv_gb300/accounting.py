@@ -34,8 +34,9 @@ def piece_counts(seq_lens, Hkv: int, G: int, S: int, D: int) -> np.ndarray:
     """Pieces of every segment, shape [B, Hkv * ceil(G/8)].
 
     The library's split plan: segments lie end to end on one line, each taking
-    gap + n_b positions (gap = 2816 / D positions without blocks, then its
-    blocks); the line is cut into ranges of q positions."""
+    gap + 4 ceil(n_b / 4) positions (gap = 4 ceil((2816 / D) / 4) positions
+    without blocks, then its blocks, then padding); the line is cut into ranges
+    of q positions."""
     lens = np.asarray(seq_lens, dtype=np.int64)
     ng, _ = _groups(G)
     U = Hkv * ng
@@ -43,8 +44,8 @@ def piece_counts(seq_lens, Hkv: int, G: int, S: int, D: int) -> np.ndarray:
     B = len(lens)
     if S == 1:
         return np.where(nblk[:, None] > 0, 1, 0) * np.ones((B, U), dtype=np.int64)
-    gap = 2816 // D
-    w = np.where(nblk > 0, nblk + gap, 0)
+    gap = (2816 // D + 3) // 4 * 4
+    w = np.where(nblk > 0, (nblk + 3) // 4 * 4 + gap, 0)
     P = np.concatenate([[0], np.cumsum(w)])
     NB = U * int(P[-1])
     R = (S - 1) * U

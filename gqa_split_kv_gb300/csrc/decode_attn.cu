@@ -119,7 +119,7 @@ struct Launch {
   const void* q;
   const int* seq_lens;
   const int* page_table;
-  int page_size, max_pages;
+  int page_size, max_pages, box_shift;
   float* part_acc;
   float* part_ml;
   unsigned long long* seg_counters;
@@ -229,13 +229,17 @@ int run_decode(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, in
   prm.max_len = a.max_len;
   prm.page_size = a.page_size;
   prm.max_pages = a.max_pages;
+  prm.box_shift = a.box_shift;
+  prm.page_shift = -1;
+  for (int s = 4; s < 31; ++s)
+    if (a.page_size == (1 << s)) prm.page_shift = s;
   prm.S = a.S;
   prm.scale_log2 = a.scale * 1.4426950408889634f;
   prm.timeout_ns = kWaitTimeoutNs;
 
   // one persistent CTA per SM, never more CTAs than ranges or blocks of work
   const long long nblk_max = (a.max_len + kBlockTokens - 1) / kBlockTokens;
-  if ((long long)a.B * prm.U * (nblk_max + plan_gap_blocks(D)) >= (1LL << 30) || (long long)a.B * a.Hq >= (1LL << 30))
+  if ((long long)a.B * prm.U * (nblk_max + 3 + plan_gap_blocks(D)) >= (1LL << 30) || (long long)a.B * a.Hq >= (1LL << 30))
     return DA_ERR_UNSUPPORTED;  // the device plan counts line positions in 32 bits
   long long ranges = a.S == 1 ? (long long)a.B * prm.U : (long long)(a.S - 1) * prm.U;
   const long long work = (long long)a.B * prm.U * (nblk_max > 0 ? nblk_max : 1);
@@ -365,6 +369,7 @@ extern "C" int decode_attn_contig(const void* q, const void* k, const void* v, c
   a.page_table = nullptr;
   a.page_size = 0;
   a.max_pages = 0;
+  a.box_shift = 0;
   a.part_acc = part_acc;
   a.part_ml = part_ml;
   a.seg_counters = seg_counters;
@@ -396,13 +401,16 @@ extern "C" int decode_attn_paged(const void* q, const void* k_pool, const void* 
   if (current_device(&dev) || device_info(dev, &sms, &smem_optin)) return DA_ERR_CUDA;
 
   // dims (swizzle row, row in page, swizzle column, head, page): one box fills every
-  // swizzle column of a 16-token block, [D/SW][16][SW] in shared memory
+  // swizzle column of R rows of one page, [D/SW][R][SW] in shared memory, with
+  // R = 64, 32 or 16, the largest that divides the page size (tiles start on
+  // 64-token boundaries, so such a box never crosses a page)
+  const int box_shift = page_size % 64 == 0 ? 2 : page_size % 32 == 0 ? 1 : 0;
   const int SW = sub_width(D);
   const cuuint64_t row = (cuuint64_t)Hkv * D * 2;
   const cuuint64_t dims[5] = {(cuuint64_t)SW, (cuuint64_t)page_size, (cuuint64_t)(D / SW), (cuuint64_t)Hkv,
                               (cuuint64_t)num_pages};
   const cuuint64_t strides[4] = {row, (cuuint64_t)SW * 2, (cuuint64_t)D * 2, row * (cuuint64_t)page_size};
-  const cuuint32_t box[5] = {(cuuint32_t)SW, 16, (cuuint32_t)(D / SW), 1, 1};
+  const cuuint32_t box[5] = {(cuuint32_t)SW, (cuuint32_t)(16 << box_shift), (cuuint32_t)(D / SW), 1, 1};
   CUtensorMap tk, tv;
   if (int e = encode_map(&tk, k_pool, 5, dims, strides, box, D)) return e;
   if (int e = encode_map(&tv, v_pool, 5, dims, strides, box, D)) return e;
@@ -420,6 +428,7 @@ extern "C" int decode_attn_paged(const void* q, const void* k_pool, const void* 
   a.page_table = page_table;
   a.page_size = page_size;
   a.max_pages = max_pages_per_seq;
+  a.box_shift = box_shift;
   a.part_acc = part_acc;
   a.part_ml = part_ml;
   a.seg_counters = seg_counters;

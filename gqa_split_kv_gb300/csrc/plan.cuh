@@ -7,19 +7,22 @@
 // ranges, so a persistent grid stays balanced for any mix of lengths.  Every
 // segment is preceded by a gap of c positions that stands for the fixed cost of
 // a piece (epilogue, partial tile, query load), so a range full of short
-// sequences holds fewer blocks than one inside a long sequence.
+// sequences holds fewer blocks than one inside a long sequence.  Segments are
+// padded to whole 64-token units, so every piece starts on a 64-token boundary
+// of its sequence (a paged tile then never splits a box of 16, 32 or 64 rows
+// across pages).
 //
 //   n_b  = ceil(L_b / 16)                     blocks of sequence b
-//   w_b  = n_b + c if n_b > 0, else 0         line positions of one segment
-//   c    = 2816 / head_dim                    (about 176 KB of K+V streaming)
+//   w_b  = 4 ceil(n_b / 4) + c if n_b > 0, else 0   line positions of one segment
+//   c    = 4 ceil((2816 / head_dim) / 4)      (about 176 KB of K+V streaming)
 //   P_b  = w_0 + ... + w_{b-1}                (prefix, P_B = line length / U)
 //   U    = Hkv * ceil(G / 8)                  sub-group slots per sequence
 //   segment (b, u) = positions [s0, s0 + w_b), s0 = U P_b + u w_b; its blocks
-//                    sit at [s0 + c, s0 + c + n_b)
+//                    sit at [s0 + c, s0 + c + n_b), the rest hold none
 //   S >= 2: q = ceil(U P_B / ((S - 1) U)) rounded up to a multiple of 4
 //           positions (at least 4), range r = [r q, (r + 1) q); a piece is the
-//           blocks of one segment inside one range (ranges that meet only a gap
-//           give none)
+//           blocks of one segment inside one range (ranges that meet none of a
+//           segment's blocks give no piece of it)
 //   S == 1: range r = segment (r / U, r % U), whole.
 #pragma once
 
@@ -33,8 +36,12 @@ constexpr int kRangeQuantum = 4;  // ranges are whole 64-token tiles
 // by the CTA that finishes the last piece; longer ones by the combine kernel.
 constexpr int kFusedMergeMax = 8;
 
-// Line positions charged to every segment for the fixed cost of a piece.
-__host__ __device__ constexpr int plan_gap_blocks(int head_dim) { return 2816 / head_dim; }
+// Line positions charged to every segment for the fixed cost of a piece (a
+// multiple of 4, so segments keep 64-token alignment on the line).
+__host__ __device__ constexpr int plan_gap_blocks(int head_dim) { return (2816 / head_dim + 3) / 4 * 4; }
+
+// Line positions of one segment with n blocks (0 for an empty sequence).
+__device__ __forceinline__ int segment_width(int nb, int gap) { return nb > 0 ? ((nb + 3) & ~3) + gap : 0; }
 
 
 // Block counts are 32-bit: the host rejects problems with 2^30 blocks or more.
@@ -55,7 +62,7 @@ struct Piece {
 };
 
 // lens[b] = clamp(seq_lens[b] or max_len, 0, max_len); P[0..B] = prefix of the
-// segment weights w_b = n_b + gap (0 for empty sequences); P[B + 1] = the largest
+// segment widths w_b (segment_width); P[B + 1] = the largest
 // block count of one sequence.  Called by every thread of the block (contains
 // __syncthreads).
 __device__ __forceinline__ void build_plan_arrays(const int* __restrict__ seq_lens, int B, int max_len, int gap,
@@ -74,7 +81,7 @@ __device__ __forceinline__ void build_plan_arrays(const int* __restrict__ seq_le
     int s = 0, mx = 0;
     for (int b = b0; b < b1; ++b) {
       const int nb = (lens[b] + kBlockTokens - 1) / kBlockTokens;
-      s += nb > 0 ? nb + gap : 0;
+      s += segment_width(nb, gap);
       mx = max(mx, nb);
     }
     int incl = s;
@@ -88,7 +95,7 @@ __device__ __forceinline__ void build_plan_arrays(const int* __restrict__ seq_le
     for (int b = b0; b < b1; ++b) {
       P[b] = run;
       const int nb = (lens[b] + kBlockTokens - 1) / kBlockTokens;
-      run += nb > 0 ? nb + gap : 0;
+      run += segment_width(nb, gap);
     }
     if (lane == 31) {
       P[B] = incl;
@@ -121,13 +128,13 @@ __device__ __forceinline__ Plan make_plan(int B, int U, int S, int gap, const in
 __device__ __forceinline__ int segment_pieces(const Plan& pl, const int* lens, const int* P, int b, int u) {
   const int nb = (lens[b] + kBlockTokens - 1) / kBlockTokens;
   if (nb == 0) return 0;
-  const int bs = pl.U * P[b] + u * (nb + pl.gap) + pl.gap;  // first block
+  const int bs = pl.U * P[b] + u * segment_width(nb, pl.gap) + pl.gap;  // first block
   return (bs + nb - 1) / pl.q - bs / pl.q + 1;
 }
 
 // S >= 2: the blocks of the segment at line position x that lie in [x, xe), the
-// rest of range r.  Returns the position where the next piece of the range
-// starts; pc.t0 == pc.t1 when [x, pe) holds only the segment's gap.
+// rest of range r.  Returns the position where the next segment of the range
+// starts (or xe); pc.t0 == pc.t1 when [x, xe) meets none of the segment's blocks.
 __device__ __forceinline__ int piece_at(const Plan& pl, const int* lens, const int* P, int B, int x, int xe, int r,
                                         Piece& pc) {
   // sequence b: the last with U * P[b] <= x (sequences with no blocks are skipped
@@ -142,11 +149,12 @@ __device__ __forceinline__ int piece_at(const Plan& pl, const int* lens, const i
   }
   const int b = lo;
   const int nb = (lens[b] + kBlockTokens - 1) / kBlockTokens;
-  const int w = nb + pl.gap;
+  const int w = segment_width(nb, pl.gap);
   const int base = pl.U * P[b];
   const int u = (x - base) / w;
-  const int bs = base + u * w + pl.gap;  // first block of the segment
-  const int be = bs + nb;                // end of the segment
+  const int s0 = base + u * w;
+  const int bs = s0 + pl.gap;  // first block of the segment
+  const int be = bs + nb;      // end of its blocks
   const int pe = xe < be ? xe : be;
   const int x0 = x > bs ? x : bs;
   pc.b = b;
@@ -155,7 +163,7 @@ __device__ __forceinline__ int piece_at(const Plan& pl, const int* lens, const i
   pc.t1 = pe > x0 ? min((pe - bs) * kBlockTokens, lens[b]) : pc.t0;
   pc.j = r - bs / pl.q;
   pc.npieces = (be - 1) / pl.q - bs / pl.q + 1;
-  return pe;
+  return xe < s0 + w ? xe : s0 + w;
 }
 
 // Walks the pieces of the ranges blockIdx.x, blockIdx.x + gridDim.x, ...

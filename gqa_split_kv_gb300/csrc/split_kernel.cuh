@@ -7,7 +7,8 @@
 //   warp W (producer): one elected lane waits for a free stage, posts the byte
 //     count and issues the TMA tile copies (K, V and, for the first tile of a
 //     piece, the query rows).  Paged caches: the lanes resolve one page-table
-//     entry per 16-token block, prefetched LA tiles ahead with cp.async.
+//     entry per box (16, 32 or 64 rows of one page), prefetched LA tiles ahead
+//     with cp.async.
 //   warps 0..W-1 (consumers): warp w owns the 16-token sub-blocks w, w + W, ... of
 //     every tile.
 //
@@ -59,6 +60,8 @@ struct SplitParams {
   int B, Hq, G, U, ng, gr;
   int max_len;       // lengths are clamped to [0, max_len]
   int page_size, max_pages;
+  int box_shift;     // paged: a TMA box holds 16 << box_shift rows of one page (16, 32 or 64)
+  int page_shift;    // log2(page_size) when it is a power of two, else -1
   int S;
   float scale_log2;  // scale * log2(e)
   unsigned long long timeout_ns;
@@ -80,15 +83,15 @@ struct SplitGeo {
   static constexpr int CPR = SUBW / 8;              // 16-byte chunks per swizzle row
   static constexpr int STAGES = D == 256 ? 2 : D == 128 ? 3 : 5;
   static constexpr int FD = D;                      // fold scratch columns per pass (one pass)
-  static constexpr int SUB_BYTES = T * ROWB;        // one swizzle column of a contiguous tile
-  // One TMA box fills all NSUB swizzle columns of its rows: a contiguous tile is
-  // [NSUB][T][SUBW]; a paged tile is block-major, [T/16][NSUB][16][SUBW].
-  static constexpr int BLK_BYTES = 16 * D * 2;      // one 16-token block of one tensor
+  // One TMA box fills all NSUB swizzle columns of its R rows, so a tile is
+  // box-major, [T/R][NSUB][R][SUBW]: R = T for a contiguous cache (one box per
+  // tile), R = 16, 32 or 64 rows of one page for a paged cache.
+  static constexpr int LOG_SB = SB == 16 ? 4 : SB == 8 ? 3 : SB == 4 ? 2 : SB == 2 ? 1 : 0;
   static constexpr int KV_BYTES = T * D * 2;        // one tensor, one stage
   static constexpr int Q_SUB_BYTES = 8 * ROWB;
   static constexpr int Q_BYTES = 8 * D * 2;
   static constexpr int RING = 16;                   // page-entry ring slots
-  static constexpr int LA = 8;                      // page-entry prefetch distance (tiles)
+  static constexpr int LA = 4;                      // page-entry prefetch distance (tiles, 128-256 KB)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_Q = OFF_V + STAGES * KV_BYTES;
@@ -102,6 +105,7 @@ struct SplitGeo {
   static constexpr int OFF_PLAN = OFF_MISC + 16;
   static constexpr int smem_bytes(int B) { return OFF_PLAN + (2 * B + 2) * 4 + 1024; }
   static_assert(SB % W == 0 && SB <= 32, "whole sub-blocks per warp; one producer lane per block");
+  static_assert((1 << LOG_SB) == SB && T >= 64, "power-of-two tiles of whole 64-token units");
   static_assert(SBW % NP == 0, "softmax steps cover whole sub-blocks");
   static_assert(RING >= LA + 2, "page ring must hold the prefetch window");
   static_assert(smem_bytes(64) <= 227 * 1024, "shared memory budget");
@@ -141,6 +145,11 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Page-table column of token tok (a shift for power-of-two page sizes).
+__device__ __forceinline__ int page_of(const SplitParams& p, int tok) {
+  return p.page_shift >= 0 ? tok >> p.page_shift : tok / p.page_size;
+}
+
 // Piece + tile cursor used by the producer (pieces without tokens are skipped).
 struct TileCursor {
   PieceWalker walk;
@@ -175,23 +184,24 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
   TileCursor cur;
   cur.init(pl, lens, P, p.B);
   TileCursor look = cur;
+  const int box_rows = PAGED ? 16 << p.box_shift : Gm::T;
 
-  // prologue of the page-entry prefetch: tiles 0 .. LA-1
-  if (PAGED) {
-#pragma unroll
-    for (int k = 0; k < Gm::LA; ++k) {
-      if (look.valid) {
-        const int nblk = min(Gm::T, look.pc.t1 - look.t + 15) / 16;
-        if (lane < nblk) {
-          const int tok = look.t + 16 * lane;
-          cp_async_4(pg_ring + (uint32_t)((k % Gm::RING) * 32 + lane) * 4,
-                     p.page_table + (size_t)look.pc.b * p.max_pages + tok / p.page_size);
-        }
-        look.advance(pl, lens, P, p.B, Gm::T);
+  // Page entries of tile k go to ring slot k % RING, one cp.async group per
+  // tile.  Tile 0's group is requested first, and tiles 1 .. LA only after tile
+  // 0's copies are out, so the first tile waits on one lookup, not LA of them.
+  auto request_pages = [&](int k) {
+    if (look.valid) {
+      const int nb = (min(Gm::T, look.pc.t1 - look.t) + box_rows - 1) >> (4 + p.box_shift);
+      if (lane < nb) {
+        const int tok = look.t + lane * box_rows;
+        cp_async_4(pg_ring + (uint32_t)((k % Gm::RING) * 32 + lane) * 4,
+                   p.page_table + (size_t)look.pc.b * p.max_pages + page_of(p, tok));
       }
-      cp_async_commit();
+      look.advance(pl, lens, P, p.B, Gm::T);
     }
-  }
+    cp_async_commit();
+  };
+  if (PAGED) request_pages(0);
 
   int n = 0;  // tiles issued
   int stage = 0;
@@ -202,23 +212,18 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
     const int first_head = h * p.G + (pc.u % p.ng) * p.gr;
     const bool first_tile = cur.t == pc.t0;
     const int ntok = min(Gm::T, pc.t1 - cur.t);
-    const int nblk = (ntok + 15) / 16;
+    const int nbox = PAGED ? (ntok + box_rows - 1) >> (4 + p.box_shift) : 1;  // boxes of this tile
 
     int page = 0;
     if (PAGED) {
-      if (look.valid) {
-        const int lblk = min(Gm::T, look.pc.t1 - look.t + 15) / 16;
-        if (lane < lblk) {
-          const int tok = look.t + 16 * lane;
-          cp_async_4(pg_ring + (uint32_t)(((n + Gm::LA) % Gm::RING) * 32 + lane) * 4,
-                     p.page_table + (size_t)look.pc.b * p.max_pages + tok / p.page_size);
-        }
-        look.advance(pl, lens, P, p.B, Gm::T);
+      if (n > 0) {  // groups 0 .. n + LA requested; tile n's must be complete
+        request_pages(n + Gm::LA);
+        cp_async_wait<Gm::LA>();
+      } else {
+        cp_async_wait<0>();
       }
-      cp_async_commit();
-      cp_async_wait<Gm::LA>();
       __syncwarp();
-      if (lane < nblk) page = pg_ring_ptr[(n % Gm::RING) * 32 + lane];
+      if (lane < nbox) page = pg_ring_ptr[(n % Gm::RING) * 32 + lane];
     }
 
     // wait until the consumers have released this stage (first pass: free)
@@ -232,14 +237,17 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
     const uint32_t vdst = sbase + Gm::OFF_V + stage * Gm::KV_BYTES;
     const uint32_t qdst = sbase + Gm::OFF_Q + stage * Gm::Q_BYTES;
     const uint32_t qbytes = first_tile ? (uint32_t)(Gm::NSUB * p.gr * Gm::ROWB) : 0u;
-    const uint32_t kvbytes = PAGED ? (uint32_t)(nblk * 16 * D * 2) : (uint32_t)Gm::KV_BYTES;
+    const uint32_t kvbytes = PAGED ? (uint32_t)(nbox * box_rows * D * 2) : (uint32_t)Gm::KV_BYTES;
     if (lane == 0) mbar_arrive_expect_tx(full, 2u * kvbytes + qbytes);
     __syncwarp();
     if (PAGED) {
-      if (lane < nblk) {
-        const int tok = cur.t + 16 * lane;
-        const int row0 = tok % p.page_size;
-        const uint32_t off = (uint32_t)(lane * Gm::BLK_BYTES);
+      // tiles start on 64-token boundaries (the plan pads segments to whole
+      // 64-token units) and box_rows divides both 64 and the page size, so a
+      // box never crosses a page
+      if (lane < nbox) {
+        const int tok = cur.t + lane * box_rows;
+        const int row0 = tok - page_of(p, tok) * p.page_size;
+        const uint32_t off = (uint32_t)(lane * box_rows * D * 2);
         tma_load_5d(kdst + off, &p.tm_k, full, 0, row0, 0, h, page);
         tma_load_5d(vdst + off, &p.tm_v, full, 0, row0, 0, h, page);
       }
@@ -251,6 +259,10 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
 #pragma unroll
       for (int sub = 0; sub < Gm::NSUB; ++sub)
         tma_load_4d(qdst + sub * Gm::Q_SUB_BYTES, &p.tm_q, full, 0, sub, first_head, pc.b);
+    }
+    if (PAGED && n == 0) {
+#pragma unroll 1
+      for (int k = 1; k <= Gm::LA; ++k) request_pages(k);
     }
     ++n;
     if (++stage == Gm::STAGES) {
@@ -291,14 +303,14 @@ __device__ __forceinline__ bool claim_last_piece(unsigned long long* c, unsigned
 
 // Log-sum-exp merge of the n <= kFusedMergeMax partials of one segment into its
 // bf16 output rows, in ascending piece order (run by the CTA that finished the
-// segment's last piece; the 4 consumer warps, 128 threads).  Partials written by
+// segment's last piece; the W consumer warps).  Partials written by
 // other CTAs are read through L2 (ld.global.cg).
-template <int D>
+template <int D, int W>
 __device__ __forceinline__ void merge_segment(const SplitParams& p, int b, int first_head, int nrows, int n,
                                               float* rowM) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float kNegInf = -__int_as_float(0x7f800000);
-  for (int r = warp; r < nrows; r += 4) {
+  for (int r = warp; r < nrows; r += W) {
     const float* ml = p.part_ml + ((size_t)b * p.Hq + first_head + r) * p.S * 2;
     float M = kNegInf;
     for (int j = lane; j < n; j += 32) M = fmaxf(M, __ldcg(ml + 2 * j));
@@ -306,8 +318,8 @@ __device__ __forceinline__ void merge_segment(const SplitParams& p, int b, int f
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     if (lane == 0) rowM[r] = M;
   }
-  named_bar_sync(1, 128);
-  for (int e = tid; e < nrows * (D / 4); e += 128) {
+  named_bar_sync(1, W * 32);
+  for (int e = tid; e < nrows * (D / 4); e += W * 32) {
     const int r = e / (D / 4), c4 = e % (D / 4);
     const size_t row = (size_t)b * p.Hq + first_head + r;
     const float2* ml = reinterpret_cast<const float2*>(p.part_ml + row * p.S * 2);
@@ -364,9 +376,14 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
   float* fml = reinterpret_cast<float*>(smem + Gm::OFF_FML);
   const float kNegInf = -__int_as_float(0x7f800000);
 
-  // shared-memory strides of a 16-token block and of a swizzle column (see SplitGeo)
-  constexpr int BLK_STRIDE = PAGED ? Gm::NSUB * 16 * Gm::ROWB : 16 * Gm::ROWB;
-  constexpr int COL_STRIDE = PAGED ? 16 * Gm::ROWB : Gm::SUB_BYTES;
+  // box-major tile (see SplitGeo): a box of 16 << rsh rows spans NSUB swizzle columns
+  const int rsh = PAGED ? p.box_shift : Gm::LOG_SB;
+  const uint32_t col_stride = (uint32_t)(16 * Gm::ROWB) << rsh;
+  const uint32_t box_bytes = col_stride * Gm::NSUB;
+  const int in_box = (1 << rsh) - 1;
+  auto blk_off = [&](int kb) -> uint32_t {
+    return (uint32_t)(kb >> rsh) * box_bytes + (uint32_t)((kb & in_box) * 16 * Gm::ROWB);
+  };
   // ldmatrix lane -> (row, chunk) patterns
   const int k_row0 = (lane & 7) + ((lane >> 4) << 3);
   const int k_chk = (lane >> 3) & 1;
@@ -429,7 +446,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
         for (int i = 0; i < NP; ++i) {
           const int kb = warp + Gm::W * (sb + i);
           const int tok0 = t + 16 * kb;
-          const uint32_t blk = (uint32_t)(kb * BLK_STRIDE);
+          const uint32_t blk = blk_off(kb);
           // even and odd k-chunks go to separate accumulators (two short dependency
           // chains per 8-token half instead of one long one), added at the end
           float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -438,7 +455,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
           for (int kk = 0; kk < KCH; ++kk) {
             const int c = 2 * kk + k_chk;
             uint32_t b0, b1, b2, b3;
-            ldsm_x4(kst + blk + (c / Gm::CPR) * COL_STRIDE + swz<Gm::ROWB>(k_row0, c % Gm::CPR), b0, b1, b2, b3);
+            ldsm_x4(kst + blk + (c / Gm::CPR) * col_stride + swz<Gm::ROWB>(k_row0, c % Gm::CPR), b0, b1, b2, b3);
             if (KCH >= 4 && (kk & 1)) {
               mma_bf16_16816(s2, qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
               mma_bf16_16816(s3, qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
@@ -499,7 +516,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
         m_run = m_new;
 #pragma unroll
         for (int i = 0; i < NP; ++i) {
-          const uint32_t blk = (uint32_t)((warp + Gm::W * (sb + i)) * BLK_STRIDE);
+          const uint32_t blk = blk_off(warp + Gm::W * (sb + i));
           // P = hi + lo in bf16: rows g (hi) and g + 8 (lo) of the A operand
           const uint32_t ph0 = pack_bf16x2(pr[i][0], pr[i][1]), ph1 = pack_bf16x2(pr[i][2], pr[i][3]);
           const uint32_t pl0 = pack_bf16x2(pr[i][0] - bf16lo_to_f32(ph0), pr[i][1] - bf16hi_to_f32(ph0));
@@ -508,7 +525,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
           for (int c2 = 0; c2 < NB8 / 2; ++c2) {
             const int c = 2 * c2 + v_chk;
             uint32_t v0, v1, v2, v3;
-            ldsm_x4_t(vst + blk + (c / Gm::CPR) * COL_STRIDE + swz<Gm::ROWB>(v_row0, c % Gm::CPR), v0, v1, v2, v3);
+            ldsm_x4_t(vst + blk + (c / Gm::CPR) * col_stride + swz<Gm::ROWB>(v_row0, c % Gm::CPR), v0, v1, v2, v3);
             if (tail[i]) {
               v0 &= vm_lo[i];
               v1 &= vm_hi[i];
@@ -608,7 +625,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
         if (*last) __threadfence();  // acquire: the other pieces' partials are read next
       }
       named_bar_sync(1, Gm::W * 32);
-      if (*last) merge_segment<D>(p, pc.b, first_head, nrows, pc.npieces, fsc);
+      if (*last) merge_segment<D, Gm::W>(p, pc.b, first_head, nrows, pc.npieces, fsc);
     }
     named_bar_sync(1, Gm::W * 32);
   }
@@ -641,6 +658,7 @@ __global__ void __launch_bounds__(SplitGeo<D>::NTHREADS, 1) split_kernel(const _
     prefetch_tensormap(&p.tm_v);
     prefetch_tensormap(&p.tm_q);
   }
+
   // The combine kernel (launched only when a segment can have more than 8 pieces)
   // may start now; it waits on the device for this grid to finish.
   pdl_launch_dependents();

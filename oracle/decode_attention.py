@@ -240,8 +240,9 @@ def _decode_all(inp: dict) -> np.ndarray:
 # ------------------------------------------------------------ split rule
 
 def piece_gap_blocks(head_dim: int) -> int:
-    """Line positions charged to each segment for the fixed cost of one piece."""
-    return 2816 // head_dim
+    """Line positions charged to each segment for the fixed cost of one piece
+    (a multiple of 4)."""
+    return (2816 // head_dim + 3) // 4 * 4
 
 
 def split_pieces(seq_lens: Sequence[int], Hkv: int, G: int, num_splits: int, gap: int = 0):
@@ -250,9 +251,11 @@ def split_pieces(seq_lens: Sequence[int], Hkv: int, G: int, num_splits: int, gap
     Work units are 16-token blocks; sequence b has n_b = ceil(L_b / 16) of them.
     A segment is one (b, KV head h, head sub-group j); with U = Hkv * len(head_groups(G))
     sub-group slots u = h * ngroups + j.  The segments lie end to end on one line,
-    in (b, u) order; segment (b, u) takes w_b = gap + n_b positions (none when the
-    sequence is empty): first `gap` positions that hold no block, then its n_b
-    blocks.  NB = U * (w_0 + ... + w_{B-1}) positions in total.
+    in (b, u) order; segment (b, u) takes w_b = gap + 4 * ceil(n_b / 4) positions
+    (none when the sequence is empty): first `gap` positions that hold no block,
+    then its n_b blocks, then empty positions up to the width.  NB = U * (w_0 +
+    ... + w_{B-1}) positions in total.  With gap a multiple of 4, every piece
+    starts on a 64-token boundary of its sequence.
 
     num_splits == 1: every segment is one piece.
     num_splits >= 2: the line is cut into ranges of q positions, q = ceil(NB / R)
@@ -276,7 +279,7 @@ def split_pieces(seq_lens: Sequence[int], Hkv: int, G: int, num_splits: int, gap
                     out.append(dict(b=b, u=u, h=u // ng, group=groups[u % ng], piece=0,
                                     t0=0, t1=L, npieces=1))
         return out
-    w = [gap + n if n > 0 else 0 for n in nblk]
+    w = [gap + -(-n // 4) * 4 if n > 0 else 0 for n in nblk]
     P = [0]
     for x in w:
         P.append(P[-1] + x)
