@@ -33,7 +33,8 @@ def _groups(G: int):
 def piece_counts(seq_lens, Hkv: int, G: int, S: int, D: int) -> np.ndarray:
     """Pieces of every segment, shape [B, Hkv * ceil(G/8)].
 
-    The library's split plan: segments lie end to end on one line, each taking
+    The library's split plan: segments lie end to end on one line in (u, b)
+    order (slot-major), each taking
     gap + 4 ceil(n_b / 4) positions (gap = 4 ceil((2816 / D) / 4) positions
     without blocks, then its blocks, then padding); the line is cut into ranges
     of q positions."""
@@ -50,7 +51,7 @@ def piece_counts(seq_lens, Hkv: int, G: int, S: int, D: int) -> np.ndarray:
     NB = U * int(P[-1])
     R = (S - 1) * U
     q = max(4, -(-max(1, -(-NB // R)) // 4) * 4)
-    s0 = U * P[:-1, None] + np.arange(U)[None, :] * w[:, None] + gap
+    s0 = np.arange(U)[None, :] * int(P[-1]) + P[:-1, None] + gap
     s1 = s0 + nblk[:, None]
     n = (s1 - 1) // q - s0 // q + 1
     return np.where(nblk[:, None] > 0, n, 0)

@@ -94,7 +94,7 @@ __global__ void __maxnreg__(40) combine_kernel(const CombineParams p) {  // 512 
         if (p.planned) {
           const int b = row / p.Hq, h = row % p.Hq;
           const int u = (h / p.G) * p.ng + (h % p.G) / p.gr;
-          n = segment_pieces(pl, lens, P, b, u);
+          n = segment_pieces(pl, lens, P, p.B, b, u);
         }
         if (!p.planned || n > kFusedMergeMax) {  // smaller segments were merged by the split kernel
           const int k = atomicAdd(&todo[0], 1);

@@ -4,7 +4,9 @@
 // The pages choose one split count for all sequences and cap it by the tile
 // count (AstrAI commit 988e013 "csrc", split-KV items).  This library instead
 // lays all segments end to end on one weighted line and cuts the line into equal
-// ranges, so a persistent grid stays balanced for any mix of lengths.  Every
+// ranges, so a persistent grid stays balanced for any mix of lengths.  The line
+// is head-major (every sequence of slot u, then of slot u + 1), so CTAs that run
+// at the same time read the KV heads of the same tokens, which share DRAM pages.  Every
 // segment is preceded by a gap of c positions that stands for the fixed cost of
 // a piece (epilogue, partial tile, query load), so a range full of short
 // sequences holds fewer blocks than one inside a long sequence.  Segments are
@@ -17,7 +19,7 @@
 //   c    = 4 ceil((2816 / head_dim) / 4)      (about 176 KB of K+V streaming)
 //   P_b  = w_0 + ... + w_{b-1}                (prefix, P_B = line length / U)
 //   U    = Hkv * ceil(G / 8)                  sub-group slots per sequence
-//   segment (b, u) = positions [s0, s0 + w_b), s0 = U P_b + u w_b; its blocks
+//   segment (b, u) = positions [s0, s0 + w_b), s0 = u P_B + P_b; its blocks
 //                    sit at [s0 + c, s0 + c + n_b), the rest hold none
 //   S >= 2: q = ceil(U P_B / ((S - 1) U)) rounded up to a multiple of 4
 //           positions (at least 4), range r = [r q, (r + 1) q); a piece is the
@@ -125,10 +127,10 @@ __device__ __forceinline__ Plan make_plan(int B, int U, int S, int gap, const in
 }
 
 // Number of pieces of segment (b, u) under plan pl (S >= 2).
-__device__ __forceinline__ int segment_pieces(const Plan& pl, const int* lens, const int* P, int b, int u) {
+__device__ __forceinline__ int segment_pieces(const Plan& pl, const int* lens, const int* P, int B, int b, int u) {
   const int nb = (lens[b] + kBlockTokens - 1) / kBlockTokens;
   if (nb == 0) return 0;
-  const int bs = pl.U * P[b] + u * segment_width(nb, pl.gap) + pl.gap;  // first block
+  const int bs = u * P[B] + P[b] + pl.gap;  // first block
   return (bs + nb - 1) / pl.q - bs / pl.q + 1;
 }
 
@@ -137,12 +139,14 @@ __device__ __forceinline__ int segment_pieces(const Plan& pl, const int* lens, c
 // starts (or xe); pc.t0 == pc.t1 when [x, xe) meets none of the segment's blocks.
 __device__ __forceinline__ int piece_at(const Plan& pl, const int* lens, const int* P, int B, int x, int xe, int r,
                                         Piece& pc) {
-  // sequence b: the last with U * P[b] <= x (sequences with no blocks are skipped
-  // because the following non-empty one shares their prefix value)
+  // slot u, then sequence b: the last with P[b] <= x - u P_B (sequences with no
+  // blocks are skipped because the following non-empty one shares their prefix)
+  const int u = x / P[B];
+  const int y = x - u * P[B];
   int lo = 0, hi = B - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (pl.U * P[mid] <= x)
+    if (P[mid] <= y)
       lo = mid;
     else
       hi = mid - 1;
@@ -150,9 +154,7 @@ __device__ __forceinline__ int piece_at(const Plan& pl, const int* lens, const i
   const int b = lo;
   const int nb = (lens[b] + kBlockTokens - 1) / kBlockTokens;
   const int w = segment_width(nb, pl.gap);
-  const int base = pl.U * P[b];
-  const int u = (x - base) / w;
-  const int s0 = base + u * w;
+  const int s0 = u * P[B] + P[b];
   const int bs = s0 + pl.gap;  // first block of the segment
   const int be = bs + nb;      // end of its blocks
   const int pe = xe < be ? xe : be;

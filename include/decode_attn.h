@@ -35,10 +35,12 @@
  * The split plan.  Work is counted in 16-token blocks, n_b = ceil(L_b / 16).
  * The query heads of one KV head are processed in ceil(G / 8) equal sub-groups
  * (one pass over the KV head each); U = Hkv * ceil(G / 8) sub-group slots.
- * The segments (b, u) lie end to end on one line in (b, u) order; a segment of a
- * non-empty sequence takes w_b = c + n_b positions, c = 2816 / head_dim of them
- * without blocks (they stand for the fixed cost of a piece) followed by its n_b
- * blocks; P_b = w_0 + ... + w_{b-1}, NB = U * P_B positions in all.
+ * The segments (b, u) lie end to end on one line in (u, b) order (slot-major);
+ * segment (b, u) takes w_b = c + 4*ceil(n_b / 4) positions, c = 4*ceil((2816 /
+ * head_dim) / 4) of them without blocks (they stand for the fixed cost of a
+ * piece), then its n_b blocks, then padding to whole 64-token units; an empty
+ * sequence takes none.  P_b = w_0 + ... + w_{b-1}; segment (b, u) starts at
+ * u*P_B + P_b; NB = U * P_B positions in all.
  *   num_splits == 1: every segment is computed whole and written directly.
  *   num_splits >= 2: the line is cut into ranges of q positions, q = ceil(NB / R)
  *     with R = (num_splits - 1) * U, rounded up to a multiple of 4 (at least 4);

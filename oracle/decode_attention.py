@@ -251,7 +251,7 @@ def split_pieces(seq_lens: Sequence[int], Hkv: int, G: int, num_splits: int, gap
     Work units are 16-token blocks; sequence b has n_b = ceil(L_b / 16) of them.
     A segment is one (b, KV head h, head sub-group j); with U = Hkv * len(head_groups(G))
     sub-group slots u = h * ngroups + j.  The segments lie end to end on one line,
-    in (b, u) order; segment (b, u) takes w_b = gap + 4 * ceil(n_b / 4) positions
+    in (u, b) order (slot-major); segment (b, u) takes w_b = gap + 4 * ceil(n_b / 4) positions
     (none when the sequence is empty): first `gap` positions that hold no block,
     then its n_b blocks, then empty positions up to the width.  NB = U * (w_0 +
     ... + w_{B-1}) positions in total.  With gap a multiple of 4, every piece
@@ -290,7 +290,7 @@ def split_pieces(seq_lens: Sequence[int], Hkv: int, G: int, num_splits: int, gap
         for u in range(U):
             if nblk[b] == 0:
                 continue
-            start = U * P[b] + u * w[b] + gap  # first block
+            start = u * P[-1] + P[b] + gap  # first block
             end = start + nblk[b]
             r_first, r_last = start // q, (end - 1) // q
             for r in range(r_first, r_last + 1):

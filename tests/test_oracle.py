@@ -289,10 +289,10 @@ def test_split_rule_matches_block_by_block_brute_force():
         gap = int(rng.choice([0, 1, 3, 6, 12, 24]))
         ng = -(-G // 8)
         U = Hkv * ng
-        line = []  # one entry per position: None (gap) or (b, u, block index in segment)
-        for b, L in enumerate(lens):
-            n = -(-L // 16)
-            for u in range(U):
+        line = []  # one entry per position: None (gap or padding) or (b, u, block index in segment)
+        for u in range(U):
+            for b, L in enumerate(lens):
+                n = -(-L // 16)
                 if n:
                     line += [None] * gap + [(b, u, i) for i in range(n)] + [None] * (-n % 4)
         R = (S - 1) * U
