@@ -137,6 +137,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Each rank's timings (ms) -> the maximum over ranks of each, in order."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_value(world: int, bytes_per_step: int, steps: int, total_ms: float) -> float:
+    """Whole-job throughput in GB/s: every rank moved bytes_per_step per step (weak
+    scaling, one replica per GPU), and the slowest rank's time counts."""
+    return world * bytes_per_step * steps / (total_ms / 1e3) / 1e9
+
+
 # ------------------------------------------------------------ CPU baseline
 
 def cpu_child(workload: str, seconds: float):
@@ -317,16 +334,10 @@ def ours(args):
     sampler = ClockSampler(phys) if rank == 0 else None
     r = measure(wl, inp, args.steps, args.warmup, flush_bytes, dist=dist, sampler=sampler,
                 e2e_steps=max(3, min(args.steps, 200)))
-    total_ms = sum(r["times_ms"])
-    if dist is not None:
-        t = torch.tensor([total_ms, r["e2e_ms"]], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
-    else:
-        e2e_ms = r["e2e_ms"]
+    total_ms, e2e_ms = max_over_ranks([sum(r["times_ms"]), r["e2e_ms"]], dist, "cuda")
     K = args.steps
     alg = r["bytes"]["algorithmic"]
-    value = ws * alg * K / (total_ms / 1e3) / 1e9
+    value = job_value(ws, alg, K, total_ms)
     per = sorted(r["times_ms"])
     us_med = 1e3 * per[len(per) // 2]
     achieved = alg / (total_ms / K / 1e3) / 1e9
@@ -349,7 +360,7 @@ def ours(args):
                      "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
                      "traffic": ncu_traffic(wl.name)},
-        "e2e": {"value": round(ws * alg / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(job_value(ws, alg, 1, e2e_ms), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": r["launches_per_step"] * K,
         "clocks": r["clocks"],

@@ -23,6 +23,7 @@ __all__ = [
     "decode_attn_paged",
     "decode_combine",
     "device_error",
+    "selftest_bounded_wait",
     "counters_len",
     "STATUS",
 ]
@@ -60,6 +61,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.decode_status_string.argtypes = [i]
     lib.decode_status_string.restype = ctypes.c_char_p
     lib.decode_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+    lib.decode_selftest_bounded_wait.argtypes = [ctypes.c_ulonglong, vp]
+    lib.decode_selftest_bounded_wait.restype = i
     lib.decode_device_error.restype = i
     if path is None:
         _lib = lib
@@ -171,6 +174,14 @@ def decode_combine(part_acc, part_ml, out=None, stream=None):
     st = load().decode_combine(_ptr(part_acc), _ptr(part_ml), B, Hq, D, S, _ptr(out), _stream(stream))
     _check("decode_combine", st)
     return out
+
+
+def selftest_bounded_wait(timeout_ns: int, stream=None) -> None:
+    """Enqueue the diagnostic kernel whose wait can never complete; it gives up
+    after timeout_ns and sets bit 0 of the device error word (see device_error)."""
+    st = load().decode_selftest_bounded_wait(int(timeout_ns), _stream(stream))
+    if st != 0:
+        raise DecodeAttnError("decode_selftest_bounded_wait", st)
 
 
 def device_error(stream=None) -> int:

@@ -478,6 +478,28 @@ extern "C" const char* decode_status_string(int status) {
   }
 }
 
+// One CTA waits on an mbarrier that expects an arrival nobody makes; the bounded
+// wait gives up after the timeout and records it in the device error word.
+__global__ void selftest_wait_kernel(unsigned long long timeout_ns) {
+  __shared__ __align__(8) unsigned long long bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) wait_bounded(smem_u32(&bar), 0, &abort_flag, timeout_ns);
+  __syncthreads();
+}
+
+extern "C" int decode_selftest_bounded_wait(unsigned long long timeout_ns, void* stream) {
+  if (timeout_ns == 0 || timeout_ns > 1000000000ull) return DA_ERR_INVALID_ARG;
+  selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(timeout_ns);
+  if (cudaGetLastError() != cudaSuccess) return DA_ERR_CUDA;
+  return DA_OK;
+}
+
 extern "C" int decode_device_error(void* stream, unsigned int* flags) {
   if (!flags) return DA_ERR_INVALID_ARG;
   *flags = 0;

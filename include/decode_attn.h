@@ -177,6 +177,18 @@ const char* decode_status_string(int status);
  */
 int decode_device_error(void* stream, unsigned int* flags);
 
+/*
+ * decode_selftest_bounded_wait — diagnostic of the bounded waits that every
+ * kernel of this library uses (the pages have no counterpart).  Enqueues on
+ * `stream` one CTA that waits on a shared-memory mbarrier that nothing ever
+ * completes; the wait gives up after timeout_ns nanoseconds of the GPU's global
+ * timer, sets bit 0 of the device error word and the kernel returns normally, so
+ * the context stays usable.  decode_device_error() then reports DA_ERR_TIMEOUT
+ * with flags bit 0 set.  timeout_ns must be in (0, 10^9]; returns DA_OK,
+ * DA_ERR_INVALID_ARG or DA_ERR_CUDA (launch failure).
+ */
+int decode_selftest_bounded_wait(unsigned long long timeout_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -127,3 +127,9 @@ def test_combine_argument_errors(clib):
 
 def test_device_error_rejects_null(clib):
     assert clib.decode_device_error(None, None) == 1
+
+
+def test_selftest_rejects_bad_timeouts(clib):
+    clib.decode_selftest_bounded_wait.argtypes = [ctypes.c_ulonglong, ctypes.c_void_p]
+    assert clib.decode_selftest_bounded_wait(0, None) == 1
+    assert clib.decode_selftest_bounded_wait(10 ** 9 + 1, None) == 1

@@ -171,3 +171,20 @@ def test_counters_are_reused_without_reset():
     # counters left with arbitrary values by someone else
     ctr.copy_(torch.randint(0, 2 ** 31, ctr.shape, device="cuda"))
     assert np.array_equal(run(inp, 9, counters=ctr)[0], first)
+
+
+def test_bounded_wait_gives_up_and_the_context_stays_usable():
+    """A wait that nothing completes (the diagnostic kernel's mbarrier) ends after its
+    limit with the timeout bit set in the device error word; later calls still work."""
+    import time
+
+    from gqa_split_kv_gb300 import binding
+    assert binding.device_error() == 0
+    t0 = time.perf_counter()
+    binding.selftest_bounded_wait(2_000_000)  # 2 ms
+    assert binding.device_error() == 1        # bit 0: a bounded wait ran out (read and cleared)
+    assert time.perf_counter() - t0 < 5.0
+    assert binding.device_error() == 0
+    inp = contig_case(16, 2, 8, 2, 64, ctx=300, lens=[300, 45])
+    ref = oracle.decode_contig(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["scale"])
+    check_out(run(inp, 3)[0], ref, "after the self-test")
