@@ -53,6 +53,9 @@ __all__ = [
     "split_pieces",
     "decode_partials",
     "combine_partials",
+    "visible_tokens",
+    "decode_multi",
+    "decode_multi_partials",
     "BLOCK_TOKENS",
     "MAX_GROUP_ROWS",
 ]
@@ -348,3 +351,78 @@ def combine_partials(part_acc: np.ndarray, part_ml: np.ndarray) -> np.ndarray:
                       np.array([float(part_ml[b, h, j, 1])])) for j in range(S)]
             out[b, h] = merge_partials(parts)[0]
     return out
+
+
+# ------------------------------------------------------------ multi-query decode
+#
+# Speculative verification ("perf(dspark): overlap KV staging with compute via
+# cp.async", section "sparkinfer DSpark auto-eval — eval-dspark:XL", which scores a
+# draft block of 7): a sequence of L cached tokens whose last q_len tokens are the
+# new block scores q_len queries at once.  Query token i (0-based) sits at position
+# L - q_len + i and sees every token up to and including itself.  q and the output
+# are [B, Hq, q_len, D]; the pages do not fix the layout (head-major is this
+# library's choice).
+
+def visible_tokens(L: int, q_len: int, i: int) -> int:
+    """Tokens that query token i of the block sees: positions 0 .. L - q_len + i."""
+    return max(0, min(L, L - q_len + 1 + i))
+
+
+def decode_multi(inp: dict, rows: Optional[Iterable[Tuple[int, int, int]]] = None) -> np.ndarray:
+    """fp64 multi-query outputs.  inp["q"] is [B, Hq, q_len, D] bf16 bits; the cache
+    is contiguous ("k", "v") or paged ("k_pool", "v_pool", "page_table", "page_size").
+    Returns [B, Hq, q_len, D], or [n, D] for the selected (b, h, i) rows.  A query
+    that sees no token gives zeros."""
+    q = inp["q"]
+    B, Hq, qlen, D = q.shape
+    Hkv = (inp["k"] if "k" in inp else inp["k_pool"]).shape[2]
+    G = Hq // Hkv
+    want = [(b, h, i) for b in range(B) for h in range(Hq) for i in range(qlen)] if rows is None else list(rows)
+    res = np.zeros((len(want), D))
+    cache = {}
+    for n, (b, h, i) in enumerate(want):
+        L = int(inp["seq_lens"][b])
+        if b not in cache:
+            cache = {b: _kv_rows(inp, b, L)}
+        Kb, Vb = cache[b]
+        t = visible_tokens(L, qlen, i)
+        if t == 0:
+            continue
+        g = h // G
+        res[n] = attend(widen_bf16(q[b, h, i])[None], widen_bf16(Kb[:t, g]), widen_bf16(Vb[:t, g]), inp["scale"])[0]
+    return res.reshape(B, Hq, qlen, D) if rows is None else res
+
+
+def decode_multi_partials(inp: dict, num_splits: int):
+    """fp64 partials of every piece for multi-query decode, laid out as the library's
+    buffers: (part_acc [B, Hq, q_len, S, D], part_ml [B, Hq, q_len, S, 2], npieces
+    [B, Hq, q_len]).  The split rule is split_pieces with G * q_len rows per KV head
+    (rows ordered head-major: row r is head r // q_len, query token r % q_len); a
+    row's piece covers its tokens [t0, min(t1, visible)), and a piece in which the
+    row sees no token gives (0, -inf, 0).  Unfilled slots are NaN."""
+    q = inp["q"]
+    B, Hq, qlen, D = q.shape
+    Hkv = (inp["k"] if "k" in inp else inp["k_pool"]).shape[2]
+    G = Hq // Hkv
+    S = num_splits
+    acc = np.full((B, Hq, qlen, S, D), np.nan)
+    ml = np.full((B, Hq, qlen, S, 2), np.nan)
+    npieces = np.zeros((B, Hq, qlen), dtype=np.int64)
+    cache = {}
+    for pc in split_pieces(inp["seq_lens"], Hkv, G * qlen, S, piece_gap_blocks(D)):
+        b, kv = pc["b"], pc["h"]
+        L = int(inp["seq_lens"][b])
+        if b not in cache:
+            cache = {b: _kv_rows(inp, b, L)}
+        Kb, Vb = cache[b]
+        first, count = pc["group"]
+        for r in range(first, first + count):
+            h, i = kv * G + r // qlen, r % qlen
+            t1 = min(pc["t1"], visible_tokens(L, qlen, i))
+            t0 = min(pc["t0"], t1)
+            a, m, l = attend_partial(widen_bf16(q[b, h, i])[None], widen_bf16(Kb[t0:t1, kv]),
+                                     widen_bf16(Vb[t0:t1, kv]), inp["scale"])
+            acc[b, h, i, pc["piece"]] = a[0]
+            ml[b, h, i, pc["piece"]] = (m[0], l[0])
+            npieces[b, h, i] = pc["npieces"]
+    return acc, ml, npieces

@@ -453,3 +453,106 @@ def test_generator_workloads_have_the_stated_structure():
     assert len(inp2["outlier_pos"]) == 5
     big = np.abs(od.widen_bf16(inp2["k"][0])).max(axis=(1, 2))
     assert np.all(big[inp2["outlier_pos"]] > 8.0)
+
+
+# ------------------------------------------------------------ multi-query decode
+
+def _multi_case(rng, B, Hq, Hkv, D, qlen, ctx, lens, kstd=1.0):
+    inp = _contig_case(rng, B, Hq, Hkv, D, ctx, lens, kstd)
+    inp["q"] = _rand_bits(rng, (B, Hq, qlen, D))
+    return inp
+
+
+def _masked_softmax_reference(inp):
+    """Independent formulation: all L scores per query row, a causal mask matrix
+    mask[i, t] = (t <= L - q_len + i), softmax over the unmasked entries."""
+    q = inp["q"]
+    B, Hq, qlen, D = q.shape
+    Hkv = inp["k"].shape[2]
+    G = Hq // Hkv
+    out = np.zeros((B, Hq, qlen, D))
+    for b in range(B):
+        L = int(inp["seq_lens"][b])
+        t = np.arange(L)
+        mask = t[None, :] <= (L - qlen + np.arange(qlen))[:, None]
+        for h in range(Hq):
+            K = od.widen_bf16(inp["k"][b, :L, h // G])
+            V = od.widen_bf16(inp["v"][b, :L, h // G])
+            s = od.widen_bf16(q[b, h]) @ K.T * inp["scale"]
+            for i in range(qlen):
+                if not mask[i].any():
+                    continue
+                m = s[i][mask[i]].max()
+                w = np.where(mask[i], np.exp(np.where(mask[i], s[i], m) - m), 0.0)
+                out[b, h, i] = w @ V / w.sum()
+    return out
+
+
+def test_multi_query_matches_a_masked_softmax():
+    rng = np.random.default_rng(60)
+    for qlen, lens in [(1, [9, 40]), (3, [3, 40]), (7, [7, 100]), (4, [2, 33]), (8, [1, 17])]:
+        inp = _multi_case(rng, 2, 6, 2, 16, qlen, ctx=max(lens), lens=lens)
+        got = od.decode_multi(inp)
+        assert np.allclose(got, _masked_softmax_reference(inp), rtol=0, atol=1e-12), qlen
+
+
+def test_multi_query_row_is_decode_over_its_visible_prefix():
+    rng = np.random.default_rng(61)
+    inp = _multi_case(rng, 2, 8, 2, 32, 5, ctx=60, lens=[60, 23])
+    out = od.decode_multi(inp)
+    for b in range(2):
+        for i in range(5):
+            n = od.visible_tokens(int(inp["seq_lens"][b]), 5, i)
+            one = dict(inp, q=inp["q"][:, :, i], seq_lens=np.array([n if bb == b else 1 for bb in range(2)], np.int32))
+            for h in range(8):
+                assert np.array_equal(out[b, h, i], od.decode_rows(one, [(b, h)])[0])
+    # the last query token sees the whole sequence; one token equals plain decode
+    single = dict(inp, q=inp["q"][:, :, 4])
+    assert np.allclose(out[:, :, 4], od.decode_contig(**single), rtol=0, atol=1e-12)
+    one = dict(inp, q=inp["q"][:, :, :1])
+    assert np.allclose(od.decode_multi(one)[:, :, 0], od.decode_contig(**dict(inp, q=inp["q"][:, :, 0])),
+                       rtol=0, atol=1e-12)
+
+
+def test_multi_query_edge_lengths():
+    assert [od.visible_tokens(10, 4, i) for i in range(4)] == [7, 8, 9, 10]
+    assert [od.visible_tokens(2, 4, i) for i in range(4)] == [0, 0, 1, 2]
+    assert od.visible_tokens(0, 1, 0) == 0
+    rng = np.random.default_rng(62)
+    inp = _multi_case(rng, 1, 2, 1, 16, 4, ctx=2, lens=[2])
+    out = od.decode_multi(inp)
+    assert np.all(out[0, :, :2] == 0)  # queries that see no token
+    assert np.array_equal(od.round_to_bf16(out[0, :, 2]),
+                          inp["v"][0, 0, 0][None].repeat(2, 0))  # one visible key: its V row
+
+
+def test_multi_query_merge_of_partials_equals_unsplit():
+    rng = np.random.default_rng(63)
+    inp = _multi_case(rng, 3, 4, 1, 32, 6, ctx=400, lens=[400, 5, 130])
+    ref = od.decode_multi(inp)
+    cut = 0
+    for S in (1, 3, 9, 40):
+        acc, ml, npc = od.decode_multi_partials(inp, S)
+        assert npc.max() <= S
+        cut += int((npc >= 2).sum())
+        for b in range(3):
+            for h in range(4):
+                for i in range(6):
+                    n = npc[b, h, i]
+                    parts = [(acc[b, h, i, j][None], ml[b, h, i, j, :1], ml[b, h, i, j, 1:]) for j in range(n)
+                             if ml[b, h, i, j, 1] > 0]
+                    got = od.merge_partials(parts)[0] if parts else np.zeros(32)
+                    assert np.allclose(got, ref[b, h, i], rtol=0, atol=1e-12), (S, b, h, i)
+    assert cut > 0
+
+
+def test_multi_query_planted_off_by_one_is_caught(monkeypatch):
+    rng = np.random.default_rng(64)
+    inp = _multi_case(rng, 2, 4, 2, 16, 4, ctx=30, lens=[30, 6])
+    ref = _masked_softmax_reference(inp)
+    assert np.allclose(od.decode_multi(inp), ref, rtol=0, atol=1e-12)
+    for wrong in (lambda L, q, i: max(0, min(L, L - q + i)), lambda L, q, i: max(0, min(L, L - q + 2 + i)),
+                  lambda L, q, i: max(0, min(L, L - i))):
+        with monkeypatch.context() as m:
+            m.setattr(od, "visible_tokens", wrong)
+            assert not np.allclose(od.decode_multi(inp), ref, rtol=0, atol=1e-12)
