@@ -156,26 +156,33 @@ def job_value(world: int, bytes_per_step: int, steps: int, total_ms: float) -> f
 
 # ------------------------------------------------------------ CPU baseline
 
+def oracle_unit(oracle, wl, inp, b: int, g: int) -> int:
+    """The oracle on one sample unit: every query row of KV head g of sequence b.
+    Returns the unit's algorithmic bytes (its K/V rows and query rows)."""
+    G = wl.Hq // wl.Hkv
+    if wl.q_len == 1:
+        oracle.decode_rows(inp, [(b, g * G + i) for i in range(G)])
+    else:
+        oracle.decode_multi(inp, [(b, g * G + i, j) for i in range(G) for j in range(wl.q_len)])
+    return 2 * wl.D * 2 * int(inp["seq_lens"][b]) + G * wl.q_len * wl.D * 2
+
+
 def cpu_child(workload: str, seconds: float):
     """Runs in a subprocess with the BLAS thread count fixed: times the oracle."""
     import numpy as np  # noqa: F401
 
     import oracle
-    from gqa_split_kv_gb300.accounting import traffic_bytes
     from gqa_split_kv_gb300.workloads import WORKLOADS, make_inputs
 
     wl = WORKLOADS[workload]
     inp = make_inputs(wl)
-    G = wl.Hq // wl.Hkv
-    # sample unit: all G query heads of one (sequence, KV head) over its full context
+    # sample unit: all G query heads (x q_len query tokens) of one (sequence, KV head)
     groups = [(b, g) for b in range(wl.B) for g in range(wl.Hkv)]
     done_bytes, n = 0, 0
     t0 = time.perf_counter()
     while time.perf_counter() - t0 < seconds or n == 0:
         b, g = groups[n % len(groups)]
-        oracle.decode_rows(inp, [(b, g * G + i) for i in range(G)])
-        L = int(inp["seq_lens"][b])
-        done_bytes += 2 * wl.D * 2 * L + G * wl.D * 2
+        done_bytes += oracle_unit(oracle, wl, inp, b, g)
         n += 1
     dt = time.perf_counter() - t0
     print(json.dumps({"gbs": done_bytes / dt / 1e9, "units": n, "seconds": dt}))
@@ -224,10 +231,11 @@ def measure(wl, inp, steps: int, warmup: int, flush_bytes: int, dist=None, sampl
         table = None
         max_len = wl.max_ctx
     S = binding.num_splits(wl.B, wl.Hkv, max_len, wl.D)
-    out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.bfloat16, device="cuda")
-    pa = torch.empty((wl.B, wl.Hq, S, wl.D), dtype=torch.float32, device="cuda") if S > 1 else None
-    pm = torch.empty((wl.B, wl.Hq, S, 2), dtype=torch.float32, device="cuda") if S > 1 else None
-    ctr = torch.zeros(binding.counters_len(wl.B, wl.Hq, wl.Hkv), dtype=torch.int64, device="cuda")
+    rows = (wl.B, wl.Hq) if wl.q_len == 1 else (wl.B, wl.Hq, wl.q_len)  # multi-query: q_len rows per head
+    out = torch.empty(rows + (wl.D,), dtype=torch.bfloat16, device="cuda")
+    pa = torch.empty(rows + (S, wl.D), dtype=torch.float32, device="cuda") if S > 1 else None
+    pm = torch.empty(rows + (S, 2), dtype=torch.float32, device="cuda") if S > 1 else None
+    ctr = torch.zeros(binding.counters_len(wl.B, wl.Hq, wl.Hkv, wl.q_len), dtype=torch.int64, device="cuda")
     flush = torch.empty(flush_bytes, dtype=torch.uint8, device="cuda")
     flush_src = torch.empty(flush_bytes // 4, dtype=torch.float32, device="cuda").zero_()
     stream = torch.cuda.current_stream()
@@ -238,13 +246,16 @@ def measure(wl, inp, steps: int, warmup: int, flush_bytes: int, dist=None, sampl
         flush.zero_()
         torch.sum(flush_src)
 
+    attn_paged = binding.decode_attn_paged if wl.q_len == 1 else binding.decode_attn_multi_paged
+    attn_contig = binding.decode_attn_contig if wl.q_len == 1 else binding.decode_attn_multi_contig
+
     def call(qq=q, kk=kc, vv=vc, ll=lens, oo=out):
         if paged:
-            binding.decode_attn_paged(qq, kk, vv, table, ll, max_len, scale=wl.scale, splits=S, part_acc=pa,
-                                      part_ml=pm, seg_counters=ctr, out=oo)
+            attn_paged(qq, kk, vv, table, ll, max_len, scale=wl.scale, splits=S, part_acc=pa, part_ml=pm,
+                       seg_counters=ctr, out=oo)
         else:
-            binding.decode_attn_contig(qq, kk, vv, ll, scale=wl.scale, splits=S, part_acc=pa, part_ml=pm,
-                                       seg_counters=ctr, out=oo)
+            attn_contig(qq, kk, vv, ll, scale=wl.scale, splits=S, part_acc=pa, part_ml=pm, seg_counters=ctr,
+                        out=oo)
 
     for _ in range(warmup):
         flush_l2()
@@ -272,7 +283,7 @@ def measure(wl, inp, steps: int, warmup: int, flush_bytes: int, dist=None, sampl
         dist.barrier()
     times = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]  # ms
     assert binding.device_error() == 0
-    tb = traffic_bytes(wl.B, wl.Hq, wl.Hkv, wl.D, inp["seq_lens"], S, wl.page_size if paged else None)
+    tb = traffic_bytes(wl.B, wl.Hq, wl.Hkv, wl.D, inp["seq_lens"], S, wl.page_size if paged else None, wl.q_len)
     # the split kernel, plus the combine kernel when a segment can have more than 8 pieces
     res = {"S": S, "times_ms": times, "bytes": tb, "clocks": clocks, "launches_per_step": 1 if S <= 8 else 2}
 
@@ -282,7 +293,7 @@ def measure(wl, inp, steps: int, warmup: int, flush_bytes: int, dist=None, sampl
                 "lens": torch.from_numpy(inp["seq_lens"]).pin_memory()}
         host["k"] = torch.from_numpy(np.ascontiguousarray(inp["k_pool" if paged else "k"]).view(np.int16)).pin_memory()
         host["v"] = torch.from_numpy(np.ascontiguousarray(inp["v_pool" if paged else "v"]).view(np.int16)).pin_memory()
-        out_h = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.int16).pin_memory()
+        out_h = torch.empty(rows + (wl.D,), dtype=torch.int16).pin_memory()
         qi, ki, vi = q.view(torch.int16), kc.view(torch.int16), vc.view(torch.int16)
         h2d = sum(t.numel() * t.element_size() for t in (host["q"], host["k"], host["v"], host["lens"]))
         d2h = out_h.numel() * 2
@@ -349,7 +360,7 @@ def ours(args):
         "vs_baseline_basis": "pages' fa_split_gqa_kernel 1.11 ms/call on RTX 5090, same workload (µs ratio)",
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "head_dim": wl.D,
-                   "ctx": wl.max_ctx, "layout": wl.layout, "num_splits": r["S"], "accum": "fp32",
+                   "ctx": wl.max_ctx, "q_len": wl.q_len, "layout": wl.layout, "num_splits": r["S"], "accum": "fp32",
                    "l2": f"flushed before every step ({flush_bytes >> 20} MiB write + {flush_bytes >> 20} MiB read, "
                          "outside the timed pair)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
@@ -399,13 +410,11 @@ def reference(args):
 
     wl = WORKLOADS[args.workload]
     inp = make_inputs(wl)
-    G = wl.Hq // wl.Hkv
     groups = [(b, g) for b in range(wl.B) for g in range(wl.Hkv)]
 
     def step(i):
         b, g = groups[i % len(groups)]
-        oracle.decode_rows(inp, [(b, g * G + j) for j in range(G)])
-        return 2 * wl.D * 2 * int(inp["seq_lens"][b]) + G * wl.D * 2
+        return oracle_unit(oracle, wl, inp, b, g)
 
     for i in range(args.warmup):
         step(i)

@@ -57,13 +57,16 @@ def piece_counts(seq_lens, Hkv: int, G: int, S: int, D: int) -> np.ndarray:
     return np.where(nblk[:, None] > 0, n, 0)
 
 
-def traffic_bytes(B: int, Hq: int, Hkv: int, D: int, seq_lens, S: int, page_size: Optional[int] = None) -> dict:
+def traffic_bytes(B: int, Hq: int, Hkv: int, D: int, seq_lens, S: int, page_size: Optional[int] = None,
+                  q_len: int = 1) -> dict:
+    """Bytes of one call; with q_len > 1 (multi-query decode) the rows of a KV head
+    are its G query heads x q_len query tokens, and K/V are still read once."""
     lens = np.asarray(seq_lens, dtype=np.int64)
-    G = Hq // Hkv
+    G = Hq // Hkv * q_len
     ng, gr = _groups(G)
     kv = 2 * D * 2 * Hkv * int(lens.sum())
-    q = B * Hq * D * 2
-    out = B * Hq * D * 2
+    q = B * Hq * q_len * D * 2
+    out = B * Hq * q_len * D * 2
     n = piece_counts(lens, Hkv, G, S, D)                      # [B, U]
     # heads per sub-group slot u = h * ng + j
     heads = np.array([min(gr, G - (u % ng) * gr) for u in range(Hkv * ng)])

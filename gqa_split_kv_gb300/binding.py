@@ -21,6 +21,8 @@ __all__ = [
     "num_splits",
     "decode_attn_contig",
     "decode_attn_paged",
+    "decode_attn_multi_contig",
+    "decode_attn_multi_paged",
     "decode_combine",
     "device_error",
     "selftest_bounded_wait",
@@ -56,6 +58,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.decode_attn_contig.restype = i
     lib.decode_attn_paged.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, vp, vp, vp, vp]
     lib.decode_attn_paged.restype = i
+    lib.decode_attn_multi_contig.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp, vp, vp, vp]
+    lib.decode_attn_multi_contig.restype = i
+    lib.decode_attn_multi_paged.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, vp, vp, vp, vp, vp]
+    lib.decode_attn_multi_paged.restype = i
     lib.decode_combine.argtypes = [vp, vp, i, i, i, i, vp, vp]
     lib.decode_combine.restype = i
     lib.decode_status_string.argtypes = [i]
@@ -98,9 +104,9 @@ def num_splits(batch: int, num_kv_heads: int, max_seq_len: int, head_dim: int, n
     return s
 
 
-def counters_len(batch: int, num_q_heads: int, num_kv_heads: int) -> int:
-    """Entries of the per-segment counter array: batch * Hkv * ceil(G / 8)."""
-    G = num_q_heads // num_kv_heads
+def counters_len(batch: int, num_q_heads: int, num_kv_heads: int, q_len: int = 1) -> int:
+    """Entries of the per-segment counter array: batch * Hkv * ceil(G * q_len / 8)."""
+    G = num_q_heads // num_kv_heads * q_len
     return batch * num_kv_heads * ((G + 7) // 8)
 
 
@@ -160,6 +166,70 @@ def decode_attn_paged(q, k_pool, v_pool, page_table, seq_lens, max_seq_len: int,
                                   D, ps, max_pages, num_pages, int(max_seq_len), scale, S, _ptr(part_acc),
                                   _ptr(part_ml), _ptr(seg_counters), _ptr(out), _stream(stream))
     _check("decode_attn_paged", st)
+    return out
+
+
+def _multi_workspace(B, Hq, qlen, Hkv, D, S, part_acc, part_ml, seg_counters, device):
+    import torch
+    if S >= 2:
+        if part_acc is None:
+            part_acc = torch.empty((B, Hq, qlen, S, D), dtype=torch.float32, device=device)
+        if part_ml is None:
+            part_ml = torch.empty((B, Hq, qlen, S, 2), dtype=torch.float32, device=device)
+        if seg_counters is None:
+            seg_counters = torch.zeros(counters_len(B, Hq, Hkv, qlen), dtype=torch.int64, device=device)
+    return part_acc, part_ml, seg_counters
+
+
+def decode_attn_multi_contig(q, k, v, seq_lens=None, scale: Optional[float] = None, splits: Optional[int] = None,
+                             part_acc=None, part_ml=None, seg_counters=None, out=None, stream=None):
+    """Multi-query decode: q [B,Hq,q_len,D]; k/v [B,max_ctx,Hkv,D] bf16; seq_lens int32 [B] or None.
+    Query token i of sequence b sees its first seq_lens[b] - q_len + 1 + i tokens.  Returns out [B,Hq,q_len,D]."""
+    import torch
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k, "k", torch.bfloat16, 4)
+    _need(v, "v", torch.bfloat16, 4)
+    B, Hq, qlen, D = q.shape
+    _, ctx, Hkv, _ = k.shape
+    if seq_lens is not None:
+        _need(seq_lens, "seq_lens", torch.int32, 1)
+    scale = D ** -0.5 if scale is None else float(scale)
+    S = num_splits(B, Hkv, ctx, D) if splits is None else int(splits)
+    part_acc, part_ml, seg_counters = _multi_workspace(B, Hq, qlen, Hkv, D, S, part_acc, part_ml, seg_counters,
+                                                       q.device)
+    if out is None:
+        out = torch.empty((B, Hq, qlen, D), dtype=torch.bfloat16, device=q.device)
+    st = load().decode_attn_multi_contig(_ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), B, qlen, Hq, Hkv, D, ctx, scale,
+                                         S, _ptr(part_acc), _ptr(part_ml), _ptr(seg_counters), _ptr(out),
+                                         _stream(stream))
+    _check("decode_attn_multi_contig", st)
+    return out
+
+
+def decode_attn_multi_paged(q, k_pool, v_pool, page_table, seq_lens, max_seq_len: int,
+                            scale: Optional[float] = None, splits: Optional[int] = None, part_acc=None, part_ml=None,
+                            seg_counters=None, out=None, stream=None):
+    """Multi-query decode over a paged cache: q [B,Hq,q_len,D]; pools [num_pages,page_size,Hkv,D] bf16."""
+    import torch
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k_pool, "k_pool", torch.bfloat16, 4)
+    _need(v_pool, "v_pool", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, Hq, qlen, D = q.shape
+    num_pages, ps, Hkv, _ = k_pool.shape
+    max_pages = page_table.shape[1]
+    scale = D ** -0.5 if scale is None else float(scale)
+    S = num_splits(B, Hkv, max_seq_len, D) if splits is None else int(splits)
+    part_acc, part_ml, seg_counters = _multi_workspace(B, Hq, qlen, Hkv, D, S, part_acc, part_ml, seg_counters,
+                                                       q.device)
+    if out is None:
+        out = torch.empty((B, Hq, qlen, D), dtype=torch.bfloat16, device=q.device)
+    st = load().decode_attn_multi_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(seq_lens), B,
+                                        qlen, Hq, Hkv, D, ps, max_pages, num_pages, int(max_seq_len), scale, S,
+                                        _ptr(part_acc), _ptr(part_ml), _ptr(seg_counters), _ptr(out),
+                                        _stream(stream))
+    _check("decode_attn_multi_paged", st)
     return out
 
 

@@ -114,7 +114,8 @@ void head_groups(int G, int* ng, int* gr) {
 }
 
 struct Launch {
-  int B, Hq, Hkv, D, max_len, S;
+  int B, Hq, Hkv, D, max_len, S;  // Hq counts rows: query heads x qlen
+  int qlen;
   float scale;
   const void* q;
   const int* seq_lens;
@@ -227,6 +228,7 @@ int run_decode(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, in
   prm.gr = gr;
   prm.U = a.Hkv * ng;
   prm.max_len = a.max_len;
+  prm.qlen = a.qlen;
   prm.page_size = a.page_size;
   prm.max_pages = a.max_pages;
   prm.box_shift = a.box_shift;
@@ -330,11 +332,14 @@ extern "C" int decode_num_splits(int batch, int num_kv_heads, int max_seq_len, i
   return (int)S;
 }
 
-extern "C" int decode_attn_contig(const void* q, const void* k, const void* v, const int* seq_lens, int batch,
-                                  int num_q_heads, int num_kv_heads, int head_dim, int max_ctx, float scale,
-                                  int num_splits, float* part_acc, float* part_ml,
-                                  unsigned long long* seg_counters, void* out, void* stream) {
-  const int B = batch, Hq = num_q_heads, Hkv = num_kv_heads, D = head_dim, S = num_splits;
+// Contiguous cache, qlen query tokens per sequence (rows = Hq * qlen).
+static int contig_call(const void* q, const void* k, const void* v, const int* seq_lens, int batch, int qlen,
+                int num_q_heads, int num_kv_heads, int head_dim, int max_ctx, float scale, int num_splits,
+                float* part_acc, float* part_ml, unsigned long long* seg_counters, void* out, void* stream) {
+  if (qlen < 1 || qlen > DA_MAX_QLEN || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      num_q_heads % num_kv_heads != 0 || (long long)num_q_heads * qlen > (1 << 24))
+    return DA_ERR_INVALID_ARG;
+  const int B = batch, Hq = num_q_heads * qlen, Hkv = num_kv_heads, D = head_dim, S = num_splits;
   if (int st = check_common(q, out, B, Hq, Hkv, D, scale, S, part_acc, part_ml, seg_counters)) return st;
   if (max_ctx < 0) return DA_ERR_INVALID_ARG;
   if (B == 0) return DA_OK;
@@ -370,6 +375,7 @@ extern "C" int decode_attn_contig(const void* q, const void* k, const void* v, c
   a.page_size = 0;
   a.max_pages = 0;
   a.box_shift = 0;
+  a.qlen = qlen;
   a.part_acc = part_acc;
   a.part_ml = part_ml;
   a.seg_counters = seg_counters;
@@ -379,12 +385,15 @@ extern "C" int decode_attn_contig(const void* q, const void* k, const void* v, c
   return dispatch(a, tk, tv, dev, sms, smem_optin);
 }
 
-extern "C" int decode_attn_paged(const void* q, const void* k_pool, const void* v_pool, const int* page_table,
-                                 const int* seq_lens, int batch, int num_q_heads, int num_kv_heads, int head_dim,
-                                 int page_size, int max_pages_per_seq, int num_pages, int max_seq_len, float scale,
-                                 int num_splits, float* part_acc, float* part_ml, unsigned long long* seg_counters,
-                                 void* out, void* stream) {
-  const int B = batch, Hq = num_q_heads, Hkv = num_kv_heads, D = head_dim, S = num_splits;
+// Paged cache, qlen query tokens per sequence (rows = Hq * qlen).
+static int paged_call(const void* q, const void* k_pool, const void* v_pool, const int* page_table, const int* seq_lens,
+               int batch, int qlen, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+               int max_pages_per_seq, int num_pages, int max_seq_len, float scale, int num_splits, float* part_acc,
+               float* part_ml, unsigned long long* seg_counters, void* out, void* stream) {
+  if (qlen < 1 || qlen > DA_MAX_QLEN || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      num_q_heads % num_kv_heads != 0 || (long long)num_q_heads * qlen > (1 << 24))
+    return DA_ERR_INVALID_ARG;
+  const int B = batch, Hq = num_q_heads * qlen, Hkv = num_kv_heads, D = head_dim, S = num_splits;
   if (int st = check_common(q, out, B, Hq, Hkv, D, scale, S, part_acc, part_ml, seg_counters)) return st;
   if (page_size <= 0 || max_pages_per_seq < 0 || num_pages < 0 || max_seq_len < 0) return DA_ERR_INVALID_ARG;
   if (page_size % 16 != 0) return DA_ERR_UNSUPPORTED;
@@ -429,6 +438,7 @@ extern "C" int decode_attn_paged(const void* q, const void* k_pool, const void* 
   a.page_size = page_size;
   a.max_pages = max_pages_per_seq;
   a.box_shift = box_shift;
+  a.qlen = qlen;
   a.part_acc = part_acc;
   a.part_ml = part_ml;
   a.seg_counters = seg_counters;
@@ -436,6 +446,42 @@ extern "C" int decode_attn_paged(const void* q, const void* k_pool, const void* 
   a.stream = st;
   a.paged = true;
   return dispatch(a, tk, tv, dev, sms, smem_optin);
+}
+
+extern "C" int decode_attn_contig(const void* q, const void* k, const void* v, const int* seq_lens, int batch,
+                                  int num_q_heads, int num_kv_heads, int head_dim, int max_ctx, float scale,
+                                  int num_splits, float* part_acc, float* part_ml,
+                                  unsigned long long* seg_counters, void* out, void* stream) {
+  return contig_call(q, k, v, seq_lens, batch, 1, num_q_heads, num_kv_heads, head_dim, max_ctx, scale, num_splits,
+                     part_acc, part_ml, seg_counters, out, stream);
+}
+
+extern "C" int decode_attn_paged(const void* q, const void* k_pool, const void* v_pool, const int* page_table,
+                                 const int* seq_lens, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int page_size, int max_pages_per_seq, int num_pages, int max_seq_len, float scale,
+                                 int num_splits, float* part_acc, float* part_ml, unsigned long long* seg_counters,
+                                 void* out, void* stream) {
+  return paged_call(q, k_pool, v_pool, page_table, seq_lens, batch, 1, num_q_heads, num_kv_heads, head_dim,
+                    page_size, max_pages_per_seq, num_pages, max_seq_len, scale, num_splits, part_acc, part_ml,
+                    seg_counters, out, stream);
+}
+
+extern "C" int decode_attn_multi_contig(const void* q, const void* k, const void* v, const int* seq_lens, int batch,
+                                        int q_len, int num_q_heads, int num_kv_heads, int head_dim, int max_ctx,
+                                        float scale, int num_splits, float* part_acc, float* part_ml,
+                                        unsigned long long* seg_counters, void* out, void* stream) {
+  return contig_call(q, k, v, seq_lens, batch, q_len, num_q_heads, num_kv_heads, head_dim, max_ctx, scale,
+                     num_splits, part_acc, part_ml, seg_counters, out, stream);
+}
+
+extern "C" int decode_attn_multi_paged(const void* q, const void* k_pool, const void* v_pool, const int* page_table,
+                                       const int* seq_lens, int batch, int q_len, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int page_size, int max_pages_per_seq, int num_pages,
+                                       int max_seq_len, float scale, int num_splits, float* part_acc, float* part_ml,
+                                       unsigned long long* seg_counters, void* out, void* stream) {
+  return paged_call(q, k_pool, v_pool, page_table, seq_lens, batch, q_len, num_q_heads, num_kv_heads, head_dim,
+                    page_size, max_pages_per_seq, num_pages, max_seq_len, scale, num_splits, part_acc, part_ml,
+                    seg_counters, out, stream);
 }
 
 extern "C" int decode_combine(const float* part_acc, const float* part_ml, int batch, int num_q_heads,

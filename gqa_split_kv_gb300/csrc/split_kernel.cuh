@@ -57,7 +57,8 @@ struct SplitParams {
   unsigned long long* seg_counters;  // one per segment (b, u): (epoch << 32) | pieces done
   __nv_bfloat16* out;
   unsigned int epoch;                // tags this call's counter updates (never 0)
-  int B, Hq, G, U, ng, gr;
+  int B, Hq, G, U, ng, gr;  // Hq, G count rows: query heads x qlen query tokens
+  int qlen;          // query tokens per sequence (1: decode; > 1: causal block at the end)
   int max_len;       // lengths are clamped to [0, max_len]
   int page_size, max_pages;
   int box_shift;     // paged: a TMA box holds 16 << box_shift rows of one page (16, 32 or 64)
@@ -312,8 +313,11 @@ __device__ __forceinline__ void merge_segment(const SplitParams& p, int b, int f
   const float kNegInf = -__int_as_float(0x7f800000);
   for (int r = warp; r < nrows; r += W) {
     const float* ml = p.part_ml + ((size_t)b * p.Hq + first_head + r) * p.S * 2;
-    float M = kNegInf;
-    for (int j = lane; j < n; j += 32) M = fmaxf(M, __ldcg(ml + 2 * j));
+    float M = kNegInf;  // over the slots that saw a token (l > 0)
+    for (int j = lane; j < n; j += 32) {
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(ml) + j);
+      if (v.y > 0.f) M = fmaxf(M, v.x);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     if (lane == 0) rowM[r] = M;
@@ -342,7 +346,7 @@ __device__ __forceinline__ void merge_segment(const SplitParams& p, int b, int f
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         if (j0 + u < n) {
-          const float w = exp2_approx((v[u].x - M) * 1.4426950408889634f);
+          const float w = v[u].y > 0.f ? exp2_approx((v[u].x - M) * 1.4426950408889634f) : 0.f;
           num.x += w * a[u].x;
           num.y += w * a[u].y;
           num.z += w * a[u].z;
@@ -351,7 +355,7 @@ __device__ __forceinline__ void merge_segment(const SplitParams& p, int b, int f
         }
       }
     }
-    const float inv = 1.f / den;
+    const float inv = den > 0.f ? 1.f / den : 0.f;  // a row that saw no token: zeros
     uint2 o;
     o.x = pack_bf16x2(num.x * inv, num.y * inv);
     o.y = pack_bf16x2(num.z * inv, num.w * inv);
@@ -413,6 +417,15 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
     const int h = pc.u / p.ng;
     const int first_head = h * p.G + (pc.u % p.ng) * p.gr;
     const int nrows = min(p.gr, p.G - (pc.u % p.ng) * p.gr);
+    // Rows are (query head, query token i); query token i of a block of qlen sees
+    // the tokens before L - qlen + 1 + i.  lim_row bounds this thread's MMA row,
+    // lim_min every row of the warp (qlen == 1: both are the piece end).
+    int lim_row = pc.t1, lim_min = pc.t1;
+    if (p.qlen > 1) {
+      const int L = lens[pc.b];
+      lim_row = min(pc.t1, L - (p.qlen - 1 - ((pc.u % p.ng) * p.gr + g) % p.qlen));
+      lim_min = min(pc.t1, L - p.qlen + 1);
+    }
 
     for (int t = pc.t0; t < pc.t1; t += Gm::T) {
       wait_bounded(bar_full + stage * 8, parity, abort_flag, p.timeout_ns);
@@ -474,16 +487,17 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
           x[i][1] = s0[1] * p.scale_log2;
           x[i][2] = s1[0] * p.scale_log2;
           x[i][3] = s1[1] * p.scale_log2;
-          // tokens at or past the piece end: score -inf, V row zeroed (its shared
-          // memory may hold anything, and 0 * NaN would poison the accumulator)
-          tail[i] = tok0 + 16 > pc.t1;
+          // tokens at or past the row's limit: score -inf; at or past the piece end
+          // also V row zeroed (its shared memory may hold anything, and 0 * NaN
+          // would poison the accumulator)
+          tail[i] = tok0 + 16 > lim_min;
           vm_lo[i] = vm_hi[i] = 0xffffffffu;
           if (tail[i]) {
             const int ta = tok0 + 2 * i4, tb = tok0 + 8 + 2 * i4;
-            x[i][0] = ta < pc.t1 ? x[i][0] : kNegInf;
-            x[i][1] = ta + 1 < pc.t1 ? x[i][1] : kNegInf;
-            x[i][2] = tb < pc.t1 ? x[i][2] : kNegInf;
-            x[i][3] = tb + 1 < pc.t1 ? x[i][3] : kNegInf;
+            x[i][0] = ta < lim_row ? x[i][0] : kNegInf;
+            x[i][1] = ta + 1 < lim_row ? x[i][1] : kNegInf;
+            x[i][2] = tb < lim_row ? x[i][2] : kNegInf;
+            x[i][3] = tb + 1 < lim_row ? x[i][3] : kNegInf;
             vm_lo[i] = (ta < pc.t1 ? 0x0000ffffu : 0u) | (ta + 1 < pc.t1 ? 0xffff0000u : 0u);
             vm_hi[i] = (tb < pc.t1 ? 0x0000ffffu : 0u) | (tb + 1 < pc.t1 ? 0xffff0000u : 0u);
           }
@@ -494,13 +508,14 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
         const float m_new = fmaxf(m_run, mx);
-        const float alpha = exp2_approx(m_run - m_new);
+        const float m_use = m_new == kNegInf ? 0.f : m_new;  // a row that has seen no token yet
+        const float alpha = exp2_approx(m_run - m_use);
         float pr[NP][4];
         float psum = 0.f;
 #pragma unroll
         for (int i = 0; i < NP; ++i) {
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) pr[i][k4] = exp2_approx(x[i][k4] - m_new);
+          for (int k4 = 0; k4 < 4; ++k4) pr[i][k4] = exp2_approx(x[i][k4] - m_use);
           psum += (pr[i][0] + pr[i][1]) + (pr[i][2] + pr[i][3]);
         }
         l_run = l_run * alpha + psum;

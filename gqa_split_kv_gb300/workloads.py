@@ -79,6 +79,7 @@ class Workload:
     outlier_frac: float = 0.0
     outlier_mult: float = 20.0
     seed: int = 1234
+    q_len: int = 1  # query tokens per sequence (> 1: multi-query decode, q is [B, Hq, q_len, D])
 
     @property
     def G(self) -> int:
@@ -92,7 +93,8 @@ class Workload:
         return dataclasses.replace(self, **kw)
 
 
-# The five workload families; each name states its shape.
+# The five workload families of the decode configurations, plus two multi-query
+# (verification) workloads; each name states its shape.
 WORKLOADS = {
     "tiny_contig_b1_hq8_hkv2_d64_ctx512": Workload(
         "tiny_contig_b1_hq8_hkv2_d64_ctx512", B=1, Hq=8, Hkv=2, D=64, max_ctx=512, seed=1235),
@@ -116,6 +118,13 @@ WORKLOADS = {
     "sweep_paged_b64_hq64_hkv8_d64_ctx2048_ps16": Workload(
         "sweep_paged_b64_hq64_hkv8_d64_ctx2048_ps16", B=64, Hq=64, Hkv=8, D=64, max_ctx=2048,
         layout="paged", page_size=16, seed=1242),
+    # multi-query decode (speculative verification of a draft block)
+    "verify_contig_b1_hq24_hkv4_d256_ctx4096_q7": Workload(
+        "verify_contig_b1_hq24_hkv4_d256_ctx4096_q7", B=1, Hq=24, Hkv=4, D=256, max_ctx=4096, q_len=7,
+        seed=1243),
+    "verify_paged_b16_hq32_hkv8_d128_u256_8192_ps32_q4": Workload(
+        "verify_paged_b16_hq32_hkv8_d128_u256_8192_ps32_q4", B=16, Hq=32, Hkv=8, D=128, max_ctx=8192,
+        layout="paged", page_size=32, lens="uniform", lens_lo=256, lens_hi=8192, q_len=4, seed=1244),
 }
 
 
@@ -155,7 +164,7 @@ def _outlier_keys(rng: np.random.Generator, shape, frac: float, mult: float, tok
 def make_inputs(wl: Workload, seed: Optional[int] = None) -> dict:
     """Draw one problem.  Returns a dict of numpy arrays (bf16 as uint16 bits).
 
-    Keys: q [B,Hq,D]; seq_lens int32[B]; for "contig": k, v [B,max_ctx,Hkv,D];
+    Keys: q [B,Hq,D] ([B,Hq,q_len,D] when q_len > 1); seq_lens int32[B]; for "contig": k, v [B,max_ctx,Hkv,D];
     for "paged": k_pool, v_pool [num_pages,page_size,Hkv,D] and page_table
     int32[B,max_pages_per_seq] (unused entries are -1, never read); plus
     "scale" (float32 value 1/sqrt(D)) and "outlier_pos" when present.
@@ -164,7 +173,7 @@ def make_inputs(wl: Workload, seed: Optional[int] = None) -> dict:
     """
     rng = np.random.default_rng(wl.seed if seed is None else seed)
     seq_lens = draw_seq_lens(wl, rng)
-    q = _normal_bf16(rng, (wl.B, wl.Hq, wl.D))
+    q = _normal_bf16(rng, (wl.B, wl.Hq, wl.D) if wl.q_len == 1 else (wl.B, wl.Hq, wl.q_len, wl.D))
     out = {"q": q, "seq_lens": seq_lens, "scale": wl.scale}
     if wl.layout == "contig":
         shape = (wl.B, wl.max_ctx, wl.Hkv, wl.D)

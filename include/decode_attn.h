@@ -70,6 +70,7 @@ typedef enum {
 } da_status;
 
 #define DA_MAX_SPLITS 1024
+#define DA_MAX_QLEN 16  /* query tokens per sequence of decode_attn_multi_* */
 
 /*
  * decode_num_splits — the split count for a decode shape (host only, pure).
@@ -166,6 +167,35 @@ int decode_combine(const float* part_acc, const float* part_ml, int batch, int n
 int decode_attn_contig_noalloc(const void* q, const void* k, const void* v, const int* seq_lens,
                                int batch, int num_q_heads, int num_kv_heads, int head_dim, int max_ctx,
                                float scale, void* out, void* stream);
+
+/*
+ * decode_attn_multi_contig / decode_attn_multi_paged — multi-query decode, the
+ * verification step of speculative decoding scored on "perf(dspark): overlap KV
+ * staging with compute via cp.async", section "sparkinfer DSpark auto-eval —
+ * eval-dspark:XL" (a draft block of 7): every sequence scores q_len new tokens at once, the last q_len of its
+ * L_b cached tokens, causally within the block.  Query token i (0-based) of
+ * sequence b attends to cached tokens [0, L_b - q_len + 1 + i); a token that
+ * sees none (L_b < q_len - i) gets a zero output.  q_len == 1 is exactly
+ * decode_attn_contig / decode_attn_paged.
+ *  q, out        bf16 [batch, num_q_heads, q_len, head_dim] (head-major: the q_len
+ *                rows of one head are consecutive)
+ *  part_acc      float [batch, num_q_heads, q_len, num_splits, head_dim];
+ *  part_ml       float [batch, num_q_heads, q_len, num_splits, 2]
+ *  seg_counters  uint64 [batch * num_kv_heads * ceil(G * q_len / 8)], zeroed once
+ *  Every other argument as for decode_attn_contig / decode_attn_paged (the same
+ *  split plan, with G * q_len rows per KV head in sub-groups of at most 8).
+ *  1 <= q_len <= DA_MAX_QLEN and G * q_len <= 64, else DA_ERR_INVALID_ARG /
+ *  DA_ERR_UNSUPPORTED.  num_splits: decode_num_splits(batch, num_kv_heads, ...).
+ */
+int decode_attn_multi_contig(const void* q, const void* k, const void* v, const int* seq_lens, int batch,
+                             int q_len, int num_q_heads, int num_kv_heads, int head_dim, int max_ctx, float scale,
+                             int num_splits, float* part_acc, float* part_ml, unsigned long long* seg_counters,
+                             void* out, void* stream);
+int decode_attn_multi_paged(const void* q, const void* k_pool, const void* v_pool, const int* page_table,
+                            const int* seq_lens, int batch, int q_len, int num_q_heads, int num_kv_heads,
+                            int head_dim, int page_size, int max_pages_per_seq, int num_pages, int max_seq_len,
+                            float scale, int num_splits, float* part_acc, float* part_ml,
+                            unsigned long long* seg_counters, void* out, void* stream);
 
 /* Human-readable name of a da_status value (static string). */
 const char* decode_status_string(int status);

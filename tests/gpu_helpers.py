@@ -103,3 +103,50 @@ def check_partials(acc: np.ndarray, ml: np.ndarray, ref_acc: np.ndarray, ref_ml:
                 assert da <= PART_RTOL * np.abs(ref_acc[b, h, j]).max(), (what, b, h, j, da)
                 checked += 1
     return checked
+
+
+def run_multi(inp, S=None, max_seq_len=None, dev_inputs=None):
+    """One multi-query call (q [B, Hq, q_len, D]); returns (out bits, part_acc, part_ml, S) as numpy."""
+    B, Hq, qlen, D = inp["q"].shape
+    d = dev_inputs if dev_inputs is not None else to_device(inp)
+    q = d["q"]
+    if "k" in inp:
+        Hkv, ctx = inp["k"].shape[2], inp["k"].shape[1]
+    else:
+        Hkv, ctx = inp["k_pool"].shape[2], max_seq_len
+    S = binding.num_splits(B, Hkv, ctx, D) if S is None else S
+    acc = torch.full((B, Hq, qlen, S, D), float("nan"), dtype=torch.float32, device="cuda")
+    ml = torch.full((B, Hq, qlen, S, 2), float("nan"), dtype=torch.float32, device="cuda")
+    out = torch.full((B, Hq, qlen, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ctr = torch.zeros(binding.counters_len(B, Hq, Hkv, qlen), dtype=torch.int64, device="cuda")
+    if "k" in inp:
+        binding.decode_attn_multi_contig(q, d["k"], d["v"], d["seq_lens"],
+                                         scale=inp["scale"], splits=S, part_acc=acc, part_ml=ml, seg_counters=ctr,
+                                         out=out)
+    else:
+        binding.decode_attn_multi_paged(q, d["k_pool"], d["v_pool"], d["page_table"], d["seq_lens"], max_seq_len,
+                                        scale=inp["scale"], splits=S, part_acc=acc, part_ml=ml, seg_counters=ctr,
+                                        out=out)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    return host_bits(out), acc.cpu().numpy(), ml.cpu().numpy(), S
+
+
+def check_multi_partials(acc, ml, inp, S):
+    """Slots of rows whose segment has >= 2 pieces; a piece in which the row sees no
+    token must be (0, -inf, 0)."""
+    ra, rm, npc = oracle.decode_multi_partials(inp, S)
+    checked = 0
+    for idx in zip(*np.nonzero(npc >= 2)):
+        for j in range(npc[idx]):
+            m_ref, l_ref = rm[idx + (j,)]
+            m_got, l_got = ml[idx + (j,)]
+            if l_ref == 0:
+                assert m_got == -np.inf and l_got == 0 and np.all(acc[idx + (j,)] == 0), (idx, j)
+                continue
+            assert abs(m_got - m_ref) <= PART_RTOL * max(1.0, abs(m_ref)), (idx, j, m_got, m_ref)
+            assert abs(l_got - l_ref) <= PART_RTOL * l_ref, (idx, j, l_got, l_ref)
+            da = np.abs(acc[idx + (j,)].astype(np.float64) - ra[idx + (j,)]).max()
+            assert da <= PART_RTOL * np.abs(ra[idx + (j,)]).max(), (idx, j, da)
+            checked += 1
+    return checked

@@ -116,6 +116,19 @@ def test_paged_argument_errors(clib):
     assert paged(clib, maxlen=-3) == 1
 
 
+def test_multi_argument_errors(clib):
+    def multi(qlen=4, Hq=8, Hkv=2, D=64):
+        return clib.decode_attn_multi_contig(A, A, A, None, 1, qlen, Hq, Hkv, D, 64, ctypes.c_float(0.125), 2, A, A,
+                                             A, A, None)
+    assert multi(qlen=0) == 1
+    assert multi(qlen=17) == 1
+    assert multi(Hq=6, Hkv=4) == 1          # Hq % Hkv
+    assert multi(Hq=32, Hkv=2, qlen=5) == 2  # G * q_len = 80 > 64
+    assert multi(D=48) == 2
+    assert clib.decode_attn_multi_paged(A, A, A, A, A, 1, 2, 8, 2, 64, 24, 4, 4, 64, ctypes.c_float(0.125), 2, A, A,
+                                        A, A, None) == 2  # page size not a multiple of 16
+
+
 def test_combine_argument_errors(clib):
     assert clib.decode_combine(A, A, 1, 8, 48, 4, A, None) == 2
     assert clib.decode_combine(A, A, 1, 8, 64, 0, A, None) == 1

@@ -14,7 +14,7 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
-from gpu_helpers import OUT_ATOL, OUT_RTOL, PART_RTOL, run, to_device  # noqa: E402
+from gpu_helpers import OUT_ATOL, OUT_RTOL, PART_RTOL, run, run_multi, to_device  # noqa: E402
 from gqa_split_kv_gb300.workloads import bf16_bits_to_f32  # noqa: E402
 
 N_ROWS = 24       # sampled (b, query head) outputs per workload
@@ -32,11 +32,33 @@ def _sample_rows(inp, rng):
     return sorted(picks)
 
 
+def _full_size_multi(wl, inp, d):
+    """Multi-query workloads: sampled (b, h, i) outputs against the oracle, and bitwise
+    run-to-run determinism (partials are checked at parity sizes)."""
+    max_len = wl.max_ctx if "k_pool" in inp else None
+    out, acc, ml, S = run_multi(inp, None, max_seq_len=max_len, dev_inputs=d)
+    assert np.all(np.isfinite(bf16_bits_to_f32(out)))
+    rng = np.random.default_rng(4343)
+    lens = inp["seq_lens"]
+    picks = {(int(np.argmax(lens)), 0, wl.q_len - 1), (int(np.argmin(lens)), wl.Hq - 1, 0)}
+    while len(picks) < min(N_ROWS, wl.B * wl.Hq * wl.q_len):
+        picks.add((int(rng.integers(wl.B)), int(rng.integers(wl.Hq)), int(rng.integers(wl.q_len))))
+    rows = sorted(picks)
+    ref = oracle.decode_multi(inp, rows)
+    got = np.stack([bf16_bits_to_f32(out[b, h, i]).astype(np.float64) for b, h, i in rows])
+    err = np.abs(got - ref)
+    assert np.all(err <= OUT_ATOL + OUT_RTOL * np.abs(ref)), f"{wl.name}: max abs err {err.max():.3e}"
+    out2, *_ = run_multi(inp, S, max_seq_len=max_len, dev_inputs=d)
+    assert np.array_equal(out, out2)
+
+
 @pytest.mark.parametrize("name", list(WORKLOADS))
 def test_full_size_workload(name):
     wl = WORKLOADS[name]
     inp = make_inputs(wl)
     d = to_device(inp)
+    if wl.q_len > 1:
+        return _full_size_multi(wl, inp, d)
     max_len = wl.max_ctx
     out, acc, ml, S = run(inp, None, dev_inputs=d, max_seq_len=max_len if "k_pool" in inp else None)
     assert np.all(np.isfinite(bf16_bits_to_f32(out)))
