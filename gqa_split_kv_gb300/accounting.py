@@ -30,6 +30,17 @@ def _groups(G: int):
     return ng, gr
 
 
+def _passes(G: int, D: int):
+    """(sub-groups per pass, passes per KV head, rows per sub-group): a pass runs the
+    largest power of two of sub-groups that divides their number, at most 2 at
+    D = 128, else 4."""
+    ng, gr = _groups(G)
+    per, cap = 1, (2 if D == 128 else 4)
+    while per * 2 <= cap and ng % (per * 2) == 0:
+        per *= 2
+    return per, -(-ng // per), gr
+
+
 def piece_counts(seq_lens, Hkv: int, G: int, S: int, D: int) -> np.ndarray:
     """Pieces of every segment, shape [B, Hkv * ceil(G/8)].
 
@@ -39,8 +50,8 @@ def piece_counts(seq_lens, Hkv: int, G: int, S: int, D: int) -> np.ndarray:
     without blocks, then its blocks, then padding); the line is cut into ranges
     of q positions."""
     lens = np.asarray(seq_lens, dtype=np.int64)
-    ng, _ = _groups(G)
-    U = Hkv * ng
+    _, npass, _ = _passes(G, D)
+    U = Hkv * npass
     nblk = (lens + BLOCK - 1) // BLOCK
     B = len(lens)
     if S == 1:
@@ -63,13 +74,13 @@ def traffic_bytes(B: int, Hq: int, Hkv: int, D: int, seq_lens, S: int, page_size
     are its G query heads x q_len query tokens, and K/V are still read once."""
     lens = np.asarray(seq_lens, dtype=np.int64)
     G = Hq // Hkv * q_len
-    ng, gr = _groups(G)
+    per, npass, gr = _passes(G, D)
     kv = 2 * D * 2 * Hkv * int(lens.sum())
     q = B * Hq * q_len * D * 2
     out = B * Hq * q_len * D * 2
     n = piece_counts(lens, Hkv, G, S, D)                      # [B, U]
-    # heads per sub-group slot u = h * ng + j
-    heads = np.array([min(gr, G - (u % ng) * gr) for u in range(Hkv * ng)])
+    # rows of segment slot u = h * npass + pass
+    heads = np.array([min(per * gr, G - (u % npass) * per * gr) for u in range(Hkv * npass)])
     part_rows = int(((n >= 2) * n * heads[None, :]).sum())
     partials = part_rows * (D + 2) * 4
     pt = 0 if page_size is None else 4 * int(((lens + page_size - 1) // page_size).sum())

@@ -38,7 +38,7 @@ struct CombineParams {
   const int* seq_lens;  // planned mode
   int B, Hq, S;
   int planned;
-  int G, U, ng, gr, max_len;
+  int G, U, ng, gr, ngp, npass, max_len;  // rows per KV head, segments per sequence, grouping
 };
 
 template <int D>
@@ -93,7 +93,7 @@ __global__ void __maxnreg__(40) combine_kernel(const CombineParams p) {  // 512 
         int n = p.S;
         if (p.planned) {
           const int b = row / p.Hq, h = row % p.Hq;
-          const int u = (h / p.G) * p.ng + (h % p.G) / p.gr;
+          const int u = (h / p.G) * p.npass + (h % p.G) / p.gr / p.ngp;
           n = segment_pieces(pl, lens, P, p.B, b, u);
         }
         if (!p.planned || n > kFusedMergeMax) {  // smaller segments were merged by the split kernel

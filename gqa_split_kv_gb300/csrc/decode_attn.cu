@@ -129,10 +129,10 @@ struct Launch {
   bool paged;
 };
 
-template <int D, bool PAGED>
-int launch_split(const SplitParams& prm, int grid, int smem, int dev, cudaStream_t st) {
+template <int D, bool PAGED, int NGP>
+int launch_split_ngp(const SplitParams& prm, int grid, int smem, int dev, cudaStream_t st) {
   static bool attr_done[kMaxDevices] = {false};
-  auto kern = split_kernel<D, PAGED>;
+  auto kern = split_kernel<D, PAGED, NGP>;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!attr_done[dev]) {
@@ -155,6 +155,17 @@ int launch_split(const SplitParams& prm, int grid, int smem, int dev, cudaStream
     return DA_ERR_CUDA;
   }
   return DA_OK;
+}
+
+// The split kernel is built for 1, 2 and 4 sub-groups per pass (up to NGP_MAX).
+template <int D, bool PAGED>
+int launch_split(const SplitParams& prm, int grid, int smem, int dev, cudaStream_t st) {
+  if (prm.ngp == 1) return launch_split_ngp<D, PAGED, 1>(prm, grid, smem, dev, st);
+  if (prm.ngp == 2) return launch_split_ngp<D, PAGED, 2>(prm, grid, smem, dev, st);
+  if constexpr (SplitGeo<D>::NGP_MAX >= 4) {
+    if (prm.ngp == 4) return launch_split_ngp<D, PAGED, 4>(prm, grid, smem, dev, st);
+  }
+  return DA_ERR_UNSUPPORTED;
 }
 
 template <int D>
@@ -203,6 +214,11 @@ int run_decode(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, in
   using Gm = SplitGeo<D>;
   int ng, gr;
   head_groups(a.Hq / a.Hkv, &ng, &gr);
+  // sub-groups per pass: the largest power of two, up to what the shared memory
+  // holds, that divides the sub-group count (no warp group sits idle in a pass)
+  int ngp = 1;
+  while (ngp * 2 <= SplitGeo<D>::NGP_MAX && ng % (ngp * 2) == 0) ngp *= 2;
+  const int npass = ng / ngp;
   SplitParams prm;
   std::memset(&prm, 0, sizeof(prm));
   prm.tm_k = tk;
@@ -226,7 +242,9 @@ int run_decode(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, in
   prm.G = a.Hq / a.Hkv;
   prm.ng = ng;
   prm.gr = gr;
-  prm.U = a.Hkv * ng;
+  prm.ngp = ngp;
+  prm.npass = npass;
+  prm.U = a.Hkv * npass;
   prm.max_len = a.max_len;
   prm.qlen = a.qlen;
   prm.page_size = a.page_size;
@@ -266,6 +284,8 @@ int run_decode(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, in
   cp.U = prm.U;
   cp.ng = ng;
   cp.gr = gr;
+  cp.ngp = ngp;
+  cp.npass = npass;
   cp.max_len = a.max_len;
   return launch_combine<D>(cp, dev, sms, a.stream, true);
 }

@@ -58,6 +58,7 @@ struct SplitParams {
   __nv_bfloat16* out;
   unsigned int epoch;                // tags this call's counter updates (never 0)
   int B, Hq, G, U, ng, gr;  // Hq, G count rows: query heads x qlen query tokens
+  int ngp, npass;    // sub-groups (of gr <= 8 rows) per pass over a KV head; passes per head
   int qlen;          // query tokens per sequence (1: decode; > 1: causal block at the end)
   int max_len;       // lengths are clamped to [0, max_len]
   int page_size, max_pages;
@@ -75,7 +76,9 @@ struct SplitGeo {
   static constexpr int T = D == 32 ? 256 : D <= 128 ? 128 : 64;  // tokens per tile
   static constexpr int W = 4;                       // consumer warps
   static constexpr int SB = T / 16;                 // 16-token sub-blocks per tile
-  static constexpr int SBW = SB / W;                // sub-blocks per warp: k = warp + W * i
+  // A pass runs ngp <= NGP_MAX sub-groups of <= 8 rows, one per group of W / ngp
+  // warps; the warps of a sub-group take the sub-blocks ws, ws + W / ngp, ... of a tile.
+  static constexpr int NGP_MAX = D == 128 ? 2 : 4;
   static constexpr int NP = D <= 128 ? 2 : 1;       // sub-blocks per online-softmax step
   static constexpr int NTHREADS = (W + 1) * 32;
   static constexpr int SUBW = D >= 64 ? 64 : 32;    // elements per swizzle row
@@ -83,14 +86,15 @@ struct SplitGeo {
   static constexpr int ROWB = SUBW * 2;             // 128 or 64 bytes
   static constexpr int CPR = SUBW / 8;              // 16-byte chunks per swizzle row
   static constexpr int STAGES = D == 256 ? 2 : D == 128 ? 3 : 5;
-  static constexpr int FD = D;                      // fold scratch columns per pass (one pass)
+  static constexpr int FD = D == 128 ? 64 : D;       // fold scratch columns per fold pass
   // One TMA box fills all NSUB swizzle columns of its R rows, so a tile is
   // box-major, [T/R][NSUB][R][SUBW]: R = T for a contiguous cache (one box per
   // tile), R = 16, 32 or 64 rows of one page for a paged cache.
   static constexpr int LOG_SB = SB == 16 ? 4 : SB == 8 ? 3 : SB == 4 ? 2 : SB == 2 ? 1 : 0;
   static constexpr int KV_BYTES = T * D * 2;        // one tensor, one stage
-  static constexpr int Q_SUB_BYTES = 8 * ROWB;
-  static constexpr int Q_BYTES = 8 * D * 2;
+  static constexpr int Q_SUB_BYTES = 8 * ROWB;      // one swizzle column of 8 query rows
+  static constexpr int Q_SG_BYTES = 8 * D * 2;      // the query rows of one sub-group
+  static constexpr int Q_BYTES = NGP_MAX * Q_SG_BYTES;
   static constexpr int RING = 16;                   // page-entry ring slots
   static constexpr int LA = 4;                      // page-entry prefetch distance (tiles, 128-256 KB)
   static constexpr int OFF_K = 0;
@@ -99,15 +103,16 @@ struct SplitGeo {
   static constexpr int OFF_FACC = OFF_Q + STAGES * Q_BYTES;
   static constexpr int OFF_FML = OFF_FACC + W * 8 * FD * 4;
   static constexpr int OFF_FSC = OFF_FML + W * 8 * 2 * 4;   // per-(warp, row) merge weights
-  static constexpr int OFF_FROW = OFF_FSC + W * 8 * 4;      // per-row (M, L, 1/L, -)
-  static constexpr int OFF_BAR = OFF_FROW + 8 * 4 * 4;
+  static constexpr int OFF_FROW = OFF_FSC + W * 8 * 4;      // per-row (M, L, 1/L, -), 32 rows
+  static constexpr int OFF_BAR = OFF_FROW + 32 * 4 * 4;
   static constexpr int OFF_PG = OFF_BAR + 2 * STAGES * 8;
   static constexpr int OFF_MISC = OFF_PG + RING * 32 * 4;
   static constexpr int OFF_PLAN = OFF_MISC + 16;
   static constexpr int smem_bytes(int B) { return OFF_PLAN + (2 * B + 2) * 4 + 1024; }
   static_assert(SB % W == 0 && SB <= 32, "whole sub-blocks per warp; one producer lane per block");
   static_assert((1 << LOG_SB) == SB && T >= 64, "power-of-two tiles of whole 64-token units");
-  static_assert(SBW % NP == 0, "softmax steps cover whole sub-blocks");
+  static_assert((SB / W) % NP == 0, "softmax steps cover whole sub-blocks");
+  static_assert(NGP_MAX <= W && W % NGP_MAX == 0 && D % FD == 0, "warp groups and fold passes divide evenly");
   static_assert(RING >= LA + 2, "page ring must hold the prefetch window");
   static_assert(smem_bytes(64) <= 227 * 1024, "shared memory budget");
 };
@@ -209,8 +214,9 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
   uint32_t parity = 0;
   while (cur.valid) {
     const Piece& pc = cur.pc;
-    const int h = pc.u / p.ng;
-    const int first_head = h * p.G + (pc.u % p.ng) * p.gr;
+    const int h = pc.u / p.npass;
+    const int g0 = (pc.u % p.npass) * p.ngp;  // first sub-group of this pass
+    const int nsg = min(p.ngp, p.ng - g0);     // sub-groups in this pass
     const bool first_tile = cur.t == pc.t0;
     const int ntok = min(Gm::T, pc.t1 - cur.t);
     const int nbox = PAGED ? (ntok + box_rows - 1) >> (4 + p.box_shift) : 1;  // boxes of this tile
@@ -237,7 +243,7 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
     const uint32_t kdst = sbase + Gm::OFF_K + stage * Gm::KV_BYTES;
     const uint32_t vdst = sbase + Gm::OFF_V + stage * Gm::KV_BYTES;
     const uint32_t qdst = sbase + Gm::OFF_Q + stage * Gm::Q_BYTES;
-    const uint32_t qbytes = first_tile ? (uint32_t)(Gm::NSUB * p.gr * Gm::ROWB) : 0u;
+    const uint32_t qbytes = first_tile ? (uint32_t)(nsg * Gm::NSUB * p.gr * Gm::ROWB) : 0u;
     const uint32_t kvbytes = PAGED ? (uint32_t)(nbox * box_rows * D * 2) : (uint32_t)Gm::KV_BYTES;
     if (lane == 0) mbar_arrive_expect_tx(full, 2u * kvbytes + qbytes);
     __syncwarp();
@@ -256,10 +262,10 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
       tma_load_5d(kdst, &p.tm_k, full, 0, cur.t, 0, h, pc.b);
       tma_load_5d(vdst, &p.tm_v, full, 0, cur.t, 0, h, pc.b);
     }
-    if (first_tile && lane == 0) {
-#pragma unroll
-      for (int sub = 0; sub < Gm::NSUB; ++sub)
-        tma_load_4d(qdst + sub * Gm::Q_SUB_BYTES, &p.tm_q, full, 0, sub, first_head, pc.b);
+    if (first_tile && lane < nsg * Gm::NSUB) {  // one box per (sub-group, swizzle column)
+      const int sg = lane / Gm::NSUB, sub = lane % Gm::NSUB;
+      tma_load_4d(qdst + sg * Gm::Q_SG_BYTES + sub * Gm::Q_SUB_BYTES, &p.tm_q, full, 0, sub,
+                  h * p.G + (g0 + sg) * p.gr, pc.b);
     }
     if (PAGED && n == 0) {
 #pragma unroll 1
@@ -363,7 +369,7 @@ __device__ __forceinline__ void merge_segment(const SplitParams& p, int b, int f
   }
 }
 
-template <int D, bool PAGED>
+template <int D, bool PAGED, int NGP>
 __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan& pl, const int* lens, const int* P,
                                                uint8_t* smem, uint32_t sbase, volatile int* abort_flag) {
   using Gm = SplitGeo<D>;
@@ -393,6 +399,11 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
   const int k_chk = (lane >> 3) & 1;
   const int v_row0 = (lane & 7) + (((lane >> 3) & 1) << 3);
   const int v_chk = lane >> 4;
+  // warp group of this warp's sub-group (NGP sub-groups per pass, p.ngp == NGP),
+  // and its stripe within the group
+  constexpr int WS = Gm::W / NGP;  // warps per sub-group
+  constexpr int SBW = Gm::SB / WS; // sub-blocks per warp and tile
+  const int sg = warp / WS, ws = warp % WS;
 
   if (p.S >= 2) {
     // empty sequences have no pieces on the block line: write their zero outputs
@@ -414,23 +425,25 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
 #pragma unroll
     for (int c = 0; c < NB8; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
     float m_run = kNegInf, l_run = 0.f;
-    const int h = pc.u / p.ng;
-    const int first_head = h * p.G + (pc.u % p.ng) * p.gr;
-    const int nrows = min(p.gr, p.G - (pc.u % p.ng) * p.gr);
+    const int h = pc.u / p.npass;
+    const int pass_u = pc.u % p.npass;
+    const int gidx = pass_u * p.ngp + sg;  // this warp's sub-group
+    const int first_head = h * p.G + gidx * p.gr;
+    const int nrows = gidx < p.ng ? min(p.gr, p.G - gidx * p.gr) : 0;  // 0: nothing to do this piece
     // Rows are (query head, query token i); query token i of a block of qlen sees
     // the tokens before L - qlen + 1 + i.  lim_row bounds this thread's MMA row,
     // lim_min every row of the warp (qlen == 1: both are the piece end).
     int lim_row = pc.t1, lim_min = pc.t1;
     if (p.qlen > 1) {
       const int L = lens[pc.b];
-      lim_row = min(pc.t1, L - (p.qlen - 1 - ((pc.u % p.ng) * p.gr + g) % p.qlen));
+      lim_row = min(pc.t1, L - (p.qlen - 1 - (gidx * p.gr + g) % p.qlen));
       lim_min = min(pc.t1, L - p.qlen + 1);
     }
 
     for (int t = pc.t0; t < pc.t1; t += Gm::T) {
       wait_bounded(bar_full + stage * 8, parity, abort_flag, p.timeout_ns);
-      if (t == pc.t0) {
-        const uint32_t qst = sbase + Gm::OFF_Q + stage * Gm::Q_BYTES;
+      if (t == pc.t0 && nrows > 0) {
+        const uint32_t qst = sbase + Gm::OFF_Q + stage * Gm::Q_BYTES + sg * Gm::Q_SG_BYTES;
 #pragma unroll
         for (int jq = 0; jq < D / 32; ++jq) {
           const int c = 4 * jq + (lane >> 3);
@@ -449,15 +462,15 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
       const uint32_t kst = sbase + Gm::OFF_K + stage * Gm::KV_BYTES;
       const uint32_t vst = sbase + Gm::OFF_V + stage * Gm::KV_BYTES;
 #pragma unroll 1
-      for (int sb = 0; sb < Gm::SBW; sb += NP) {
+      for (int sb = 0; sb < (nrows > 0 ? SBW : 0); sb += NP) {  // idle warps only release the stage
         // NP sub-blocks of this warp share one online-softmax step
-        if (t + 16 * (warp + Gm::W * sb) >= pc.t1) break;  // later sub-blocks lie further out
+        if (t + 16 * (ws + WS * sb) >= pc.t1) break;  // later sub-blocks lie further out
         float x[NP][4];
         uint32_t vm_lo[NP], vm_hi[NP];
         bool tail[NP];
 #pragma unroll
         for (int i = 0; i < NP; ++i) {
-          const int kb = warp + Gm::W * (sb + i);
+          const int kb = ws + WS * (sb + i);
           const int tok0 = t + 16 * kb;
           const uint32_t blk = blk_off(kb);
           // even and odd k-chunks go to separate accumulators (two short dependency
@@ -531,7 +544,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
         m_run = m_new;
 #pragma unroll
         for (int i = 0; i < NP; ++i) {
-          const uint32_t blk = blk_off(warp + Gm::W * (sb + i));
+          const uint32_t blk = blk_off(ws + WS * (sb + i));
           // P = hi + lo in bf16: rows g (hi) and g + 8 (lo) of the A operand
           const uint32_t ph0 = pack_bf16x2(pr[i][0], pr[i][1]), ph1 = pack_bf16x2(pr[i][2], pr[i][3]);
           const uint32_t pl0 = pack_bf16x2(pr[i][0] - bf16lo_to_f32(ph0), pr[i][1] - bf16hi_to_f32(ph0));
@@ -560,8 +573,9 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
       }
     }
 
-    // ---- fold the W warps' (m, l, acc) in ascending warp order, then write.  The
-    // scratch holds FD columns per warp and row; wider heads fold in D / FD passes.
+    // ---- fold each sub-group's warps' (m, l, acc) in ascending warp order, then
+    // write.  The scratch holds FD columns per warp and row; wider heads fold in
+    // D / FD passes.  Rows of the pass: row0 + s * gr + r for sub-group s.
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
     if (g < nrows && i4 == 0) {
@@ -572,6 +586,9 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
     float* fsc = reinterpret_cast<float*>(smem + Gm::OFF_FSC);
     float* frow = reinterpret_cast<float*>(smem + Gm::OFF_FROW);
     const bool direct = pc.npieces == 1;
+    const int nsg = min(p.ngp, p.ng - pass_u * p.ngp);     // sub-groups of this pass
+    const int row0 = h * p.G + pass_u * p.ngp * p.gr;     // its first row
+    const int nrows_pass = min(nsg * p.gr, p.G - pass_u * p.ngp * p.gr);
     constexpr int FD = Gm::FD;
 #pragma unroll
     for (int pass = 0; pass < D / FD; ++pass) {
@@ -584,17 +601,17 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
       }
       named_bar_sync(1, Gm::W * 32);
       if (pass == 0) {
-        if (tid < nrows) {  // one thread per row: the W warps' merge weights and the row's (M, L)
+        // one thread per (sub-group, row): its warps' merge weights and the row's (M, L)
+        const int s = tid >> 3, r = tid & 7;
+        if (s < nsg && r < min(p.gr, p.G - (pass_u * p.ngp + s) * p.gr)) {
           float M = kNegInf;
-#pragma unroll
-          for (int w = 0; w < Gm::W; ++w) M = fmaxf(M, fml[(w * 8 + tid) * 2]);
+          for (int w = s * WS; w < (s + 1) * WS; ++w) M = fmaxf(M, fml[(w * 8 + r) * 2]);
           float L = 0.f;
-#pragma unroll
-          for (int w = 0; w < Gm::W; ++w) {
-            const float mw = fml[(w * 8 + tid) * 2];
+          for (int w = s * WS; w < (s + 1) * WS; ++w) {
+            const float mw = fml[(w * 8 + r) * 2];
             const float sc = mw == kNegInf ? 0.f : exp2_approx(mw - M);
-            fsc[w * 8 + tid] = sc;
-            L += sc * fml[(w * 8 + tid) * 2 + 1];
+            fsc[w * 8 + r] = sc;
+            L += sc * fml[(w * 8 + r) * 2 + 1];
           }
           frow[tid * 4 + 0] = M;
           frow[tid * 4 + 1] = L;
@@ -602,28 +619,29 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
         }
         named_bar_sync(1, Gm::W * 32);
       }
-      for (int e = tid; e < nrows * (FD / 2); e += Gm::W * 32) {
-        const int r = e / (FD / 2);
+      for (int e = tid; e < nsg * 8 * (FD / 2); e += Gm::W * 32) {
+        const int sr = e / (FD / 2);  // s * 8 + r
+        const int s = sr >> 3, r = sr & 7;
+        if (r >= min(p.gr, p.G - (pass_u * p.ngp + s) * p.gr)) continue;
         const int dl = 2 * (e % (FD / 2));
         const int d = pass * FD + dl;
         float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int w = 0; w < Gm::W; ++w) {
+        for (int w = s * WS; w < (s + 1) * WS; ++w) {
           const float sc = fsc[w * 8 + r];
           const float2 v = *reinterpret_cast<const float2*>(facc + (w * 8 + r) * FD + dl);
           a0 += sc * v.x;
           a1 += sc * v.y;
         }
-        const size_t row = (size_t)pc.b * p.Hq + first_head + r;
+        const size_t row = (size_t)pc.b * p.Hq + row0 + s * p.gr + r;
         if (direct) {
-          const float inv = frow[r * 4 + 2];
+          const float inv = frow[sr * 4 + 2];
           *reinterpret_cast<uint32_t*>(p.out + row * D + d) = pack_bf16x2(a0 * inv, a1 * inv);
         } else {
           const size_t slot = row * p.S + pc.j;
           *reinterpret_cast<float2*>(p.part_acc + slot * D + d) = make_float2(a0, a1);
           if (d == 0)
             *reinterpret_cast<float2*>(p.part_ml + slot * 2) =
-                make_float2(frow[r * 4] * 0.69314718055994531f, frow[r * 4 + 1]);
+                make_float2(frow[sr * 4] * 0.69314718055994531f, frow[sr * 4 + 1]);
         }
       }
       if (pass + 1 < D / FD) named_bar_sync(1, Gm::W * 32);  // scratch reused by the next pass
@@ -640,13 +658,13 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
         if (*last) __threadfence();  // acquire: the other pieces' partials are read next
       }
       named_bar_sync(1, Gm::W * 32);
-      if (*last) merge_segment<D, Gm::W>(p, pc.b, first_head, nrows, pc.npieces, fsc);
+      if (*last) merge_segment<D, Gm::W>(p, pc.b, row0, nrows_pass, pc.npieces, fsc);
     }
     named_bar_sync(1, Gm::W * 32);
   }
 }
 
-template <int D, bool PAGED>
+template <int D, bool PAGED, int NGP>
 __global__ void __launch_bounds__(SplitGeo<D>::NTHREADS, 1) split_kernel(const __grid_constant__ SplitParams p) {
   using Gm = SplitGeo<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -682,7 +700,7 @@ __global__ void __launch_bounds__(SplitGeo<D>::NTHREADS, 1) split_kernel(const _
   if (warp == Gm::W)
     split_producer<D, PAGED>(p, pl, lens, P, smem, sbase, abort_flag);
   else
-    split_consumer<D, PAGED>(p, pl, lens, P, smem, sbase, abort_flag);
+    split_consumer<D, PAGED, NGP>(p, pl, lens, P, smem, sbase, abort_flag);
 }
 
 }  // namespace da

@@ -50,6 +50,7 @@ __all__ = [
     "decode_rows",
     "head_groups",
     "piece_gap_blocks",
+    "groups_per_pass",
     "split_pieces",
     "decode_partials",
     "combine_partials",
@@ -248,12 +249,24 @@ def piece_gap_blocks(head_dim: int) -> int:
     return (2816 // head_dim + 3) // 4 * 4
 
 
-def split_pieces(seq_lens: Sequence[int], Hkv: int, G: int, num_splits: int, gap: int = 0):
-    """The partition of every (sequence, KV-head sub-group) token range into pieces.
+def groups_per_pass(G: int, head_dim: int) -> int:
+    """Sub-groups of head_groups(G) that one pass over a KV head runs together: the
+    largest power of two that divides their number, at most 2 for head_dim 128 and
+    4 otherwise."""
+    ng, per, cap = len(head_groups(G)), 1, (2 if head_dim == 128 else 4)
+    while per * 2 <= cap and ng % (per * 2) == 0:
+        per *= 2
+    return per
+
+
+def split_pieces(seq_lens: Sequence[int], Hkv: int, G: int, num_splits: int, gap: int = 0, per_pass: int = 1):
+    """The partition of every (sequence, KV head, pass) token range into pieces.
 
     Work units are 16-token blocks; sequence b has n_b = ceil(L_b / 16) of them.
-    A segment is one (b, KV head h, head sub-group j); with U = Hkv * len(head_groups(G))
-    sub-group slots u = h * ngroups + j.  The segments lie end to end on one line,
+    The G rows of a KV head form the sub-groups head_groups(G); a pass runs
+    per_pass consecutive sub-groups, npass = ceil(len(head_groups(G)) / per_pass).
+    A segment is one (b, KV head h, pass p), slot u = h * npass + p, U = Hkv * npass
+    slots per sequence.  The segments lie end to end on one line,
     in (u, b) order (slot-major); segment (b, u) takes w_b = gap + 4 * ceil(n_b / 4) positions
     (none when the sequence is empty): first `gap` positions that hold no block,
     then its n_b blocks, then empty positions up to the width.  NB = U * (w_0 +
@@ -267,10 +280,15 @@ def split_pieces(seq_lens: Sequence[int], Hkv: int, G: int, num_splits: int, gap
     blocks that share a range, in order; piece index j = r - (range of its first
     block).  This never gives a segment more than num_splits pieces.
 
-    Returns a list of dicts {b, u, h, group (first, count), piece, t0, t1, npieces}.
+    Returns a list of dicts {b, u, h, group (first row, row count), piece, t0, t1, npieces}.
     """
-    groups = head_groups(G)
-    ng = len(groups)
+    subs = head_groups(G)
+    npass = -(-len(subs) // per_pass)
+    groups = []
+    for j in range(npass):
+        part = subs[j * per_pass:(j + 1) * per_pass]
+        groups.append((part[0][0], sum(c for _, c in part)))
+    ng = npass
     U = Hkv * ng
     lens = [int(x) for x in seq_lens]
     nblk = [-(-L // BLOCK_TOKENS) for L in lens]
@@ -320,7 +338,7 @@ def decode_partials(inp: dict, num_splits: int):
     ml = np.full((B, Hq, S, 2), np.nan)
     npieces = np.zeros((B, Hq), dtype=np.int64)
     cache = {}
-    for pc in split_pieces(inp["seq_lens"], Hkv, G, S, piece_gap_blocks(D)):
+    for pc in split_pieces(inp["seq_lens"], Hkv, G, S, piece_gap_blocks(D), groups_per_pass(G, D)):
         b, h = pc["b"], pc["h"]
         if b not in cache:
             cache = {b: _kv_rows(inp, b, int(inp["seq_lens"][b]))}
@@ -409,7 +427,7 @@ def decode_multi_partials(inp: dict, num_splits: int):
     ml = np.full((B, Hq, qlen, S, 2), np.nan)
     npieces = np.zeros((B, Hq, qlen), dtype=np.int64)
     cache = {}
-    for pc in split_pieces(inp["seq_lens"], Hkv, G * qlen, S, piece_gap_blocks(D)):
+    for pc in split_pieces(inp["seq_lens"], Hkv, G * qlen, S, piece_gap_blocks(D), groups_per_pass(G * qlen, D)):
         b, kv = pc["b"], pc["h"]
         L = int(inp["seq_lens"][b])
         if b not in cache:

@@ -72,7 +72,8 @@ def test_full_size_workload(name):
     # partials of sampled segments cut into several pieces, at the same plan
     if S >= 2:
         G = wl.Hq // wl.Hkv
-        pieces = [pc for pc in oracle.split_pieces(inp["seq_lens"], wl.Hkv, G, S, oracle.piece_gap_blocks(wl.D)) if pc["npieces"] >= 2]
+        pieces = [pc for pc in oracle.split_pieces(inp["seq_lens"], wl.Hkv, G, S, oracle.piece_gap_blocks(wl.D),
+                                                    oracle.groups_per_pass(G, wl.D)) if pc["npieces"] >= 2]
         if pieces:
             segs = sorted({(pc["b"], pc["u"]) for pc in pieces})
             chosen = [segs[i] for i in rng.choice(len(segs), size=min(N_SEGMENTS, len(segs)), replace=False)]

@@ -243,9 +243,9 @@ def test_single_group_is_per_head_attention():
 
 # ------------------------------------------------------------ split rule
 
-def _check_plan(lens, Hkv, G, S, gap=0):
-    pieces = od.split_pieces(lens, Hkv, G, S, gap)
-    ng = len(od.head_groups(G))
+def _check_plan(lens, Hkv, G, S, gap=0, per=1):
+    pieces = od.split_pieces(lens, Hkv, G, S, gap, per)
+    ng = -(-len(od.head_groups(G)) // per)
     by_seg = {}
     for p in pieces:
         by_seg.setdefault((p["b"], p["u"]), []).append(p)
@@ -274,7 +274,16 @@ def test_split_rule_partitions_every_segment():
         G = int(rng.integers(1, 18))
         S = int(rng.integers(1, 12))
         gap = int(rng.choice([0, 1, 6, 12, 24, 48]))
-        pieces = _check_plan(lens, Hkv, G, S, gap)
+        per = int(rng.choice([1, 2, 4]))
+        pieces = _check_plan(lens, Hkv, G, S, gap, per)
+        # every row of every KV head is in exactly one slot's group
+        for b, L in enumerate(lens):
+            if L == 0:
+                continue
+            for h in range(Hkv):
+                rows = sorted(r for p in pieces if p["b"] == b and p["h"] == h and p["piece"] == 0
+                              for r in range(p["group"][0], p["group"][0] + p["group"][1]))
+                assert rows == list(range(G))
         if gap % 4 == 0:  # segments padded to 64-token units: pieces start on 64-token boundaries
             assert all(p["t0"] % 64 == 0 for p in pieces)
 
@@ -287,7 +296,8 @@ def test_split_rule_matches_block_by_block_brute_force():
         lens = rng.integers(0, 200, size=B).tolist()
         Hkv, G, S = int(rng.integers(1, 4)), int(rng.integers(1, 10)), int(rng.integers(2, 9))
         gap = int(rng.choice([0, 1, 3, 6, 12, 24]))
-        ng = -(-G // 8)
+        per = int(rng.choice([1, 2, 4]))
+        ng = -(-(-(-G // 8)) // per)  # passes of `per` sub-groups of <= 8 rows
         U = Hkv * ng
         line = []  # one entry per position: None (gap or padding) or (b, u, block index in segment)
         for u in range(U):
@@ -302,7 +312,7 @@ def test_split_rule_matches_block_by_block_brute_force():
             if e is not None:
                 want.setdefault((e[0], e[1], x // q), []).append(e[2])
         got = {}
-        for p in od.split_pieces(lens, Hkv, G, S, gap):
+        for p in od.split_pieces(lens, Hkv, G, S, gap, per):
             got[(p["b"], p["u"], p["t0"], p["t1"])] = True
         want_pieces = set()
         for (b, u, r), blocks in want.items():
@@ -331,7 +341,7 @@ def test_partials_follow_their_definition():
     rng = np.random.default_rng(34)
     inp = _contig_case(rng, 1, 4, 1, 32, ctx=200)
     acc, ml, npc = od.decode_partials(inp, 4)
-    pieces = od.split_pieces([200], 1, 4, 4, od.piece_gap_blocks(32))
+    pieces = od.split_pieces([200], 1, 4, 4, od.piece_gap_blocks(32), od.groups_per_pass(4, 32))
     qf, kf, vf = (od.widen_bf16(inp[n]) for n in ("q", "k", "v"))
     for p in pieces:
         for h in range(4):
@@ -351,6 +361,15 @@ def test_combine_skips_empty_slots():
     ml[..., 1] = np.nan_to_num(ml[..., 1], nan=0.0)
     out = od.combine_partials(acc, ml)
     assert np.allclose(out, od.decode_contig(**inp), rtol=0, atol=1e-12)
+
+
+def test_groups_per_pass():
+    # sub-group counts 1, 1, 2, 2, 3, 3, 6, 8
+    assert [od.groups_per_pass(G, 64) for G in (1, 8, 9, 16, 17, 24, 42, 64)] == [1, 1, 2, 2, 1, 1, 2, 4]
+    assert [od.groups_per_pass(G, 128) for G in (8, 9, 42, 64)] == [1, 2, 2, 2]
+    groups = {p["u"]: p["group"] for p in od.split_pieces([40], 2, 42, 1, 0, 2)}
+    # 42 rows = 6 sub-groups of 7; three passes of 2 sub-groups per KV head
+    assert groups == {0: (0, 14), 1: (14, 14), 2: (28, 14), 3: (0, 14), 4: (14, 14), 5: (28, 14)}
 
 
 def test_groups_larger_than_eight_are_split_evenly():
