@@ -230,7 +230,7 @@ def measure(wl, inp, steps: int, warmup: int, flush_bytes: int, dist=None, sampl
         kc, vc = to_dev(inp["k"]), to_dev(inp["v"])
         table = None
         max_len = wl.max_ctx
-    S = binding.num_splits(wl.B, wl.Hkv, max_len, wl.D)
+    S = binding.num_splits_multi(wl.B, wl.q_len, wl.Hq, wl.Hkv, max_len, wl.D)
     rows = (wl.B, wl.Hq) if wl.q_len == 1 else (wl.B, wl.Hq, wl.q_len)  # multi-query: q_len rows per head
     out = torch.empty(rows + (wl.D,), dtype=torch.bfloat16, device="cuda")
     pa = torch.empty(rows + (S, wl.D), dtype=torch.float32, device="cuda") if S > 1 else None

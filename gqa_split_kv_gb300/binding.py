@@ -19,6 +19,7 @@ __all__ = [
     "load",
     "DecodeAttnError",
     "num_splits",
+    "num_splits_multi",
     "decode_attn_contig",
     "decode_attn_paged",
     "decode_attn_multi_contig",
@@ -58,6 +59,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.decode_attn_contig.restype = i
     lib.decode_attn_paged.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, vp, vp, vp, vp]
     lib.decode_attn_paged.restype = i
+    lib.decode_num_splits_multi.argtypes = [i, i, i, i, i, i, i]
+    lib.decode_num_splits_multi.restype = i
     lib.decode_attn_multi_contig.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp, vp, vp, vp]
     lib.decode_attn_multi_contig.restype = i
     lib.decode_attn_multi_paged.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, vp, vp, vp, vp, vp]
@@ -101,6 +104,15 @@ def num_splits(batch: int, num_kv_heads: int, max_seq_len: int, head_dim: int, n
     s = load().decode_num_splits(batch, num_kv_heads, max_seq_len, head_dim, num_sms)
     if s < 0:
         raise DecodeAttnError("decode_num_splits", -s)
+    return s
+
+
+def num_splits_multi(batch: int, q_len: int, num_q_heads: int, num_kv_heads: int, max_seq_len: int,
+                     head_dim: int, num_sms: int = 0) -> int:
+    """Split count that counts every pass over a KV head (multi-query or G > 8)."""
+    s = load().decode_num_splits_multi(batch, q_len, num_q_heads, num_kv_heads, max_seq_len, head_dim, num_sms)
+    if s < 0:
+        raise DecodeAttnError("decode_num_splits_multi", -s)
     return s
 
 
@@ -194,7 +206,7 @@ def decode_attn_multi_contig(q, k, v, seq_lens=None, scale: Optional[float] = No
     if seq_lens is not None:
         _need(seq_lens, "seq_lens", torch.int32, 1)
     scale = D ** -0.5 if scale is None else float(scale)
-    S = num_splits(B, Hkv, ctx, D) if splits is None else int(splits)
+    S = num_splits_multi(B, qlen, Hq, Hkv, ctx, D) if splits is None else int(splits)
     part_acc, part_ml, seg_counters = _multi_workspace(B, Hq, qlen, Hkv, D, S, part_acc, part_ml, seg_counters,
                                                        q.device)
     if out is None:
@@ -220,7 +232,7 @@ def decode_attn_multi_paged(q, k_pool, v_pool, page_table, seq_lens, max_seq_len
     num_pages, ps, Hkv, _ = k_pool.shape
     max_pages = page_table.shape[1]
     scale = D ** -0.5 if scale is None else float(scale)
-    S = num_splits(B, Hkv, max_seq_len, D) if splits is None else int(splits)
+    S = num_splits_multi(B, qlen, Hq, Hkv, max_seq_len, D) if splits is None else int(splits)
     part_acc, part_ml, seg_counters = _multi_workspace(B, Hq, qlen, Hkv, D, S, part_acc, part_ml, seg_counters,
                                                        q.device)
     if out is None:

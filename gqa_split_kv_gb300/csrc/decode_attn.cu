@@ -113,6 +113,18 @@ void head_groups(int G, int* ng, int* gr) {
   *gr = (G + *ng - 1) / *ng;
 }
 
+// Sub-groups per pass over a KV head: the largest power of two, up to what the
+// shared memory holds, that divides the sub-group count (no warp group sits
+// idle in a pass); npass passes per KV head.
+void group_passes(int ng, int D, int* ngp, int* npass) {
+  const int cap = D == 128 ? SplitGeo<128>::NGP_MAX : D == 256 ? SplitGeo<256>::NGP_MAX
+                : D == 64 ? SplitGeo<64>::NGP_MAX : SplitGeo<32>::NGP_MAX;
+  int g = 1;
+  while (g * 2 <= cap && ng % (g * 2) == 0) g *= 2;
+  *ngp = g;
+  *npass = ng / g;
+}
+
 struct Launch {
   int B, Hq, Hkv, D, max_len, S;  // Hq counts rows: query heads x qlen
   int qlen;
@@ -214,11 +226,8 @@ int run_decode(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, in
   using Gm = SplitGeo<D>;
   int ng, gr;
   head_groups(a.Hq / a.Hkv, &ng, &gr);
-  // sub-groups per pass: the largest power of two, up to what the shared memory
-  // holds, that divides the sub-group count (no warp group sits idle in a pass)
-  int ngp = 1;
-  while (ngp * 2 <= SplitGeo<D>::NGP_MAX && ng % (ngp * 2) == 0) ngp *= 2;
-  const int npass = ng / ngp;
+  int ngp, npass;
+  group_passes(ng, D, &ngp, &npass);
   SplitParams prm;
   std::memset(&prm, 0, sizeof(prm));
   prm.tm_k = tk;
@@ -350,6 +359,18 @@ extern "C" int decode_num_splits(int batch, int num_kv_heads, int max_seq_len, i
   if (S > DA_MAX_SPLITS) S = DA_MAX_SPLITS;
   if (S < 2) S = 2;
   return (int)S;
+}
+
+extern "C" int decode_num_splits_multi(int batch, int q_len, int num_q_heads, int num_kv_heads, int max_seq_len,
+                                       int head_dim, int num_sms) {
+  if (q_len < 1 || q_len > DA_MAX_QLEN || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads * q_len > 64)
+    return -DA_ERR_INVALID_ARG;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128 && head_dim != 256) return -DA_ERR_UNSUPPORTED;
+  int ng, gr, ngp, npass;
+  head_groups(num_q_heads / num_kv_heads * q_len, &ng, &gr);
+  group_passes(ng, head_dim, &ngp, &npass);
+  return decode_num_splits(batch, num_kv_heads * npass, max_seq_len, head_dim, num_sms);
 }
 
 // Contiguous cache, qlen query tokens per sequence (rows = Hq * qlen).

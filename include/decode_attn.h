@@ -169,6 +169,19 @@ int decode_attn_contig_noalloc(const void* q, const void* k, const void* v, cons
                                float scale, void* out, void* stream);
 
 /*
+ * decode_num_splits_multi — the split count for a shape given its query heads and
+ * query tokens per sequence (host only, pure): decode_num_splits with the KV
+ * heads counted once per pass.  The G * q_len rows of a KV head form ceil(G*q_len/8)
+ * sub-groups of at most 8 rows; one pass over the KV head runs ngp of them, the
+ * largest power of two that divides their number, at most 2 for head_dim 128 and
+ * 4 otherwise; so a sequence has num_kv_heads * (sub-groups / ngp) segments.
+ * Gives the same value as decode_num_splits when G * q_len <= 8.  Returns
+ * -DA_ERR_INVALID_ARG / -DA_ERR_UNSUPPORTED for bad shapes.
+ */
+int decode_num_splits_multi(int batch, int q_len, int num_q_heads, int num_kv_heads, int max_seq_len,
+                            int head_dim, int num_sms);
+
+/*
  * decode_attn_multi_contig / decode_attn_multi_paged — multi-query decode, the
  * verification step of speculative decoding scored on "perf(dspark): overlap KV
  * staging with compute via cp.async", section "sparkinfer DSpark auto-eval —
@@ -185,7 +198,7 @@ int decode_attn_contig_noalloc(const void* q, const void* k, const void* v, cons
  *  Every other argument as for decode_attn_contig / decode_attn_paged (the same
  *  split plan, with G * q_len rows per KV head in sub-groups of at most 8).
  *  1 <= q_len <= DA_MAX_QLEN and G * q_len <= 64, else DA_ERR_INVALID_ARG /
- *  DA_ERR_UNSUPPORTED.  num_splits: decode_num_splits(batch, num_kv_heads, ...).
+ *  DA_ERR_UNSUPPORTED.  num_splits: decode_num_splits_multi(batch, q_len, ...).
  */
 int decode_attn_multi_contig(const void* q, const void* k, const void* v, const int* seq_lens, int batch,
                              int q_len, int num_q_heads, int num_kv_heads, int head_dim, int max_ctx, float scale,

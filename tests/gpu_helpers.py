@@ -114,7 +114,7 @@ def run_multi(inp, S=None, max_seq_len=None, dev_inputs=None):
         Hkv, ctx = inp["k"].shape[2], inp["k"].shape[1]
     else:
         Hkv, ctx = inp["k_pool"].shape[2], max_seq_len
-    S = binding.num_splits(B, Hkv, ctx, D) if S is None else S
+    S = binding.num_splits_multi(B, qlen, Hq, Hkv, ctx, D) if S is None else S
     acc = torch.full((B, Hq, qlen, S, D), float("nan"), dtype=torch.float32, device="cuda")
     ml = torch.full((B, Hq, qlen, S, 2), float("nan"), dtype=torch.float32, device="cuda")
     out = torch.full((B, Hq, qlen, D), float("nan"), dtype=torch.bfloat16, device="cuda")

@@ -32,7 +32,8 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(clib):
     names = declared_functions()
-    assert {"decode_num_splits", "decode_attn_contig", "decode_attn_paged", "decode_combine"} <= set(names)
+    assert {"decode_num_splits", "decode_attn_contig", "decode_attn_paged", "decode_combine",
+            "decode_num_splits_multi", "decode_attn_multi_contig", "decode_attn_multi_paged"} <= set(names)
     for n in names:
         assert hasattr(clib, n), n
 
@@ -55,6 +56,20 @@ def test_status_strings(clib):
 ])
 def test_num_splits_values(clib, args, want):
     assert clib.decode_num_splits(*args) == want
+
+
+def test_num_splits_multi(clib):
+    # 42 rows (GQA-6 x 7 tokens) = 6 sub-groups of 7; 2 per pass at D=256 -> 3 passes x 4 KV heads = 12 segments
+    assert clib.decode_num_splits_multi(1, 7, 24, 4, 4096, 256, 152) == clib.decode_num_splits(1, 12, 4096, 256, 152)
+    assert clib.decode_num_splits_multi(1, 7, 24, 4, 4096, 256, 152) == 14
+    # 16 rows at D=128: 2 sub-groups in one pass -> as many segments as KV heads
+    assert clib.decode_num_splits_multi(16, 4, 32, 8, 8192, 128, 152) == clib.decode_num_splits(16, 8, 8192, 128, 152)
+    for args in [(1, 4, 4096, 256, 152), (16, 8, 8192, 128, 152), (64, 8, 32768, 128, 152)]:
+        B, Hkv, L, D, sms = args
+        assert clib.decode_num_splits_multi(B, 1, 6 * Hkv, Hkv, L, D, sms) == clib.decode_num_splits(*args)
+    assert clib.decode_num_splits_multi(1, 0, 8, 2, 64, 64, 152) == -1
+    assert clib.decode_num_splits_multi(1, 9, 16, 2, 64, 64, 152) == -1   # 72 rows per KV head
+    assert clib.decode_num_splits_multi(1, 2, 8, 2, 64, 48, 152) == -2
 
 
 def test_num_splits_rejects_bad_shapes(clib):
