@@ -132,7 +132,7 @@ struct Launch {
   const void* q;
   const int* seq_lens;
   const int* page_table;
-  int page_size, max_pages, box_shift;
+  int page_size, max_pages, num_pages, box_shift;
   float* part_acc;
   float* part_ml;
   unsigned long long* seg_counters;
@@ -258,6 +258,7 @@ int run_decode(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, in
   prm.qlen = a.qlen;
   prm.page_size = a.page_size;
   prm.max_pages = a.max_pages;
+  prm.num_pages = a.num_pages;
   prm.box_shift = a.box_shift;
   prm.page_shift = -1;
   for (int s = 4; s < 31; ++s)
@@ -415,6 +416,7 @@ static int contig_call(const void* q, const void* k, const void* v, const int* s
   a.page_table = nullptr;
   a.page_size = 0;
   a.max_pages = 0;
+  a.num_pages = 0;
   a.box_shift = 0;
   a.qlen = qlen;
   a.part_acc = part_acc;
@@ -478,6 +480,7 @@ static int paged_call(const void* q, const void* k_pool, const void* v_pool, con
   a.page_table = page_table;
   a.page_size = page_size;
   a.max_pages = max_pages_per_seq;
+  a.num_pages = num_pages;
   a.box_shift = box_shift;
   a.qlen = qlen;
   a.part_acc = part_acc;

@@ -41,9 +41,10 @@
 
 namespace da {
 
-// Device error word (bit 0: a bounded wait ran out).  The library is one
-// translation unit, so the definition lives here; the host reads and clears it
-// through decode_device_error().
+// Device error word (bit 0: a bounded wait ran out; bit 1: a segment counter
+// update gave up; bit 2: a page-table entry outside [0, num_pages)).  The
+// library is one translation unit, so the definition lives here; the host reads
+// and clears it through decode_device_error().
 __device__ unsigned int g_error_word = 0;
 
 struct SplitParams {
@@ -61,7 +62,7 @@ struct SplitParams {
   int ngp, npass;    // sub-groups (of gr <= 8 rows) per pass over a KV head; passes per head
   int qlen;          // query tokens per sequence (1: decode; > 1: causal block at the end)
   int max_len;       // lengths are clamped to [0, max_len]
-  int page_size, max_pages;
+  int page_size, max_pages, num_pages;
   int box_shift;     // paged: a TMA box holds 16 << box_shift rows of one page (16, 32 or 64)
   int page_shift;    // log2(page_size) when it is a power of two, else -1
   int S;
@@ -230,7 +231,13 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
         cp_async_wait<0>();
       }
       __syncwarp();
-      if (lane < nbox) page = pg_ring_ptr[(n % Gm::RING) * 32 + lane];
+      if (lane < nbox) {
+        page = pg_ring_ptr[(n % Gm::RING) * 32 + lane];
+        if ((unsigned)page >= (unsigned)p.num_pages) {  // a bad entry: flag it, read page 0 instead
+          atomicOr(&g_error_word, 4u);
+          page = 0;
+        }
+      }
     }
 
     // wait until the consumers have released this stage (first pass: free)

@@ -120,7 +120,8 @@ int decode_attn_contig(const void* q, const void* k, const void* v, const int* s
  *  page_table     int32 [batch, max_pages_per_seq] on the device: token t of
  *                 sequence b is row t % page_size of page page_table[b, t / page_size].
  *                 Entries past ceil(L_b / page_size) are never read.  Entries that
- *                 are read must lie in [0, num_pages).
+ *                 are read must lie in [0, num_pages); one that does not sets bit 2
+ *                 of the device error word (decode_device_error) and reads page 0.
  *  seq_lens       int32 [batch] on the device (required); clamped to
  *                 [0, min(max_seq_len, max_pages_per_seq * page_size)]
  *  Other arguments as for decode_attn_contig.  Each 16-token block is fetched from
@@ -215,8 +216,12 @@ const char* decode_status_string(int status);
 
 /*
  * decode_device_error — synchronise `stream`, then read and clear the device error
- * word of the current device.  *flags receives the word (0 = no kernel gave up on a
- * wait).  Returns DA_OK, DA_ERR_TIMEOUT when flags != 0, or DA_ERR_CUDA.
+ * word of the current device.  *flags receives the word: bit 0 a kernel gave up on
+ * a bounded wait, bit 1 a segment-counter update gave up, bit 2 a page-table entry
+ * read by decode_attn_paged / decode_attn_multi_paged was outside [0, num_pages)
+ * (that box was read from page 0 instead, so the affected rows are wrong but no
+ * copy leaves the pool).  Returns DA_OK when flags == 0, DA_ERR_TIMEOUT otherwise,
+ * or DA_ERR_CUDA.
  */
 int decode_device_error(void* stream, unsigned int* flags);
 

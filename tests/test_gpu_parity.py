@@ -188,3 +188,54 @@ def test_bounded_wait_gives_up_and_the_context_stays_usable():
     inp = contig_case(16, 2, 8, 2, 64, ctx=300, lens=[300, 45])
     ref = oracle.decode_contig(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["scale"])
     check_out(run(inp, 3)[0], ref, "after the self-test")
+
+
+def test_out_of_range_page_entry_is_flagged_not_followed():
+    """A page-table entry outside the pool sets bit 2 of the device error word; the
+    box is read from page 0 instead, so nothing outside the pool is read and the
+    sequences whose entries are valid are still exact."""
+    from gqa_split_kv_gb300 import binding
+    inp = contig_case(17, 3, 16, 4, 128, ctx=300, lens=[300, 90, 200])
+    rng = np.random.default_rng(17)
+    kp, vp, table = contig_to_paged(inp["k"], inp["v"], inp["seq_lens"], 32, rng)
+    ref = oracle.decode_contig(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["scale"])
+    for bad in (-7, kp.shape[0], 1 << 30):
+        t = table.copy()
+        t[1, 1] = bad  # sequence 1, tokens 32..63
+        pin = dict(q=inp["q"], k_pool=kp, v_pool=vp, page_table=t, seq_lens=inp["seq_lens"], page_size=32,
+                   scale=inp["scale"])
+        B, Hq, D = inp["q"].shape
+        d = to_device(pin)
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+        binding.decode_attn_paged(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["seq_lens"], 300,
+                                  scale=inp["scale"], splits=1, out=out)
+        assert binding.device_error() == 4
+        from gpu_helpers import host_bits
+        got = host_bits(out)
+        check_out(got[[0, 2]], ref[[0, 2]], "valid sequences beside a bad entry")
+    assert binding.device_error() == 0
+
+
+def test_kernels_write_nothing_outside_their_buffers():
+    """Guard bands (canaries) around the output and partial buffers stay untouched."""
+    from gqa_split_kv_gb300 import binding
+    inp = contig_case(18, 4, 24, 4, 256, ctx=700, lens=[700, 1, 333, 0])
+    B, Hq, D = inp["q"].shape
+    d = to_device(inp)
+    GUARD = 4096
+    for S in (1, 6, 40):
+        out_raw = torch.full((2 * GUARD + B * Hq * D,), -3.0, dtype=torch.bfloat16, device="cuda")
+        acc_raw = torch.full((2 * GUARD + B * Hq * S * D,), 7.0, dtype=torch.float32, device="cuda")
+        ml_raw = torch.full((2 * GUARD + B * Hq * S * 2,), 9.0, dtype=torch.float32, device="cuda")
+        out = out_raw[GUARD:GUARD + B * Hq * D].view(B, Hq, D)
+        acc = acc_raw[GUARD:GUARD + B * Hq * S * D].view(B, Hq, S, D)
+        ml = ml_raw[GUARD:GUARD + B * Hq * S * 2].view(B, Hq, S, 2)
+        binding.decode_attn_contig(d["q"], d["k"], d["v"], d["seq_lens"], scale=inp["scale"], splits=S,
+                                   part_acc=acc, part_ml=ml, out=out)
+        torch.cuda.synchronize()
+        assert binding.device_error() == 0
+        for raw, val in ((out_raw, -3.0), (acc_raw, 7.0), (ml_raw, 9.0)):
+            assert torch.all(raw[:GUARD] == val) and torch.all(raw[-GUARD:] == val), S
+        ref = oracle.decode_contig(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["scale"])
+        from gpu_helpers import host_bits
+        check_out(host_bits(out), ref, f"canaries S={S}")
