@@ -72,21 +72,21 @@ struct SplitParams {
 
 template <int D>
 struct SplitGeo {
-  // Tiles carry 32 KB (D <= 64) or 64 KB (D >= 128) of K+V so the per-tile costs
-  // (barrier round trip, TMA issue) stay small against the bytes moved.
-  static constexpr int T = D == 32 ? 256 : D <= 128 ? 128 : 64;  // tokens per tile
+  // Tiles carry 32 KB (D = 32) or 64 KB of K+V so the per-tile costs (barrier
+  // round trip, TMA issue) stay small against the bytes moved.
+  static constexpr int T = D <= 64 ? 256 : D <= 128 ? 128 : 64;  // tokens per tile
   static constexpr int W = 4;                       // consumer warps
   static constexpr int SB = T / 16;                 // 16-token sub-blocks per tile
   // A pass runs ngp <= NGP_MAX sub-groups of <= 8 rows, one per group of W / ngp
   // warps; the warps of a sub-group take the sub-blocks ws, ws + W / ngp, ... of a tile.
   static constexpr int NGP_MAX = D == 128 ? 2 : 4;
-  static constexpr int NP = D <= 128 ? 2 : 1;       // sub-blocks per online-softmax step
+  static constexpr int NP = D <= 64 ? 4 : D <= 128 ? 2 : 1;  // sub-blocks per online-softmax step
   static constexpr int NTHREADS = (W + 1) * 32;
   static constexpr int SUBW = D >= 64 ? 64 : 32;    // elements per swizzle row
   static constexpr int NSUB = D / SUBW;             // swizzle rows per token
   static constexpr int ROWB = SUBW * 2;             // 128 or 64 bytes
   static constexpr int CPR = SUBW / 8;              // 16-byte chunks per swizzle row
-  static constexpr int STAGES = D == 256 ? 2 : D == 128 ? 3 : 5;
+  static constexpr int STAGES = D == 256 ? 2 : D >= 64 ? 3 : 5;
   static constexpr int FD = D == 128 ? 64 : D;       // fold scratch columns per fold pass
   // One TMA box fills all NSUB swizzle columns of its R rows, so a tile is
   // box-major, [T/R][NSUB][R][SUBW]: R = T for a contiguous cache (one box per
