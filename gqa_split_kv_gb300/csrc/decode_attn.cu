@@ -142,9 +142,11 @@ struct Launch {
 };
 
 template <int D, bool PAGED, int NGP>
-int launch_split_ngp(const SplitParams& prm, int grid, int smem, int dev, cudaStream_t st) {
+int launch_split_ngp(const SplitParams& prm, int grid, int smem_optin, int dev, cudaStream_t st) {
   static bool attr_done[kMaxDevices] = {false};
   auto kern = split_kernel<D, PAGED, NGP>;
+  const int smem = SplitGeo<D, NGP>::smem_bytes(prm.B);
+  if (smem > smem_optin || smem > 227 * 1024) return DA_ERR_UNSUPPORTED;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!attr_done[dev]) {
@@ -171,11 +173,11 @@ int launch_split_ngp(const SplitParams& prm, int grid, int smem, int dev, cudaSt
 
 // The split kernel is built for 1, 2 and 4 sub-groups per pass (up to NGP_MAX).
 template <int D, bool PAGED>
-int launch_split(const SplitParams& prm, int grid, int smem, int dev, cudaStream_t st) {
-  if (prm.ngp == 1) return launch_split_ngp<D, PAGED, 1>(prm, grid, smem, dev, st);
-  if (prm.ngp == 2) return launch_split_ngp<D, PAGED, 2>(prm, grid, smem, dev, st);
+int launch_split(const SplitParams& prm, int grid, int smem_optin, int dev, cudaStream_t st) {
+  if (prm.ngp == 1) return launch_split_ngp<D, PAGED, 1>(prm, grid, smem_optin, dev, st);
+  if (prm.ngp == 2) return launch_split_ngp<D, PAGED, 2>(prm, grid, smem_optin, dev, st);
   if constexpr (SplitGeo<D>::NGP_MAX >= 4) {
-    if (prm.ngp == 4) return launch_split_ngp<D, PAGED, 4>(prm, grid, smem, dev, st);
+    if (prm.ngp == 4) return launch_split_ngp<D, PAGED, 4>(prm, grid, smem_optin, dev, st);
   }
   return DA_ERR_UNSUPPORTED;
 }
@@ -222,8 +224,7 @@ int launch_combine(const CombineParams& prm, int dev, int sms, cudaStream_t st, 
 }
 
 template <int D>
-int run_decode(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, int dev, int sms) {
-  using Gm = SplitGeo<D>;
+int run_decode(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, int dev, int sms, int smem_optin) {
   int ng, gr;
   head_groups(a.Hq / a.Hkv, &ng, &gr);
   int ngp, npass;
@@ -275,9 +276,8 @@ int run_decode(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, in
   const long long work = (long long)a.B * prm.U * (nblk_max > 0 ? nblk_max : 1);
   if (ranges > work) ranges = work;
   const int grid = (int)(ranges < sms ? ranges : sms);
-  const int smem = Gm::smem_bytes(a.B);
-  if (int st = (a.paged ? launch_split<D, true>(prm, grid, smem, dev, a.stream)
-                        : launch_split<D, false>(prm, grid, smem, dev, a.stream)))
+  if (int st = (a.paged ? launch_split<D, true>(prm, grid, smem_optin, dev, a.stream)
+                        : launch_split<D, false>(prm, grid, smem_optin, dev, a.stream)))
     return st;
   if (a.S <= kFusedMergeMax) return DA_OK;  // every segment is merged inside the split kernel
   CombineParams cp;
@@ -327,10 +327,10 @@ int dispatch(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, int 
   }
   if (need > smem_optin || need > 227 * 1024) return DA_ERR_UNSUPPORTED;
   switch (a.D) {
-    case 32: return run_decode<32>(a, tk, tv, dev, sms);
-    case 64: return run_decode<64>(a, tk, tv, dev, sms);
-    case 128: return run_decode<128>(a, tk, tv, dev, sms);
-    default: return run_decode<256>(a, tk, tv, dev, sms);
+    case 32: return run_decode<32>(a, tk, tv, dev, sms, smem_optin);
+    case 64: return run_decode<64>(a, tk, tv, dev, sms, smem_optin);
+    case 128: return run_decode<128>(a, tk, tv, dev, sms, smem_optin);
+    default: return run_decode<256>(a, tk, tv, dev, sms, smem_optin);
   }
 }
 

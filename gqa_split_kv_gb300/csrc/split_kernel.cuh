@@ -70,7 +70,7 @@ struct SplitParams {
   unsigned long long timeout_ns;
 };
 
-template <int D>
+template <int D, int NGP = 1>  // NGP: sub-groups per pass (the query-row slots per stage)
 struct SplitGeo {
   // Tiles carry 32 KB (D = 32) or 64 KB of K+V so the per-tile costs (barrier
   // round trip, TMA issue) stay small against the bytes moved.
@@ -87,7 +87,8 @@ struct SplitGeo {
   static constexpr int ROWB = SUBW * 2;             // 128 or 64 bytes
   static constexpr int CPR = SUBW / 8;              // 16-byte chunks per swizzle row
   static constexpr int STAGES = D == 256 ? 2 : D >= 64 ? 3 : 5;
-  static constexpr int FD = D == 128 ? 64 : D;       // fold scratch columns per fold pass
+  // fold scratch columns per fold pass (two passes at D = 128 with extra query rows)
+  static constexpr int FD = D == 128 && NGP > 1 ? 64 : D;
   // One TMA box fills all NSUB swizzle columns of its R rows, so a tile is
   // box-major, [T/R][NSUB][R][SUBW]: R = T for a contiguous cache (one box per
   // tile), R = 16, 32 or 64 rows of one page for a paged cache.
@@ -95,7 +96,7 @@ struct SplitGeo {
   static constexpr int KV_BYTES = T * D * 2;        // one tensor, one stage
   static constexpr int Q_SUB_BYTES = 8 * ROWB;      // one swizzle column of 8 query rows
   static constexpr int Q_SG_BYTES = 8 * D * 2;      // the query rows of one sub-group
-  static constexpr int Q_BYTES = NGP_MAX * Q_SG_BYTES;
+  static constexpr int Q_BYTES = NGP * Q_SG_BYTES;
   static constexpr int RING = 16;                   // page-entry ring slots
   static constexpr int LA = 4;                      // page-entry prefetch distance (tiles, 128-256 KB)
   static constexpr int OFF_K = 0;
@@ -113,7 +114,8 @@ struct SplitGeo {
   static_assert(SB % W == 0 && SB <= 32, "whole sub-blocks per warp; one producer lane per block");
   static_assert((1 << LOG_SB) == SB && T >= 64, "power-of-two tiles of whole 64-token units");
   static_assert((SB / W) % NP == 0, "softmax steps cover whole sub-blocks");
-  static_assert(NGP_MAX <= W && W % NGP_MAX == 0 && D % FD == 0, "warp groups and fold passes divide evenly");
+  static_assert(NGP <= NGP_MAX && NGP_MAX <= W && W % NGP_MAX == 0 && D % FD == 0,
+                "warp groups and fold passes divide evenly");
   static_assert(RING >= LA + 2, "page ring must hold the prefetch window");
   static_assert(smem_bytes(64) <= 227 * 1024, "shared memory budget");
 };
@@ -178,10 +180,10 @@ struct TileCursor {
   }
 };
 
-template <int D, bool PAGED>
+template <int D, bool PAGED, int NGP>
 __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan& pl, const int* lens, const int* P,
                                                uint8_t* smem, uint32_t sbase, volatile int* abort_flag) {
-  using Gm = SplitGeo<D>;
+  using Gm = SplitGeo<D, NGP>;
   const int lane = threadIdx.x & 31;
   const uint32_t bar_full = sbase + Gm::OFF_BAR;
   const uint32_t bar_empty = bar_full + Gm::STAGES * 8;
@@ -379,7 +381,7 @@ __device__ __forceinline__ void merge_segment(const SplitParams& p, int b, int f
 template <int D, bool PAGED, int NGP>
 __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan& pl, const int* lens, const int* P,
                                                uint8_t* smem, uint32_t sbase, volatile int* abort_flag) {
-  using Gm = SplitGeo<D>;
+  using Gm = SplitGeo<D, NGP>;
   constexpr int KCH = D / 16;  // k-chunks of the QK^T product
   constexpr int NB8 = D / 8;   // 8-column blocks of the PV product
   constexpr int NP = Gm::NP;
@@ -608,9 +610,11 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
       }
       named_bar_sync(1, Gm::W * 32);
       if (pass == 0) {
-        // one thread per (sub-group, row): its warps' merge weights and the row's (M, L)
-        const int s = tid >> 3, r = tid & 7;
-        if (s < nsg && r < min(p.gr, p.G - (pass_u * p.ngp + s) * p.gr)) {
+        // one thread per row of the pass: its sub-group's warps' merge weights and
+        // the row's (M, L); row sr is row r of sub-group s
+        const int sr = tid;
+        const int s = NGP == 1 ? 0 : sr / p.gr, r = NGP == 1 ? sr : sr - s * p.gr;
+        if (sr < nrows_pass) {
           float M = kNegInf;
           for (int w = s * WS; w < (s + 1) * WS; ++w) M = fmaxf(M, fml[(w * 8 + r) * 2]);
           float L = 0.f;
@@ -620,16 +624,15 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
             fsc[w * 8 + r] = sc;
             L += sc * fml[(w * 8 + r) * 2 + 1];
           }
-          frow[tid * 4 + 0] = M;
-          frow[tid * 4 + 1] = L;
-          frow[tid * 4 + 2] = L > 0.f ? 1.f / L : 0.f;
+          frow[sr * 4 + 0] = M;
+          frow[sr * 4 + 1] = L;
+          frow[sr * 4 + 2] = L > 0.f ? 1.f / L : 0.f;
         }
         named_bar_sync(1, Gm::W * 32);
       }
-      for (int e = tid; e < nsg * 8 * (FD / 2); e += Gm::W * 32) {
-        const int sr = e / (FD / 2);  // s * 8 + r
-        const int s = sr >> 3, r = sr & 7;
-        if (r >= min(p.gr, p.G - (pass_u * p.ngp + s) * p.gr)) continue;
+      for (int e = tid; e < nrows_pass * (FD / 2); e += Gm::W * 32) {
+        const int sr = e / (FD / 2);  // row of the pass: row r of sub-group s
+        const int s = NGP == 1 ? 0 : sr / p.gr, r = NGP == 1 ? sr : sr - s * p.gr;
         const int dl = 2 * (e % (FD / 2));
         const int d = pass * FD + dl;
         float a0 = 0.f, a1 = 0.f;
@@ -639,7 +642,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
           a0 += sc * v.x;
           a1 += sc * v.y;
         }
-        const size_t row = (size_t)pc.b * p.Hq + row0 + s * p.gr + r;
+        const size_t row = (size_t)pc.b * p.Hq + row0 + sr;
         if (direct) {
           const float inv = frow[sr * 4 + 2];
           *reinterpret_cast<uint32_t*>(p.out + row * D + d) = pack_bf16x2(a0 * inv, a1 * inv);
@@ -673,7 +676,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
 
 template <int D, bool PAGED, int NGP>
 __global__ void __launch_bounds__(SplitGeo<D>::NTHREADS, 1) split_kernel(const __grid_constant__ SplitParams p) {
-  using Gm = SplitGeo<D>;
+  using Gm = SplitGeo<D, NGP>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
@@ -705,7 +708,7 @@ __global__ void __launch_bounds__(SplitGeo<D>::NTHREADS, 1) split_kernel(const _
   build_plan_arrays(p.seq_lens, p.B, p.max_len, plan_gap_blocks(D), lens, P);
   const Plan pl = make_plan(p.B, p.U, p.S, plan_gap_blocks(D), P);
   if (warp == Gm::W)
-    split_producer<D, PAGED>(p, pl, lens, P, smem, sbase, abort_flag);
+    split_producer<D, PAGED, NGP>(p, pl, lens, P, smem, sbase, abort_flag);
   else
     split_consumer<D, PAGED, NGP>(p, pl, lens, P, smem, sbase, abort_flag);
 }
