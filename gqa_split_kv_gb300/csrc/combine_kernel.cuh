@@ -75,7 +75,16 @@ __global__ void __maxnreg__(40) combine_kernel(const CombineParams p) {  // 512 
     build_plan_arrays(p.seq_lens, p.B, p.max_len, plan_gap_blocks(D), lens, P);
     pl = make_plan(p.B, p.U, p.S, plan_gap_blocks(D), P);
   }
+  // A segment of n blocks meets at most (n - 1) / q + 2 ranges; when even the
+  // longest sequence stays within kFusedMergeMax pieces, the split kernel merged
+  // everything (batch workloads) and the CTA only waits for it.
+  if (p.planned && threadIdx.x == 0) {
+    const int nb_max = P[p.B + 1];
+    red[31] = (nb_max == 0 || (nb_max - 1) / pl.q + 2 <= kFusedMergeMax) ? 1.f : 0.f;
+  }
+  __syncthreads();
   pdl_wait_primary();
+  if (p.planned && red[31] != 0.f) return;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int jl = tid / Cg::TPS, c4 = tid % Cg::TPS;
