@@ -303,14 +303,19 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
 
 // Counts one finished piece of a segment; true for the piece that completes it.
 // The counter holds (epoch << 32) | count; a value from another call (another
-// epoch) counts as zero, so counters never need resetting.  Bounded retries.
+// epoch) counts as zero, so counters never need resetting between calls.  The
+// piece that completes the segment puts the count back to zero (no other piece
+// of this call touches the counter after it), so a replayed CUDA graph, whose
+// calls all carry the captured epoch, also starts every segment from zero.
+// Bounded retries.
 __device__ __forceinline__ bool claim_last_piece(unsigned long long* c, unsigned int epoch, int npieces) {
   unsigned long long v = *reinterpret_cast<volatile unsigned long long*>(c);
   for (int it = 0; it < (1 << 20); ++it) {
     const unsigned int cnt = (unsigned int)(v >> 32) == epoch ? (unsigned int)v : 0u;
-    const unsigned long long nv = ((unsigned long long)epoch << 32) | (unsigned long long)(cnt + 1);
+    const bool last = (int)(cnt + 1) == npieces;
+    const unsigned long long nv = ((unsigned long long)epoch << 32) | (unsigned long long)(last ? 0u : cnt + 1);
     const unsigned long long prev = atomicCAS(c, v, nv);
-    if (prev == v) return (int)(cnt + 1) == npieces;
+    if (prev == v) return last;
     v = prev;
   }
   atomicOr(&g_error_word, 2u);

@@ -104,6 +104,10 @@ int decode_num_splits(int batch, int num_kv_heads, int max_seq_len, int head_dim
  *           (each call tags its updates, so no reset is needed, even after a
  *           failed call); unused (may be NULL) when num_splits == 1.  Calls that
  *           share partial buffers or counters must not overlap on the GPU.
+ *           A call may be captured in a CUDA graph and replayed: every call
+ *           leaves the counters it used at zero.  Only after a call that ended in
+ *           DA_ERR_TIMEOUT must the counters be zeroed again before a captured
+ *           graph that uses them is replayed.
  *  out      bf16 [batch, num_q_heads, head_dim]
  *  stream   cudaStream_t
  * Enqueues the split kernel, and the combine kernel when num_splits > 8.

@@ -239,3 +239,43 @@ def test_kernels_write_nothing_outside_their_buffers():
         ref = oracle.decode_contig(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["scale"])
         from gpu_helpers import host_bits
         check_out(host_bits(out), ref, f"canaries S={S}")
+
+
+@pytest.mark.parametrize("S", [5, 40])
+def test_cuda_graph_replays_are_exact(S):
+    """A call captured in a CUDA graph carries one epoch for every replay; the
+    segment counters still restart at zero each replay (the completing piece resets
+    them), so in-kernel merges (S=5) and the combine path (S=40) stay exact."""
+    from gqa_split_kv_gb300 import binding
+    from gpu_helpers import host_bits
+    inp = contig_case(19, 3, 16, 4, 128, ctx=1500, lens=[1500, 900, 40])
+    B, Hq, D = inp["q"].shape
+    d = to_device(inp)
+    acc = torch.empty((B, Hq, S, D), dtype=torch.float32, device="cuda")
+    ml = torch.empty((B, Hq, S, 2), dtype=torch.float32, device="cuda")
+    ctr = torch.zeros(binding.counters_len(B, Hq, 4), dtype=torch.int64, device="cuda")
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+    q = d["q"].clone()
+
+    def call():
+        binding.decode_attn_contig(q, d["k"], d["v"], d["seq_lens"], scale=inp["scale"], splits=S, part_acc=acc,
+                                   part_ml=ml, seg_counters=ctr, out=out)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()  # first call outside capture: device attributes and kernel attributes are set here
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    rng = np.random.default_rng(19)
+    for rep in range(4):
+        qbits = f32_to_bf16_bits(rng.standard_normal((B, Hq, D), dtype=np.float32))
+        q.copy_(torch.from_numpy(qbits.view(np.int16)).cuda().view(torch.bfloat16))
+        g.replay()
+        torch.cuda.synchronize()
+        assert binding.device_error() == 0
+        ref = oracle.decode_contig(qbits, inp["k"], inp["v"], inp["seq_lens"], inp["scale"])
+        check_out(host_bits(out), ref, f"graph replay {rep} S={S}")
