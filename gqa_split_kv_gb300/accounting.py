@@ -42,7 +42,7 @@ def _passes(G: int, D: int):
 
 
 def piece_counts(seq_lens, Hkv: int, G: int, S: int, D: int) -> np.ndarray:
-    """Pieces of every segment, shape [B, Hkv * ceil(G/8)].
+    """Pieces of every segment, shape [B, Hkv * passes].
 
     The library's split plan: segments lie end to end on one line in (u, b)
     order (slot-major), each taking

@@ -18,7 +18,8 @@
 //   w_b  = 4 ceil(n_b / 4) + c if n_b > 0, else 0   line positions of one segment
 //   c    = 4 ceil((2816 / head_dim) / 4)      (about 176 KB of K+V streaming)
 //   P_b  = w_0 + ... + w_{b-1}                (prefix, P_B = line length / U)
-//   U    = Hkv * ceil(G / 8)                  sub-group slots per sequence
+//   U    = Hkv * passes                       segment slots per sequence (a pass runs
+//                                             one or more sub-groups of <= 8 rows)
 //   segment (b, u) = positions [s0, s0 + w_b), s0 = u P_B + P_b; its blocks
 //                    sit at [s0 + c, s0 + c + n_b), the rest hold none
 //   S >= 2: q = ceil(U P_B / ((S - 1) U)) rounded up to a multiple of 4
@@ -33,7 +34,7 @@
 namespace da {
 
 constexpr int kBlockTokens = 16;
-constexpr int kRangeQuantum = 4;  // ranges are whole 64-token tiles
+constexpr int kRangeQuantum = 4;  // ranges start on 64-token units of the line
 // Segments cut into at most this many pieces are merged inside the split kernel
 // by the CTA that finishes the last piece; longer ones by the combine kernel.
 constexpr int kFusedMergeMax = 8;
@@ -51,13 +52,13 @@ struct Plan {
   int NB;      // positions on the line (blocks and gaps)
   int q;       // blocks per range (S >= 2)
   int ranges;  // ranges that hold work
-  int U;             // sub-group slots per sequence
+  int U;             // segment slots per sequence (KV head x pass)
   int S;             // partial slots per (b, h)
   int gap;           // positions before each segment's blocks
 };
 
 struct Piece {
-  int b, u;      // sequence, sub-group slot
+  int b, u;      // sequence, segment slot
   int t0, t1;    // token range [t0, t1) within the sequence
   int j;         // piece index within the segment (partial slot)
   int npieces;   // pieces of this segment

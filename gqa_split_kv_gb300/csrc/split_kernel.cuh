@@ -1,7 +1,9 @@
 // Split-KV decode kernel: one persistent CTA per SM walks its ranges of the
-// block line; for every piece it streams the K/V tiles of one (sequence, KV head)
-// through a TMA-fed shared-memory ring and runs the G query heads of the KV head
-// over them with head-packed bf16 tensor-core MMAs and an fp32 online softmax.
+// block line; for every piece it streams the K/V tiles of one (sequence, KV head,
+// pass) through a TMA-fed shared-memory ring and runs the pass's query rows over
+// them with head-packed bf16 tensor-core MMAs and an fp32 online softmax.  The
+// rows of a KV head are its G query heads (x q_len query tokens for multi-query
+// decode), in sub-groups of at most 8; a pass runs NGP sub-groups.
 //
 // Roles (warp-specialised):
 //   warp W (producer): one elected lane waits for a free stage, posts the byte
@@ -9,8 +11,8 @@
 //     piece, the query rows).  Paged caches: the lanes resolve one page-table
 //     entry per box (16, 32 or 64 rows of one page), prefetched LA tiles ahead
 //     with cp.async.
-//   warps 0..W-1 (consumers): warp w owns the 16-token sub-blocks w, w + W, ... of
-//     every tile.
+//   warps 0..W-1 (consumers): W / NGP warps per sub-group; warp ws of a group owns
+//     the 16-token sub-blocks ws, ws + W / NGP, ... of every tile.
 //
 // Prior art on the pages: the two-stage cp.async ring of "perf(dspark): overlap
 // KV staging with compute via cp.async" (section "Summary"); the per-warp-group

@@ -33,8 +33,10 @@
  *    word and returns; decode_device_error() reads it.
  *
  * The split plan.  Work is counted in 16-token blocks, n_b = ceil(L_b / 16).
- * The query heads of one KV head are processed in ceil(G / 8) equal sub-groups
- * (one pass over the KV head each); U = Hkv * ceil(G / 8) sub-group slots.
+ * The query heads of one KV head form ceil(G / 8) equal sub-groups of at most 8
+ * rows; one pass over the KV head runs ngp of them (the largest power of two that
+ * divides their number, at most 2 for head_dim 128 and 4 otherwise), so a
+ * sequence has U = Hkv * ceil(G / 8) / ngp segment slots (U = Hkv when G <= 8).
  * The segments (b, u) lie end to end on one line in (u, b) order (slot-major);
  * segment (b, u) takes w_b = c + 4*ceil(n_b / 4) positions, c = 4*ceil((2816 /
  * head_dim) / 4) of them without blocks (they stand for the fixed cost of a
@@ -99,7 +101,8 @@ int decode_num_splits(int batch, int num_kv_heads, int max_seq_len, int head_dim
  *           natural-log units of the scaled score: caller-owned scratch, unused
  *           (may be NULL) when num_splits == 1.  Slots the plan does not use are not
  *           written.
- *  seg_counters  uint64 [batch * num_kv_heads * ceil(G / 8)]: caller-owned, zeroed
+ *  seg_counters  uint64 [batch * num_kv_heads * ceil(G / 8)] (at least batch * U entries are
+ *           used): caller-owned, zeroed
  *           once before the first call and then reusable by every later call
  *           (each call tags its updates, so no reset is needed, even after a
  *           failed call); unused (may be NULL) when num_splits == 1.  Calls that
