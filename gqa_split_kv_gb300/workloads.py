@@ -31,6 +31,9 @@ __all__ = [
     "draw_seq_lens",
     "make_inputs",
     "contig_to_paged",
+    "quantize_int8_rows",
+    "make_int8_cache",
+    "int8_to_paged",
 ]
 
 
@@ -237,3 +240,58 @@ def contig_to_paged(k: np.ndarray, v: np.ndarray, seq_lens: np.ndarray, page_siz
             kp[phys, : t1 - t0] = k[b, t0:t1]
             vp[phys, : t1 - t0] = v[b, t0:t1]
     return kp, vp, table
+
+
+def quantize_int8_rows(x: np.ndarray):
+    """Symmetric int8 quantization of the last axis: scale = max|x| / 127 per row
+    (1 for an all-zero row), values rint(x / scale) clipped to [-127, 127].
+    Returns (int8 values, float32 scales with the last axis dropped)."""
+    x = x.astype(np.float32)
+    amax = np.abs(x).max(axis=-1)
+    scale = np.where(amax > 0, amax / np.float32(127.0), np.float32(1.0)).astype(np.float32)
+    q = np.clip(np.rint(x / scale[..., None]), -127, 127).astype(np.int8)
+    return q, scale
+
+
+def make_int8_cache(rng: np.random.Generator, B: int, ctx: int, Hkv: int, D: int):
+    """A contiguous int8 KV cache from N(0, 1) values: k_i8, v_i8 [B, ctx, Hkv, D]
+    and fp32 scales k_scale, v_scale stored head-major, [B, Hkv, ctx]."""
+    out = {}
+    for name in ("k", "v"):
+        x = rng.standard_normal((B, ctx, Hkv, D), dtype=np.float32)
+        q, s = quantize_int8_rows(x)
+        out[name + "_i8"] = q
+        out[name + "_scale"] = np.ascontiguousarray(s.transpose(0, 2, 1))
+    return out
+
+
+def int8_to_paged(cache: dict, seq_lens: np.ndarray, page_size: int, rng: np.random.Generator,
+                  spare_pages: int = 0):
+    """Scatter a contiguous int8 cache (make_int8_cache) into a shuffled page pool.
+
+    Returns dict(k_pool_i8, v_pool_i8 [num_pages, page_size, Hkv, D] int8,
+    k_scale_pool, v_scale_pool [num_pages, Hkv, page_size] fp32, page_table).
+    Pages no sequence uses carry NaN scales."""
+    B, max_ctx, Hkv, D = cache["k_i8"].shape
+    ps = page_size
+    npages_b = (seq_lens.astype(np.int64) + ps - 1) // ps
+    num_pages = int(npages_b.sum()) + spare_pages
+    perm = rng.permutation(num_pages).astype(np.int32)
+    table = np.full((B, (max_ctx + ps - 1) // ps), -1, dtype=np.int32)
+    out = {n: np.zeros((max(num_pages, 1), ps, Hkv, D), np.int8) for n in ("k_pool_i8", "v_pool_i8")}
+    for n in ("k_scale_pool", "v_scale_pool"):
+        out[n] = np.full((max(num_pages, 1), Hkv, ps), np.nan, np.float32)
+    cur = 0
+    for b in range(B):
+        L = int(seq_lens[b])
+        for p in range(int(npages_b[b])):
+            phys = int(perm[cur])
+            cur += 1
+            table[b, p] = phys
+            t0, t1 = p * ps, min(L, (p + 1) * ps)
+            out["k_pool_i8"][phys, : t1 - t0] = cache["k_i8"][b, t0:t1]
+            out["v_pool_i8"][phys, : t1 - t0] = cache["v_i8"][b, t0:t1]
+            out["k_scale_pool"][phys, :, : t1 - t0] = cache["k_scale"][b, :, t0:t1]
+            out["v_scale_pool"][phys, :, : t1 - t0] = cache["v_scale"][b, :, t0:t1]
+    out["page_table"] = table
+    return out

@@ -57,6 +57,9 @@ __all__ = [
     "visible_tokens",
     "decode_multi",
     "decode_multi_partials",
+    "dequant_rows",
+    "decode_int8",
+    "decode_int8_partials",
     "BLOCK_TOKENS",
     "MAX_GROUP_ROWS",
 ]
@@ -443,4 +446,82 @@ def decode_multi_partials(inp: dict, num_splits: int):
             acc[b, h, i, pc["piece"]] = a[0]
             ml[b, h, i, pc["piece"]] = (m[0], l[0])
             npieces[b, h, i] = pc["npieces"]
+    return acc, ml, npieces
+
+
+# ------------------------------------------------------------ int8 KV cache
+#
+# "perf(dspark): overlap KV staging with compute via cp.async", section "Cost and
+# fallbacks", names an int8 KV pool read through a dequant-into-shared-memory path
+# but fixes no format.  Reading used here: symmetric int8 per (token, KV head),
+# K[t, g, :] = k_i8[t, g, :] * k_scale[g, t] (V likewise), with fp32 scales stored
+# head-major ([B, Hkv, max_ctx] contiguous, [num_pages, Hkv, page_size] paged).
+
+def dequant_rows(inp: dict, b: int, L: int):
+    """fp64 (K, V) rows [L, Hkv, D] of sequence b of an int8 cache, dequantized."""
+    if "k_i8" in inp:
+        k = inp["k_i8"][b, :L].astype(np.float64) * inp["k_scale"][b, :, :L].T.astype(np.float64)[:, :, None]
+        v = inp["v_i8"][b, :L].astype(np.float64) * inp["v_scale"][b, :, :L].T.astype(np.float64)[:, :, None]
+        return k, v
+    ps = int(inp["page_size"])
+    table = inp["page_table"]
+    ks, vs = [], []
+    for t in range(L):
+        page, row = table[b, t // ps], t % ps
+        ks.append(inp["k_pool_i8"][page, row].astype(np.float64) * inp["k_scale_pool"][page, :, row][:, None])
+        vs.append(inp["v_pool_i8"][page, row].astype(np.float64) * inp["v_scale_pool"][page, :, row][:, None])
+    if not ks:
+        Hkv, D = inp["k_pool_i8"].shape[2:]
+        return np.zeros((0, Hkv, D)), np.zeros((0, Hkv, D))
+    return np.stack(ks), np.stack(vs)
+
+
+def decode_int8(inp: dict, rows: Optional[Iterable[Tuple[int, int]]] = None) -> np.ndarray:
+    """fp64 decode over an int8 KV cache (single query token per sequence): the
+    attention definition with K, V the dequantized values.  Returns [B, Hq, D], or
+    [n, D] for the selected (b, h) rows."""
+    q = inp["q"]
+    B, Hq, D = q.shape
+    Hkv = (inp["k_i8"] if "k_i8" in inp else inp["k_pool_i8"]).shape[2]
+    G = Hq // Hkv
+    want = [(b, h) for b in range(B) for h in range(Hq)] if rows is None else list(rows)
+    res = np.zeros((len(want), D))
+    cache = {}
+    for n, (b, h) in enumerate(want):
+        L = int(inp["seq_lens"][b])
+        if L == 0:
+            continue
+        if b not in cache:
+            cache = {b: dequant_rows(inp, b, L)}
+        K, V = cache[b]
+        res[n] = attend(widen_bf16(q[b, h])[None], K[:, h // G], V[:, h // G], inp["scale"])[0]
+    return res.reshape(B, Hq, D) if rows is None else res
+
+
+def decode_int8_partials(inp: dict, num_splits: int):
+    """fp64 partials of every piece over an int8 cache, laid out as the library's
+    buffers (part_acc [B, Hq, S, D], part_ml [B, Hq, S, 2], npieces [B, Hq]); the
+    split rule is the one of decode_partials."""
+    q = inp["q"]
+    B, Hq, D = q.shape
+    Hkv = (inp["k_i8"] if "k_i8" in inp else inp["k_pool_i8"]).shape[2]
+    G = Hq // Hkv
+    S = num_splits
+    acc = np.full((B, Hq, S, D), np.nan)
+    ml = np.full((B, Hq, S, 2), np.nan)
+    npieces = np.zeros((B, Hq), dtype=np.int64)
+    cache = {}
+    for pc in split_pieces(inp["seq_lens"], Hkv, G, S, piece_gap_blocks(D), groups_per_pass(G, D)):
+        b, h = pc["b"], pc["h"]
+        if b not in cache:
+            cache = {b: dequant_rows(inp, b, int(inp["seq_lens"][b]))}
+        K, V = cache[b]
+        first, count = pc["group"]
+        heads = slice(h * G + first, h * G + first + count)
+        a, m, l = attend_partial(widen_bf16(q[b, heads]), K[pc["t0"]:pc["t1"], h], V[pc["t0"]:pc["t1"], h],
+                                 inp["scale"])
+        acc[b, heads, pc["piece"]] = a
+        ml[b, heads, pc["piece"], 0] = m
+        ml[b, heads, pc["piece"], 1] = l
+        npieces[b, heads] = pc["npieces"]
     return acc, ml, npieces

@@ -575,3 +575,114 @@ def test_multi_query_planted_off_by_one_is_caught(monkeypatch):
         with monkeypatch.context() as m:
             m.setattr(od, "visible_tokens", wrong)
             assert not np.allclose(od.decode_multi(inp), ref, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------ int8 KV cache
+
+def _int8_case(seed, B, Hq, Hkv, D, ctx, lens):
+    from gqa_split_kv_gb300.workloads import make_int8_cache
+    rng = np.random.default_rng(seed)
+    inp = make_int8_cache(rng, B, ctx, Hkv, D)
+    inp.update(q=_rand_bits(rng, (B, Hq, D)), seq_lens=np.asarray(lens, np.int32),
+               scale=float(np.float32(1 / math.sqrt(D))))
+    return inp
+
+
+def test_int8_with_unit_scales_is_decode_of_the_integers():
+    inp = _int8_case(70, 2, 8, 2, 32, 50, [50, 9])
+    inp["k_scale"][:] = 1.0
+    inp["v_scale"][:] = 1.0
+    from gqa_split_kv_gb300.workloads import f32_to_bf16_bits
+    k = f32_to_bf16_bits(inp["k_i8"].astype(np.float32))  # integers |x| <= 127 are exact in bf16
+    v = f32_to_bf16_bits(inp["v_i8"].astype(np.float32))
+    ref = od.decode_contig(inp["q"], k, v, inp["seq_lens"], inp["scale"])
+    assert np.allclose(od.decode_int8(inp), ref, rtol=0, atol=1e-12)
+
+
+def test_int8_scales_act_as_documented():
+    inp = _int8_case(71, 2, 6, 2, 16, 40, [40, 13])
+    base = od.decode_int8(inp)
+    # V scales multiply the output; K scales multiply the softmax scale
+    twice_v = dict(inp, v_scale=inp["v_scale"] * 2)
+    assert np.allclose(od.decode_int8(twice_v), 2 * base, rtol=1e-13, atol=0)
+    twice_k = dict(inp, k_scale=inp["k_scale"] * 2)
+    assert np.allclose(od.decode_int8(twice_k), od.decode_int8(dict(inp, scale=inp["scale"] * 2)), rtol=0,
+                       atol=1e-12)
+
+
+def test_int8_brute_force_and_paged():
+    from gqa_split_kv_gb300.workloads import int8_to_paged
+    inp = _int8_case(72, 2, 4, 2, 8, 12, [12, 5])
+    got = od.decode_int8(inp)
+    for b, L in enumerate([12, 5]):
+        for h in range(4):
+            g = h // 2
+            q = od.widen_bf16(inp["q"][b, h])
+            num, den = np.zeros(8), 0.0
+            s = [inp["scale"] * sum(q[d] * float(inp["k_i8"][b, t, g, d]) * float(inp["k_scale"][b, g, t])
+                                    for d in range(8)) for t in range(L)]
+            m = max(s)
+            for t in range(L):
+                w = math.exp(s[t] - m)
+                den += w
+                num += w * inp["v_i8"][b, t, g].astype(np.float64) * float(inp["v_scale"][b, g, t])
+            assert np.allclose(got[b, h], num / den, rtol=0, atol=1e-12)
+    pin = dict(int8_to_paged(inp, inp["seq_lens"], 4, np.random.default_rng(1), spare_pages=2),
+               q=inp["q"], seq_lens=inp["seq_lens"], page_size=4, scale=inp["scale"])
+    assert np.array_equal(od.decode_int8(pin), got)
+
+
+def test_int8_merge_of_partials_equals_unsplit():
+    inp = _int8_case(73, 3, 8, 2, 64, 600, [600, 70, 0])
+    ref = od.decode_int8(inp)
+    cut = 0
+    for S in (1, 4, 40):
+        acc, ml, npc = od.decode_int8_partials(inp, S)
+        cut += int((npc >= 2).sum())
+        for b in range(3):
+            for h in range(8):
+                n = npc[b, h]
+                parts = [(acc[b, h, j][None], ml[b, h, j, :1], ml[b, h, j, 1:]) for j in range(n)]
+                got = od.merge_partials(parts)[0] if parts else np.zeros(64)
+                assert np.allclose(got, ref[b, h], rtol=0, atol=1e-12)
+    assert cut > 0
+
+
+def test_int8_planted_mistakes_are_caught(monkeypatch):
+    inp = _int8_case(74, 2, 4, 2, 16, 30, [30, 7])
+    ref = _int8_reference_by_hand(inp)
+    assert np.allclose(od.decode_int8(inp), ref, rtol=0, atol=1e-12)
+    good = od.dequant_rows
+
+    def k_scale_for_v(inp_, b, L):
+        k, v = good(inp_, b, L)
+        return k, v / inp_["v_scale"][b, :, :L].T[:, :, None] * inp_["k_scale"][b, :, :L].T[:, :, None]
+
+    def scales_transposed(inp_, b, L):
+        k, v = good(inp_, b, L)
+        ks = inp_["k_scale"][b, :, :L].T[:, :, None]
+        return k / ks * ks[::-1], v
+
+    for bad in (k_scale_for_v, scales_transposed):
+        with monkeypatch.context() as m:
+            m.setattr(od, "dequant_rows", bad)
+            assert not np.allclose(od.decode_int8(inp), ref, rtol=0, atol=1e-12), bad.__name__
+
+
+def _int8_reference_by_hand(inp):
+    """Dequantize with explicit loops (independent of dequant_rows), then attend."""
+    B, Hq, D = inp["q"].shape
+    Hkv = inp["k_i8"].shape[2]
+    out = np.zeros((B, Hq, D))
+    for b in range(B):
+        L = int(inp["seq_lens"][b])
+        K = np.zeros((L, Hkv, D))
+        V = np.zeros((L, Hkv, D))
+        for t in range(L):
+            for g in range(Hkv):
+                K[t, g] = inp["k_i8"][b, t, g].astype(np.float64) * float(inp["k_scale"][b, g, t])
+                V[t, g] = inp["v_i8"][b, t, g].astype(np.float64) * float(inp["v_scale"][b, g, t])
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            out[b, h] = od.attend(od.widen_bf16(inp["q"][b, h])[None], K[:, g], V[:, g], inp["scale"])[0]
+    return out
