@@ -160,6 +160,9 @@ def oracle_unit(oracle, wl, inp, b: int, g: int) -> int:
     """The oracle on one sample unit: every query row of KV head g of sequence b.
     Returns the unit's algorithmic bytes (its K/V rows and query rows)."""
     G = wl.Hq // wl.Hkv
+    if wl.kv_dtype == "int8":
+        oracle.decode_int8(inp, [(b, g * G + i) for i in range(G)])
+        return 2 * (wl.D + 4) * int(inp["seq_lens"][b]) + G * wl.D * 2
     if wl.q_len == 1:
         oracle.decode_rows(inp, [(b, g * G + i) for i in range(G)])
     else:
@@ -219,17 +222,20 @@ def measure(wl, inp, steps: int, warmup: int, flush_bytes: int, dist=None, sampl
     def to_dev(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
 
-    paged = "k_pool" in inp
+    kv8 = wl.kv_dtype == "int8"
+    paged = wl.layout == "paged"
     q = to_dev(inp["q"])
     lens = torch.from_numpy(inp["seq_lens"]).cuda()
-    if paged:
-        kc, vc = to_dev(inp["k_pool"]), to_dev(inp["v_pool"])
-        table = torch.from_numpy(inp["page_table"]).cuda()
-        max_len = wl.max_ctx
+    table = torch.from_numpy(inp["page_table"]).cuda() if paged else None
+    max_len = wl.max_ctx
+    # host arrays of the cache: (K, V) or, for int8, (K, V, K scales, V scales)
+    kv_names = ((("k_pool_i8", "v_pool_i8", "k_scale_pool", "v_scale_pool") if paged else
+                 ("k_i8", "v_i8", "k_scale", "v_scale")) if kv8 else (("k_pool", "v_pool") if paged else ("k", "v")))
+    if kv8:
+        kv_dev = [torch.from_numpy(np.ascontiguousarray(inp[n])).cuda() for n in kv_names]
     else:
-        kc, vc = to_dev(inp["k"]), to_dev(inp["v"])
-        table = None
-        max_len = wl.max_ctx
+        kv_dev = [to_dev(inp[n]) for n in kv_names]
+    kc, vc = kv_dev[0], kv_dev[1]
     S = binding.num_splits_multi(wl.B, wl.q_len, wl.Hq, wl.Hkv, max_len, wl.D)
     rows = (wl.B, wl.Hq) if wl.q_len == 1 else (wl.B, wl.Hq, wl.q_len)  # multi-query: q_len rows per head
     out = torch.empty(rows + (wl.D,), dtype=torch.bfloat16, device="cuda")
@@ -250,7 +256,13 @@ def measure(wl, inp, steps: int, warmup: int, flush_bytes: int, dist=None, sampl
     attn_contig = binding.decode_attn_contig if wl.q_len == 1 else binding.decode_attn_multi_contig
 
     def call(qq=q, kk=kc, vv=vc, ll=lens, oo=out):
-        if paged:
+        if kv8 and paged:
+            binding.decode_attn_int8_paged(qq, kk, vv, kv_dev[2], kv_dev[3], table, ll, max_len, scale=wl.scale,
+                                           splits=S, part_acc=pa, part_ml=pm, seg_counters=ctr, out=oo)
+        elif kv8:
+            binding.decode_attn_int8_contig(qq, kk, vv, kv_dev[2], kv_dev[3], ll, scale=wl.scale, splits=S,
+                                            part_acc=pa, part_ml=pm, seg_counters=ctr, out=oo)
+        elif paged:
             attn_paged(qq, kk, vv, table, ll, max_len, scale=wl.scale, splits=S, part_acc=pa, part_ml=pm,
                        seg_counters=ctr, out=oo)
         else:
@@ -283,7 +295,8 @@ def measure(wl, inp, steps: int, warmup: int, flush_bytes: int, dist=None, sampl
         dist.barrier()
     times = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]  # ms
     assert binding.device_error() == 0
-    tb = traffic_bytes(wl.B, wl.Hq, wl.Hkv, wl.D, inp["seq_lens"], S, wl.page_size if paged else None, wl.q_len)
+    tb = traffic_bytes(wl.B, wl.Hq, wl.Hkv, wl.D, inp["seq_lens"], S, wl.page_size if paged else None, wl.q_len,
+                       wl.kv_dtype)
     # the split kernel, plus the combine kernel when a segment can have more than 8 pieces
     res = {"S": S, "times_ms": times, "bytes": tb, "clocks": clocks, "launches_per_step": 1 if S <= 8 else 2}
 
@@ -291,11 +304,13 @@ def measure(wl, inp, steps: int, warmup: int, flush_bytes: int, dist=None, sampl
         # end to end through the public call: pinned host inputs -> device, call, output -> host
         host = {"q": torch.from_numpy(np.ascontiguousarray(inp["q"]).view(np.int16)).pin_memory(),
                 "lens": torch.from_numpy(inp["seq_lens"]).pin_memory()}
-        host["k"] = torch.from_numpy(np.ascontiguousarray(inp["k_pool" if paged else "k"]).view(np.int16)).pin_memory()
-        host["v"] = torch.from_numpy(np.ascontiguousarray(inp["v_pool" if paged else "v"]).view(np.int16)).pin_memory()
+        kv_host = [torch.from_numpy(np.ascontiguousarray(inp[n])).pin_memory() for n in kv_names]
+        # bf16 caches travel as their int16 bit patterns
+        kv_dst = [t if kv8 else t.view(torch.int16) for t in kv_dev]
+        kv_host = [h if kv8 else h.view(torch.int16) for h in kv_host]
         out_h = torch.empty(rows + (wl.D,), dtype=torch.int16).pin_memory()
-        qi, ki, vi = q.view(torch.int16), kc.view(torch.int16), vc.view(torch.int16)
-        h2d = sum(t.numel() * t.element_size() for t in (host["q"], host["k"], host["v"], host["lens"]))
+        qi = q.view(torch.int16)
+        h2d = sum(t.numel() * t.element_size() for t in [host["q"], host["lens"]] + kv_host)
         d2h = out_h.numel() * 2
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -305,8 +320,8 @@ def measure(wl, inp, steps: int, warmup: int, flush_bytes: int, dist=None, sampl
             e0.record(stream)
             for _ in range(n):
                 qi.copy_(host["q"], non_blocking=True)
-                ki.copy_(host["k"], non_blocking=True)
-                vi.copy_(host["v"], non_blocking=True)
+                for d, h in zip(kv_dst, kv_host):
+                    d.copy_(h, non_blocking=True)
                 lens.copy_(host["lens"], non_blocking=True)
                 call()
                 out_h.copy_(out.view(torch.int16), non_blocking=True)
@@ -358,9 +373,9 @@ def ours(args):
         "vs_baseline": (round(PAGES_US_PER_CALL[wl.name] / (1e3 * total_ms / K), 2)
                         if wl.name in PAGES_US_PER_CALL else None),
         "vs_baseline_basis": "pages' fa_split_gqa_kernel 1.11 ms/call on RTX 5090, same workload (µs ratio)",
-        "dtype": "bf16", "data": "synthetic",
+        "dtype": "bf16" if wl.kv_dtype == "bf16" else "f16 (int8 KV dequantized exactly)", "data": "synthetic",
         "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "head_dim": wl.D,
-                   "ctx": wl.max_ctx, "q_len": wl.q_len, "layout": wl.layout, "num_splits": r["S"], "accum": "fp32",
+                   "ctx": wl.max_ctx, "q_len": wl.q_len, "layout": wl.layout, "kv_dtype": wl.kv_dtype, "num_splits": r["S"], "accum": "fp32",
                    "l2": f"flushed before every step ({flush_bytes >> 20} MiB write + {flush_bytes >> 20} MiB read, "
                          "outside the timed pair)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},

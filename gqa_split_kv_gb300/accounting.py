@@ -69,13 +69,14 @@ def piece_counts(seq_lens, Hkv: int, G: int, S: int, D: int) -> np.ndarray:
 
 
 def traffic_bytes(B: int, Hq: int, Hkv: int, D: int, seq_lens, S: int, page_size: Optional[int] = None,
-                  q_len: int = 1) -> dict:
+                  q_len: int = 1, kv_dtype: str = "bf16") -> dict:
     """Bytes of one call; with q_len > 1 (multi-query decode) the rows of a KV head
-    are its G query heads x q_len query tokens, and K/V are still read once."""
+    are its G query heads x q_len query tokens, and K/V are still read once.  An
+    int8 cache moves D bytes plus a 4-byte scale per (token, KV head) and tensor."""
     lens = np.asarray(seq_lens, dtype=np.int64)
     G = Hq // Hkv * q_len
     per, npass, gr = _passes(G, D)
-    kv = 2 * D * 2 * Hkv * int(lens.sum())
+    kv = 2 * (D + 4 if kv_dtype == "int8" else 2 * D) * Hkv * int(lens.sum())
     q = B * Hq * q_len * D * 2
     out = B * Hq * q_len * D * 2
     n = piece_counts(lens, Hkv, G, S, D)                      # [B, U]

@@ -24,6 +24,8 @@ __all__ = [
     "decode_attn_paged",
     "decode_attn_multi_contig",
     "decode_attn_multi_paged",
+    "decode_attn_int8_contig",
+    "decode_attn_int8_paged",
     "decode_combine",
     "device_error",
     "selftest_bounded_wait",
@@ -65,6 +67,11 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.decode_attn_multi_contig.restype = i
     lib.decode_attn_multi_paged.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, vp, vp, vp, vp, vp]
     lib.decode_attn_multi_paged.restype = i
+    lib.decode_attn_int8_contig.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, vp, vp, vp]
+    lib.decode_attn_int8_contig.restype = i
+    lib.decode_attn_int8_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, vp, vp, vp,
+                                           vp]
+    lib.decode_attn_int8_paged.restype = i
     lib.decode_combine.argtypes = [vp, vp, i, i, i, i, vp, vp]
     lib.decode_combine.restype = i
     lib.decode_status_string.argtypes = [i]
@@ -242,6 +249,62 @@ def decode_attn_multi_paged(q, k_pool, v_pool, page_table, seq_lens, max_seq_len
                                         _ptr(part_acc), _ptr(part_ml), _ptr(seg_counters), _ptr(out),
                                         _stream(stream))
     _check("decode_attn_multi_paged", st)
+    return out
+
+
+def decode_attn_int8_contig(q, k_i8, v_i8, k_scale, v_scale, seq_lens=None, scale: Optional[float] = None,
+                            splits: Optional[int] = None, part_acc=None, part_ml=None, seg_counters=None, out=None,
+                            stream=None):
+    """Decode over an int8 cache: q [B,Hq,D] bf16; k_i8/v_i8 int8 [B,max_ctx,Hkv,D]; k_scale/v_scale fp32
+    [B,Hkv,max_ctx] (K = k_i8 * k_scale per token and KV head).  Returns out [B,Hq,D] bf16."""
+    import torch
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_i8, "k_i8", torch.int8, 4)
+    _need(v_i8, "v_i8", torch.int8, 4)
+    _need(k_scale, "k_scale", torch.float32, 3)
+    _need(v_scale, "v_scale", torch.float32, 3)
+    B, Hq, D = q.shape
+    _, ctx, Hkv, _ = k_i8.shape
+    if seq_lens is not None:
+        _need(seq_lens, "seq_lens", torch.int32, 1)
+    scale = D ** -0.5 if scale is None else float(scale)
+    S = num_splits_multi(B, 1, Hq, Hkv, ctx, D) if splits is None else int(splits)
+    part_acc, part_ml, seg_counters = _workspace(B, Hq, Hkv, D, S, part_acc, part_ml, seg_counters, q.device)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    st = load().decode_attn_int8_contig(_ptr(q), _ptr(k_i8), _ptr(v_i8), _ptr(k_scale), _ptr(v_scale),
+                                        _ptr(seq_lens), B, Hq, Hkv, D, ctx, scale, S, _ptr(part_acc), _ptr(part_ml),
+                                        _ptr(seg_counters), _ptr(out), _stream(stream))
+    _check("decode_attn_int8_contig", st)
+    return out
+
+
+def decode_attn_int8_paged(q, k_pool_i8, v_pool_i8, k_scale_pool, v_scale_pool, page_table, seq_lens,
+                           max_seq_len: int, scale: Optional[float] = None, splits: Optional[int] = None,
+                           part_acc=None, part_ml=None, seg_counters=None, out=None, stream=None):
+    """Decode over a paged int8 cache: pools int8 [num_pages,page_size,Hkv,D], scale pools fp32
+    [num_pages,Hkv,page_size]; page_table int32 [B,max_pages]; seq_lens int32 [B]."""
+    import torch
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pool_i8, "k_pool_i8", torch.int8, 4)
+    _need(v_pool_i8, "v_pool_i8", torch.int8, 4)
+    _need(k_scale_pool, "k_scale_pool", torch.float32, 3)
+    _need(v_scale_pool, "v_scale_pool", torch.float32, 3)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, Hq, D = q.shape
+    num_pages, ps, Hkv, _ = k_pool_i8.shape
+    max_pages = page_table.shape[1]
+    scale = D ** -0.5 if scale is None else float(scale)
+    S = num_splits_multi(B, 1, Hq, Hkv, max_seq_len, D) if splits is None else int(splits)
+    part_acc, part_ml, seg_counters = _workspace(B, Hq, Hkv, D, S, part_acc, part_ml, seg_counters, q.device)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    st = load().decode_attn_int8_paged(_ptr(q), _ptr(k_pool_i8), _ptr(v_pool_i8), _ptr(k_scale_pool),
+                                       _ptr(v_scale_pool), _ptr(page_table), _ptr(seq_lens), B, Hq, Hkv, D, ps,
+                                       max_pages, num_pages, int(max_seq_len), scale, S, _ptr(part_acc),
+                                       _ptr(part_ml), _ptr(seg_counters), _ptr(out), _stream(stream))
+    _check("decode_attn_int8_paged", st)
     return out
 
 

@@ -80,17 +80,24 @@ int get_encoder(EncodeTiledFn* fn) {
   return DA_OK;
 }
 
-// Tiled bf16 map; dims/box innermost first, strides in bytes for dims 1..rank-1.
-int encode_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-               const cuuint32_t* box, int head_dim) {
+// Tiled map; dims/box innermost first, strides in bytes for dims 1..rank-1.
+int encode_map_t(CUtensorMap* m, CUtensorMapDataType type, CUtensorMapSwizzle swz, const void* base, int rank,
+                 const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box) {
   EncodeTiledFn enc;
   if (int st = get_encoder(&enc)) return st;
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  const CUtensorMapSwizzle swz = head_dim >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  CUresult r = enc(m, type, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DA_OK : DA_ERR_INVALID_ARG;
+}
+
+// Tiled bf16 map with the swizzle the kernels read (128-byte rows, 64-byte at D = 32).
+int encode_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+               const cuuint32_t* box, int head_dim) {
+  return encode_map_t(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      head_dim >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, base, rank, dims,
+                      strides, box);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -139,13 +146,16 @@ struct Launch {
   void* out;
   cudaStream_t stream;
   bool paged;
+  bool kv8;                           // int8 K/V with per-(token, KV head) scales
+  const CUtensorMap* tks = nullptr;   // their scale maps
+  const CUtensorMap* tvs = nullptr;
 };
 
-template <int D, bool PAGED, int NGP>
+template <int D, bool PAGED, int NGP, bool KV8>
 int launch_split_ngp(const SplitParams& prm, int grid, int smem_optin, int dev, cudaStream_t st) {
   static bool attr_done[kMaxDevices] = {false};
-  auto kern = split_kernel<D, PAGED, NGP>;
-  const int smem = SplitGeo<D, NGP>::smem_bytes(prm.B);
+  auto kern = split_kernel<D, PAGED, NGP, KV8>;
+  const int smem = SplitGeo<D, NGP, KV8>::smem_bytes(prm.B);
   if (smem > smem_optin || smem > 227 * 1024) return DA_ERR_UNSUPPORTED;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -171,15 +181,22 @@ int launch_split_ngp(const SplitParams& prm, int grid, int smem_optin, int dev, 
   return DA_OK;
 }
 
-// The split kernel is built for 1, 2 and 4 sub-groups per pass (up to NGP_MAX).
-template <int D, bool PAGED>
-int launch_split(const SplitParams& prm, int grid, int smem_optin, int dev, cudaStream_t st) {
-  if (prm.ngp == 1) return launch_split_ngp<D, PAGED, 1>(prm, grid, smem_optin, dev, st);
-  if (prm.ngp == 2) return launch_split_ngp<D, PAGED, 2>(prm, grid, smem_optin, dev, st);
+// The split kernel is built for 1, 2 and 4 sub-groups per pass (up to NGP_MAX),
+// for bf16 and for int8 caches.
+template <int D, bool PAGED, bool KV8>
+int launch_split_kv(const SplitParams& prm, int grid, int smem_optin, int dev, cudaStream_t st) {
+  if (prm.ngp == 1) return launch_split_ngp<D, PAGED, 1, KV8>(prm, grid, smem_optin, dev, st);
+  if (prm.ngp == 2) return launch_split_ngp<D, PAGED, 2, KV8>(prm, grid, smem_optin, dev, st);
   if constexpr (SplitGeo<D>::NGP_MAX >= 4) {
-    if (prm.ngp == 4) return launch_split_ngp<D, PAGED, 4>(prm, grid, smem_optin, dev, st);
+    if (prm.ngp == 4) return launch_split_ngp<D, PAGED, 4, KV8>(prm, grid, smem_optin, dev, st);
   }
   return DA_ERR_UNSUPPORTED;
+}
+
+template <int D, bool PAGED>
+int launch_split(const SplitParams& prm, int grid, int smem_optin, int dev, cudaStream_t st, bool kv8) {
+  return kv8 ? launch_split_kv<D, PAGED, true>(prm, grid, smem_optin, dev, st)
+             : launch_split_kv<D, PAGED, false>(prm, grid, smem_optin, dev, st);
 }
 
 template <int D>
@@ -276,8 +293,12 @@ int run_decode(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, in
   const long long work = (long long)a.B * prm.U * (nblk_max > 0 ? nblk_max : 1);
   if (ranges > work) ranges = work;
   const int grid = (int)(ranges < sms ? ranges : sms);
-  if (int st = (a.paged ? launch_split<D, true>(prm, grid, smem_optin, dev, a.stream)
-                        : launch_split<D, false>(prm, grid, smem_optin, dev, a.stream)))
+  if (a.kv8) {
+    prm.tm_ks = *a.tks;
+    prm.tm_vs = *a.tvs;
+  }
+  if (int st = (a.paged ? launch_split<D, true>(prm, grid, smem_optin, dev, a.stream, a.kv8)
+                        : launch_split<D, false>(prm, grid, smem_optin, dev, a.stream, a.kv8)))
     return st;
   if (a.S <= kFusedMergeMax) return DA_OK;  // every segment is merged inside the split kernel
   CombineParams cp;
@@ -375,9 +396,11 @@ extern "C" int decode_num_splits_multi(int batch, int q_len, int num_q_heads, in
 }
 
 // Contiguous cache, qlen query tokens per sequence (rows = Hq * qlen).
+// kv8: k, v are int8 values with fp32 scales ks, vs [B, Hkv, max_ctx] (head-major).
 static int contig_call(const void* q, const void* k, const void* v, const int* seq_lens, int batch, int qlen,
                 int num_q_heads, int num_kv_heads, int head_dim, int max_ctx, float scale, int num_splits,
-                float* part_acc, float* part_ml, unsigned long long* seg_counters, void* out, void* stream) {
+                float* part_acc, float* part_ml, unsigned long long* seg_counters, void* out, void* stream,
+                bool kv8 = false, const float* ks = nullptr, const float* vs = nullptr) {
   if (qlen < 1 || qlen > DA_MAX_QLEN || num_q_heads <= 0 || num_kv_heads <= 0 ||
       num_q_heads % num_kv_heads != 0 || (long long)num_q_heads * qlen > (1 << 24))
     return DA_ERR_INVALID_ARG;
@@ -386,22 +409,41 @@ static int contig_call(const void* q, const void* k, const void* v, const int* s
   if (max_ctx < 0) return DA_ERR_INVALID_ARG;
   if (B == 0) return DA_OK;
   if (max_ctx > 0 && (!k || !v || !aligned(k, 16) || !aligned(v, 16))) return DA_ERR_INVALID_ARG;
+  if (kv8 && max_ctx > 0 && (!ks || !vs || !aligned(ks, 16) || !aligned(vs, 16))) return DA_ERR_INVALID_ARG;
+  if (kv8 && max_ctx % 4 != 0) return DA_ERR_UNSUPPORTED;  // scale rows are copied with 16-byte strides
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (max_ctx == 0) return zero_output(out, B, Hq, D, st);
   int dev, sms, smem_optin;
   if (current_device(&dev) || device_info(dev, &sms, &smem_optin)) return DA_ERR_CUDA;
 
-  // dims (swizzle row, token, swizzle column, head, batch): one box fills every
-  // swizzle column of T tokens of one head, [D/SW][T][SW] in shared memory
-  const int SW = sub_width(D);
-  const cuuint64_t row = (cuuint64_t)Hkv * D * 2;
-  const cuuint64_t dims[5] = {(cuuint64_t)SW, (cuuint64_t)max_ctx, (cuuint64_t)(D / SW), (cuuint64_t)Hkv,
-                              (cuuint64_t)B};
-  const cuuint64_t strides[4] = {row, (cuuint64_t)SW * 2, (cuuint64_t)D * 2, row * (cuuint64_t)max_ctx};
-  const cuuint32_t box[5] = {(cuuint32_t)SW, (cuuint32_t)tile_tokens(D), (cuuint32_t)(D / SW), 1, 1};
-  CUtensorMap tk, tv;
-  if (int e = encode_map(&tk, k, 5, dims, strides, box, D)) return e;
-  if (int e = encode_map(&tv, v, 5, dims, strides, box, D)) return e;
+  CUtensorMap tk, tv, tks, tvs;
+  const int T = tile_tokens(D);
+  if (!kv8) {
+    // dims (swizzle row, token, swizzle column, head, batch): one box fills every
+    // swizzle column of T tokens of one head, [D/SW][T][SW] in shared memory
+    const int SW = sub_width(D);
+    const cuuint64_t row = (cuuint64_t)Hkv * D * 2;
+    const cuuint64_t dims[5] = {(cuuint64_t)SW, (cuuint64_t)max_ctx, (cuuint64_t)(D / SW), (cuuint64_t)Hkv,
+                                (cuuint64_t)B};
+    const cuuint64_t strides[4] = {row, (cuuint64_t)SW * 2, (cuuint64_t)D * 2, row * (cuuint64_t)max_ctx};
+    const cuuint32_t box[5] = {(cuuint32_t)SW, (cuuint32_t)T, (cuuint32_t)(D / SW), 1, 1};
+    if (int e = encode_map(&tk, k, 5, dims, strides, box, D)) return e;
+    if (int e = encode_map(&tv, v, 5, dims, strides, box, D)) return e;
+  } else {
+    // int8 values: dims (D, head, token, batch), one box = [T][D] bytes of one head;
+    // scales: dims (token, head, batch), one box = the T scales of one head
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)max_ctx, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)D, (cuuint64_t)Hkv * D, (cuuint64_t)max_ctx * Hkv * D};
+    const cuuint32_t box[4] = {(cuuint32_t)D, 1, (cuuint32_t)T, 1};
+    const cuuint64_t sdims[3] = {(cuuint64_t)max_ctx, (cuuint64_t)Hkv, (cuuint64_t)B};
+    const cuuint64_t sstrides[2] = {(cuuint64_t)max_ctx * 4, (cuuint64_t)Hkv * max_ctx * 4};
+    const cuuint32_t sbox[3] = {(cuuint32_t)T, 1, 1};
+    const auto none = CU_TENSOR_MAP_SWIZZLE_NONE;
+    if (int e = encode_map_t(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, none, k, 4, dims, strides, box)) return e;
+    if (int e = encode_map_t(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, none, v, 4, dims, strides, box)) return e;
+    if (int e = encode_map_t(&tks, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, none, ks, 3, sdims, sstrides, sbox)) return e;
+    if (int e = encode_map_t(&tvs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, none, vs, 3, sdims, sstrides, sbox)) return e;
+  }
 
   Launch a;
   a.B = B;
@@ -425,14 +467,19 @@ static int contig_call(const void* q, const void* k, const void* v, const int* s
   a.out = out;
   a.stream = st;
   a.paged = false;
+  a.kv8 = kv8;
+  a.tks = &tks;
+  a.tvs = &tvs;
   return dispatch(a, tk, tv, dev, sms, smem_optin);
 }
 
 // Paged cache, qlen query tokens per sequence (rows = Hq * qlen).
+// kv8: the pools hold int8 values with fp32 scale pools ks, vs [num_pages, Hkv, page_size].
 static int paged_call(const void* q, const void* k_pool, const void* v_pool, const int* page_table, const int* seq_lens,
                int batch, int qlen, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
                int max_pages_per_seq, int num_pages, int max_seq_len, float scale, int num_splits, float* part_acc,
-               float* part_ml, unsigned long long* seg_counters, void* out, void* stream) {
+               float* part_ml, unsigned long long* seg_counters, void* out, void* stream, bool kv8 = false,
+               const float* ks = nullptr, const float* vs = nullptr) {
   if (qlen < 1 || qlen > DA_MAX_QLEN || num_q_heads <= 0 || num_kv_heads <= 0 ||
       num_q_heads % num_kv_heads != 0 || (long long)num_q_heads * qlen > (1 << 24))
     return DA_ERR_INVALID_ARG;
@@ -449,23 +496,41 @@ static int paged_call(const void* q, const void* k_pool, const void* v_pool, con
   if (cap > 0x7fffffffLL) return DA_ERR_UNSUPPORTED;
   if (!k_pool || !v_pool || !page_table || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(page_table, 4))
     return DA_ERR_INVALID_ARG;
+  if (kv8 && (!ks || !vs || !aligned(ks, 16) || !aligned(vs, 16))) return DA_ERR_INVALID_ARG;
   int dev, sms, smem_optin;
   if (current_device(&dev) || device_info(dev, &sms, &smem_optin)) return DA_ERR_CUDA;
 
-  // dims (swizzle row, row in page, swizzle column, head, page): one box fills every
-  // swizzle column of R rows of one page, [D/SW][R][SW] in shared memory, with
-  // R = 64, 32 or 16, the largest that divides the page size (tiles start on
-  // 64-token boundaries, so such a box never crosses a page)
+  // One box covers R rows of one page, R = 64, 32 or 16, the largest that divides
+  // the page size (tiles start on 64-token boundaries, so a box never crosses a page).
   const int box_shift = page_size % 64 == 0 ? 2 : page_size % 32 == 0 ? 1 : 0;
-  const int SW = sub_width(D);
-  const cuuint64_t row = (cuuint64_t)Hkv * D * 2;
-  const cuuint64_t dims[5] = {(cuuint64_t)SW, (cuuint64_t)page_size, (cuuint64_t)(D / SW), (cuuint64_t)Hkv,
-                              (cuuint64_t)num_pages};
-  const cuuint64_t strides[4] = {row, (cuuint64_t)SW * 2, (cuuint64_t)D * 2, row * (cuuint64_t)page_size};
-  const cuuint32_t box[5] = {(cuuint32_t)SW, (cuuint32_t)(16 << box_shift), (cuuint32_t)(D / SW), 1, 1};
-  CUtensorMap tk, tv;
-  if (int e = encode_map(&tk, k_pool, 5, dims, strides, box, D)) return e;
-  if (int e = encode_map(&tv, v_pool, 5, dims, strides, box, D)) return e;
+  const cuuint32_t R = (cuuint32_t)(16 << box_shift);
+  CUtensorMap tk, tv, tks, tvs;
+  if (!kv8) {
+    // dims (swizzle row, row in page, swizzle column, head, page): one box fills every
+    // swizzle column of its rows, [D/SW][R][SW] in shared memory
+    const int SW = sub_width(D);
+    const cuuint64_t row = (cuuint64_t)Hkv * D * 2;
+    const cuuint64_t dims[5] = {(cuuint64_t)SW, (cuuint64_t)page_size, (cuuint64_t)(D / SW), (cuuint64_t)Hkv,
+                                (cuuint64_t)num_pages};
+    const cuuint64_t strides[4] = {row, (cuuint64_t)SW * 2, (cuuint64_t)D * 2, row * (cuuint64_t)page_size};
+    const cuuint32_t box[5] = {(cuuint32_t)SW, R, (cuuint32_t)(D / SW), 1, 1};
+    if (int e = encode_map(&tk, k_pool, 5, dims, strides, box, D)) return e;
+    if (int e = encode_map(&tv, v_pool, 5, dims, strides, box, D)) return e;
+  } else {
+    // int8 values: dims (D, head, row in page, page), one box = [R][D] bytes;
+    // scales: dims (row in page, head, page), one box = R scales of one head
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)page_size, (cuuint64_t)num_pages};
+    const cuuint64_t strides[3] = {(cuuint64_t)D, (cuuint64_t)Hkv * D, (cuuint64_t)page_size * Hkv * D};
+    const cuuint32_t box[4] = {(cuuint32_t)D, 1, R, 1};
+    const cuuint64_t sdims[3] = {(cuuint64_t)page_size, (cuuint64_t)Hkv, (cuuint64_t)num_pages};
+    const cuuint64_t sstrides[2] = {(cuuint64_t)page_size * 4, (cuuint64_t)Hkv * page_size * 4};
+    const cuuint32_t sbox[3] = {R, 1, 1};
+    const auto none = CU_TENSOR_MAP_SWIZZLE_NONE;
+    if (int e = encode_map_t(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, none, k_pool, 4, dims, strides, box)) return e;
+    if (int e = encode_map_t(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, none, v_pool, 4, dims, strides, box)) return e;
+    if (int e = encode_map_t(&tks, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, none, ks, 3, sdims, sstrides, sbox)) return e;
+    if (int e = encode_map_t(&tvs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, none, vs, 3, sdims, sstrides, sbox)) return e;
+  }
 
   Launch a;
   a.B = B;
@@ -489,6 +554,9 @@ static int paged_call(const void* q, const void* k_pool, const void* v_pool, con
   a.out = out;
   a.stream = st;
   a.paged = true;
+  a.kv8 = kv8;
+  a.tks = &tks;
+  a.tvs = &tvs;
   return dispatch(a, tk, tv, dev, sms, smem_optin);
 }
 
@@ -526,6 +594,26 @@ extern "C" int decode_attn_multi_paged(const void* q, const void* k_pool, const 
   return paged_call(q, k_pool, v_pool, page_table, seq_lens, batch, q_len, num_q_heads, num_kv_heads, head_dim,
                     page_size, max_pages_per_seq, num_pages, max_seq_len, scale, num_splits, part_acc, part_ml,
                     seg_counters, out, stream);
+}
+
+extern "C" int decode_attn_int8_contig(const void* q, const void* k_i8, const void* v_i8, const float* k_scale,
+                                       const float* v_scale, const int* seq_lens, int batch, int num_q_heads,
+                                       int num_kv_heads, int head_dim, int max_ctx, float scale, int num_splits,
+                                       float* part_acc, float* part_ml, unsigned long long* seg_counters, void* out,
+                                       void* stream) {
+  return contig_call(q, k_i8, v_i8, seq_lens, batch, 1, num_q_heads, num_kv_heads, head_dim, max_ctx, scale,
+                     num_splits, part_acc, part_ml, seg_counters, out, stream, true, k_scale, v_scale);
+}
+
+extern "C" int decode_attn_int8_paged(const void* q, const void* k_pool_i8, const void* v_pool_i8,
+                                      const float* k_scale_pool, const float* v_scale_pool, const int* page_table,
+                                      const int* seq_lens, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                      int page_size, int max_pages_per_seq, int num_pages, int max_seq_len,
+                                      float scale, int num_splits, float* part_acc, float* part_ml,
+                                      unsigned long long* seg_counters, void* out, void* stream) {
+  return paged_call(q, k_pool_i8, v_pool_i8, page_table, seq_lens, batch, 1, num_q_heads, num_kv_heads, head_dim,
+                    page_size, max_pages_per_seq, num_pages, max_seq_len, scale, num_splits, part_acc, part_ml,
+                    seg_counters, out, stream, true, k_scale_pool, v_scale_pool);
 }
 
 extern "C" int decode_combine(const float* part_acc, const float* part_ml, int batch, int num_q_heads,

@@ -50,9 +50,11 @@ namespace da {
 __device__ unsigned int g_error_word = 0;
 
 struct SplitParams {
-  CUtensorMap tm_k;  // K cache / pool
-  CUtensorMap tm_v;  // V cache / pool
-  CUtensorMap tm_q;  // Q [B, Hq, D]
+  CUtensorMap tm_k;   // K cache / pool (bf16, or int8 values)
+  CUtensorMap tm_v;   // V cache / pool
+  CUtensorMap tm_q;   // Q [B, Hq, D]
+  CUtensorMap tm_ks;  // int8 caches: K scales per (token, KV head), head-major
+  CUtensorMap tm_vs;  // int8 caches: V scales
   const int* seq_lens;
   const int* page_table;
   float* part_acc;
@@ -72,7 +74,9 @@ struct SplitParams {
   unsigned long long timeout_ns;
 };
 
-template <int D, int NGP = 1>  // NGP: sub-groups per pass (the query-row slots per stage)
+// NGP: sub-groups per pass (the query-row slots per stage); KV8: int8 K/V with
+// fp32 scales per (token, KV head), dequantized per warp into an f16 staging tile.
+template <int D, int NGP = 1, bool KV8 = false>
 struct SplitGeo {
   // Tiles carry 32 KB (D = 32) or 64 KB of K+V so the per-tile costs (barrier
   // round trip, TMA issue) stay small against the bytes moved.
@@ -88,14 +92,20 @@ struct SplitGeo {
   static constexpr int NSUB = D / SUBW;             // swizzle rows per token
   static constexpr int ROWB = SUBW * 2;             // 128 or 64 bytes
   static constexpr int CPR = SUBW / 8;              // 16-byte chunks per swizzle row
-  static constexpr int STAGES = D == 256 ? 2 : D >= 64 ? 3 : 5;
+  static constexpr int STAGES = KV8 ? (D == 256 ? 3 : D == 32 ? 6 : 4) : (D == 256 ? 2 : D >= 64 ? 3 : 5);
   // fold scratch columns per fold pass (two passes at D = 128 with extra query rows)
   static constexpr int FD = D == 128 && NGP > 1 ? 64 : D;
   // One TMA box fills all NSUB swizzle columns of its R rows, so a tile is
   // box-major, [T/R][NSUB][R][SUBW]: R = T for a contiguous cache (one box per
   // tile), R = 16, 32 or 64 rows of one page for a paged cache.
   static constexpr int LOG_SB = SB == 16 ? 4 : SB == 8 ? 3 : SB == 4 ? 2 : SB == 2 ? 1 : 0;
-  static constexpr int KV_BYTES = T * D * 2;        // one tensor, one stage
+  static constexpr int KV_BYTES = T * D * (KV8 ? 1 : 2);  // one tensor, one stage
+  // per-token scales of one tensor and stage (int8 caches): one slot of max(R, 32)
+  // floats per box, so every box lands 128-byte aligned (16-row paged boxes leave
+  // 16 floats unused per slot)
+  static constexpr int SC_BYTES = KV8 ? T * 8 : 0;
+  static constexpr int STG_BYTES = KV8 ? NP * 16 * D * 2 : 0;  // per-warp f16 tile of NP sub-blocks
+  static constexpr int al1k(int x) { return (x + 1023) / 1024 * 1024; }
   static constexpr int Q_SUB_BYTES = 8 * ROWB;      // one swizzle column of 8 query rows
   static constexpr int Q_SG_BYTES = 8 * D * 2;      // the query rows of one sub-group
   static constexpr int Q_BYTES = NGP * Q_SG_BYTES;
@@ -103,8 +113,11 @@ struct SplitGeo {
   static constexpr int LA = 4;                      // page-entry prefetch distance (tiles, 128-256 KB)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
-  static constexpr int OFF_Q = OFF_V + STAGES * KV_BYTES;
-  static constexpr int OFF_FACC = OFF_Q + STAGES * Q_BYTES;
+  static constexpr int OFF_KS = OFF_V + STAGES * KV_BYTES;
+  static constexpr int OFF_VS = OFF_KS + STAGES * SC_BYTES;
+  static constexpr int OFF_Q = al1k(OFF_VS + STAGES * SC_BYTES);
+  static constexpr int OFF_STG = OFF_Q + STAGES * Q_BYTES;
+  static constexpr int OFF_FACC = OFF_STG + W * STG_BYTES;
   static constexpr int OFF_FML = OFF_FACC + W * 8 * FD * 4;
   static constexpr int OFF_FSC = OFF_FML + W * 8 * 2 * 4;   // per-(warp, row) merge weights
   static constexpr int OFF_FROW = OFF_FSC + W * 8 * 4;      // per-row (M, L, 1/L, -), 32 rows
@@ -182,10 +195,10 @@ struct TileCursor {
   }
 };
 
-template <int D, bool PAGED, int NGP>
+template <int D, bool PAGED, int NGP, bool KV8>
 __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan& pl, const int* lens, const int* P,
                                                uint8_t* smem, uint32_t sbase, volatile int* abort_flag) {
-  using Gm = SplitGeo<D, NGP>;
+  using Gm = SplitGeo<D, NGP, KV8>;
   const int lane = threadIdx.x & 31;
   const uint32_t bar_full = sbase + Gm::OFF_BAR;
   const uint32_t bar_empty = bar_full + Gm::STAGES * 8;
@@ -255,7 +268,9 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
     const uint32_t vdst = sbase + Gm::OFF_V + stage * Gm::KV_BYTES;
     const uint32_t qdst = sbase + Gm::OFF_Q + stage * Gm::Q_BYTES;
     const uint32_t qbytes = first_tile ? (uint32_t)(nsg * Gm::NSUB * p.gr * Gm::ROWB) : 0u;
-    const uint32_t kvbytes = PAGED ? (uint32_t)(nbox * box_rows * D * 2) : (uint32_t)Gm::KV_BYTES;
+    // K/V boxes (and, for int8 caches, their per-token scales) move whole
+    const uint32_t kvbytes = PAGED ? (uint32_t)(nbox * box_rows * (D * (KV8 ? 1 : 2) + (KV8 ? 4 : 0)))
+                                   : (uint32_t)(Gm::KV_BYTES + (KV8 ? Gm::T * 4 : 0));
     if (lane == 0) mbar_arrive_expect_tx(full, 2u * kvbytes + qbytes);
     __syncwarp();
     if (PAGED) {
@@ -265,13 +280,29 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
       if (lane < nbox) {
         const int tok = cur.t + lane * box_rows;
         const int row0 = tok - page_of(p, tok) * p.page_size;
-        const uint32_t off = (uint32_t)(lane * box_rows * D * 2);
-        tma_load_5d(kdst + off, &p.tm_k, full, 0, row0, 0, h, page);
-        tma_load_5d(vdst + off, &p.tm_v, full, 0, row0, 0, h, page);
+        if constexpr (KV8) {  // [rows][D] int8 boxes and [rows] fp32 scale boxes
+          const uint32_t off = (uint32_t)(lane * box_rows * D);
+          tma_load_4d(kdst + off, &p.tm_k, full, 0, h, row0, page);
+          tma_load_4d(vdst + off, &p.tm_v, full, 0, h, row0, page);
+          const uint32_t soff = (uint32_t)(lane * max(box_rows, 32) * 4);  // 128-byte aligned slots
+          tma_load_3d(sbase + Gm::OFF_KS + stage * Gm::SC_BYTES + soff, &p.tm_ks, full, row0, h, page);
+          tma_load_3d(sbase + Gm::OFF_VS + stage * Gm::SC_BYTES + soff, &p.tm_vs, full, row0, h, page);
+        } else {
+          const uint32_t off = (uint32_t)(lane * box_rows * D * 2);
+          tma_load_5d(kdst + off, &p.tm_k, full, 0, row0, 0, h, page);
+          tma_load_5d(vdst + off, &p.tm_v, full, 0, row0, 0, h, page);
+        }
       }
     } else if (lane == 0) {
-      tma_load_5d(kdst, &p.tm_k, full, 0, cur.t, 0, h, pc.b);
-      tma_load_5d(vdst, &p.tm_v, full, 0, cur.t, 0, h, pc.b);
+      if constexpr (KV8) {
+        tma_load_4d(kdst, &p.tm_k, full, 0, h, cur.t, pc.b);
+        tma_load_4d(vdst, &p.tm_v, full, 0, h, cur.t, pc.b);
+        tma_load_3d(sbase + Gm::OFF_KS + stage * Gm::SC_BYTES, &p.tm_ks, full, cur.t, h, pc.b);
+        tma_load_3d(sbase + Gm::OFF_VS + stage * Gm::SC_BYTES, &p.tm_vs, full, cur.t, h, pc.b);
+      } else {
+        tma_load_5d(kdst, &p.tm_k, full, 0, cur.t, 0, h, pc.b);
+        tma_load_5d(vdst, &p.tm_v, full, 0, cur.t, 0, h, pc.b);
+      }
     }
     if (first_tile && lane < nsg * Gm::NSUB) {  // one box per (sub-group, swizzle column)
       const int sg = lane / Gm::NSUB, sub = lane % Gm::NSUB;
@@ -385,10 +416,35 @@ __device__ __forceinline__ void merge_segment(const SplitParams& p, int b, int f
   }
 }
 
-template <int D, bool PAGED, int NGP>
+// int8 caches: the rows of NP sub-blocks (kb0, kb0 + kbstride, ...) of an int8
+// tile [T][D] in shared memory become f16 rows of the warp's staging tile, laid out
+// like a 16-row TMA box per sub-block ([NSUB][16][SUBW], swizzled), so the bf16
+// path's ldmatrix addressing reads them unchanged.  Exact (int8 -> f16).
+template <int D, int NP, int ROWB, int SUBW>
+__device__ __forceinline__ void dequant_subblocks(const uint8_t* tile, int kb0, int kbstride, uint8_t* stg,
+                                                  int lane) {
+  constexpr int CH = D / 16;  // 16-byte int8 chunks per row
+#pragma unroll(D == 256 ? 1 : 4)
+  for (int c = lane; c < NP * 16 * CH; c += 32) {
+    const int i = c / (16 * CH), r = (c / CH) % 16, cc = c % CH;
+    const uint4 w = *reinterpret_cast<const uint4*>(tile + ((kb0 + kbstride * i) * 16 + r) * D + cc * 16);
+    uint4 lo, hi;
+    int8x4_to_f16x4(w.x, lo.x, lo.y);
+    int8x4_to_f16x4(w.y, lo.z, lo.w);
+    int8x4_to_f16x4(w.z, hi.x, hi.y);
+    int8x4_to_f16x4(w.w, hi.z, hi.w);
+    const int e0 = cc * 16;  // first f16 column of the chunk
+    uint8_t* base = stg + i * (16 * D * 2) + (e0 / SUBW) * (16 * ROWB);
+    const int ch = (e0 % SUBW) / 8;
+    *reinterpret_cast<uint4*>(base + swz<ROWB>(r, ch)) = lo;
+    *reinterpret_cast<uint4*>(base + swz<ROWB>(r, ch + 1)) = hi;
+  }
+}
+
+template <int D, bool PAGED, int NGP, bool KV8>
 __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan& pl, const int* lens, const int* P,
                                                uint8_t* smem, uint32_t sbase, volatile int* abort_flag) {
-  using Gm = SplitGeo<D, NGP>;
+  using Gm = SplitGeo<D, NGP, KV8>;
   constexpr int KCH = D / 16;  // k-chunks of the QK^T product
   constexpr int NB8 = D / 8;   // 8-column blocks of the PV product
   constexpr int NP = Gm::NP;
@@ -474,9 +530,22 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
 #pragma unroll
           for (int c = 0; c < KCH; ++c) qa[c][0] = qa[c][1] = 0u;
         }
+        if constexpr (KV8) {  // the int8 path multiplies in f16: bf16 -> f16, exact in f16's range
+#pragma unroll
+          for (int c = 0; c < KCH; ++c) {
+            qa[c][0] = pack_f16x2(bf16lo_to_f32(qa[c][0]), bf16hi_to_f32(qa[c][0]));
+            qa[c][1] = pack_f16x2(bf16lo_to_f32(qa[c][1]), bf16hi_to_f32(qa[c][1]));
+          }
+        }
       }
       const uint32_t kst = sbase + Gm::OFF_K + stage * Gm::KV_BYTES;
       const uint32_t vst = sbase + Gm::OFF_V + stage * Gm::KV_BYTES;
+      // int8 caches: this warp's f16 staging tile and the stage's per-token scales
+      uint8_t* stg = smem + Gm::OFF_STG + warp * Gm::STG_BYTES;
+      const uint32_t stg_s = sbase + Gm::OFF_STG + warp * Gm::STG_BYTES;
+      const float* ksc = reinterpret_cast<const float*>(smem + Gm::OFF_KS + stage * Gm::SC_BYTES);
+      const float* vsc = reinterpret_cast<const float*>(smem + Gm::OFF_VS + stage * Gm::SC_BYTES);
+      const int sc_blk = PAGED && rsh == 0 ? 32 : 16;  // floats from one sub-block's scales to the next
 #pragma unroll 1
       for (int sb = 0; sb < (nrows > 0 ? SBW : 0); sb += NP) {  // idle warps only release the stage
         // NP sub-blocks of this warp share one online-softmax step
@@ -484,11 +553,17 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
         float x[NP][4];
         uint32_t vm_lo[NP], vm_hi[NP];
         bool tail[NP];
+        if constexpr (KV8) {
+          dequant_subblocks<D, NP, Gm::ROWB, Gm::SUBW>(smem + Gm::OFF_K + stage * Gm::KV_BYTES, ws + WS * sb, WS,
+                                                        stg, lane);
+          __syncwarp();
+        }
 #pragma unroll
         for (int i = 0; i < NP; ++i) {
           const int kb = ws + WS * (sb + i);
           const int tok0 = t + 16 * kb;
-          const uint32_t blk = blk_off(kb);
+          const uint32_t kbase = KV8 ? stg_s + i * (16 * D * 2) : kst + blk_off(kb);
+          const uint32_t kcol = KV8 ? 16 * Gm::ROWB : col_stride;
           // even and odd k-chunks go to separate accumulators (two short dependency
           // chains per 8-token half instead of one long one), added at the end
           float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -497,13 +572,15 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
           for (int kk = 0; kk < KCH; ++kk) {
             const int c = 2 * kk + k_chk;
             uint32_t b0, b1, b2, b3;
-            ldsm_x4(kst + blk + (c / Gm::CPR) * col_stride + swz<Gm::ROWB>(k_row0, c % Gm::CPR), b0, b1, b2, b3);
-            if (KCH >= 4 && (kk & 1)) {
-              mma_bf16_16816(s2, qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
-              mma_bf16_16816(s3, qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
+            ldsm_x4(kbase + (c / Gm::CPR) * kcol + swz<Gm::ROWB>(k_row0, c % Gm::CPR), b0, b1, b2, b3);
+            float(&sa)[4] = (KCH >= 4 && (kk & 1)) ? s2 : s0;
+            float(&sb_)[4] = (KCH >= 4 && (kk & 1)) ? s3 : s1;
+            if constexpr (KV8) {
+              mma_f16_16816(sa, qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+              mma_f16_16816(sb_, qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
             } else {
-              mma_bf16_16816(s0, qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
-              mma_bf16_16816(s1, qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
+              mma_bf16_16816(sa, qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+              mma_bf16_16816(sb_, qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
             }
           }
           if (KCH >= 4) {
@@ -516,6 +593,14 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
           x[i][1] = s0[1] * p.scale_log2;
           x[i][2] = s1[0] * p.scale_log2;
           x[i][3] = s1[1] * p.scale_log2;
+          if constexpr (KV8) {  // K = k_i8 * k_scale: the scale of token t multiplies its score
+            const float2 ka = *reinterpret_cast<const float2*>(ksc + kb * sc_blk + 2 * i4);
+            const float2 kc = *reinterpret_cast<const float2*>(ksc + kb * sc_blk + 8 + 2 * i4);
+            x[i][0] *= ka.x;
+            x[i][1] *= ka.y;
+            x[i][2] *= kc.x;
+            x[i][3] *= kc.y;
+          }
           // tokens at or past the row's limit: score -inf; at or past the piece end
           // also V row zeroed (its shared memory may hold anything, and 0 * NaN
           // would poison the accumulator)
@@ -558,26 +643,61 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
           }
         }
         m_run = m_new;
+        if constexpr (KV8) {  // V rows of the same sub-blocks replace the K rows in the staging tile
+          __syncwarp();
+          dequant_subblocks<D, NP, Gm::ROWB, Gm::SUBW>(smem + Gm::OFF_V + stage * Gm::KV_BYTES, ws + WS * sb, WS,
+                                                        stg, lane);
+          __syncwarp();
+        }
 #pragma unroll
         for (int i = 0; i < NP; ++i) {
-          const uint32_t blk = blk_off(ws + WS * (sb + i));
-          // P = hi + lo in bf16: rows g (hi) and g + 8 (lo) of the A operand
-          const uint32_t ph0 = pack_bf16x2(pr[i][0], pr[i][1]), ph1 = pack_bf16x2(pr[i][2], pr[i][3]);
-          const uint32_t pl0 = pack_bf16x2(pr[i][0] - bf16lo_to_f32(ph0), pr[i][1] - bf16hi_to_f32(ph0));
-          const uint32_t pl1 = pack_bf16x2(pr[i][2] - bf16lo_to_f32(ph1), pr[i][3] - bf16hi_to_f32(ph1));
+          const int kb = ws + WS * (sb + i);
+          const uint32_t vbase = KV8 ? stg_s + i * (16 * D * 2) : vst + blk_off(kb);
+          const uint32_t vcol = KV8 ? 16 * Gm::ROWB : col_stride;
+          uint32_t ph0, ph1, pl0, pl1;
+          if constexpr (KV8) {
+            // V = v_i8 * v_scale: the scale of token t multiplies its probability (tokens
+            // past the piece end have p = 0 but scales that may be anything)
+            const float2 va = *reinterpret_cast<const float2*>(vsc + kb * sc_blk + 2 * i4);
+            const float2 vc = *reinterpret_cast<const float2*>(vsc + kb * sc_blk + 8 + 2 * i4);
+            float pv[4] = {pr[i][0] * va.x, pr[i][1] * va.y, pr[i][2] * vc.x, pr[i][3] * vc.y};
+            if (tail[i]) {
+              const int ta = t + 16 * kb + 2 * i4, tb = ta + 8;
+              pv[0] = ta < pc.t1 ? pv[0] : 0.f;
+              pv[1] = ta + 1 < pc.t1 ? pv[1] : 0.f;
+              pv[2] = tb < pc.t1 ? pv[2] : 0.f;
+              pv[3] = tb + 1 < pc.t1 ? pv[3] : 0.f;
+            }
+            // P' = hi + lo in f16
+            ph0 = pack_f16x2(pv[0], pv[1]);
+            ph1 = pack_f16x2(pv[2], pv[3]);
+            pl0 = pack_f16x2(pv[0] - f16lo_to_f32(ph0), pv[1] - f16hi_to_f32(ph0));
+            pl1 = pack_f16x2(pv[2] - f16lo_to_f32(ph1), pv[3] - f16hi_to_f32(ph1));
+          } else {
+            // P = hi + lo in bf16: rows g (hi) and g + 8 (lo) of the A operand
+            ph0 = pack_bf16x2(pr[i][0], pr[i][1]);
+            ph1 = pack_bf16x2(pr[i][2], pr[i][3]);
+            pl0 = pack_bf16x2(pr[i][0] - bf16lo_to_f32(ph0), pr[i][1] - bf16hi_to_f32(ph0));
+            pl1 = pack_bf16x2(pr[i][2] - bf16lo_to_f32(ph1), pr[i][3] - bf16hi_to_f32(ph1));
+          }
 #pragma unroll
           for (int c2 = 0; c2 < NB8 / 2; ++c2) {
             const int c = 2 * c2 + v_chk;
             uint32_t v0, v1, v2, v3;
-            ldsm_x4_t(vst + blk + (c / Gm::CPR) * col_stride + swz<Gm::ROWB>(v_row0, c % Gm::CPR), v0, v1, v2, v3);
+            ldsm_x4_t(vbase + (c / Gm::CPR) * vcol + swz<Gm::ROWB>(v_row0, c % Gm::CPR), v0, v1, v2, v3);
             if (tail[i]) {
               v0 &= vm_lo[i];
               v1 &= vm_hi[i];
               v2 &= vm_lo[i];
               v3 &= vm_hi[i];
             }
-            mma_bf16_16816(acc[2 * c2], ph0, pl0, ph1, pl1, v0, v1);
-            mma_bf16_16816(acc[2 * c2 + 1], ph0, pl0, ph1, pl1, v2, v3);
+            if constexpr (KV8) {
+              mma_f16_16816(acc[2 * c2], ph0, pl0, ph1, pl1, v0, v1);
+              mma_f16_16816(acc[2 * c2 + 1], ph0, pl0, ph1, pl1, v2, v3);
+            } else {
+              mma_bf16_16816(acc[2 * c2], ph0, pl0, ph1, pl1, v0, v1);
+              mma_bf16_16816(acc[2 * c2 + 1], ph0, pl0, ph1, pl1, v2, v3);
+            }
           }
         }
       }
@@ -681,9 +801,9 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
   }
 }
 
-template <int D, bool PAGED, int NGP>
+template <int D, bool PAGED, int NGP, bool KV8>
 __global__ void __launch_bounds__(SplitGeo<D>::NTHREADS, 1) split_kernel(const __grid_constant__ SplitParams p) {
-  using Gm = SplitGeo<D, NGP>;
+  using Gm = SplitGeo<D, NGP, KV8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
@@ -707,6 +827,10 @@ __global__ void __launch_bounds__(SplitGeo<D>::NTHREADS, 1) split_kernel(const _
     prefetch_tensormap(&p.tm_k);
     prefetch_tensormap(&p.tm_v);
     prefetch_tensormap(&p.tm_q);
+    if (KV8) {
+      prefetch_tensormap(&p.tm_ks);
+      prefetch_tensormap(&p.tm_vs);
+    }
   }
 
   // The combine kernel (launched only when a segment can have more than 8 pieces)
@@ -715,9 +839,9 @@ __global__ void __launch_bounds__(SplitGeo<D>::NTHREADS, 1) split_kernel(const _
   build_plan_arrays(p.seq_lens, p.B, p.max_len, plan_gap_blocks(D), lens, P);
   const Plan pl = make_plan(p.B, p.U, p.S, plan_gap_blocks(D), P);
   if (warp == Gm::W)
-    split_producer<D, PAGED, NGP>(p, pl, lens, P, smem, sbase, abort_flag);
+    split_producer<D, PAGED, NGP, KV8>(p, pl, lens, P, smem, sbase, abort_flag);
   else
-    split_consumer<D, PAGED, NGP>(p, pl, lens, P, smem, sbase, abort_flag);
+    split_consumer<D, PAGED, NGP, KV8>(p, pl, lens, P, smem, sbase, abort_flag);
 }
 
 }  // namespace da

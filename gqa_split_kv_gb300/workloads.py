@@ -83,6 +83,7 @@ class Workload:
     outlier_mult: float = 20.0
     seed: int = 1234
     q_len: int = 1  # query tokens per sequence (> 1: multi-query decode, q is [B, Hq, q_len, D])
+    kv_dtype: str = "bf16"  # "int8": symmetric int8 K/V with fp32 scales per (token, KV head)
 
     @property
     def G(self) -> int:
@@ -128,6 +129,13 @@ WORKLOADS = {
     "verify_paged_b16_hq32_hkv8_d128_u256_8192_ps32_q4": Workload(
         "verify_paged_b16_hq32_hkv8_d128_u256_8192_ps32_q4", B=16, Hq=32, Hkv=8, D=128, max_ctx=8192,
         layout="paged", page_size=32, lens="uniform", lens_lo=256, lens_hi=8192, q_len=4, seed=1244),
+    # int8 KV cache (per (token, KV head) fp32 scales)
+    "int8_long_contig_b1_hq32_hkv8_d128_ctx65536": Workload(
+        "int8_long_contig_b1_hq32_hkv8_d128_ctx65536", B=1, Hq=32, Hkv=8, D=128, max_ctx=65536, kv_dtype="int8",
+        seed=1245),
+    "int8_paged_b16_hq32_hkv8_d128_u256_8192_ps32": Workload(
+        "int8_paged_b16_hq32_hkv8_d128_u256_8192_ps32", B=16, Hq=32, Hkv=8, D=128, max_ctx=8192,
+        layout="paged", page_size=32, lens="uniform", lens_lo=256, lens_hi=8192, kv_dtype="int8", seed=1246),
 }
 
 
@@ -178,6 +186,13 @@ def make_inputs(wl: Workload, seed: Optional[int] = None) -> dict:
     seq_lens = draw_seq_lens(wl, rng)
     q = _normal_bf16(rng, (wl.B, wl.Hq, wl.D) if wl.q_len == 1 else (wl.B, wl.Hq, wl.q_len, wl.D))
     out = {"q": q, "seq_lens": seq_lens, "scale": wl.scale}
+    if wl.kv_dtype == "int8":  # keys k_i8, v_i8, k_scale, v_scale (or their page pools)
+        cache = make_int8_cache(rng, wl.B, wl.max_ctx, wl.Hkv, wl.D)
+        if wl.layout == "contig":
+            out.update(cache)
+        else:
+            out.update(int8_to_paged(cache, seq_lens, wl.page_size, rng), page_size=wl.page_size)
+        return out
     if wl.layout == "contig":
         shape = (wl.B, wl.max_ctx, wl.Hkv, wl.D)
         if wl.outlier_frac > 0:

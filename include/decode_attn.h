@@ -218,6 +218,32 @@ int decode_attn_multi_paged(const void* q, const void* k_pool, const void* v_poo
                             float scale, int num_splits, float* part_acc, float* part_ml,
                             unsigned long long* seg_counters, void* out, void* stream);
 
+/*
+ * decode_attn_int8_contig / decode_attn_int8_paged — decode over an int8 KV cache.
+ * "perf(dspark): overlap KV staging with compute via cp.async", section "Cost and
+ * fallbacks", names an int8 pool read through a dequant-into-shared-memory path; its
+ * format is not given there.  Here K and V are symmetric int8 values with one fp32
+ * scale per (token, KV head): K[t, g, :] = k_i8[t, g, :] * k_scale[g, t] (V likewise).
+ *  k_i8, v_i8       int8 [batch, max_ctx, num_kv_heads, head_dim] (16-byte aligned)
+ *  k_scale, v_scale float [batch, num_kv_heads, max_ctx], head-major (16-byte aligned;
+ *                   max_ctx a multiple of 4)
+ *  paged:  k_pool_i8, v_pool_i8 int8 [num_pages, page_size, num_kv_heads, head_dim],
+ *          k_scale_pool, v_scale_pool float [num_pages, num_kv_heads, page_size]
+ *  Every other argument, the split plan, the partials and the error behaviour are
+ *  those of decode_attn_contig / decode_attn_paged.  The kernels dequantize each
+ *  16-token block into f16 in shared memory (exact) and multiply in f16 with fp32
+ *  accumulation; q is converted to f16, which is exact for |q| in [2^-14, 65504].
+ */
+int decode_attn_int8_contig(const void* q, const void* k_i8, const void* v_i8, const float* k_scale,
+                            const float* v_scale, const int* seq_lens, int batch, int num_q_heads, int num_kv_heads,
+                            int head_dim, int max_ctx, float scale, int num_splits, float* part_acc, float* part_ml,
+                            unsigned long long* seg_counters, void* out, void* stream);
+int decode_attn_int8_paged(const void* q, const void* k_pool_i8, const void* v_pool_i8, const float* k_scale_pool,
+                           const float* v_scale_pool, const int* page_table, const int* seq_lens, int batch,
+                           int num_q_heads, int num_kv_heads, int head_dim, int page_size, int max_pages_per_seq,
+                           int num_pages, int max_seq_len, float scale, int num_splits, float* part_acc,
+                           float* part_ml, unsigned long long* seg_counters, void* out, void* stream);
+
 /* Human-readable name of a da_status value (static string). */
 const char* decode_status_string(int status);
 

@@ -150,3 +150,34 @@ def check_multi_partials(acc, ml, inp, S):
             assert da <= PART_RTOL * np.abs(ra[idx + (j,)]).max(), (idx, j, da)
             checked += 1
     return checked
+
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def run_int8(inp, S=None, max_seq_len=None):
+    """One int8-cache call (contiguous k_i8/v_i8/k_scale/v_scale or paged pools).
+    Returns (out bits, part_acc, part_ml, S)."""
+    B, Hq, D = inp["q"].shape
+    q = dev_bf16(inp["q"])
+    paged = "k_pool_i8" in inp
+    Hkv = (inp["k_pool_i8"] if paged else inp["k_i8"]).shape[2]
+    ctx = max_seq_len if paged else inp["k_i8"].shape[1]
+    S = binding.num_splits_multi(B, 1, Hq, Hkv, ctx, D) if S is None else S
+    acc = torch.full((B, Hq, S, D), float("nan"), dtype=torch.float32, device="cuda")
+    ml = torch.full((B, Hq, S, 2), float("nan"), dtype=torch.float32, device="cuda")
+    out = torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ctr = torch.zeros(binding.counters_len(B, Hq, Hkv), dtype=torch.int64, device="cuda")
+    if paged:
+        binding.decode_attn_int8_paged(q, dev(inp["k_pool_i8"]), dev(inp["v_pool_i8"]), dev(inp["k_scale_pool"]),
+                                       dev(inp["v_scale_pool"]), dev_i32(inp["page_table"]),
+                                       dev_i32(inp["seq_lens"]), max_seq_len, scale=inp["scale"], splits=S,
+                                       part_acc=acc, part_ml=ml, seg_counters=ctr, out=out)
+    else:
+        binding.decode_attn_int8_contig(q, dev(inp["k_i8"]), dev(inp["v_i8"]), dev(inp["k_scale"]),
+                                        dev(inp["v_scale"]), dev_i32(inp["seq_lens"]), scale=inp["scale"], splits=S,
+                                        part_acc=acc, part_ml=ml, seg_counters=ctr, out=out)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    return host_bits(out), acc.cpu().numpy(), ml.cpu().numpy(), S

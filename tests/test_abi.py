@@ -161,3 +161,15 @@ def test_selftest_rejects_bad_timeouts(clib):
     clib.decode_selftest_bounded_wait.argtypes = [ctypes.c_ulonglong, ctypes.c_void_p]
     assert clib.decode_selftest_bounded_wait(0, None) == 1
     assert clib.decode_selftest_bounded_wait(10 ** 9 + 1, None) == 1
+
+
+def test_int8_argument_errors(clib):
+    def i8(ks=A, vs=A, ctx=64, D=64):
+        return clib.decode_attn_int8_contig(A, A, A, ks, vs, None, 1, 8, 2, D, ctx, ctypes.c_float(0.125), 2, A, A,
+                                            A, A, None)
+    assert i8(ks=None) == 1
+    assert i8(vs=A + 4) == 1
+    assert i8(ctx=66) == 2   # scale rows need 16-byte strides: max_ctx a multiple of 4
+    assert i8(D=48) == 2
+    assert clib.decode_attn_int8_paged(A, A, A, None, A, A, A, 1, 8, 2, 64, 16, 4, 4, 64, ctypes.c_float(0.125), 2,
+                                       A, A, A, A, None) == 1

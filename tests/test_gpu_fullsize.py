@@ -14,7 +14,7 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
-from gpu_helpers import OUT_ATOL, OUT_RTOL, PART_RTOL, run, run_multi, to_device  # noqa: E402
+from gpu_helpers import OUT_ATOL, OUT_RTOL, PART_RTOL, run, run_int8, run_multi, to_device  # noqa: E402
 from gqa_split_kv_gb300.workloads import bf16_bits_to_f32  # noqa: E402
 
 N_ROWS = 24       # sampled (b, query head) outputs per workload
@@ -52,10 +52,27 @@ def _full_size_multi(wl, inp, d):
     assert np.array_equal(out, out2)
 
 
+def _full_size_int8(wl, inp):
+    """int8-cache workloads: sampled outputs against the oracle, and bitwise run-to-run
+    determinism (partials are checked at parity sizes)."""
+    max_len = wl.max_ctx if wl.layout == "paged" else None
+    out, acc, ml, S = run_int8(inp, None, max_seq_len=max_len)
+    assert np.all(np.isfinite(bf16_bits_to_f32(out)))
+    pairs = _sample_rows(inp, np.random.default_rng(4444))
+    ref = oracle.decode_int8(inp, pairs)
+    got = np.stack([bf16_bits_to_f32(out[b, h]).astype(np.float64) for b, h in pairs])
+    err = np.abs(got - ref)
+    assert np.all(err <= OUT_ATOL + OUT_RTOL * np.abs(ref)), f"{wl.name}: max abs err {err.max():.3e}"
+    out2, *_ = run_int8(inp, S, max_seq_len=max_len)
+    assert np.array_equal(out, out2)
+
+
 @pytest.mark.parametrize("name", list(WORKLOADS))
 def test_full_size_workload(name):
     wl = WORKLOADS[name]
     inp = make_inputs(wl)
+    if wl.kv_dtype == "int8":
+        return _full_size_int8(wl, inp)
     d = to_device(inp)
     if wl.q_len > 1:
         return _full_size_multi(wl, inp, d)
