@@ -103,6 +103,9 @@ int encode_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dim
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int sub_width(int D) { return D >= 64 ? 64 : 32; }
+// int8 tiles: bytes per swizzle row and the swizzle the kernels read
+int sub_width8(int D) { return D >= 128 ? 128 : D; }
+CUtensorMapSwizzle swizzle8(int D) { return D >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE; }
 
 // tokens per tile of the split kernel for head_dim D (the TMA box height of a contiguous cache)
 int tile_tokens(int D) {
@@ -430,17 +433,21 @@ static int contig_call(const void* q, const void* k, const void* v, const int* s
     if (int e = encode_map(&tk, k, 5, dims, strides, box, D)) return e;
     if (int e = encode_map(&tv, v, 5, dims, strides, box, D)) return e;
   } else {
-    // int8 values: dims (D, head, token, batch), one box = [T][D] bytes of one head;
-    // scales: dims (token, head, batch), one box = the T scales of one head
-    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)max_ctx, (cuuint64_t)B};
-    const cuuint64_t strides[3] = {(cuuint64_t)D, (cuuint64_t)Hkv * D, (cuuint64_t)max_ctx * Hkv * D};
-    const cuuint32_t box[4] = {(cuuint32_t)D, 1, (cuuint32_t)T, 1};
+    // int8 values: dims (byte of a swizzle row, token, swizzle column, head, batch),
+    // one box = [D/SW8][T][SW8] bytes of one head; scales: dims (token, head,
+    // batch), one box = the T scales of one head
+    const int SW8 = sub_width8(D);
+    const cuuint64_t row = (cuuint64_t)Hkv * D;
+    const cuuint64_t dims[5] = {(cuuint64_t)SW8, (cuuint64_t)max_ctx, (cuuint64_t)(D / SW8), (cuuint64_t)Hkv,
+                                (cuuint64_t)B};
+    const cuuint64_t strides[4] = {row, (cuuint64_t)SW8, (cuuint64_t)D, row * (cuuint64_t)max_ctx};
+    const cuuint32_t box[5] = {(cuuint32_t)SW8, (cuuint32_t)T, (cuuint32_t)(D / SW8), 1, 1};
     const cuuint64_t sdims[3] = {(cuuint64_t)max_ctx, (cuuint64_t)Hkv, (cuuint64_t)B};
     const cuuint64_t sstrides[2] = {(cuuint64_t)max_ctx * 4, (cuuint64_t)Hkv * max_ctx * 4};
     const cuuint32_t sbox[3] = {(cuuint32_t)T, 1, 1};
     const auto none = CU_TENSOR_MAP_SWIZZLE_NONE;
-    if (int e = encode_map_t(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, none, k, 4, dims, strides, box)) return e;
-    if (int e = encode_map_t(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, none, v, 4, dims, strides, box)) return e;
+    if (int e = encode_map_t(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, swizzle8(D), k, 5, dims, strides, box)) return e;
+    if (int e = encode_map_t(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, swizzle8(D), v, 5, dims, strides, box)) return e;
     if (int e = encode_map_t(&tks, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, none, ks, 3, sdims, sstrides, sbox)) return e;
     if (int e = encode_map_t(&tvs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, none, vs, 3, sdims, sstrides, sbox)) return e;
   }
@@ -517,17 +524,21 @@ static int paged_call(const void* q, const void* k_pool, const void* v_pool, con
     if (int e = encode_map(&tk, k_pool, 5, dims, strides, box, D)) return e;
     if (int e = encode_map(&tv, v_pool, 5, dims, strides, box, D)) return e;
   } else {
-    // int8 values: dims (D, head, row in page, page), one box = [R][D] bytes;
-    // scales: dims (row in page, head, page), one box = R scales of one head
-    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)page_size, (cuuint64_t)num_pages};
-    const cuuint64_t strides[3] = {(cuuint64_t)D, (cuuint64_t)Hkv * D, (cuuint64_t)page_size * Hkv * D};
-    const cuuint32_t box[4] = {(cuuint32_t)D, 1, R, 1};
+    // int8 values: dims (byte of a swizzle row, row in page, swizzle column, head,
+    // page), one box = [D/SW8][R][SW8] bytes; scales: dims (row in page, head,
+    // page), one box = R scales of one head
+    const int SW8 = sub_width8(D);
+    const cuuint64_t row = (cuuint64_t)Hkv * D;
+    const cuuint64_t dims[5] = {(cuuint64_t)SW8, (cuuint64_t)page_size, (cuuint64_t)(D / SW8), (cuuint64_t)Hkv,
+                                (cuuint64_t)num_pages};
+    const cuuint64_t strides[4] = {row, (cuuint64_t)SW8, (cuuint64_t)D, row * (cuuint64_t)page_size};
+    const cuuint32_t box[5] = {(cuuint32_t)SW8, R, (cuuint32_t)(D / SW8), 1, 1};
     const cuuint64_t sdims[3] = {(cuuint64_t)page_size, (cuuint64_t)Hkv, (cuuint64_t)num_pages};
     const cuuint64_t sstrides[2] = {(cuuint64_t)page_size * 4, (cuuint64_t)Hkv * page_size * 4};
     const cuuint32_t sbox[3] = {R, 1, 1};
     const auto none = CU_TENSOR_MAP_SWIZZLE_NONE;
-    if (int e = encode_map_t(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, none, k_pool, 4, dims, strides, box)) return e;
-    if (int e = encode_map_t(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, none, v_pool, 4, dims, strides, box)) return e;
+    if (int e = encode_map_t(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, swizzle8(D), k_pool, 5, dims, strides, box)) return e;
+    if (int e = encode_map_t(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, swizzle8(D), v_pool, 5, dims, strides, box)) return e;
     if (int e = encode_map_t(&tks, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, none, ks, 3, sdims, sstrides, sbox)) return e;
     if (int e = encode_map_t(&tvs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, none, vs, 3, sdims, sstrides, sbox)) return e;
   }

@@ -75,7 +75,7 @@ struct SplitParams {
 };
 
 // NGP: sub-groups per pass (the query-row slots per stage); KV8: int8 K/V with
-// fp32 scales per (token, KV head), dequantized per warp into an f16 staging tile.
+// fp32 scales per (token, KV head), widened to f16 in registers by the MMA warps.
 template <int D, int NGP = 1, bool KV8 = false>
 struct SplitGeo {
   // Tiles carry 32 KB (D = 32) or 64 KB of K+V so the per-tile costs (barrier
@@ -104,7 +104,10 @@ struct SplitGeo {
   // floats per box, so every box lands 128-byte aligned (16-row paged boxes leave
   // 16 floats unused per slot)
   static constexpr int SC_BYTES = KV8 ? T * 8 : 0;
-  static constexpr int STG_BYTES = KV8 ? NP * 16 * D * 2 : 0;  // per-warp f16 tile of NP sub-blocks
+  // int8 tiles use the same box-major form with byte rows: [T/R][NSUB8][R][SW8],
+  // 128-byte swizzled rows at D >= 128, plain D-byte rows below
+  static constexpr int SW8 = D >= 128 ? 128 : D;
+  static constexpr int NSUB8 = D / SW8;
   static constexpr int al1k(int x) { return (x + 1023) / 1024 * 1024; }
   static constexpr int Q_SUB_BYTES = 8 * ROWB;      // one swizzle column of 8 query rows
   static constexpr int Q_SG_BYTES = 8 * D * 2;      // the query rows of one sub-group
@@ -116,8 +119,12 @@ struct SplitGeo {
   static constexpr int OFF_KS = OFF_V + STAGES * KV_BYTES;
   static constexpr int OFF_VS = OFF_KS + STAGES * SC_BYTES;
   static constexpr int OFF_Q = al1k(OFF_VS + STAGES * SC_BYTES);
-  static constexpr int OFF_STG = OFF_Q + STAGES * Q_BYTES;
-  static constexpr int OFF_FACC = OFF_STG + W * STG_BYTES;
+  // D = 256 int8: each warp keeps its f16 query fragment here ([D/32][32 lanes][4
+  // words]) instead of in 32 registers
+  static constexpr bool Q_SMEM = KV8 && D == 256;
+  static constexpr int QF_BYTES = Q_SMEM ? W * D / 32 * 32 * 16 : 0;
+  static constexpr int OFF_QF = OFF_Q + STAGES * Q_BYTES;
+  static constexpr int OFF_FACC = OFF_QF + QF_BYTES;
   static constexpr int OFF_FML = OFF_FACC + W * 8 * FD * 4;
   static constexpr int OFF_FSC = OFF_FML + W * 8 * 2 * 4;   // per-(warp, row) merge weights
   static constexpr int OFF_FROW = OFF_FSC + W * 8 * 4;      // per-row (M, L, 1/L, -), 32 rows
@@ -280,28 +287,21 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
       if (lane < nbox) {
         const int tok = cur.t + lane * box_rows;
         const int row0 = tok - page_of(p, tok) * p.page_size;
-        if constexpr (KV8) {  // [rows][D] int8 boxes and [rows] fp32 scale boxes
-          const uint32_t off = (uint32_t)(lane * box_rows * D);
-          tma_load_4d(kdst + off, &p.tm_k, full, 0, h, row0, page);
-          tma_load_4d(vdst + off, &p.tm_v, full, 0, h, row0, page);
-          const uint32_t soff = (uint32_t)(lane * max(box_rows, 32) * 4);  // 128-byte aligned slots
+        const uint32_t off = (uint32_t)(lane * box_rows * D * (KV8 ? 1 : 2));
+        tma_load_5d(kdst + off, &p.tm_k, full, 0, row0, 0, h, page);
+        tma_load_5d(vdst + off, &p.tm_v, full, 0, row0, 0, h, page);
+        if constexpr (KV8) {  // [rows] fp32 scale boxes, one 128-byte aligned slot per box
+          const uint32_t soff = (uint32_t)(lane * max(box_rows, 32) * 4);
           tma_load_3d(sbase + Gm::OFF_KS + stage * Gm::SC_BYTES + soff, &p.tm_ks, full, row0, h, page);
           tma_load_3d(sbase + Gm::OFF_VS + stage * Gm::SC_BYTES + soff, &p.tm_vs, full, row0, h, page);
-        } else {
-          const uint32_t off = (uint32_t)(lane * box_rows * D * 2);
-          tma_load_5d(kdst + off, &p.tm_k, full, 0, row0, 0, h, page);
-          tma_load_5d(vdst + off, &p.tm_v, full, 0, row0, 0, h, page);
         }
       }
     } else if (lane == 0) {
+      tma_load_5d(kdst, &p.tm_k, full, 0, cur.t, 0, h, pc.b);
+      tma_load_5d(vdst, &p.tm_v, full, 0, cur.t, 0, h, pc.b);
       if constexpr (KV8) {
-        tma_load_4d(kdst, &p.tm_k, full, 0, h, cur.t, pc.b);
-        tma_load_4d(vdst, &p.tm_v, full, 0, h, cur.t, pc.b);
         tma_load_3d(sbase + Gm::OFF_KS + stage * Gm::SC_BYTES, &p.tm_ks, full, cur.t, h, pc.b);
         tma_load_3d(sbase + Gm::OFF_VS + stage * Gm::SC_BYTES, &p.tm_vs, full, cur.t, h, pc.b);
-      } else {
-        tma_load_5d(kdst, &p.tm_k, full, 0, cur.t, 0, h, pc.b);
-        tma_load_5d(vdst, &p.tm_v, full, 0, cur.t, 0, h, pc.b);
       }
     }
     if (first_tile && lane < nsg * Gm::NSUB) {  // one box per (sub-group, swizzle column)
@@ -416,28 +416,57 @@ __device__ __forceinline__ void merge_segment(const SplitParams& p, int b, int f
   }
 }
 
-// int8 caches: the rows of NP sub-blocks (kb0, kb0 + kbstride, ...) of an int8
-// tile [T][D] in shared memory become f16 rows of the warp's staging tile, laid out
-// like a 16-row TMA box per sub-block ([NSUB][16][SUBW], swizzled), so the bf16
-// path's ldmatrix addressing reads them unchanged.  Exact (int8 -> f16).
-template <int D, int NP, int ROWB, int SUBW>
-__device__ __forceinline__ void dequant_subblocks(const uint8_t* tile, int kb0, int kbstride, uint8_t* stg,
-                                                  int lane) {
-  constexpr int CH = D / 16;  // 16-byte int8 chunks per row
-#pragma unroll(D == 256 ? 1 : 4)
-  for (int c = lane; c < NP * 16 * CH; c += 32) {
-    const int i = c / (16 * CH), r = (c / CH) % 16, cc = c % CH;
-    const uint4 w = *reinterpret_cast<const uint4*>(tile + ((kb0 + kbstride * i) * 16 + r) * D + cc * 16);
-    uint4 lo, hi;
-    int8x4_to_f16x4(w.x, lo.x, lo.y);
-    int8x4_to_f16x4(w.y, lo.z, lo.w);
-    int8x4_to_f16x4(w.z, hi.x, hi.y);
-    int8x4_to_f16x4(w.w, hi.z, hi.w);
-    const int e0 = cc * 16;  // first f16 column of the chunk
-    uint8_t* base = stg + i * (16 * D * 2) + (e0 / SUBW) * (16 * ROWB);
-    const int ch = (e0 % SUBW) / 8;
-    *reinterpret_cast<uint4*>(base + swz<ROWB>(r, ch)) = lo;
-    *reinterpret_cast<uint4*>(base + swz<ROWB>(r, ch + 1)) = hi;
+// int8 sub-blocks (16 tokens) are multiplied straight from the int8 tile, each
+// thread widening the bytes of its MMA operands to f16 in registers (exact).
+//  QK^T: thread (g, c) of a warp, g = lane / 4, c = lane % 4, holds D / 4
+//        consecutive bytes of token rows g and 8 + g; word w of them, bytes
+//        4w .. 4w + 3, is k-chunk w of the product, its four bytes filling the
+//        thread's k-slots 2c, 2c + 1, 2c + 8, 2c + 9.  The query fragment takes the
+//        same d order (kq_dim), so the dot products are unchanged.
+//  PV:   thread (g, c) needs, per 8-column block, token rows 2c, 2c + 1, 8 + 2c,
+//        9 + 2c at one d: it loads a run of d's of those four rows and transposes
+//        bytes with byte_perm.  Column n of block nt is d = pv_dim(nt, n).
+template <int D>
+__host__ __device__ constexpr int kq_dim(int kk, int c, int e) {  // d of k-chunk kk, k-slot group c, byte e
+  return D >= 64 ? 64 * (kk / 4) + 16 * c + 4 * (kk % 4) + e : 8 * c + 4 * kk + e;
+}
+template <int D>
+__host__ __device__ constexpr int pv_dim(int nt, int n) {
+  constexpr int run = D / 8 < 16 ? D / 8 : 16;  // d's of one thread's row run
+  return (nt / run) * (8 * run) + n * run + nt % run;
+}
+
+// Rows a and b, one word (the same four d's) each -> the f16 pairs (a_d, b_d) for
+// d = 0 .. 3 (a in the low half).  int8 x becomes f16 0x6400 | (x ^ 0x80), which
+// is 1152 + x exactly; subtracting 1152 in f16 is exact.
+__device__ __forceinline__ void int8_pairs_to_f16(uint32_t a, uint32_t b, uint32_t (&o)[4]) {
+  const uint32_t lo = __byte_perm(a, b, 0x5140) ^ 0x80808080u;  // a0 b0 a1 b1
+  const uint32_t hi = __byte_perm(a, b, 0x7362) ^ 0x80808080u;  // a2 b2 a3 b3
+  const uint32_t h0 = __byte_perm(lo, 0x64646464u, 0x5150);
+  const uint32_t h1 = __byte_perm(lo, 0x64646464u, 0x5352);
+  const uint32_t h2 = __byte_perm(hi, 0x64646464u, 0x5150);
+  const uint32_t h3 = __byte_perm(hi, 0x64646464u, 0x5352);
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o[0]) : "r"(h0), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o[1]) : "r"(h1), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o[2]) : "r"(h2), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o[3]) : "r"(h3), "r"(0x64806480u));
+}
+
+// n consecutive 32-bit words of shared memory (n = 1, 2 or 4; 4n-byte aligned)
+template <int N>
+__device__ __forceinline__ void lds_words(const uint8_t* p, uint32_t* w) {
+  if constexpr (N == 4) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    w[0] = v.x;
+    w[1] = v.y;
+    w[2] = v.z;
+    w[3] = v.w;
+  } else if constexpr (N == 2) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    w[0] = v.x;
+    w[1] = v.y;
+  } else {
+    w[0] = *reinterpret_cast<const uint32_t*>(p);
   }
 }
 
@@ -476,6 +505,47 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
   constexpr int WS = Gm::W / NGP;  // warps per sub-group
   constexpr int SBW = Gm::SB / WS; // sub-blocks per warp and tile
   const int sg = warp / WS, ws = warp % WS;
+  // int8 tiles: box-major [T/R][NSUB8][R][SW8] bytes
+  constexpr int SW8 = Gm::SW8;
+  const uint32_t col8 = (uint32_t)(16 * SW8) << rsh;  // one swizzle column of a box
+  const uint32_t box8 = col8 * Gm::NSUB8;
+  auto blk_off8 = [&](int kb) -> uint32_t {
+    return (uint32_t)(kb >> rsh) * box8 + (uint32_t)((kb & in_box) * 16 * SW8);
+  };
+  // 16-byte chunk ch of row r (< 16) of a sub-block, swizzled at SW8 = 128
+  auto chunk8 = [&](int r, int ch) -> uint32_t {
+    return (uint32_t)(ch / (SW8 / 16)) * col8 +
+           (SW8 == 128 ? swz<128>(r, ch % 8) : (uint32_t)(r * SW8 + (ch % (SW8 / 16)) * 16));
+  };
+  // K words of token rows g and 8 + g (k-chunk order), D / 4 bytes each
+  auto load_k8 = [&](const uint8_t* sb8, uint32_t* w0, uint32_t* w1) {
+    if constexpr (D >= 64) {
+#pragma unroll
+      for (int j = 0; j < D / 64; ++j) {
+        const uint32_t o = chunk8(g, 4 * j + i4);
+        lds_words<4>(sb8 + o, w0 + 4 * j);
+        lds_words<4>(sb8 + o + 8 * SW8, w1 + 4 * j);
+      }
+    } else {
+      const uint32_t o = (uint32_t)(g * SW8 + 8 * i4);
+      lds_words<2>(sb8 + o, w0);
+      lds_words<2>(sb8 + o + 8 * SW8, w1);
+    }
+  };
+  // V words of token rows 2c, 2c + 1, 8 + 2c, 9 + 2c: D / 8 bytes each, the runs
+  // of d's that pv_dim gives this thread's MMA column g
+  auto load_v8 = [&](const uint8_t* sb8, uint32_t (*vw)[D / 32]) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int r = (e & 1) + 2 * i4 + ((e >> 1) << 3);
+      if constexpr (D >= 128) {
+#pragma unroll
+        for (int j = 0; j < D / 128; ++j) lds_words<4>(sb8 + chunk8(r, 8 * j + g), vw[e] + 4 * j);
+      } else {
+        lds_words<D / 32>(sb8 + r * SW8 + g * (D / 8), vw[e]);
+      }
+    }
+  };
 
   if (p.S >= 2) {
     // empty sequences have no pieces on the block line: write their zero outputs
@@ -514,7 +584,33 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
 
     for (int t = pc.t0; t < pc.t1; t += Gm::T) {
       wait_bounded(bar_full + stage * 8, parity, abort_flag, p.timeout_ns);
-      if (t == pc.t0 && nrows > 0) {
+      if (t == pc.t0 && nrows > 0 && KV8) {
+        // f16 query fragment in kq_dim order: row g, d = kq_dim(kk, c, 0 .. 3)
+        const uint8_t* qs = smem + Gm::OFF_Q + stage * Gm::Q_BYTES + sg * Gm::Q_SG_BYTES;
+#pragma unroll
+        for (int j = 0; j < (D >= 64 ? D / 64 : 1); ++j) {
+          uint32_t w[8];
+          if constexpr (D >= 64) {
+            lds_words<4>(qs + j * Gm::Q_SUB_BYTES + swz<Gm::ROWB>(g, 2 * i4), w);
+            lds_words<4>(qs + j * Gm::Q_SUB_BYTES + swz<Gm::ROWB>(g, 2 * i4 + 1), w + 4);
+          } else {
+            lds_words<4>(qs + swz<Gm::ROWB>(g, i4), w);
+          }
+#pragma unroll
+          for (int m = 0; m < (D >= 64 ? 4 : 2); ++m) {
+            const uint32_t a0 = g < nrows ? w[2 * m] : 0u, a2 = g < nrows ? w[2 * m + 1] : 0u;
+            qa[(D >= 64 ? 4 : 2) * j + m][0] = pack_f16x2(bf16lo_to_f32(a0), bf16hi_to_f32(a0));
+            qa[(D >= 64 ? 4 : 2) * j + m][1] = pack_f16x2(bf16lo_to_f32(a2), bf16hi_to_f32(a2));
+          }
+        }
+        if constexpr (Gm::Q_SMEM) {  // k-chunks 2m, 2m + 1 per 16-byte slot, read back by this lane only
+          uint4* qf = reinterpret_cast<uint4*>(smem + Gm::OFF_QF) + warp * (KCH / 2) * 32 + lane;
+#pragma unroll
+          for (int m = 0; m < KCH / 2; ++m)
+            qf[m * 32] = make_uint4(qa[2 * m][0], qa[2 * m][1], qa[2 * m + 1][0], qa[2 * m + 1][1]);
+        }
+      }
+      if (t == pc.t0 && nrows > 0 && !KV8) {
         const uint32_t qst = sbase + Gm::OFF_Q + stage * Gm::Q_BYTES + sg * Gm::Q_SG_BYTES;
 #pragma unroll
         for (int jq = 0; jq < D / 32; ++jq) {
@@ -530,19 +626,12 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
 #pragma unroll
           for (int c = 0; c < KCH; ++c) qa[c][0] = qa[c][1] = 0u;
         }
-        if constexpr (KV8) {  // the int8 path multiplies in f16: bf16 -> f16, exact in f16's range
-#pragma unroll
-          for (int c = 0; c < KCH; ++c) {
-            qa[c][0] = pack_f16x2(bf16lo_to_f32(qa[c][0]), bf16hi_to_f32(qa[c][0]));
-            qa[c][1] = pack_f16x2(bf16lo_to_f32(qa[c][1]), bf16hi_to_f32(qa[c][1]));
-          }
-        }
       }
       const uint32_t kst = sbase + Gm::OFF_K + stage * Gm::KV_BYTES;
       const uint32_t vst = sbase + Gm::OFF_V + stage * Gm::KV_BYTES;
-      // int8 caches: this warp's f16 staging tile and the stage's per-token scales
-      uint8_t* stg = smem + Gm::OFF_STG + warp * Gm::STG_BYTES;
-      const uint32_t stg_s = sbase + Gm::OFF_STG + warp * Gm::STG_BYTES;
+      // int8 caches: the stage's tiles and per-token scales
+      const uint8_t* kst8 = smem + Gm::OFF_K + stage * Gm::KV_BYTES;
+      const uint8_t* vst8 = smem + Gm::OFF_V + stage * Gm::KV_BYTES;
       const float* ksc = reinterpret_cast<const float*>(smem + Gm::OFF_KS + stage * Gm::SC_BYTES);
       const float* vsc = reinterpret_cast<const float*>(smem + Gm::OFF_VS + stage * Gm::SC_BYTES);
       const int sc_blk = PAGED && rsh == 0 ? 32 : 16;  // floats from one sub-block's scales to the next
@@ -553,32 +642,48 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
         float x[NP][4];
         uint32_t vm_lo[NP], vm_hi[NP];
         bool tail[NP];
-        if constexpr (KV8) {
-          dequant_subblocks<D, NP, Gm::ROWB, Gm::SUBW>(smem + Gm::OFF_K + stage * Gm::KV_BYTES, ws + WS * sb, WS,
-                                                        stg, lane);
-          __syncwarp();
+        // int8: every K word of the step is loaded before the first MMA (at D = 256
+        // 64 d's at a time, next to their MMAs)
+        constexpr bool K_EARLY = KV8 && D <= 128;
+        uint32_t kw[KV8 ? NP : 1][2][KV8 ? KCH : 1];
+        if constexpr (K_EARLY) {
+#pragma unroll
+          for (int i = 0; i < NP; ++i) load_k8(kst8 + blk_off8(ws + WS * (sb + i)), kw[i][0], kw[i][1]);
         }
 #pragma unroll
         for (int i = 0; i < NP; ++i) {
           const int kb = ws + WS * (sb + i);
           const int tok0 = t + 16 * kb;
-          const uint32_t kbase = KV8 ? stg_s + i * (16 * D * 2) : kst + blk_off(kb);
-          const uint32_t kcol = KV8 ? 16 * Gm::ROWB : col_stride;
+          const uint32_t kbase = kst + blk_off(kb);
           // even and odd k-chunks go to separate accumulators (two short dependency
           // chains per 8-token half instead of one long one), added at the end
           float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
           float s2[4] = {0.f, 0.f, 0.f, 0.f}, s3[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int kk = 0; kk < KCH; ++kk) {
-            const int c = 2 * kk + k_chk;
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(kbase + (c / Gm::CPR) * kcol + swz<Gm::ROWB>(k_row0, c % Gm::CPR), b0, b1, b2, b3);
             float(&sa)[4] = (KCH >= 4 && (kk & 1)) ? s2 : s0;
             float(&sb_)[4] = (KCH >= 4 && (kk & 1)) ? s3 : s1;
-            if constexpr (KV8) {
-              mma_f16_16816(sa, qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
-              mma_f16_16816(sb_, qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
+            uint32_t b0, b1, b2, b3;
+            if constexpr (KV8) {  // tokens 0-7 from row g's word, 8-15 from row 8 + g's
+              if (!K_EARLY && kk % 4 == 0) {
+                const uint8_t* sb8 = kst8 + blk_off8(kb);
+                const uint32_t o = chunk8(g, kk + i4);  // 16-byte chunk 4 (kk / 4) + c
+                lds_words<4>(sb8 + o, kw[i][0] + kk);
+                lds_words<4>(sb8 + o + 8 * SW8, kw[i][1] + kk);
+              }
+              int8x4_to_f16x4(kw[i][0][kk], b0, b1);
+              int8x4_to_f16x4(kw[i][1][kk], b2, b3);
+              uint32_t a0 = qa[kk][0], a2 = qa[kk][1];
+              if constexpr (Gm::Q_SMEM) {
+                const uint4 q4 = reinterpret_cast<const uint4*>(smem + Gm::OFF_QF)[(warp * (KCH / 2) + kk / 2) * 32 + lane];
+                a0 = kk % 2 ? q4.z : q4.x;
+                a2 = kk % 2 ? q4.w : q4.y;
+              }
+              mma_f16_16816(sa, a0, 0u, a2, 0u, b0, b1);
+              mma_f16_16816(sb_, a0, 0u, a2, 0u, b2, b3);
             } else {
+              const int c = 2 * kk + k_chk;
+              ldsm_x4(kbase + (c / Gm::CPR) * col_stride + swz<Gm::ROWB>(k_row0, c % Gm::CPR), b0, b1, b2, b3);
               mma_bf16_16816(sa, qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
               mma_bf16_16816(sb_, qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
             }
@@ -616,6 +721,14 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
             vm_hi[i] = (tb < pc.t1 ? 0x0000ffffu : 0u) | (tb + 1 < pc.t1 ? 0xffff0000u : 0u);
           }
         }
+        // int8: the step's V words are requested before the softmax, which hides their
+        // latency (at D = 256 after it: 128 accumulators leave no room for them)
+        constexpr bool V_EARLY = KV8 && D <= 128;
+        uint32_t vw[KV8 ? NP : 1][4][KV8 ? D / 32 : 1];
+        if constexpr (V_EARLY) {
+#pragma unroll
+          for (int i = 0; i < NP; ++i) load_v8(vst8 + blk_off8(ws + WS * (sb + i)), vw[i]);
+        }
         float mx = kNegInf;
 #pragma unroll
         for (int i = 0; i < NP; ++i) mx = fmaxf(mx, fmaxf(fmaxf(x[i][0], x[i][1]), fmaxf(x[i][2], x[i][3])));
@@ -643,17 +756,10 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
           }
         }
         m_run = m_new;
-        if constexpr (KV8) {  // V rows of the same sub-blocks replace the K rows in the staging tile
-          __syncwarp();
-          dequant_subblocks<D, NP, Gm::ROWB, Gm::SUBW>(smem + Gm::OFF_V + stage * Gm::KV_BYTES, ws + WS * sb, WS,
-                                                        stg, lane);
-          __syncwarp();
-        }
 #pragma unroll
         for (int i = 0; i < NP; ++i) {
           const int kb = ws + WS * (sb + i);
-          const uint32_t vbase = KV8 ? stg_s + i * (16 * D * 2) : vst + blk_off(kb);
-          const uint32_t vcol = KV8 ? 16 * Gm::ROWB : col_stride;
+          const uint32_t vbase = vst + blk_off(kb);
           uint32_t ph0, ph1, pl0, pl1;
           if constexpr (KV8) {
             // V = v_i8 * v_scale: the scale of token t multiplies its probability (tokens
@@ -680,21 +786,35 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
             pl0 = pack_bf16x2(pr[i][0] - bf16lo_to_f32(ph0), pr[i][1] - bf16hi_to_f32(ph0));
             pl1 = pack_bf16x2(pr[i][2] - bf16lo_to_f32(ph1), pr[i][3] - bf16hi_to_f32(ph1));
           }
+          if constexpr (KV8) {
+            // int8 rows are finite whatever the tile holds past the piece end, and
+            // those tokens carry P' = 0: no V mask
 #pragma unroll
-          for (int c2 = 0; c2 < NB8 / 2; ++c2) {
-            const int c = 2 * c2 + v_chk;
-            uint32_t v0, v1, v2, v3;
-            ldsm_x4_t(vbase + (c / Gm::CPR) * vcol + swz<Gm::ROWB>(v_row0, c % Gm::CPR), v0, v1, v2, v3);
-            if (tail[i]) {
-              v0 &= vm_lo[i];
-              v1 &= vm_hi[i];
-              v2 &= vm_lo[i];
-              v3 &= vm_hi[i];
+            for (int wi = 0; wi < D / 32; ++wi) {
+              if (!V_EARLY && wi % 4 == 0) {  // the 16-byte run wi / 4 of the four rows
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  lds_words<4>(vst8 + blk_off8(kb) + chunk8((e & 1) + 2 * i4 + ((e >> 1) << 3), 2 * wi + g),
+                               vw[i][e] + wi);
+              }
+              uint32_t o01[4], o23[4];
+              int8_pairs_to_f16(vw[i][0][wi], vw[i][1][wi], o01);  // tokens 2c, 2c + 1
+              int8_pairs_to_f16(vw[i][2][wi], vw[i][3][wi], o23);  // tokens 8 + 2c, 9 + 2c
+#pragma unroll
+              for (int e = 0; e < 4; ++e) mma_f16_16816(acc[4 * wi + e], ph0, pl0, ph1, pl1, o01[e], o23[e]);
             }
-            if constexpr (KV8) {
-              mma_f16_16816(acc[2 * c2], ph0, pl0, ph1, pl1, v0, v1);
-              mma_f16_16816(acc[2 * c2 + 1], ph0, pl0, ph1, pl1, v2, v3);
-            } else {
+          } else {
+#pragma unroll
+            for (int c2 = 0; c2 < NB8 / 2; ++c2) {
+              const int c = 2 * c2 + v_chk;
+              uint32_t v0, v1, v2, v3;
+              ldsm_x4_t(vbase + (c / Gm::CPR) * col_stride + swz<Gm::ROWB>(v_row0, c % Gm::CPR), v0, v1, v2, v3);
+              if (tail[i]) {
+                v0 &= vm_lo[i];
+                v1 &= vm_hi[i];
+                v2 &= vm_lo[i];
+                v3 &= vm_hi[i];
+              }
               mma_bf16_16816(acc[2 * c2], ph0, pl0, ph1, pl1, v0, v1);
               mma_bf16_16816(acc[2 * c2 + 1], ph0, pl0, ph1, pl1, v2, v3);
             }
@@ -730,10 +850,21 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
     for (int pass = 0; pass < D / FD; ++pass) {
       if (g < nrows) {
         float* dst = facc + (warp * 8 + g) * FD;
+        if constexpr (KV8) {  // column n of 8-column block c is d = pv_dim(c, n)
 #pragma unroll
-        for (int c = pass * (FD / 8); c < (pass + 1) * (FD / 8); ++c)
-          *reinterpret_cast<float2*>(dst + 8 * c - pass * FD + 2 * i4) =
-              make_float2(acc[c][0] + acc[c][2], acc[c][1] + acc[c][3]);
+          for (int c = 0; c < NB8; ++c) {
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int d = pv_dim<D>(c, 2 * i4 + h2);
+              if (d / FD == pass) dst[d - pass * FD] = acc[c][h2] + acc[c][2 + h2];
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = pass * (FD / 8); c < (pass + 1) * (FD / 8); ++c)
+            *reinterpret_cast<float2*>(dst + 8 * c - pass * FD + 2 * i4) =
+                make_float2(acc[c][0] + acc[c][2], acc[c][1] + acc[c][3]);
+        }
       }
       named_bar_sync(1, Gm::W * 32);
       if (pass == 0) {
