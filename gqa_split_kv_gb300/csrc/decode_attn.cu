@@ -174,7 +174,7 @@ int launch_split_ngp(const SplitParams& prm, int grid, int smem_optin, int dev, 
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(SplitGeo<D>::NTHREADS);
+  cfg.blockDim = dim3(SplitGeo<D, NGP, KV8>::NTHREADS);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = st;
   if (cudaLaunchKernelEx(&cfg, kern, prm) != cudaSuccess) {

@@ -81,12 +81,14 @@ struct SplitGeo {
   // Tiles carry 32 KB (D = 32) or 64 KB of K+V so the per-tile costs (barrier
   // round trip, TMA issue) stay small against the bytes moved.
   static constexpr int T = D <= 64 ? 256 : D <= 128 ? 128 : 64;  // tokens per tile
-  static constexpr int W = 4;                       // consumer warps
+  // consumer warps: two per scheduler for int8 tiles up to D = 128 (their
+  // per-token work is a chain of short-latency integer steps), else one
+  static constexpr int W = KV8 && D <= 128 ? 8 : 4;
   static constexpr int SB = T / 16;                 // 16-token sub-blocks per tile
   // A pass runs ngp <= NGP_MAX sub-groups of <= 8 rows, one per group of W / ngp
   // warps; the warps of a sub-group take the sub-blocks ws, ws + W / ngp, ... of a tile.
   static constexpr int NGP_MAX = D == 128 ? 2 : 4;
-  static constexpr int NP = D <= 64 ? 4 : D <= 128 ? 2 : 1;  // sub-blocks per online-softmax step
+  static constexpr int NP = KV8 ? (D <= 64 ? 2 : 1) : (D <= 64 ? 4 : D <= 128 ? 2 : 1);  // sub-blocks per softmax step
   static constexpr int NTHREADS = (W + 1) * 32;
   static constexpr int SUBW = D >= 64 ? 64 : 32;    // elements per swizzle row
   static constexpr int NSUB = D / SUBW;             // swizzle rows per token
@@ -119,9 +121,9 @@ struct SplitGeo {
   static constexpr int OFF_KS = OFF_V + STAGES * KV_BYTES;
   static constexpr int OFF_VS = OFF_KS + STAGES * SC_BYTES;
   static constexpr int OFF_Q = al1k(OFF_VS + STAGES * SC_BYTES);
-  // D = 256 int8: each warp keeps its f16 query fragment here ([D/32][32 lanes][4
-  // words]) instead of in 32 registers
-  static constexpr bool Q_SMEM = KV8 && D == 256;
+  // int8 at D >= 128: each warp keeps its f16 query fragment here ([D/32][32
+  // lanes][4 words]) instead of in D/8 registers
+  static constexpr bool Q_SMEM = KV8 && D >= 128;
   static constexpr int QF_BYTES = Q_SMEM ? W * D / 32 * 32 * 16 : 0;
   static constexpr int OFF_QF = OFF_Q + STAGES * Q_BYTES;
   static constexpr int OFF_FACC = OFF_QF + QF_BYTES;
@@ -644,7 +646,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
         bool tail[NP];
         // int8: every K word of the step is loaded before the first MMA (at D = 256
         // 64 d's at a time, next to their MMAs)
-        constexpr bool K_EARLY = KV8 && D <= 128;
+        constexpr bool K_EARLY = KV8 && D <= 128;  // (one sub-block per step at D = 128)
         uint32_t kw[KV8 ? NP : 1][2][KV8 ? KCH : 1];
         if constexpr (K_EARLY) {
 #pragma unroll
@@ -723,7 +725,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
         }
         // int8: the step's V words are requested before the softmax, which hides their
         // latency (at D = 256 after it: 128 accumulators leave no room for them)
-        constexpr bool V_EARLY = KV8 && D <= 128;
+        constexpr bool V_EARLY = KV8 && D <= 64;
         uint32_t vw[KV8 ? NP : 1][4][KV8 ? D / 32 : 1];
         if constexpr (V_EARLY) {
 #pragma unroll
@@ -933,7 +935,7 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
 }
 
 template <int D, bool PAGED, int NGP, bool KV8>
-__global__ void __launch_bounds__(SplitGeo<D>::NTHREADS, 1) split_kernel(const __grid_constant__ SplitParams p) {
+__global__ void __launch_bounds__(SplitGeo<D, NGP, KV8>::NTHREADS, 1) split_kernel(const __grid_constant__ SplitParams p) {
   using Gm = SplitGeo<D, NGP, KV8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);

@@ -230,9 +230,10 @@ int decode_attn_multi_paged(const void* q, const void* k_pool, const void* v_poo
  *  paged:  k_pool_i8, v_pool_i8 int8 [num_pages, page_size, num_kv_heads, head_dim],
  *          k_scale_pool, v_scale_pool float [num_pages, num_kv_heads, page_size]
  *  Every other argument, the split plan, the partials and the error behaviour are
- *  those of decode_attn_contig / decode_attn_paged.  The kernels dequantize each
- *  16-token block into f16 in shared memory (exact) and multiply in f16 with fp32
- *  accumulation; q is converted to f16, which is exact for |q| in [2^-14, 65504].
+ *  those of decode_attn_contig / decode_attn_paged.  The MMA warps widen the int8
+ *  operands of each 16-token block to f16 in registers (exact) and multiply in f16
+ *  with fp32 accumulation; K's scale multiplies a token's score and V's scale its
+ *  probability.  q is converted to f16, exact for |q| in [2^-14, 65504].
  */
 int decode_attn_int8_contig(const void* q, const void* k_i8, const void* v_i8, const float* k_scale,
                             const float* v_scale, const int* seq_lens, int batch, int num_q_heads, int num_kv_heads,
@@ -251,7 +252,8 @@ const char* decode_status_string(int status);
  * decode_device_error — synchronise `stream`, then read and clear the device error
  * word of the current device.  *flags receives the word: bit 0 a kernel gave up on
  * a bounded wait, bit 1 a segment-counter update gave up, bit 2 a page-table entry
- * read by decode_attn_paged / decode_attn_multi_paged was outside [0, num_pages)
+ * read by decode_attn_paged / decode_attn_multi_paged / decode_attn_int8_paged was
+ * outside [0, num_pages)
  * (that box was read from page 0 instead, so the affected rows are wrong but no
  * copy leaves the pool).  Returns DA_OK when flags == 0, DA_ERR_TIMEOUT otherwise,
  * or DA_ERR_CUDA.
