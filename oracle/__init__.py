@@ -5,3 +5,4 @@ Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 shares no code with it.
 """
 from .decode_attention import *  # noqa: F401,F403
+from .prefill_attention import *  # noqa: F401,F403
