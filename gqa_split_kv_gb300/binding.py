@@ -72,6 +72,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.decode_attn_int8_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, vp, vp, vp,
                                            vp]
     lib.decode_attn_int8_paged.restype = i
+    lib.prefill_attn_contig.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, vp, vp]
+    lib.prefill_attn_contig.restype = i
+    lib.prefill_attn_paged.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, vp, vp]
+    lib.prefill_attn_paged.restype = i
     lib.decode_combine.argtypes = [vp, vp, i, i, i, i, vp, vp]
     lib.decode_combine.restype = i
     lib.decode_status_string.argtypes = [i]
@@ -305,6 +309,48 @@ def decode_attn_int8_paged(q, k_pool_i8, v_pool_i8, k_scale_pool, v_scale_pool, 
                                        max_pages, num_pages, int(max_seq_len), scale, S, _ptr(part_acc),
                                        _ptr(part_ml), _ptr(seg_counters), _ptr(out), _stream(stream))
     _check("decode_attn_int8_paged", st)
+    return out
+
+
+def prefill_attn_contig(q, k, v, seq_lens=None, scale: Optional[float] = None, out=None, stream=None):
+    """Causal prefill of the last q_len tokens: q [B, q_len, Hq, D] bf16 (token-major); k/v
+    [B, max_ctx, Hkv, D] bf16; seq_lens int32 [B] (None: max_ctx each).  Returns out like q."""
+    import torch
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k, "k", torch.bfloat16, 4)
+    _need(v, "v", torch.bfloat16, 4)
+    B, q_len, Hq, D = q.shape
+    _, ctx, Hkv, _ = k.shape
+    if seq_lens is not None:
+        _need(seq_lens, "seq_lens", torch.int32, 1)
+    scale = D ** -0.5 if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    st = load().prefill_attn_contig(_ptr(q), _ptr(k), _ptr(v), _ptr(seq_lens), B, q_len, Hq, Hkv, D, ctx, scale,
+                                    _ptr(out), _stream(stream))
+    _check("prefill_attn_contig", st)
+    return out
+
+
+def prefill_attn_paged(q, k_pool, v_pool, page_table, seq_lens, max_seq_len: int, scale: Optional[float] = None,
+                       out=None, stream=None):
+    """Causal prefill over a paged cache: pools [num_pages, page_size, Hkv, D] bf16, page_table
+    int32 [B, max_pages], seq_lens int32 [B]; q/out [B, q_len, Hq, D] bf16."""
+    import torch
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k_pool, "k_pool", torch.bfloat16, 4)
+    _need(v_pool, "v_pool", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, q_len, Hq, D = q.shape
+    num_pages, ps, Hkv, _ = k_pool.shape
+    scale = D ** -0.5 if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    st = load().prefill_attn_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(seq_lens), B, q_len,
+                                   Hq, Hkv, D, ps, page_table.shape[1], num_pages, int(max_seq_len), scale, _ptr(out),
+                                   _stream(stream))
+    _check("prefill_attn_paged", st)
     return out
 
 

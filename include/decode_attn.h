@@ -245,6 +245,38 @@ int decode_attn_int8_paged(const void* q, const void* k_pool_i8, const void* v_p
                            int num_pages, int max_seq_len, float scale, int num_splits, float* part_acc,
                            float* part_ml, unsigned long long* seg_counters, void* out, void* stream);
 
+/*
+ * prefill_attn_contig / prefill_attn_paged — causal GQA attention of a chunk of
+ * q_len new tokens per sequence (prefill when the chunk is the whole sequence,
+ * chunked prefill otherwise).  "gqa_prefill_attn" on the AstrAI commit page
+ * ("csrc", commit 988e013) is a tiled shared-memory kernel with mask support; the
+ * pages fix no layout, so: sequence b holds L_b cached tokens (its chunk included,
+ * already written to the cache), the chunk is its last q_len tokens, and query
+ * token i (position L_b - q_len + i) attends to positions 0 .. L_b - q_len + i.  A
+ * query that sees no token (L_b < q_len - i) gives zeros.  Query head h reads KV
+ * head h / G.
+ *  q, out   bf16 [batch, q_len, num_q_heads, head_dim], token-major (16-byte aligned)
+ *  k, v     the decode cache: contiguous [batch, max_ctx, num_kv_heads, head_dim]
+ *           (seq_lens may be NULL: every sequence max_ctx tokens), or pools
+ *           [num_pages, page_size, num_kv_heads, head_dim] with page_table
+ *           int32 [batch, max_pages_per_seq] (page_size a multiple of 16)
+ *  seq_lens int32 [batch], clamped to [0, max_ctx] (paged: to
+ *           min(max_pages_per_seq * page_size, max_seq_len))
+ *  head_dim 32, 64, 128 or 256; G = num_q_heads / num_kv_heads <= 64.
+ * Softmax in fp32 (log2 units), P rounded to bf16 for the P V product, fp32
+ * accumulation, output rounded to bf16.  No workspace; the library allocates
+ * nothing.  Argument errors return DA_ERR_INVALID_ARG / DA_ERR_UNSUPPORTED before
+ * any launch; page-table entries outside [0, num_pages) set bit 2 of the device
+ * error word (decode_device_error) and read page 0 instead.
+ */
+int prefill_attn_contig(const void* q, const void* k, const void* v, const int* seq_lens, int batch, int q_len,
+                        int num_q_heads, int num_kv_heads, int head_dim, int max_ctx, float scale, void* out,
+                        void* stream);
+int prefill_attn_paged(const void* q, const void* k_pool, const void* v_pool, const int* page_table,
+                       const int* seq_lens, int batch, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                       int page_size, int max_pages_per_seq, int num_pages, int max_seq_len, float scale, void* out,
+                       void* stream);
+
 /* Human-readable name of a da_status value (static string). */
 const char* decode_status_string(int status);
 

@@ -173,3 +173,31 @@ def test_int8_argument_errors(clib):
     assert i8(D=48) == 2
     assert clib.decode_attn_int8_paged(A, A, A, None, A, A, A, 1, 8, 2, 64, 16, 4, 4, 64, ctypes.c_float(0.125), 2,
                                        A, A, A, A, None) == 1
+
+
+def test_prefill_argument_checks_return_before_cuda(clib):
+    V = ctypes.c_void_p
+    q = V(1 << 20)  # never dereferenced: every call below is rejected or has nothing to do
+    nan = float("nan")
+    # (batch, q_len, Hq, Hkv, D, max_ctx, scale) -> status
+    cases = [((1, 4, 6, 4, 128, 64, 0.1), 1),      # Hq not a multiple of Hkv
+             ((1, 4, 8, 2, 48, 64, 0.1), 2),       # head_dim
+             ((1, 4, 130, 2, 64, 64, 0.1), 2),     # G = 65 rows per token
+             ((1, 4, 8, 2, 64, 64, nan), 1),       # scale
+             ((-1, 4, 8, 2, 64, 64, 0.1), 1),
+             ((1, -4, 8, 2, 64, 64, 0.1), 1),
+             ((1, 4, 8, 2, 64, -1, 0.1), 1),
+             ((0, 4, 8, 2, 64, 64, 0.1), 0),       # nothing to do
+             ((3, 0, 8, 2, 64, 64, 0.1), 0)]
+    for (B, n, Hq, Hkv, D, ctx, sc), want in cases:
+        got = clib.prefill_attn_contig(q, q, q, None, B, n, Hq, Hkv, D, ctx, sc, q, None)
+        assert got == want, (B, n, Hq, Hkv, D, ctx, sc, got)
+    # misaligned q / out
+    assert clib.prefill_attn_contig(V((1 << 20) + 2), q, q, None, 1, 4, 8, 2, 64, 64, 0.1, q, None) == 1
+    assert clib.prefill_attn_contig(q, q, q, None, 1, 4, 8, 2, 64, 64, 0.1, V((1 << 20) + 8), None) == 1
+    # paged: page size, missing table / lengths, negative sizes
+    assert clib.prefill_attn_paged(q, q, q, q, q, 1, 4, 8, 2, 64, 8, 4, 16, 64, 0.1, q, None) == 2
+    assert clib.prefill_attn_paged(q, q, q, None, q, 1, 4, 8, 2, 64, 16, 4, 16, 64, 0.1, q, None) == 1
+    assert clib.prefill_attn_paged(q, q, q, q, None, 1, 4, 8, 2, 64, 16, 4, 16, 64, 0.1, q, None) == 1
+    assert clib.prefill_attn_paged(q, q, q, q, q, 1, 4, 8, 2, 64, 16, -1, 16, 64, 0.1, q, None) == 1
+    assert clib.prefill_attn_paged(q, q, q, q, q, 1, 4, 8, 3, 64, 16, 4, 16, 64, 0.1, q, None) == 1
