@@ -34,6 +34,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "decode-attn µs/call and achieved HBM GB/s vs GB300 peak (1 GPU)"
+PREFILL_METRIC = "causal GQA prefill µs/call and achieved TFLOP/s vs GB300 bf16 peak (1 GPU)"
 HEADLINE = "gqa6_contig_b1_hq24_hkv4_d256_ctx4096"
 # Published time per call of the pages' fa_split_gqa_kernel on this exact workload
 # (RTX 5090, "perf(dspark): overlap KV staging with compute via cp.async",
@@ -70,8 +71,8 @@ def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
 def ncu_traffic(workload: str):
@@ -158,8 +159,13 @@ def job_value(world: int, bytes_per_step: int, steps: int, total_ms: float) -> f
 
 def oracle_unit(oracle, wl, inp, b: int, g: int) -> int:
     """The oracle on one sample unit: every query row of KV head g of sequence b.
-    Returns the unit's algorithmic bytes (its K/V rows and query rows)."""
+    Returns the unit's algorithmic bytes (its K/V rows and query rows); for a
+    prefill workload the unit is one query head's chunk and the return is flops."""
     G = wl.Hq // wl.Hkv
+    if wl.kind == "prefill":  # one query head over the whole chunk; returns flops
+        oracle.prefill(inp, [(b, i, g * G) for i in range(wl.q_len)])
+        L = int(inp["seq_lens"][b])
+        return 4 * wl.D * sum(max(0, min(L, L - wl.q_len + 1 + i)) for i in range(wl.q_len))
     if wl.kv_dtype == "int8":
         oracle.decode_int8(inp, [(b, g * G + i) for i in range(G)])
         return 2 * (wl.D + 4) * int(inp["seq_lens"][b]) + G * wl.D * 2
@@ -188,7 +194,7 @@ def cpu_child(workload: str, seconds: float):
         done_bytes += oracle_unit(oracle, wl, inp, b, g)
         n += 1
     dt = time.perf_counter() - t0
-    print(json.dumps({"gbs": done_bytes / dt / 1e9, "units": n, "seconds": dt}))
+    print(json.dumps({"gbs": done_bytes / dt / 1e9, "tflops": done_bytes / dt / 1e12, "units": n, "seconds": dt}))
 
 
 def run_cpu_baseline(workload: str, seconds: float) -> dict:
@@ -203,6 +209,11 @@ def run_cpu_baseline(workload: str, seconds: float) -> dict:
         return {"value": None, "unit": "GB/s", "cores": cores, "kind": "oracle",
                 "sample": f"failed: {res.stderr[-300:]}"}
     d = json.loads(line[-1])
+    from gqa_split_kv_gb300.workloads import WORKLOADS
+    if WORKLOADS[workload].kind == "prefill":
+        return {"value": round(d["tflops"], 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                "sample": f"{d['units']} units of one (sequence, query head) over the whole chunk, "
+                          f"{d['seconds']:.1f} s, fp64 numpy oracle, BLAS threads = {cores}"}
     return {"value": round(d["gbs"], 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"{d['units']} units of one (sequence, KV head) with its G query heads over the full "
                       f"context, {d['seconds']:.1f} s, fp64 numpy oracle, BLAS threads = {cores}"}
@@ -334,6 +345,116 @@ def measure(wl, inp, steps: int, warmup: int, flush_bytes: int, dist=None, sampl
     return res
 
 
+def measure_prefill(wl, inp, steps: int, warmup: int, flush_bytes: int, dist=None, sampler=None, e2e_steps: int = 0):
+    """Causal prefill through the public call: device-timed steps (L2 flushed before
+    each) and, optionally, end-to-end steps with the inputs copied in and the output out."""
+    import numpy as np
+    import torch
+
+    from gqa_split_kv_gb300 import binding
+    from gqa_split_kv_gb300.accounting import prefill_work
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+    paged = wl.layout == "paged"
+    names = ("k_pool", "v_pool") if paged else ("k", "v")
+    q = to_dev(inp["q"])
+    kc, vc = to_dev(inp[names[0]]), to_dev(inp[names[1]])
+    lens = torch.from_numpy(inp["seq_lens"]).cuda()
+    table = torch.from_numpy(inp["page_table"]).cuda() if paged else None
+    out = torch.empty_like(q)
+    flush = torch.empty(flush_bytes, dtype=torch.uint8, device="cuda")
+    flush_src = torch.empty(flush_bytes // 4, dtype=torch.float32, device="cuda").zero_()
+    stream = torch.cuda.current_stream()
+
+    def flush_l2():
+        flush.zero_()
+        torch.sum(flush_src)
+
+    def call():
+        if paged:
+            binding.prefill_attn_paged(q, kc, vc, table, lens, wl.max_ctx, scale=wl.scale, out=out)
+        else:
+            binding.prefill_attn_contig(q, kc, vc, lens, scale=wl.scale, out=out)
+
+    for _ in range(warmup):
+        flush_l2()
+        call()
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    for i in range(steps):
+        flush_l2()
+        ev0[i].record(stream)
+        call()
+        ev1[i].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    if dist is not None:
+        dist.barrier()
+    assert binding.device_error() == 0
+    res = {"times_ms": [a.elapsed_time(b) for a, b in zip(ev0, ev1)], "clocks": clocks, "launches_per_step": 1,
+           "work": prefill_work(wl.B, wl.Hq, wl.Hkv, wl.D, inp["seq_lens"], wl.q_len)}
+    if e2e_steps > 0:
+        hq = torch.from_numpy(np.ascontiguousarray(inp["q"]).view(np.int16)).pin_memory()
+        hk = torch.from_numpy(np.ascontiguousarray(inp[names[0]]).view(np.int16)).pin_memory()
+        hv = torch.from_numpy(np.ascontiguousarray(inp[names[1]]).view(np.int16)).pin_memory()
+        hl = torch.from_numpy(inp["seq_lens"]).pin_memory()
+        out_h = torch.empty(tuple(q.shape), dtype=torch.int16).pin_memory()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        for it in range(2):
+            n = 3 if it == 0 else e2e_steps
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(n):
+                q.view(torch.int16).copy_(hq, non_blocking=True)
+                kc.view(torch.int16).copy_(hk, non_blocking=True)
+                vc.view(torch.int16).copy_(hv, non_blocking=True)
+                lens.copy_(hl, non_blocking=True)
+                call()
+                out_h.copy_(out.view(torch.int16), non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize()
+        res["e2e_ms"] = e0.elapsed_time(e1) / e2e_steps
+        res["h2d"] = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hl))
+        res["d2h"] = out_h.numel() * 2
+    del flush, flush_src
+    return res
+
+
+def prefill_line(wl, r, ws, K, W, total_ms, e2e_ms, peaks) -> dict:
+    flops = r["work"]["flops"]
+    per = sorted(r["times_ms"])
+    achieved = flops / (total_ms / K / 1e3) / 1e12
+    return {
+        "metric": PREFILL_METRIC, "value": round(ws * flops * K / (total_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": K, "warmup": W, "ms_per_step": round(total_ms / K, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "head_dim": wl.D, "ctx": wl.max_ctx,
+                   "q_len": wl.q_len, "layout": wl.layout, "kind": "prefill", "accum": "fp32",
+                   "l2": "flushed before every step (outside the timed pair)",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "us_per_call": {"mean": round(1e3 * total_ms / K, 3), "median": round(1e3 * per[len(per) // 2], 3)},
+        "work_per_call": r["work"],
+        "roofline": {"bound": "tensor", "kernel": "prefill_kernel (mma.sync bf16), events around the call",
+                     "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["bf16_tflops"], 4),
+                     "peak_source": f"{peaks['source']} cuBLAS bf16 burst", "traffic": ncu_traffic(wl.name)},
+        "e2e": {"value": round(ws * flops / (e2e_ms / 1e3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": r["launches_per_step"] * K,
+        "clocks": r["clocks"],
+    }
+
+
 def ours(args):
     import torch
 
@@ -358,6 +479,19 @@ def ours(args):
     vis = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
     phys = vis[local] if local < len(vis) else str(local)
     sampler = ClockSampler(phys) if rank == 0 else None
+    if wl.kind == "prefill":
+        steps = min(args.steps, 200)  # a prefill call is ~1000x a decode call
+        r = measure_prefill(wl, inp, steps, args.warmup, flush_bytes, dist=dist, sampler=sampler,
+                            e2e_steps=max(3, min(steps, 20)))
+        total_ms, e2e_ms = max_over_ranks([sum(r["times_ms"]), r["e2e_ms"]], dist, "cuda")
+        line = prefill_line(wl, r, ws, steps, args.warmup, total_ms, e2e_ms, peaks)
+        if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = run_cpu_baseline(wl.name, args.cpu_seconds)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
     r = measure(wl, inp, args.steps, args.warmup, flush_bytes, dist=dist, sampler=sampler,
                 e2e_steps=max(3, min(args.steps, 200)))
     total_ms, e2e_ms = max_over_ranks([sum(r["times_ms"]), r["e2e_ms"]], dist, "cuda")
@@ -400,6 +534,16 @@ def ours(args):
             if name == wl.name:
                 continue
             oi = make_inputs(other)
+            if other.kind == "prefill":
+                rr = measure_prefill(other, oi, 20, 3, flush_bytes)
+                t = sorted(rr["times_ms"])
+                med = t[len(t) // 2]
+                tf = rr["work"]["flops"] / (med / 1e3) / 1e12
+                print(json.dumps({"suite": name, "us_per_call_median": round(1e3 * med, 3),
+                                  "achieved_tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+                                  "work": rr["work"]}), flush=True)
+                del oi
+                continue
             rr = measure(other, oi, 50, 5, flush_bytes)
             t = sorted(rr["times_ms"])
             med = t[len(t) // 2]
@@ -436,17 +580,21 @@ def reference(args):
     t0 = time.perf_counter()
     nbytes = sum(step(i) for i in range(args.steps))
     dt = time.perf_counter() - t0
-    v = nbytes / dt / 1e9
+    pre = wl.kind == "prefill"
+    v = nbytes / dt / (1e12 if pre else 1e9)
+    unit = "TFLOP/s" if pre else "GB/s"
     cores = os.cpu_count() or 1
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": ws,
+        "impl": "reference", "metric": PREFILL_METRIC if pre else METRIC, "value": round(v, 6), "unit": unit,
+        "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "head_dim": wl.D, "ctx": wl.max_ctx,
                    "layout": wl.layout},
-        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": "per step: all G query heads of one (sequence, KV head) over its full context"},
-        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": round(v, 6), "unit": unit, "cores": cores, "kind": "oracle",
+                         "sample": ("per step: one query head of one sequence over the whole chunk" if pre else
+                                    "per step: all G query heads of one (sequence, KV head) over its full context")},
+        "e2e": {"value": round(v, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
 

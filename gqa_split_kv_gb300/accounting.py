@@ -89,3 +89,27 @@ def traffic_bytes(B: int, Hq: int, Hkv: int, D: int, seq_lens, S: int, page_size
     return {"kv": kv, "q": q, "out": out, "partials_read": partials, "partials_written": partials,
             "page_table": pt, "seq_lens": sl,
             "algorithmic": kv + q + partials + pt + sl, "strict": kv + q + out}
+
+
+def prefill_visible(seq_lens, q_len: int) -> int:
+    """Keys seen by all query tokens of a causal chunk, summed over sequences (per
+    query head): query i of a sequence of L tokens sees max(0, min(L, L - q_len + 1 + i))."""
+    total = 0
+    for L in np.asarray(seq_lens, dtype=np.int64):
+        L = int(L)
+        lo = L - q_len + 1  # keys of query 0
+        # sum over i of clamp(lo + i, 0, L)
+        for_i = np.clip(lo + np.arange(q_len, dtype=np.int64), 0, L)
+        total += int(for_i.sum())
+    return total
+
+
+def prefill_work(B: int, Hq: int, Hkv: int, D: int, seq_lens, q_len: int) -> dict:
+    """Algorithmic flops and bytes of one causal prefill call: 2 D flops for each
+    (query, key) score and 2 D for its share of P V, per query head; bytes of q,
+    out and of K/V read once."""
+    vis = prefill_visible(seq_lens, q_len)
+    flops = 4 * D * Hq * vis
+    kv = 2 * 2 * D * Hkv * int(np.clip(np.asarray(seq_lens, dtype=np.int64), 0, None).sum())
+    qo = 2 * 2 * B * q_len * Hq * D
+    return {"flops": flops, "visible_pairs_per_head": vis, "kv_bytes": kv, "q_out_bytes": qo}

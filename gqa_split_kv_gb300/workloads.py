@@ -84,6 +84,7 @@ class Workload:
     seed: int = 1234
     q_len: int = 1  # query tokens per sequence (> 1: multi-query decode, q is [B, Hq, q_len, D])
     kv_dtype: str = "bf16"  # "int8": symmetric int8 K/V with fp32 scales per (token, KV head)
+    kind: str = "decode"    # "prefill": causal attention of the last q_len tokens, q is [B, q_len, Hq, D]
 
     @property
     def G(self) -> int:
@@ -136,6 +137,17 @@ WORKLOADS = {
     "int8_paged_b16_hq32_hkv8_d128_u256_8192_ps32": Workload(
         "int8_paged_b16_hq32_hkv8_d128_u256_8192_ps32", B=16, Hq=32, Hkv=8, D=128, max_ctx=8192,
         layout="paged", page_size=32, lens="uniform", lens_lo=256, lens_hi=8192, kv_dtype="int8", seed=1246),
+    # causal prefill: a full 4096-token prompt, a 1024-token chunk after 7168 cached
+    # tokens (paged), and the GQA-6 head_dim 256 shape of the decode configurations
+    "prefill_contig_b1_hq32_hkv8_d128_L4096": Workload(
+        "prefill_contig_b1_hq32_hkv8_d128_L4096", B=1, Hq=32, Hkv=8, D=128, max_ctx=4096, q_len=4096,
+        kind="prefill", seed=1247),
+    "prefill_chunk_paged_b4_hq32_hkv8_d128_ctx8192_q1024_ps32": Workload(
+        "prefill_chunk_paged_b4_hq32_hkv8_d128_ctx8192_q1024_ps32", B=4, Hq=32, Hkv=8, D=128, max_ctx=8192,
+        layout="paged", page_size=32, q_len=1024, kind="prefill", seed=1248),
+    "prefill_gqa6_contig_b1_hq24_hkv4_d256_L4096": Workload(
+        "prefill_gqa6_contig_b1_hq24_hkv4_d256_L4096", B=1, Hq=24, Hkv=4, D=256, max_ctx=4096, q_len=4096,
+        kind="prefill", seed=1249),
 }
 
 
@@ -184,7 +196,10 @@ def make_inputs(wl: Workload, seed: Optional[int] = None) -> dict:
     """
     rng = np.random.default_rng(wl.seed if seed is None else seed)
     seq_lens = draw_seq_lens(wl, rng)
-    q = _normal_bf16(rng, (wl.B, wl.Hq, wl.D) if wl.q_len == 1 else (wl.B, wl.Hq, wl.q_len, wl.D))
+    if wl.kind == "prefill":  # token-major chunk queries
+        q = _normal_bf16(rng, (wl.B, wl.q_len, wl.Hq, wl.D))
+    else:
+        q = _normal_bf16(rng, (wl.B, wl.Hq, wl.D) if wl.q_len == 1 else (wl.B, wl.Hq, wl.q_len, wl.D))
     out = {"q": q, "seq_lens": seq_lens, "scale": wl.scale}
     if wl.kv_dtype == "int8":  # keys k_i8, v_i8, k_scale, v_scale (or their page pools)
         cache = make_int8_cache(rng, wl.B, wl.max_ctx, wl.Hkv, wl.D)

@@ -67,10 +67,42 @@ def _full_size_int8(wl, inp):
     assert np.array_equal(out, out2)
 
 
+def _full_size_prefill(wl, inp):
+    """Causal prefill workloads: sampled (b, i, h) outputs against the oracle (a few
+    query heads, each over the whole chunk) and bitwise run-to-run determinism."""
+    from gqa_split_kv_gb300 import binding
+    d = to_device(inp)
+    out = torch.empty_like(d["q"])
+
+    def call():
+        if wl.layout == "paged":
+            binding.prefill_attn_paged(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["seq_lens"], wl.max_ctx,
+                                       scale=inp["scale"], out=out)
+        else:
+            binding.prefill_attn_contig(d["q"], d["k"], d["v"], d["seq_lens"], scale=inp["scale"], out=out)
+        torch.cuda.synchronize()
+        assert binding.device_error() == 0
+        return out.view(torch.int16).cpu().numpy().view(np.uint16).copy()
+
+    got_bits = call()
+    assert np.all(np.isfinite(bf16_bits_to_f32(got_bits)))
+    rng = np.random.default_rng(4545)
+    heads = [0, wl.Hq - 1, int(rng.integers(wl.Hq))]
+    rows = sorted({(int(rng.integers(wl.B)), i, h) for h in heads
+                   for i in [0, wl.q_len - 1] + [int(x) for x in rng.integers(wl.q_len, size=6)]})
+    ref = oracle.prefill(inp, rows)
+    got = np.stack([bf16_bits_to_f32(got_bits[b, i, h]).astype(np.float64) for b, i, h in rows])
+    err = np.abs(got - ref)
+    assert np.all(err <= OUT_ATOL + OUT_RTOL * np.abs(ref)), f"{wl.name}: max abs err {err.max():.3e}"
+    assert np.array_equal(call(), got_bits)
+
+
 @pytest.mark.parametrize("name", list(WORKLOADS))
 def test_full_size_workload(name):
     wl = WORKLOADS[name]
     inp = make_inputs(wl)
+    if wl.kind == "prefill":
+        return _full_size_prefill(wl, inp)
     if wl.kv_dtype == "int8":
         return _full_size_int8(wl, inp)
     d = to_device(inp)

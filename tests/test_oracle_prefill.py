@@ -120,3 +120,11 @@ def test_planted_off_by_one_limits_are_caught(monkeypatch):
         with monkeypatch.context() as m:
             m.setattr(op, "visible_tokens", bad)
             assert np.abs(op.prefill(inp) - ref).max() > 1e-6
+
+
+def test_bench_flop_count_matches_the_oracle_row_count():
+    from gqa_split_kv_gb300.accounting import prefill_visible, prefill_work
+    for lens, q_len in [([5], 5), ([9, 3], 5), ([205, 75, 40, 0], 75), ([4096], 4096), ([8192] * 4, 1024)]:
+        assert prefill_visible(lens, q_len) == op.prefill_row_count(lens, q_len)
+    w = prefill_work(1, 32, 8, 128, [4096], 4096)
+    assert w["flops"] == 4 * 128 * 32 * (4096 * 4097 // 2)
