@@ -877,6 +877,14 @@ int prefill_call(bool paged, const void* q, const void* k, const void* v, const 
   prm.G = G;
   prm.BQ = BQ;
   prm.nqb = (int)nqb;
+  {
+    // launch groups of (b, h) units whose K/V (bf16 K + V of max_len tokens) fit in
+    // about 48 MB of L2 together
+    const long long unit_bytes = 4LL * D * (max_len > 0 ? max_len : 1);
+    long long g = (48LL << 20) / unit_bytes;
+    g = g < 1 ? 1 : g;
+    prm.grp = (int)(g < (long long)B * Hkv ? g : (long long)B * Hkv);
+  }
   prm.max_len = max_len;
   prm.page_size = paged ? page_size : 0;
   prm.max_pages = paged ? max_pages : 0;

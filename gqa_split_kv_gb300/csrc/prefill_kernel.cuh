@@ -15,8 +15,10 @@
 // causal limit; four MMA warps each own 16 rows: S = Q K^T into registers, a masked
 // online softmax in log2 units, P packed to bf16 (the C fragment of S is the A
 // fragment of P V), and P V accumulated in fp32.  Masks apply only to tiles that
-// reach past the block's first row limit.  The heaviest blocks (latest query
-// tokens) are launched first.
+// reach past the block's first row limit.  Blocks launch in groups of grp
+// (sequence, KV head) units whose K/V fit in L2 together, and within a group the
+// heaviest blocks (latest query tokens) first, so the CTAs in flight stream the
+// same few K/V ranges from L2.
 #pragma once
 
 #include <cstdint>
@@ -31,6 +33,7 @@ struct PrefillParams {
   const int* seq_lens;     // [B] or null (every sequence max_len tokens)
   const int* page_table;   // paged: [B, max_pages]
   int B, q_len, Hq, Hkv, G, BQ, nqb;
+  int grp;  // (sequence, KV head) units per launch group (their K/V fit in L2 together)
   int max_len;
   int page_size, max_pages, num_pages, box_shift, page_shift;
   float scale_log2;
@@ -79,11 +82,16 @@ __global__ void __launch_bounds__(PrefillGeo<D>::NTHREADS, PrefillGeo<D>::CTAS)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float kNegInf = -__int_as_float(0x7f800000);
 
-  // work unit: later query blocks first (they see the most keys)
-  const int per_qb = p.B * p.Hkv;
-  const int qb = p.nqb - 1 - (int)(blockIdx.x / per_qb);
-  const int b = (int)(blockIdx.x % per_qb) / p.Hkv;
-  const int h = (int)(blockIdx.x % per_qb) % p.Hkv;
+  // work unit: group of grp (b, h) units (the last group may be smaller), then
+  // query blocks latest first, then the units of the group
+  const int nbh = p.B * p.Hkv;
+  const long long per_grp = (long long)p.nqb * p.grp;
+  const int gi = (int)(blockIdx.x / per_grp);
+  const int gsz = min(p.grp, nbh - gi * p.grp);
+  const int in_g = (int)(blockIdx.x - gi * per_grp);
+  const int qb = p.nqb - 1 - in_g / gsz;
+  const int bh = gi * p.grp + in_g % gsz;
+  const int b = bh / p.Hkv, h = bh % p.Hkv;
   int L = p.seq_lens ? __ldg(p.seq_lens + b) : p.max_len;
   L = L < 0 ? 0 : (L > p.max_len ? p.max_len : L);
   const int q0 = qb * p.BQ;
