@@ -108,13 +108,15 @@ int sub_width(int D) { return D >= 64 ? 64 : 32; }
 int sub_width8(int D) { return D >= 128 ? 128 : D; }
 CUtensorMapSwizzle swizzle8(int D) { return D >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE; }
 
-// tokens per tile of the split kernel for head_dim D (the TMA box height of a contiguous cache)
-int tile_tokens(int D) {
+// tokens per tile of the split kernel for head_dim D and the cache's element type
+// (the TMA box height of a contiguous cache; the kernel's expected byte count uses
+// the same geometry)
+int tile_tokens(int D, bool kv8) {
   switch (D) {
-    case 32: return SplitGeo<32>::T;
-    case 64: return SplitGeo<64>::T;
-    case 128: return SplitGeo<128>::T;
-    default: return SplitGeo<256>::T;
+    case 32: return kv8 ? SplitGeo<32, 1, true>::T : SplitGeo<32>::T;
+    case 64: return kv8 ? SplitGeo<64, 1, true>::T : SplitGeo<64>::T;
+    case 128: return kv8 ? SplitGeo<128, 1, true>::T : SplitGeo<128>::T;
+    default: return kv8 ? SplitGeo<256, 1, true>::T : SplitGeo<256>::T;
   }
 }
 
@@ -421,7 +423,7 @@ static int contig_call(const void* q, const void* k, const void* v, const int* s
   if (current_device(&dev) || device_info(dev, &sms, &smem_optin)) return DA_ERR_CUDA;
 
   CUtensorMap tk, tv, tks, tvs;
-  const int T = tile_tokens(D);
+  const int T = tile_tokens(D, kv8);
   if (!kv8) {
     // dims (swizzle row, token, swizzle column, head, batch): one box fills every
     // swizzle column of T tokens of one head, [D/SW][T][SW] in shared memory

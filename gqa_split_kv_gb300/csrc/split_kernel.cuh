@@ -80,7 +80,7 @@ template <int D, int NGP = 1, bool KV8 = false>
 struct SplitGeo {
   // Tiles carry 32 KB (D = 32) or 64 KB of K+V so the per-tile costs (barrier
   // round trip, TMA issue) stay small against the bytes moved.
-  static constexpr int T = D <= 64 ? 256 : D <= 128 ? 128 : 64;  // tokens per tile
+  static constexpr int T = D <= 64 ? 256 : D <= 128 ? 128 : 64;  // tokens per tile (any NGP)
   // consumer warps: two per scheduler for int8 tiles up to D = 128 (their
   // per-token work is a chain of short-latency integer steps), else one
   static constexpr int W = KV8 && D <= 128 ? 8 : 4;
