@@ -108,8 +108,8 @@ int sub_width(int D) { return D >= 64 ? 64 : 32; }
 int sub_width8(int D) { return D >= 128 ? 128 : D; }
 CUtensorMapSwizzle swizzle8(int D) { return D >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE; }
 
-// tokens per tile of the split kernel for head_dim D and the cache's element type
-// (the TMA box height of a contiguous cache; the kernel's expected byte count uses
+// tokens per tile of the split kernel for a contiguous cache of head_dim D and the
+// cache's element type (the TMA box height; the kernel's expected byte count uses
 // the same geometry)
 int tile_tokens(int D, bool kv8) {
   switch (D) {
@@ -161,7 +161,7 @@ template <int D, bool PAGED, int NGP, bool KV8>
 int launch_split_ngp(const SplitParams& prm, int grid, int smem_optin, int dev, cudaStream_t st) {
   static bool attr_done[kMaxDevices] = {false};
   auto kern = split_kernel<D, PAGED, NGP, KV8>;
-  const int smem = SplitGeo<D, NGP, KV8>::smem_bytes(prm.B);
+  const int smem = SplitGeo<D, NGP, KV8, PAGED>::smem_bytes(prm.B);
   if (smem > smem_optin || smem > 227 * 1024) return DA_ERR_UNSUPPORTED;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -177,7 +177,7 @@ int launch_split_ngp(const SplitParams& prm, int grid, int smem_optin, int dev, 
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(SplitGeo<D, NGP, KV8>::NTHREADS);
+  cfg.blockDim = dim3(SplitGeo<D, NGP, KV8, PAGED>::NTHREADS);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = st;
   if (cudaLaunchKernelEx(&cfg, kern, prm) != cudaSuccess) {

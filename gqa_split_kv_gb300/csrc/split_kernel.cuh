@@ -75,12 +75,15 @@ struct SplitParams {
 };
 
 // NGP: sub-groups per pass (the query-row slots per stage); KV8: int8 K/V with
-// fp32 scales per (token, KV head), widened to f16 in registers by the MMA warps.
-template <int D, int NGP = 1, bool KV8 = false>
+// fp32 scales per (token, KV head), widened to f16 in registers by the MMA warps;
+// PG: a paged cache.
+template <int D, int NGP = 1, bool KV8 = false, bool PG = false>
 struct SplitGeo {
-  // Tiles carry 32 KB (D = 32) or 64 KB of K+V so the per-tile costs (barrier
-  // round trip, TMA issue) stay small against the bytes moved.
-  static constexpr int T = D <= 64 ? 256 : D <= 128 ? 128 : 64;  // tokens per tile (any NGP)
+  // bf16 tiles carry 32 KB (D = 32) or 64 KB of K+V so the per-tile costs (barrier
+  // round trip, TMA issue, page lookups) stay small against the bytes moved; int8
+  // tiles carry half as much, except paged at D = 128, where 256-token tiles (two
+  // stages) cut the per-tile cost of the many small page boxes.
+  static constexpr int T = KV8 && PG && D == 128 ? 256 : D <= 64 ? 256 : D <= 128 ? 128 : 64;  // tokens per tile
   // consumer warps: two per scheduler for int8 tiles up to D = 128 (their
   // per-token work is a chain of short-latency integer steps), else one
   static constexpr int W = KV8 && D <= 128 ? 8 : 4;
@@ -94,7 +97,8 @@ struct SplitGeo {
   static constexpr int NSUB = D / SUBW;             // swizzle rows per token
   static constexpr int ROWB = SUBW * 2;             // 128 or 64 bytes
   static constexpr int CPR = SUBW / 8;              // 16-byte chunks per swizzle row
-  static constexpr int STAGES = KV8 ? (D == 256 ? 3 : D == 32 ? 6 : 4) : (D == 256 ? 2 : D >= 64 ? 3 : 5);
+  static constexpr int STAGES = KV8 ? (D == 256 ? 3 : D == 32 ? 6 : D == 128 && PG ? 2 : 4)
+                                    : (D == 256 ? 2 : D >= 64 ? 3 : 5);
   // fold scratch columns per fold pass (two passes at D = 128 with extra query rows)
   static constexpr int FD = D == 128 && NGP > 1 ? 64 : D;
   // One TMA box fills all NSUB swizzle columns of its R rows, so a tile is
@@ -207,7 +211,7 @@ struct TileCursor {
 template <int D, bool PAGED, int NGP, bool KV8>
 __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan& pl, const int* lens, const int* P,
                                                uint8_t* smem, uint32_t sbase, volatile int* abort_flag) {
-  using Gm = SplitGeo<D, NGP, KV8>;
+  using Gm = SplitGeo<D, NGP, KV8, PAGED>;
   const int lane = threadIdx.x & 31;
   const uint32_t bar_full = sbase + Gm::OFF_BAR;
   const uint32_t bar_empty = bar_full + Gm::STAGES * 8;
@@ -475,7 +479,7 @@ __device__ __forceinline__ void lds_words(const uint8_t* p, uint32_t* w) {
 template <int D, bool PAGED, int NGP, bool KV8>
 __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan& pl, const int* lens, const int* P,
                                                uint8_t* smem, uint32_t sbase, volatile int* abort_flag) {
-  using Gm = SplitGeo<D, NGP, KV8>;
+  using Gm = SplitGeo<D, NGP, KV8, PAGED>;
   constexpr int KCH = D / 16;  // k-chunks of the QK^T product
   constexpr int NB8 = D / 8;   // 8-column blocks of the PV product
   constexpr int NP = Gm::NP;
@@ -935,8 +939,8 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
 }
 
 template <int D, bool PAGED, int NGP, bool KV8>
-__global__ void __launch_bounds__(SplitGeo<D, NGP, KV8>::NTHREADS, 1) split_kernel(const __grid_constant__ SplitParams p) {
-  using Gm = SplitGeo<D, NGP, KV8>;
+__global__ void __launch_bounds__(SplitGeo<D, NGP, KV8, PAGED>::NTHREADS, 1) split_kernel(const __grid_constant__ SplitParams p) {
+  using Gm = SplitGeo<D, NGP, KV8, PAGED>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
