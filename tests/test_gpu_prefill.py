@@ -65,6 +65,14 @@ def test_prefill_matches_oracle(D, Hq, Hkv):
     check(run_prefill(inp), oracle.prefill(inp), f"D={D} G={Hq // Hkv}")
 
 
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 2, 64), (64, 1, 32), (64, 1, 128)])
+def test_prefill_large_groups(Hq, Hkv, D):
+    # G = 16 (4 query tokens per block) and G = 64 (one token per block, all 64 rows)
+    lens = [90, 33]
+    inp = prefill_case(Hq + D, len(lens), 33, Hq, Hkv, D, 96, lens)
+    check(run_prefill(inp), oracle.prefill(inp), f"G={Hq // Hkv} D={D}")
+
+
 @pytest.mark.parametrize("D,ps", [(64, 16), (128, 32), (256, 64), (32, 48)])
 def test_prefill_paged_equals_contiguous_bitwise(D, ps):
     lens = [300, 64, 17]
