@@ -825,11 +825,12 @@ int prefill_call(bool paged, const void* q, const void* k, const void* v, const 
   if (B < 0 || q_len < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || !std::isfinite(scale)) return DA_ERR_INVALID_ARG;
   if (D != 32 && D != 64 && D != 128 && D != 256) return DA_ERR_UNSUPPORTED;
   const int G = Hq / Hkv;
-  if (G > PrefillGeo<128>::ROWS) return DA_ERR_UNSUPPORTED;  // one token's G rows must fit a CTA
+  if (G > PrefillGeo<128>::ROWS) return DA_ERR_UNSUPPORTED;  // one token's G rows must fit a CTA (64 or 128 rows)
   if ((long long)q_len * Hq > (1LL << 28)) return DA_ERR_UNSUPPORTED;
   if (B == 0 || q_len == 0) return DA_OK;
   if (!q || !out || !aligned(q, 16) || !aligned(out, 16)) return DA_ERR_INVALID_ARG;
-  const int BQ = PrefillGeo<128>::ROWS / G;  // query tokens per CTA
+  const int rows = D == 256 ? PrefillGeo<256>::ROWS : PrefillGeo<128>::ROWS;  // query rows per CTA
+  const int BQ = rows / G;  // query tokens per CTA
   const long long nqb = (q_len + BQ - 1) / BQ;
   if (nqb * B * Hkv > 0x7fffffffLL) return DA_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -10,9 +10,9 @@
 // GB300 design.  Unlike decode, a KV tile here serves many query rows, so the
 // work is a dense contraction.  One CTA owns one (sequence, KV head, block of BQ
 // query tokens); its rows are the block's tokens x the G query heads of the KV head
-// (token-major, BQ = 64 / G, at most 64 rows).  A producer warp streams 64-token K/V
-// tiles by TMA (the decode maps, 128- or 64-byte swizzle) up to the block's last
-// causal limit; four MMA warps each own 16 rows: S = Q K^T into registers, a masked
+// (token-major, BQ = ROWS / G, ROWS = 64 or 128 rows).  64-token K/V tiles come in
+// by TMA (the decode maps, 128- or 64-byte swizzle) up to the block's last causal
+// limit; each MMA warp owns 16 rows: S = Q K^T into registers, a masked
 // online softmax in log2 units, P packed to bf16 (the C fragment of S is the A
 // fragment of P V), and P V accumulated in fp32.  Masks apply only to tiles that
 // reach past the block's first row limit.  Blocks launch in groups of grp
@@ -40,12 +40,17 @@ struct PrefillParams {
   unsigned long long timeout_ns;
 };
 
+// Up to D = 128: two CTAs per SM, each 4 MMA warps plus a TMA producer warp.  At
+// D = 256 the fp32 output accumulators allow one CTA per SM, so it has 8 MMA warps
+// (two per scheduler) and no producer warp: warp 0 issues each tile's copies once
+// every warp has left the stage (a CTA barrier per tile).
 template <int D>
 struct PrefillGeo {
   static constexpr int BK = 64;                    // keys per tile
-  static constexpr int W = 4;                      // MMA warps, 16 rows each
+  static constexpr bool PRODUCER = D != 256;       // a dedicated TMA producer warp
+  static constexpr int W = PRODUCER ? 4 : 8;       // MMA warps, 16 rows each
   static constexpr int ROWS = 16 * W;              // query rows per CTA
-  static constexpr int NTHREADS = (W + 1) * 32;
+  static constexpr int NTHREADS = (W + (PRODUCER ? 1 : 0)) * 32;
   static constexpr int CTAS = D == 256 ? 1 : 2;    // CTAs per SM
   static constexpr int SUBW = D >= 64 ? 64 : 32;   // elements per swizzle row
   static constexpr int NSUB = D / SUBW;
@@ -106,75 +111,94 @@ __global__ void __launch_bounds__(PrefillGeo<D>::NTHREADS, PrefillGeo<D>::CTAS)
 #pragma unroll
     for (int s = 0; s < Gm::STAGES; ++s) {
       mbar_init(bar_full + s * 8, 1);
-      mbar_init(bar_empty + s * 8, Gm::W);
+      if (Gm::PRODUCER) mbar_init(bar_empty + s * 8, Gm::W);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == Gm::W && lane == 0) {
+  if (warp == (Gm::PRODUCER ? Gm::W : 0) && lane == 0) {
     prefetch_tensormap(&p.tm_k);
     prefetch_tensormap(&p.tm_v);
   }
   __syncthreads();
 
-  if (warp == Gm::W) {
-    // ---- producer: tile n of K and V into stage n % STAGES
-    const int box_rows = PAGED ? 16 << p.box_shift : BK;
+  // Tile n's page entries (paged: lane j < nbox reads box j's entry) and its copies
+  // into stage st (one whole warp: lane 0 sets the expected bytes, one box per lane)
+  const int box_rows = PAGED ? 16 << p.box_shift : BK;
+  auto tile_boxes = [&](int n) { return PAGED ? (min(BK, kv_end - n * BK) + box_rows - 1) / box_rows : 1; };
+  auto lookup_page = [&](int n) {
+    int page = 0;
+    if (PAGED && lane < tile_boxes(n)) {
+      const int tok = n * BK + lane * box_rows;
+      const int col = p.page_shift >= 0 ? tok >> p.page_shift : tok / p.page_size;
+      page = __ldg(p.page_table + (size_t)b * p.max_pages + col);
+      if ((unsigned)page >= (unsigned)p.num_pages) {  // a bad entry: flag it, read page 0 instead
+        atomicOr(&g_error_word, 4u);
+        page = 0;
+      }
+    }
+    return page;
+  };
+  auto issue_tile = [&](int n, int st, int page) {
+    const int t = n * BK;
+    const int nbox = tile_boxes(n);
+    const uint32_t full = bar_full + st * 8;
+    const uint32_t kdst = sbase + Gm::OFF_K + st * Gm::KV_BYTES;
+    const uint32_t vdst = sbase + Gm::OFF_V + st * Gm::KV_BYTES;
+    if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(2 * nbox * box_rows * D * 2));
+    __syncwarp();
+    if (PAGED) {
+      // tiles start on 64-token boundaries and box_rows divides 64 and the page
+      // size, so a box never crosses a page
+      if (lane < nbox) {
+        const int tok = t + lane * box_rows;
+        const int row0 = tok - (p.page_shift >= 0 ? (tok >> p.page_shift) << p.page_shift
+                                                   : tok / p.page_size * p.page_size);
+        const uint32_t off = (uint32_t)(lane * box_rows * D * 2);
+        tma_load_5d(kdst + off, &p.tm_k, full, 0, row0, 0, h, page);
+        tma_load_5d(vdst + off, &p.tm_v, full, 0, row0, 0, h, page);
+      }
+    } else if (lane == 0) {
+      tma_load_5d(kdst, &p.tm_k, full, 0, t, 0, h, b);
+      tma_load_5d(vdst, &p.tm_v, full, 0, t, 0, h, b);
+    }
+  };
+  // after an abort, let the copies already issued land before the CTA exits
+  auto drain = [&](int issued) {
+    for (int k = issued > Gm::STAGES ? issued - Gm::STAGES : 0; k < issued; ++k) {
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(bar_full + (uint32_t)(k % Gm::STAGES) * 8, (uint32_t)((k / Gm::STAGES) & 1)) &&
+             globaltimer_ns() - t0 < p.timeout_ns) {
+      }
+    }
+  };
+
+  if (Gm::PRODUCER && warp == Gm::W) {
+    // ---- producer: tile n of K and V into stage n % STAGES, once it is free
     int stage = 0;
     uint32_t parity = 0;
     int issued = 0;
     for (int n = 0; n < ntiles; ++n) {
-      const int t = n * BK;
-      const int nbox = PAGED ? (min(BK, kv_end - t) + box_rows - 1) / box_rows : 1;
-      int page = 0;
-      if (PAGED && lane < nbox) {
-        const int tok = t + lane * box_rows;
-        const int col = p.page_shift >= 0 ? tok >> p.page_shift : tok / p.page_size;
-        page = __ldg(p.page_table + (size_t)b * p.max_pages + col);
-        if ((unsigned)page >= (unsigned)p.num_pages) {  // a bad entry: flag it, read page 0 instead
-          atomicOr(&g_error_word, 4u);
-          page = 0;
-        }
-      }
+      const int page = lookup_page(n);  // before the wait: the lookup overlaps it
       bool ok = true;
       if (lane == 0) ok = wait_bounded(bar_empty + stage * 8, parity ^ 1u, abort_flag, p.timeout_ns);
       if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
-      const uint32_t full = bar_full + stage * 8;
-      const uint32_t kdst = sbase + Gm::OFF_K + stage * Gm::KV_BYTES;
-      const uint32_t vdst = sbase + Gm::OFF_V + stage * Gm::KV_BYTES;
-      if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(2 * nbox * box_rows * D * 2));
-      __syncwarp();
-      if (PAGED) {
-        // tiles start on 64-token boundaries and box_rows divides 64 and the page
-        // size, so a box never crosses a page
-        if (lane < nbox) {
-          const int tok = t + lane * box_rows;
-          const int row0 = tok - (p.page_shift >= 0 ? (tok >> p.page_shift) << p.page_shift
-                                                     : tok / p.page_size * p.page_size);
-          const uint32_t off = (uint32_t)(lane * box_rows * D * 2);
-          tma_load_5d(kdst + off, &p.tm_k, full, 0, row0, 0, h, page);
-          tma_load_5d(vdst + off, &p.tm_v, full, 0, row0, 0, h, page);
-        }
-      } else if (lane == 0) {
-        tma_load_5d(kdst, &p.tm_k, full, 0, t, 0, h, b);
-        tma_load_5d(vdst, &p.tm_v, full, 0, t, 0, h, b);
-      }
+      issue_tile(n, stage, page);
       ++issued;
       if (++stage == Gm::STAGES) {
         stage = 0;
         parity ^= 1u;
       }
     }
-    // after an abort, let the copies already issued land before the CTA exits
-    if (*abort_flag && lane == 0) {
-      for (int k = issued > Gm::STAGES ? issued - Gm::STAGES : 0; k < issued; ++k) {
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bar_full + (uint32_t)(k % Gm::STAGES) * 8, (uint32_t)((k / Gm::STAGES) & 1)) &&
-               globaltimer_ns() - t0 < p.timeout_ns) {
-        }
-      }
-    }
+    if (*abort_flag && lane == 0) drain(issued);
     return;
+  }
+  // no producer warp: warp 0 issues the first STAGES tiles now, the rest as stages
+  // free up (issued counts warp 0's tiles, for the drain after an abort)
+  int issued = 0;
+  if (!Gm::PRODUCER && warp == 0) {
+    for (int n = 0; n < min(ntiles, Gm::STAGES); ++n) issue_tile(n, n, lookup_page(n));
+    issued = min(ntiles, Gm::STAGES);
   }
 
   // ---- MMA warps.  Query tile: row r = (token r / G, head r % G) of the block,
@@ -324,13 +348,24 @@ __global__ void __launch_bounds__(PrefillGeo<D>::NTHREADS, PrefillGeo<D>::CTAS)
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar_empty + stage * 8);
+    if constexpr (Gm::PRODUCER) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + stage * 8);
+    } else {
+      // every warp has left the stage: warp 0 refills it with tile n + STAGES
+      named_bar_sync(1, Gm::W * 32);
+      if (warp == 0 && n + Gm::STAGES < ntiles && !*abort_flag) {
+        issue_tile(n + Gm::STAGES, stage, lookup_page(n + Gm::STAGES));
+        ++issued;
+      }
+    }
     if (++stage == Gm::STAGES) {
       stage = 0;
       parity ^= 1u;
     }
   }
+
+  if (!Gm::PRODUCER && *abort_flag && threadIdx.x == 0) drain(issued);
 
   // ---- normalise and write rows of the block (a row that saw nothing: zeros)
   lA += __shfl_xor_sync(0xffffffffu, lA, 1);
