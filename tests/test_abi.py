@@ -201,3 +201,20 @@ def test_prefill_argument_checks_return_before_cuda(clib):
     assert clib.prefill_attn_paged(q, q, q, q, None, 1, 4, 8, 2, 64, 16, 4, 16, 64, 0.1, q, None) == 1
     assert clib.prefill_attn_paged(q, q, q, q, q, 1, 4, 8, 2, 64, 16, -1, 16, 64, 0.1, q, None) == 1
     assert clib.prefill_attn_paged(q, q, q, q, q, 1, 4, 8, 3, 64, 16, 4, 16, 64, 0.1, q, None) == 1
+
+
+def test_binding_rejects_host_and_mistyped_tensors(clib):
+    """The Python binding only marshals arguments: host tensors, wrong dtypes and
+    wrong ranks raise before the library is called."""
+    torch = pytest.importorskip("torch")
+    from gqa_split_kv_gb300 import binding
+    q = torch.zeros((1, 8, 64), dtype=torch.bfloat16)
+    k = torch.zeros((1, 32, 2, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="q"):
+        binding.decode_attn_contig(q, k, k)                      # host tensors
+    with pytest.raises(ValueError, match="q"):
+        binding.prefill_attn_contig(q, k, k)                     # q must be [B, q_len, Hq, D]
+    with pytest.raises(ValueError, match="q"):
+        binding.decode_attn_int8_contig(q, k, k, q, q)
+    with pytest.raises(ValueError, match="q"):
+        binding.prefill_attn_paged(q.float().unsqueeze(0), k, k, None, None, 32)
