@@ -197,26 +197,35 @@ def cpu_child(workload: str, seconds: float):
     print(json.dumps({"gbs": done_bytes / dt / 1e9, "tflops": done_bytes / dt / 1e12, "units": n, "seconds": dt}))
 
 
-def run_cpu_baseline(workload: str, seconds: float) -> dict:
-    cores = os.cpu_count() or 1
+def _cpu_child_run(workload: str, seconds: float, threads: int):
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        env[k] = str(cores)
+        env[k] = str(threads)
     res = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child", workload, "--cpu-seconds",
                           str(seconds)], capture_output=True, text=True, env=env, cwd=ROOT)
     line = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
     if res.returncode != 0 or not line:
-        return {"value": None, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                "sample": f"failed: {res.stderr[-300:]}"}
-    d = json.loads(line[-1])
+        return None, res.stderr[-300:]
+    return json.loads(line[-1]), ""
+
+
+def run_cpu_baseline(workload: str, seconds: float) -> dict:
+    """The oracle on the host cores (BLAS threads = cores), plus its single-thread rate
+    on a shorter sample of the same units."""
+    cores = os.cpu_count() or 1
     from gqa_split_kv_gb300.workloads import WORKLOADS
-    if WORKLOADS[workload].kind == "prefill":
-        return {"value": round(d["tflops"], 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                "sample": f"{d['units']} units of one (sequence, query head) over the whole chunk, "
-                          f"{d['seconds']:.1f} s, fp64 numpy oracle, BLAS threads = {cores}"}
-    return {"value": round(d["gbs"], 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{d['units']} units of one (sequence, KV head) with its G query heads over the full "
-                      f"context, {d['seconds']:.1f} s, fp64 numpy oracle, BLAS threads = {cores}"}
+    pre = WORKLOADS[workload].kind == "prefill"
+    unit, key = ("TFLOP/s", "tflops") if pre else ("GB/s", "gbs")
+    d, err = _cpu_child_run(workload, seconds, cores)
+    if d is None:
+        return {"value": None, "unit": unit, "cores": cores, "kind": "oracle", "sample": f"failed: {err}"}
+    d1, _ = _cpu_child_run(workload, max(1.0, seconds / 4), 1)
+    what = ("one (sequence, query head) over the whole chunk" if pre else
+            "one (sequence, KV head) with its G query heads over the full context")
+    return {"value": round(d[key], 6 if pre else 4), "unit": unit, "cores": cores, "kind": "oracle",
+            "sample": f"{d['units']} units of {what}, {d['seconds']:.1f} s, fp64 numpy oracle, BLAS threads = {cores}",
+            "single_thread": None if d1 is None else {"value": round(d1[key], 6 if pre else 4), "units": d1["units"],
+                                                        "seconds": round(d1["seconds"], 1)}}
 
 
 # ------------------------------------------------------------ our arm
