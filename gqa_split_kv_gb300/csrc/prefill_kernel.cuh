@@ -1,9 +1,9 @@
 // Causal GQA prefill / chunked prefill over the decode cache.
 //
 // "gqa_prefill_attn" on the AstrAI commit page ("csrc", commit 988e013) is a
-// tiled shared-memory K/V kernel with mask support; the page on the cp.async
-// rewrite ("double-buffer K/V one tile ahead ...") measures it against torch
-// SDPA.  The pages give no layout or mask rule, so the reading is the plain causal
+// tiled shared-memory K/V kernel with mask support, and the same page's notes on
+// its double-buffered rework compare it with torch SDPA.  The pages give no
+// layout or mask rule, so the reading is the plain causal
 // one: sequence b holds L_b cached tokens whose last q_len are the chunk, and query
 // token i (position L_b - q_len + i) sees positions 0 .. L_b - q_len + i.
 //
