@@ -686,3 +686,16 @@ def _int8_reference_by_hand(inp):
             g = h // (Hq // Hkv)
             out[b, h] = od.attend(od.widen_bf16(inp["q"][b, h])[None], K[:, g], V[:, g], inp["scale"])[0]
     return out
+
+
+def test_int8_traffic_counts_values_and_scales():
+    """The bench's int8 byte count: D int8 bytes plus one fp32 scale per (token, KV
+    head) for each of K and V, against the bf16 count of 2 D bytes per tensor."""
+    from gqa_split_kv_gb300.accounting import traffic_bytes
+    lens = [100, 7, 0, 300]
+    for D in (32, 64, 128, 256):
+        t8 = traffic_bytes(4, 16, 4, D, lens, 1, kv_dtype="int8")
+        t16 = traffic_bytes(4, 16, 4, D, lens, 1)
+        assert t8["kv"] == 2 * 4 * sum(lens) * (D + 4)
+        assert t16["kv"] == 2 * 4 * sum(lens) * 2 * D
+        assert t8["q"] == t16["q"] and t8["partials_read"] == t16["partials_read"]
