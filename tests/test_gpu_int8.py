@@ -42,8 +42,8 @@ def test_int8_contig_matches_oracle(D, Hq, Hkv):
     assert checked > 0
 
 
-@pytest.mark.parametrize("D", [64, 128, 256])
-@pytest.mark.parametrize("ps", [16, 32, 64])
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+@pytest.mark.parametrize("ps", [16, 32, 48, 64, 96])  # 48, 96: no shift, boxes of 16 / 32 rows
 def test_int8_paged_matches_oracle_and_contiguous_bitwise(D, ps):
     inp = int8_case(3 * D + ps, len(RAGGED), 32, 8, D, ctx=780, lens=RAGGED)
     pin = dict(int8_to_paged(inp, inp["seq_lens"], ps, np.random.default_rng(ps), spare_pages=3),

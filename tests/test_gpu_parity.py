@@ -46,7 +46,7 @@ def test_contig_matches_oracle(D, Hq, Hkv):
 
 
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("ps", [16, 32, 64])
+@pytest.mark.parametrize("ps", [16, 32, 48, 64, 96])  # 48, 96: no shift, boxes of 16 / 32 rows
 def test_paged_matches_oracle_and_contiguous_bitwise(D, ps):
     inp = contig_case(7 * D + ps, len(RAGGED), 32, 8, D, ctx=max(RAGGED), lens=RAGGED)
     rng = np.random.default_rng(ps)
