@@ -10,62 +10,26 @@ The bytes a call must move at minimum, by tensor:
   seq_lens  = 4 B * B
 
 "algorithmic" = kv + q + partials read + page_table + seq_lens (what the combine
-and split kernels must read); "strict" = kv + q + out.  The piece count per
-segment restates the library's split rule (see include/decode_attn.h) for
-counting only.
+and split kernels must read); "strict" = kv + q + out.  Which segments are cut
+into pieces, and into how many, is asked of the library's own planner
+(decode_plan_pieces, host only).
 """
 from __future__ import annotations
 
-import math
 from typing import Optional
 
 import numpy as np
 
-BLOCK = 16
 
-
-def _groups(G: int):
-    ng = -(-G // 8)
-    gr = -(-G // ng)
-    return ng, gr
-
-
-def _passes(G: int, D: int):
-    """(sub-groups per pass, passes per KV head, rows per sub-group): a pass runs the
-    largest power of two of sub-groups that divides their number, at most 2 at
-    D = 128, else 4."""
-    ng, gr = _groups(G)
-    per, cap = 1, (2 if D == 128 else 4)
-    while per * 2 <= cap and ng % (per * 2) == 0:
-        per *= 2
-    return per, -(-ng // per), gr
-
-
-def piece_counts(seq_lens, Hkv: int, G: int, S: int, D: int) -> np.ndarray:
-    """Pieces of every segment, shape [B, Hkv * passes].
-
-    The library's split plan: segments lie end to end on one line in (u, b)
-    order (slot-major), each taking
-    gap + 4 ceil(n_b / 4) positions (gap = 4 ceil((2816 / D) / 4) positions
-    without blocks, then its blocks, then padding); the line is cut into ranges
-    of q positions."""
-    lens = np.asarray(seq_lens, dtype=np.int64)
-    _, npass, _ = _passes(G, D)
-    U = Hkv * npass
-    nblk = (lens + BLOCK - 1) // BLOCK
-    B = len(lens)
-    if S == 1:
-        return np.where(nblk[:, None] > 0, 1, 0) * np.ones((B, U), dtype=np.int64)
-    gap = (2816 // D + 3) // 4 * 4
-    w = np.where(nblk > 0, (nblk + 3) // 4 * 4 + gap, 0)
-    P = np.concatenate([[0], np.cumsum(w)])
-    NB = U * int(P[-1])
-    R = (S - 1) * U
-    q = max(4, -(-max(1, -(-NB // R)) // 4) * 4)
-    s0 = np.arange(U)[None, :] * int(P[-1]) + P[:-1, None] + gap
-    s1 = s0 + nblk[:, None]
-    n = (s1 - 1) // q - s0 // q + 1
-    return np.where(nblk[:, None] > 0, n, 0)
+def split_part_rows(seq_lens, Hq: int, Hkv: int, D: int, S: int, q_len: int = 1) -> int:
+    """Rows x pieces of the partials one call writes: the sum, over the pieces of
+    segments cut into two or more, of the piece's query rows."""
+    from . import binding
+    lens = np.asarray(seq_lens, dtype=np.int32)
+    if S < 2 or lens.size == 0 or int(lens.max()) == 0:
+        return 0
+    rec = binding.plan_pieces(lens, Hq, Hkv, D, int(lens.max()), S, q_len=q_len)
+    return int(rec[rec[:, 4] >= 2, 2].sum())
 
 
 def traffic_bytes(B: int, Hq: int, Hkv: int, D: int, seq_lens, S: int, page_size: Optional[int] = None,
@@ -74,16 +38,10 @@ def traffic_bytes(B: int, Hq: int, Hkv: int, D: int, seq_lens, S: int, page_size
     are its G query heads x q_len query tokens, and K/V are still read once.  An
     int8 cache moves D bytes plus a 4-byte scale per (token, KV head) and tensor."""
     lens = np.asarray(seq_lens, dtype=np.int64)
-    G = Hq // Hkv * q_len
-    per, npass, gr = _passes(G, D)
     kv = 2 * (D + 4 if kv_dtype == "int8" else 2 * D) * Hkv * int(lens.sum())
     q = B * Hq * q_len * D * 2
     out = B * Hq * q_len * D * 2
-    n = piece_counts(lens, Hkv, G, S, D)                      # [B, U]
-    # rows of segment slot u = h * npass + pass
-    heads = np.array([min(per * gr, G - (u % npass) * per * gr) for u in range(Hkv * npass)])
-    part_rows = int(((n >= 2) * n * heads[None, :]).sum())
-    partials = part_rows * (D + 2) * 4
+    partials = split_part_rows(lens, Hq, Hkv, D, S, q_len) * (D + 2) * 4
     pt = 0 if page_size is None else 4 * int(((lens + page_size - 1) // page_size).sum())
     sl = 4 * B
     return {"kv": kv, "q": q, "out": out, "partials_read": partials, "partials_written": partials,

@@ -30,6 +30,9 @@ __all__ = [
     "device_error",
     "selftest_bounded_wait",
     "counters_len",
+    "plan_pieces",
+    "max_batch",
+    "PIECE_FIELDS",
     "STATUS",
 ]
 
@@ -84,6 +87,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.decode_selftest_bounded_wait.argtypes = [ctypes.c_ulonglong, vp]
     lib.decode_selftest_bounded_wait.restype = i
     lib.decode_device_error.restype = i
+    lib.decode_plan_pieces.argtypes = [vp, i, i, i, i, i, i, i, vp, i, ctypes.POINTER(i)]
+    lib.decode_plan_pieces.restype = i
+    lib.decode_max_batch.argtypes = [i, i, i, i, i, i]
+    lib.decode_max_batch.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -125,6 +132,46 @@ def num_splits_multi(batch: int, q_len: int, num_q_heads: int, num_kv_heads: int
     if s < 0:
         raise DecodeAttnError("decode_num_splits_multi", -s)
     return s
+
+
+# Fields of one decode_plan_pieces record.
+PIECE_FIELDS = ("b", "row0", "nrows", "j", "npieces", "t0", "t1", "held_t0", "held_t1")
+
+
+def plan_pieces(seq_lens, num_q_heads: int, num_kv_heads: int, head_dim: int, max_len: int, num_splits: int,
+                q_len: int = 1):
+    """The pieces a decode call computes (host only): an int32 array [n, 9] of
+    PIECE_FIELDS records, in the order the library's planner walks them.
+
+    seq_lens: host sequence lengths (a sequence of ints or an int array), or an int
+    batch size meaning every sequence has max_len tokens."""
+    import numpy as np
+    lib = load()
+    if isinstance(seq_lens, (int, np.integer)):
+        batch, lens_ptr, keep = int(seq_lens), None, None
+    else:
+        keep = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+        batch, lens_ptr = int(keep.shape[0]), keep.ctypes.data_as(ctypes.c_void_p)
+    count = ctypes.c_int(0)
+    st = lib.decode_plan_pieces(lens_ptr, batch, q_len, num_q_heads, num_kv_heads, head_dim, max_len, num_splits,
+                                None, 0, ctypes.byref(count))
+    if st not in (0, 3):
+        raise DecodeAttnError("decode_plan_pieces", st)
+    rec = np.zeros((count.value, len(PIECE_FIELDS)), dtype=np.int32)
+    st = lib.decode_plan_pieces(lens_ptr, batch, q_len, num_q_heads, num_kv_heads, head_dim, max_len, num_splits,
+                                rec.ctypes.data_as(ctypes.c_void_p), count.value, ctypes.byref(count))
+    _check("decode_plan_pieces", st)
+    del keep
+    return rec
+
+
+def max_batch(num_q_heads: int, num_kv_heads: int, head_dim: int, q_len: int = 1, kv_int8: bool = False,
+              paged: bool = False) -> int:
+    """Largest batch the decode kernels accept for this shape (host only)."""
+    m = load().decode_max_batch(q_len, num_q_heads, num_kv_heads, head_dim, int(kv_int8), int(paged))
+    if m < 0:
+        raise DecodeAttnError("decode_max_batch", -m)
+    return m
 
 
 def counters_len(batch: int, num_q_heads: int, num_kv_heads: int, q_len: int = 1) -> int:

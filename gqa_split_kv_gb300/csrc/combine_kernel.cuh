@@ -7,8 +7,9 @@
 //
 // Work items are (row, 128-column chunk) pairs, grid-strided over CTAs; a CTA's
 // items are classified one per thread, and each item that needs merging is then
-// handled by the whole CTA, one at a time.  All (m, l) of the row are
-// loaded at once and reduced to M and the weights in shared memory; the slot x
+// handled by the whole CTA, one at a time.  Warp 0 loads the row's (m, l) once
+// and turns them into M and the weights in shared memory while every thread's
+// first acc loads are in flight; the slot x
 // column products are spread over the 512 threads (JL slot lanes x D/4 column
 // groups of 4), each thread keeping KB loads in flight; the JL lane sums
 // are added in ascending lane order.  The summation order is fixed, so results
@@ -17,8 +18,8 @@
 // Two modes:
 //   planned:  after the split kernel (programmatic dependent launch), for the
 //             segments with more than kFusedMergeMax pieces: the split kernel
-//             merges smaller segments itself, and a single CTA cannot merge a long
-//             run of partials quickly, so these rows are spread over many CTAs.
+//             merges smaller segments itself, and a longer run of partials is
+//             spread over many CTAs here.
 //             A row's slot count is its segment's piece count under the split plan.
 //   plain:    decode_combine: every S slot of every row, skipping slots with l == 0.
 #pragma once
@@ -72,7 +73,7 @@ __global__ void __maxnreg__(40) combine_kernel(const CombineParams p) {  // 512 
   Plan pl{};
   if (p.planned) {
     // seq_lens is not written by the split kernel: read it before waiting on it.
-    build_plan_arrays(p.seq_lens, p.B, p.max_len, plan_gap_blocks(D), lens, P);
+    build_plan_arrays(p.seq_lens, p.B, p.max_len, plan_gap_blocks(D), lens, P, 0, blockDim.x);
     pl = make_plan(p.B, p.U, p.S, plan_gap_blocks(D), P);
   }
   // A segment of n blocks meets at most (n - 1) / q + 2 ranges; when even the
@@ -82,17 +83,15 @@ __global__ void __maxnreg__(40) combine_kernel(const CombineParams p) {  // 512 
     const int nb_max = P[p.B + 1];
     red[31] = (nb_max == 0 || (nb_max - 1) / pl.q + 2 <= kFusedMergeMax) ? 1.f : 0.f;
   }
-  __syncthreads();
-  pdl_wait_primary();
-  if (p.planned && red[31] != 0.f) return;
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int jl = tid / Cg::TPS, c4 = tid % Cg::TPS;
   const float kNegInf = -__int_as_float(0x7f800000);
   const int items = p.B * p.Hq * Cg::NCH;        // (row, column chunk) pairs
   int* todo = reinterpret_cast<int*>(red + 32);  // [0] count, then (item, n) pairs
-  for (int base = blockIdx.x; base < items; base += Cg::CLS * gridDim.x) {
-    // CLS threads classify one of this CTA's items each; items to merge go to a list
+  // CLS threads classify one of this CTA's items each (the items base, base +
+  // gridDim.x, ...); the items to merge go to the list.  The plan depends only on
+  // seq_lens, so the first round is classified before the wait on the split kernel.
+  auto classify = [&](int base) {
     if (tid == 0) todo[0] = 0;
     __syncthreads();
     if (tid < Cg::CLS) {
@@ -113,6 +112,15 @@ __global__ void __maxnreg__(40) combine_kernel(const CombineParams p) {  // 512 
       }
     }
     __syncthreads();
+  };
+  __syncthreads();
+  const bool nothing = p.planned && red[31] != 0.f;
+  if (!nothing) classify(blockIdx.x);
+  pdl_wait_primary();
+  if (nothing) return;
+
+  for (int base = blockIdx.x; base < items; base += Cg::CLS * gridDim.x) {
+    if (base != blockIdx.x) classify(base);
     const int count = todo[0];
     for (int it = 0; it < count; ++it) {
       const int item = todo[1 + 2 * it];
@@ -128,22 +136,44 @@ __global__ void __maxnreg__(40) combine_kernel(const CombineParams p) {  // 512 
         const int j = jl + u * Cg::JL;
         a[u] = j < n ? acc[(size_t)j * (D / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      // every warp derives M and the denominator itself (same values in every warp:
-      // same loads, same butterfly order), so no barrier waits on them
-      float M = kNegInf;
-      for (int j = lane; j < n; j += 32) {
-        const float2 v = ml[j];
-        if (v.y > 0.f) M = fmaxf(M, v.x);
-      }
+      // warp 0 turns the row's (m, l) into weights in shared memory, one L2 round
+      // trip (the first 64 slots stay in registers) while the acc loads are in flight
+      if (tid < 32) {
+        float2 v[2];
+        float M = kNegInf;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      float den = 0.f;
-      for (int j = lane; j < n; j += 32) {
-        const float2 v = ml[j];
-        if (v.y > 0.f) den += expf(v.x - M) * v.y;
-      }
+        for (int k = 0; k < 2; ++k) {
+          const int j = lane + 32 * k;
+          v[k] = j < n ? ml[j] : make_float2(kNegInf, 0.f);
+          if (v[k].y > 0.f) M = fmaxf(M, v[k].x);
+        }
+        for (int j = lane + 64; j < n; j += 32) {
+          const float2 x = ml[j];
+          if (x.y > 0.f) M = fmaxf(M, x.x);
+        }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float den = 0.f;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int j = lane + 32 * k;
+          if (j < n) {
+            const float w = v[k].y > 0.f ? expf(v[k].x - M) : 0.f;
+            wts[j] = w;
+            den += w * v[k].y;
+          }
+        }
+        for (int j = lane + 64; j < n; j += 32) {
+          const float2 x = ml[j];
+          const float w = x.y > 0.f ? expf(x.x - M) : 0.f;
+          wts[j] = w;
+          den += w * x.y;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        if (lane == 0) red[17] = den;
+      }
+      __syncthreads();
       // weighted column sums over this thread's slots (jl, jl + JL, ...)
       float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int j0 = jl; j0 < n; j0 += Cg::KB * Cg::JL) {
@@ -157,18 +187,13 @@ __global__ void __maxnreg__(40) combine_kernel(const CombineParams p) {  // 512 
 #pragma unroll
         for (int u = 0; u < Cg::KB; ++u) {
           const int j = j0 + u * Cg::JL;
-          float w = 0.f;
-          if (j < n) {
-            const float2 v = ml[j];
-            w = v.y > 0.f ? expf(v.x - M) : 0.f;
-          }
+          const float w = j < n ? wts[j] : 0.f;
           s.x += w * a[u].x;
           s.y += w * a[u].y;
           s.z += w * a[u].z;
           s.w += w * a[u].w;
         }
       }
-      if (tid == 0) red[17] = den;
       lane_sum[tid] = s;
       __syncthreads();
       if (jl == 0) {

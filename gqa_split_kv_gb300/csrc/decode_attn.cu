@@ -2,10 +2,11 @@
 //
 // Host side of every call: validate the arguments, build the TMA tensor maps of
 // the caller's K/V/Q buffers and enqueue the persistent split kernel, which also
-// merges segments cut into at most 8 pieces.  When the plan allows longer
-// segments, the combine kernel follows as a programmatic dependent launch (its
-// CTAs start while the split kernel drains and wait on the device for it) and
-// merges those.  decode_combine runs the stand-alone merge.
+// merges segments cut into at most 8 pieces.
+// When the plan allows longer segments, the combine kernel follows as a
+// programmatic dependent launch (its CTAs start while the split kernel drains and
+// wait on the device for it) and merges those.  decode_combine runs the
+// stand-alone merge.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -15,6 +16,7 @@
 #include <cstring>
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "../../include/decode_attn.h"
 #include "combine_kernel.cuh"
@@ -136,6 +138,30 @@ void group_passes(int ng, int D, int* ngp, int* npass) {
   while (g * 2 <= cap && ng % (g * 2) == 0) g *= 2;
   *ngp = g;
   *npass = ng / g;
+}
+
+// Offset of the plan arrays in the split kernel's shared memory for a geometry;
+// the kernel needs OFF_PLAN + (2 B + 2) * 4 + 1024 bytes (SplitGeo::smem_bytes).
+template <int D, bool PG, bool KV8>
+int plan_offset_t(int ngp) {
+  if (ngp == 1) return SplitGeo<D, 1, KV8, PG>::OFF_PLAN;
+  if (ngp == 2) return SplitGeo<D, 2, KV8, PG>::OFF_PLAN;
+  if constexpr (SplitGeo<D>::NGP_MAX >= 4) return SplitGeo<D, 4, KV8, PG>::OFF_PLAN;
+  return 1 << 30;
+}
+
+template <int D>
+int plan_offset_d(bool paged, bool kv8, int ngp) {
+  return paged ? (kv8 ? plan_offset_t<D, true, true>(ngp) : plan_offset_t<D, true, false>(ngp))
+               : (kv8 ? plan_offset_t<D, false, true>(ngp) : plan_offset_t<D, false, false>(ngp));
+}
+
+// Largest batch whose plan fits the split kernel's shared memory (227 KB per CTA).
+int max_batch_for(int D, bool paged, bool kv8, int ngp) {
+  const int off = D == 32 ? plan_offset_d<32>(paged, kv8, ngp) : D == 64 ? plan_offset_d<64>(paged, kv8, ngp)
+                : D == 128 ? plan_offset_d<128>(paged, kv8, ngp) : plan_offset_d<256>(paged, kv8, ngp);
+  const int room = 227 * 1024 - 1024 - off;
+  return room < 16 ? 0 : (room / 4 - 2) / 2;
 }
 
 struct Launch {
@@ -288,6 +314,8 @@ int run_decode(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, in
   for (int s = 4; s < 31; ++s)
     if (a.page_size == (1 << s)) prm.page_shift = s;
   prm.S = a.S;
+  // small contiguous batches (latency-bound calls): guessed first tiles before the plan
+  prm.spec_first = !a.paged && a.B <= 4 ? 1 : 0;
   prm.scale_log2 = a.scale * 1.4426950408889634f;
   prm.timeout_ns = kWaitTimeoutNs;
 
@@ -345,14 +373,11 @@ int check_common(const void* q, const void* out, int B, int Hq, int Hkv, int D, 
 }
 
 int dispatch(const Launch& a, const CUtensorMap& tk, const CUtensorMap& tv, int dev, int sms, int smem_optin) {
-  int need = 0;
-  switch (a.D) {
-    case 32: need = SplitGeo<32>::smem_bytes(a.B); break;
-    case 64: need = SplitGeo<64>::smem_bytes(a.B); break;
-    case 128: need = SplitGeo<128>::smem_bytes(a.B); break;
-    default: need = SplitGeo<256>::smem_bytes(a.B); break;
-  }
-  if (need > smem_optin || need > 227 * 1024) return DA_ERR_UNSUPPORTED;
+  // the batch limit of the plan in shared memory (decode_max_batch)
+  int ng, gr, ngp, npass;
+  head_groups(a.Hq / a.Hkv, &ng, &gr);
+  group_passes(ng, a.D, &ngp, &npass);
+  if (a.B > max_batch_for(a.D, a.paged, a.kv8, ngp)) return DA_ERR_UNSUPPORTED;
   switch (a.D) {
     case 32: return run_decode<32>(a, tk, tv, dev, sms, smem_optin);
     case 64: return run_decode<64>(a, tk, tv, dev, sms, smem_optin);
@@ -399,6 +424,76 @@ extern "C" int decode_num_splits_multi(int batch, int q_len, int num_q_heads, in
   head_groups(num_q_heads / num_kv_heads * q_len, &ng, &gr);
   group_passes(ng, head_dim, &ngp, &npass);
   return decode_num_splits(batch, num_kv_heads * npass, max_seq_len, head_dim, num_sms);
+}
+
+extern "C" int decode_plan_pieces(const int* seq_lens, int batch, int q_len, int num_q_heads, int num_kv_heads,
+                                  int head_dim, int max_len, int num_splits, int* records, int capacity, int* count) {
+  if (!count) return DA_ERR_INVALID_ARG;
+  *count = 0;
+  if (batch < 0 || max_len < 0 || capacity < 0 || q_len < 1 || q_len > DA_MAX_QLEN || num_q_heads <= 0 ||
+      num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || num_splits < 1 || num_splits > DA_MAX_SPLITS)
+    return DA_ERR_INVALID_ARG;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128 && head_dim != 256) return DA_ERR_UNSUPPORTED;
+  const int G = num_q_heads / num_kv_heads * q_len;  // rows per KV head
+  if (G > 64) return DA_ERR_UNSUPPORTED;
+  const int B = batch, D = head_dim, S = num_splits;
+  if (B == 0) return DA_OK;
+  int ng, gr, ngp, npass;
+  head_groups(G, &ng, &gr);
+  group_passes(ng, D, &ngp, &npass);
+  const int U = num_kv_heads * npass;
+  const int gap = plan_gap_blocks(D);
+  const long long nblk_max = ((long long)max_len + kBlockTokens - 1) / kBlockTokens;
+  if ((long long)B * U * (nblk_max + 3 + gap) >= (1LL << 30)) return DA_ERR_UNSUPPORTED;
+  // the arrays build_plan_arrays forms on the device
+  std::vector<int> lens(B), P(B + 2);
+  int run = 0, mx = 0;
+  for (int b = 0; b < B; ++b) {
+    int L = seq_lens ? seq_lens[b] : max_len;
+    L = L < 0 ? 0 : (L > max_len ? max_len : L);
+    lens[b] = L;
+    P[b] = run;
+    const int nb = (L + kBlockTokens - 1) / kBlockTokens;
+    run += segment_width(nb, gap);
+    mx = nb > mx ? nb : mx;
+  }
+  P[B] = run;
+  P[B + 1] = mx;
+  const Plan pl = make_plan(B, U, S, gap, P.data());
+  // every range in order, with the walker the kernel's CTAs use
+  PieceWalker walk;
+  walk.init(0, 1);
+  Piece pc;
+  std::vector<int> rec;
+  while (walk.next(pl, lens.data(), P.data(), B, true, pc)) {
+    const int h = pc.u / npass, pass_u = pc.u % npass;
+    const int nsg = ngp < ng - pass_u * ngp ? ngp : ng - pass_u * ngp;
+    const int row0 = h * G + pass_u * ngp * gr;
+    const int nrows = nsg * gr < G - pass_u * ngp * gr ? nsg * gr : G - pass_u * ngp * gr;
+    const int fields[9] = {pc.b, row0, nrows, pc.j, pc.npieces, pc.t0, pc.t1, pc.t0, pc.t1};
+    rec.insert(rec.end(), fields, fields + 9);
+  }
+  const int n = (int)(rec.size() / 9);
+  // a segment written straight to the output leaves no partial; every other piece
+  // leaves its own in slot j
+  for (int i = 0; i < n; ++i) {
+    int* r = &rec[9 * i];
+    if (r[4] == 1) r[7] = r[8] = 0;
+  }
+  *count = n;
+  if (records) std::memcpy(records, rec.data(), sizeof(int) * 9 * (size_t)(n < capacity ? n : capacity));
+  return n <= capacity ? DA_OK : DA_ERR_WORKSPACE;
+}
+
+extern "C" int decode_max_batch(int q_len, int num_q_heads, int num_kv_heads, int head_dim, int kv_int8, int paged) {
+  if (q_len < 1 || q_len > DA_MAX_QLEN || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return -DA_ERR_INVALID_ARG;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128 && head_dim != 256) return -DA_ERR_UNSUPPORTED;
+  if (num_q_heads / num_kv_heads * q_len > 64 || (kv_int8 && q_len != 1)) return -DA_ERR_UNSUPPORTED;
+  int ng, gr, ngp, npass;
+  head_groups(num_q_heads / num_kv_heads * q_len, &ng, &gr);
+  group_passes(ng, head_dim, &ngp, &npass);
+  return max_batch_for(head_dim, paged != 0, kv_int8 != 0, ngp);
 }
 
 // Contiguous cache, qlen query tokens per sequence (rows = Hq * qlen).
@@ -721,35 +816,44 @@ extern "C" int decode_device_error(void* stream, unsigned int* flags) {
 // Some callers cannot hand this library any device workspace: a runtime that
 // owns a fixed device-memory budget and passes its plugins nothing but input
 // and output buffers, or a serving loop that must not call cudaMalloc (which
-// can synchronise the device) between steps.  For them the split partials live
-// in the file-scope array below instead of caller buffers.  Every GPU that
-// loads this library holds the array (8 MiB) until the process exits.
+// can synchronise the device) between steps.  For them the segment counters and
+// the split partials live in the file-scope array below instead of caller
+// buffers.  Every GPU that loads this library holds the array (8 MiB) until the
+// process exits.
 //
 // Host code may not use the array's name as a device address (on the host it
 // names a shadow variable), so its device address is looked up once per device
 // with cudaGetSymbolAddress, with that device current, by the first call on it.
 // All calls share the array: two calls that overlap on the GPU (different
-// streams or threads) race on it.  Nothing in it needs to start at zero: every
-// partial slot a merge reads is written earlier in the same call, and the
-// per-segment counters carry a per-call tag, so stale values count as zero.
+// streams or threads) race on it.
+//
+// Layout: the segment counters come first, at a fixed offset, with room for
+// kNoAllocMaxSegments of them, so counter words only ever hold counter values
+// (epoch << 32 | state), whatever shapes earlier calls had; the array starts
+// zeroed, and a stale counter from another call counts as zero.  The partials
+// follow; every partial slot a merge reads is written earlier in the same call,
+// so they need no clearing.
 // ---------------------------------------------------------------------------
 
 namespace da {
 namespace {
-constexpr size_t kNoAllocScratchFloats = (size_t)2 << 20;  // 8 MiB of fp32 partials
+constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;
+constexpr size_t kNoAllocMaxSegments = 16384;  // 128 KB of counters
 std::mutex g_noalloc_mu;
-float* g_noalloc_ptr[kMaxDevices] = {nullptr};
+unsigned char* g_noalloc_ptr[kMaxDevices] = {nullptr};
 }  // namespace
 }  // namespace da
 
-static __device__ __align__(256) float g_noalloc_scratch[da::kNoAllocScratchFloats];
+static __device__ __align__(256) unsigned char g_noalloc_scratch[da::kNoAllocScratchBytes];
 
 extern "C" int decode_attn_contig_noalloc(const void* q, const void* k, const void* v, const int* seq_lens,
                                           int batch, int num_q_heads, int num_kv_heads, int head_dim,
                                           int max_ctx, float scale, void* out, void* stream) {
   const int B = batch, Hq = num_q_heads, Hkv = num_kv_heads, D = head_dim;
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_ctx < 0) return DA_ERR_INVALID_ARG;
-  if (D != 32 && D != 64 && D != 128 && D != 256) return DA_ERR_UNSUPPORTED;
+  if (max_ctx < 0) return DA_ERR_INVALID_ARG;
+  // the argument checks of decode_attn_contig come first, so a bad argument gets
+  // the same status from both entry points
+  if (int st = check_common(q, out, B, Hq, Hkv, D, scale, 1, nullptr, nullptr, nullptr)) return st;
   if (B == 0) return DA_OK;
   int dev, sms, smem_optin;
   if (current_device(&dev) || device_info(dev, &sms, &smem_optin)) return DA_ERR_CUDA;
@@ -759,11 +863,13 @@ extern "C" int decode_attn_contig_noalloc(const void* q, const void* k, const vo
   float* ml = nullptr;
   unsigned long long* ctr = nullptr;
   if (S >= 2) {
-    const size_t acc_floats = ((size_t)B * Hq * S * D + 63) / 64 * 64;  // keep part_ml 256-byte aligned
-    const size_t ml_floats = ((size_t)B * Hq * S * 2 + 63) / 64 * 64;
-    const size_t ctr_floats = (size_t)B * Hkv * ((Hq / Hkv + 7) / 8) * 2;  // one 8-byte counter per segment
-    if (acc_floats + ml_floats + ctr_floats > kNoAllocScratchFloats) return DA_ERR_WORKSPACE;
-    float* base = nullptr;
+    const size_t segments = (size_t)B * Hkv * ((Hq / Hkv + 7) / 8);  // at least B * U
+    const size_t ctr_bytes = kNoAllocMaxSegments * 8;
+    const size_t acc_bytes = ((size_t)B * Hq * S * D * 4 + 255) / 256 * 256;
+    const size_t ml_bytes = (size_t)B * Hq * S * 2 * 4;
+    if (segments > kNoAllocMaxSegments || ctr_bytes + acc_bytes + ml_bytes > kNoAllocScratchBytes)
+      return DA_ERR_WORKSPACE;
+    unsigned char* base = nullptr;
     {
       std::lock_guard<std::mutex> lk(g_noalloc_mu);
       if (!g_noalloc_ptr[dev]) {
@@ -772,13 +878,13 @@ extern "C" int decode_attn_contig_noalloc(const void* q, const void* k, const vo
           cudaGetLastError();
           return DA_ERR_CUDA;
         }
-        g_noalloc_ptr[dev] = static_cast<float*>(p);
+        g_noalloc_ptr[dev] = static_cast<unsigned char*>(p);
       }
       base = g_noalloc_ptr[dev];
     }
-    acc = base;
-    ml = base + acc_floats;
-    ctr = reinterpret_cast<unsigned long long*>(base + acc_floats + ml_floats);
+    ctr = reinterpret_cast<unsigned long long*>(base);
+    acc = reinterpret_cast<float*>(base + ctr_bytes);
+    ml = reinterpret_cast<float*>(base + ctr_bytes + acc_bytes);
   }
   return decode_attn_contig(q, k, v, seq_lens, B, Hq, Hkv, D, max_ctx, scale, S, acc, ml, ctr, out, stream);
 }

@@ -44,7 +44,7 @@ constexpr int kFusedMergeMax = 8;
 __host__ __device__ constexpr int plan_gap_blocks(int head_dim) { return (2816 / head_dim + 3) / 4 * 4; }
 
 // Line positions of one segment with n blocks (0 for an empty sequence).
-__device__ __forceinline__ int segment_width(int nb, int gap) { return nb > 0 ? ((nb + 3) & ~3) + gap : 0; }
+__host__ __device__ __forceinline__ int segment_width(int nb, int gap) { return nb > 0 ? ((nb + 3) & ~3) + gap : 0; }
 
 
 // Block counts are 32-bit: the host rejects problems with 2^30 blocks or more.
@@ -65,17 +65,17 @@ struct Piece {
 };
 
 // lens[b] = clamp(seq_lens[b] or max_len, 0, max_len); P[0..B] = prefix of the
-// segment widths w_b (segment_width); P[B + 1] = the largest
-// block count of one sequence.  Called by every thread of the block (contains
-// __syncthreads).
+// segment widths w_b (segment_width); P[B + 1] = the largest block count of one
+// sequence.  Run by the first nthreads threads of the block, which synchronise on
+// named barrier bar_id (bar_id 0 with every thread: __syncthreads).
 __device__ __forceinline__ void build_plan_arrays(const int* __restrict__ seq_lens, int B, int max_len, int gap,
-                                                  int* lens, int* P) {
-  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+                                                  int* lens, int* P, int bar_id, int nthreads) {
+  for (int b = threadIdx.x; b < B; b += nthreads) {
     int L = seq_lens ? __ldg(seq_lens + b) : max_len;
     L = L < 0 ? 0 : (L > max_len ? max_len : L);
     lens[b] = L;
   }
-  __syncthreads();
+  asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(nthreads) : "memory");
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     const int per = (B + 31) / 32;
@@ -105,10 +105,10 @@ __device__ __forceinline__ void build_plan_arrays(const int* __restrict__ seq_le
       P[B + 1] = mx;
     }
   }
-  __syncthreads();
+  asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(nthreads) : "memory");
 }
 
-__device__ __forceinline__ Plan make_plan(int B, int U, int S, int gap, const int* P) {
+__host__ __device__ __forceinline__ Plan make_plan(int B, int U, int S, int gap, const int* P) {
   Plan pl;
   pl.U = U;
   pl.S = S;
@@ -128,7 +128,7 @@ __device__ __forceinline__ Plan make_plan(int B, int U, int S, int gap, const in
 }
 
 // Number of pieces of segment (b, u) under plan pl (S >= 2).
-__device__ __forceinline__ int segment_pieces(const Plan& pl, const int* lens, const int* P, int B, int b, int u) {
+__host__ __device__ __forceinline__ int segment_pieces(const Plan& pl, const int* lens, const int* P, int B, int b, int u) {
   const int nb = (lens[b] + kBlockTokens - 1) / kBlockTokens;
   if (nb == 0) return 0;
   const int bs = u * P[B] + P[b] + pl.gap;  // first block
@@ -138,7 +138,7 @@ __device__ __forceinline__ int segment_pieces(const Plan& pl, const int* lens, c
 // S >= 2: the blocks of the segment at line position x that lie in [x, xe), the
 // rest of range r.  Returns the position where the next segment of the range
 // starts (or xe); pc.t0 == pc.t1 when [x, xe) meets none of the segment's blocks.
-__device__ __forceinline__ int piece_at(const Plan& pl, const int* lens, const int* P, int B, int x, int xe, int r,
+__host__ __device__ __forceinline__ int piece_at(const Plan& pl, const int* lens, const int* P, int B, int x, int xe, int r,
                                         Piece& pc) {
   // slot u, then sequence b: the last with P[b] <= x - u P_B (sequences with no
   // blocks are skipped because the following non-empty one shares their prefix)
@@ -163,31 +163,79 @@ __device__ __forceinline__ int piece_at(const Plan& pl, const int* lens, const i
   pc.b = b;
   pc.u = u;
   pc.t0 = (x0 - bs) * kBlockTokens;
-  pc.t1 = pe > x0 ? min((pe - bs) * kBlockTokens, lens[b]) : pc.t0;
+  const int te = (pe - bs) * kBlockTokens;
+  pc.t1 = pe > x0 ? (te < lens[b] ? te : lens[b]) : pc.t0;
   pc.j = r - bs / pl.q;
   pc.npieces = (be - 1) / pl.q - bs / pl.q + 1;
   return xe < s0 + w ? xe : s0 + w;
 }
 
-// Walks the pieces of the ranges blockIdx.x, blockIdx.x + gridDim.x, ...
+// The first piece of range r if every sequence held max_len tokens: a guess made
+// before seq_lens is read, so that the first tiles can be requested early.  False
+// when the guess gives the range no piece.
+__host__ __device__ __forceinline__ bool guess_first_piece(int B, int U, int S, int gap, int max_len, int r,
+                                                           Piece& pc) {
+  const int nb = (max_len + kBlockTokens - 1) / kBlockTokens;
+  if (nb == 0 || B <= 0) return false;
+  pc.j = 0;
+  if (S == 1) {
+    if (r >= B * U) return false;
+    pc.b = r / U;
+    pc.u = r % U;
+    pc.t0 = 0;
+    pc.t1 = max_len;
+    pc.npieces = 1;
+    return true;
+  }
+  const int w = segment_width(nb, gap);
+  const int NB = U * B * w;
+  const int R = (S - 1) * U;
+  int q = (NB + R - 1) / R;
+  q = (q + kRangeQuantum - 1) / kRangeQuantum * kRangeQuantum;
+  if (q < kRangeQuantum) q = kRangeQuantum;
+  int x = r * q;
+  const int xe = x + q < NB ? x + q : NB;
+  for (int k = 0; k < 2 && x < xe; ++k) {
+    const int seg = x / w;  // segment (b, u) starts at u * B * w + b * w
+    const int s0 = seg * w, bs = s0 + gap, be = bs + nb;
+    const int x0 = x > bs ? x : bs;
+    const int pe = xe < be ? xe : be;
+    if (pe > x0) {
+      pc.b = seg % B;
+      pc.u = seg / B;
+      pc.t0 = (x0 - bs) * kBlockTokens;
+      const int te = (pe - bs) * kBlockTokens;
+      pc.t1 = te < max_len ? te : max_len;
+      return true;
+    }
+    x = s0 + w;
+  }
+  return false;
+}
+
+// Walks the pieces of the ranges r0, r0 + stride, r0 + 2 stride, ... (a CTA of the
+// persistent grid: r0 = blockIdx.x, stride = gridDim.x; the host walks every range
+// with r0 = 0, stride = 1).
 struct PieceWalker {
   int r;       // range being walked
   int x, xe;   // S >= 2: next block and end of range r
+  int stride;
   bool started;
 
-  __device__ __forceinline__ void init() {
-    r = blockIdx.x;
+  __host__ __device__ __forceinline__ void init(int r0, int step) {
+    r = r0;
+    stride = step;
     started = false;
     x = xe = 0;
   }
 
   // Next piece in walk order; false when the CTA's work is done.  With
   // skip_empty, segments of empty sequences (S == 1 only) are skipped.
-  __device__ __forceinline__ bool next(const Plan& pl, const int* lens, const int* P, int B, bool skip_empty,
-                                       Piece& pc) {
+  __host__ __device__ __forceinline__ bool next(const Plan& pl, const int* lens, const int* P, int B,
+                                                bool skip_empty, Piece& pc) {
     if (pl.S == 1) {
       while (true) {
-        if (started) r += gridDim.x;
+        if (started) r += stride;
         started = true;
         if (r >= pl.ranges) return false;
         pc.b = r / pl.U;
@@ -211,7 +259,7 @@ struct PieceWalker {
         if (pc.t1 > pc.t0) return true;
         continue;  // only a gap: no piece
       }
-      r += gridDim.x;
+      r += stride;
       if (r >= pl.ranges) return false;
       x = r * pl.q;
       xe = x + pl.q < pl.NB ? x + pl.q : pl.NB;

@@ -26,8 +26,9 @@
 //
 // A segment cut into at most 8 pieces is merged by the CTA that finishes its last
 // piece (log-sum-exp over the pieces' partials, ascending order), detected with
-// one per-segment counter.  Longer segments (long contexts over few heads) are
-// merged by the combine kernel, spread over many CTAs.
+// one per-segment counter.  Longer segments (long contexts over few KV heads) are
+// merged by the combine kernel, spread over many CTAs: one CTA alone would need
+// several dependent rounds of L2 loads (~1 us each) to read their partials.
 //
 // Head packing: the MMA tile is 16 rows; query heads fill rows 0..7 and rows
 // 8..15 carry the bf16 low part of the probabilities, so P = hi + lo reaches
@@ -70,6 +71,7 @@ struct SplitParams {
   int box_shift;     // paged: a TMA box holds 16 << box_shift rows of one page (16, 32 or 64)
   int page_shift;    // log2(page_size) when it is a power of two, else -1
   int S;
+  int spec_first;    // contiguous caches of small batches: request the guessed first tiles before the plan
   float scale_log2;  // scale * log2(e)
   unsigned long long timeout_ns;
 };
@@ -195,7 +197,7 @@ struct TileCursor {
   bool valid;
 
   __device__ __forceinline__ void init(const Plan& pl, const int* lens, const int* P, int B) {
-    walk.init();
+    walk.init(blockIdx.x, gridDim.x);
     valid = walk.next(pl, lens, P, B, true, pc);
     t = pc.t0;
   }
@@ -208,9 +210,48 @@ struct TileCursor {
   }
 };
 
+// One contiguous-cache tile (and, for a piece's first tile, the pass's query rows)
+// of piece pc into ring stage `stage`, issued by a single thread.
+template <int D, int NGP, bool KV8>
+__device__ __forceinline__ void issue_contig_tile(const SplitParams& p, uint32_t sbase, int stage, const Piece& pc,
+                                                  int t) {
+  using Gm = SplitGeo<D, NGP, KV8, false>;
+  const int h = pc.u / p.npass;
+  const int g0 = (pc.u % p.npass) * p.ngp;
+  const int nsg = min(p.ngp, p.ng - g0);
+  const bool first_tile = t == pc.t0;
+  const uint32_t full = sbase + Gm::OFF_BAR + stage * 8;
+  const uint32_t qbytes = first_tile ? (uint32_t)(nsg * Gm::NSUB * p.gr * Gm::ROWB) : 0u;
+  const uint32_t kvbytes = (uint32_t)(Gm::KV_BYTES + (KV8 ? Gm::T * 4 : 0));
+  mbar_arrive_expect_tx(full, 2u * kvbytes + qbytes);
+  tma_load_5d(sbase + Gm::OFF_K + stage * Gm::KV_BYTES, &p.tm_k, full, 0, t, 0, h, pc.b);
+  tma_load_5d(sbase + Gm::OFF_V + stage * Gm::KV_BYTES, &p.tm_v, full, 0, t, 0, h, pc.b);
+  if constexpr (KV8) {
+    tma_load_3d(sbase + Gm::OFF_KS + stage * Gm::SC_BYTES, &p.tm_ks, full, t, h, pc.b);
+    tma_load_3d(sbase + Gm::OFF_VS + stage * Gm::SC_BYTES, &p.tm_vs, full, t, h, pc.b);
+  }
+  if (first_tile) {
+    const uint32_t qdst = sbase + Gm::OFF_Q + stage * Gm::Q_BYTES;
+    for (int sg = 0; sg < nsg; ++sg)
+      for (int sub = 0; sub < Gm::NSUB; ++sub)
+        tma_load_4d(qdst + sg * Gm::Q_SG_BYTES + sub * Gm::Q_SUB_BYTES, &p.tm_q, full, 0, sub,
+                    h * p.G + (g0 + sg) * p.gr, pc.b);
+  }
+}
+
+// Whether the guessed first piece is the piece the plan gives this CTA first
+// (producer and consumers decide it alike).
+__device__ __forceinline__ bool guess_hit(const Plan& pl, const int* lens, const int* P, int B, const Piece& g) {
+  PieceWalker w;
+  w.init(blockIdx.x, gridDim.x);
+  Piece f;
+  return w.next(pl, lens, P, B, true, f) && f.b == g.b && f.u == g.u && f.t0 == g.t0 && f.t1 == g.t1;
+}
+
 template <int D, bool PAGED, int NGP, bool KV8>
 __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan& pl, const int* lens, const int* P,
-                                               uint8_t* smem, uint32_t sbase, volatile int* abort_flag) {
+                                               uint8_t* smem, uint32_t sbase, volatile int* abort_flag,
+                                               const Piece& guess, int k_spec) {
   using Gm = SplitGeo<D, NGP, KV8, PAGED>;
   const int lane = threadIdx.x & 31;
   const uint32_t bar_full = sbase + Gm::OFF_BAR;
@@ -243,6 +284,23 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
   int n = 0;  // tiles issued
   int stage = 0;
   uint32_t parity = 0;
+  if (k_spec > 0) {
+    // stages 0 .. k_spec - 1 hold the guessed first tiles: on a hit they are this
+    // CTA's first tiles; else they are drained (their copies land, then the stages
+    // are released as if consumed) and the ring starts after them
+    if (guess_hit(pl, lens, P, p.B, guess)) {
+      for (int k = 0; k < k_spec; ++k) cur.advance(pl, lens, P, p.B, Gm::T);
+    } else if (lane == 0) {
+      for (int k = 0; k < k_spec; ++k) {
+        wait_bounded(bar_full + k * 8, 0, abort_flag, p.timeout_ns);
+        mbar_arrive_cnt(bar_empty + k * 8, Gm::W);
+      }
+    }
+    __syncwarp();
+    n = k_spec;
+    stage = k_spec % Gm::STAGES;
+    parity = (uint32_t)(k_spec / Gm::STAGES);
+  }
   while (cur.valid) {
     const Piece& pc = cur.pc;
     const int h = pc.u / p.npass;
@@ -340,85 +398,110 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
   }
 }
 
-// Counts one finished piece of a segment; true for the piece that completes it.
-// The counter holds (epoch << 32) | count; a value from another call (another
-// epoch) counts as zero, so counters never need resetting between calls.  The
-// piece that completes the segment puts the count back to zero (no other piece
-// of this call touches the counter after it), so a replayed CUDA graph, whose
-// calls all carry the captured epoch, also starts every segment from zero.
-// Bounded retries.
-__device__ __forceinline__ bool claim_last_piece(unsigned long long* c, unsigned int epoch, int npieces) {
-  unsigned long long v = *reinterpret_cast<volatile unsigned long long*>(c);
+// Per-segment counters.  A counter holds (epoch << 32) | count, where the epoch
+// tags the call; a value with another epoch counts as zero, so counters never
+// need resetting between calls.  A finished piece adds one with a single
+// acquire-release atomic; the first add of a call that finds another call's
+// value replaces it by compare-and-swap.  The piece that completes a segment
+// stores (epoch + 1) << 32: the next call, which normally carries epoch + 1, then
+// finds a zero count of its own and takes the one-add path; any other call (a
+// replayed CUDA graph carries its captured epoch) treats it as another call's value.
+constexpr uint32_t kCounterError = 0xffffffffu;
+
+// Adds one to this call's count of counter c; returns the count before the add.
+__device__ __forceinline__ uint32_t counter_add(unsigned long long* c, unsigned int epoch) {
+  const unsigned long long old = atom_add_acqrel(c, 1ull);
+  if ((uint32_t)(old >> 32) == epoch) return (uint32_t)old;
+  // another call's value (the add above went to it): replace that value with
+  // this call's, or add to it if another piece of this call already did
+  unsigned long long v = old + 1ull;
   for (int it = 0; it < (1 << 20); ++it) {
-    const unsigned int cnt = (unsigned int)(v >> 32) == epoch ? (unsigned int)v : 0u;
-    const bool last = (int)(cnt + 1) == npieces;
-    const unsigned long long nv = ((unsigned long long)epoch << 32) | (unsigned long long)(last ? 0u : cnt + 1);
-    const unsigned long long prev = atomicCAS(c, v, nv);
-    if (prev == v) return last;
+    const bool ours = (uint32_t)(v >> 32) == epoch;
+    const unsigned long long nv = ours ? v + 1ull : ((unsigned long long)epoch << 32) | 1ull;
+    const unsigned long long prev = atom_cas_acqrel(c, v, nv);
+    if (prev == v) return ours ? (uint32_t)v : 0u;
     v = prev;
   }
   atomicOr(&g_error_word, 2u);
-  return false;
+  return kCounterError;
 }
 
-// Log-sum-exp merge of the n <= kFusedMergeMax partials of one segment into its
-// bf16 output rows, in ascending piece order (run by the CTA that finished the
-// segment's last piece; the W consumer warps).  Partials written by
-// other CTAs are read through L2 (ld.global.cg).
+// Counts one finished piece of a segment of n pieces; true for the piece that
+// completes it.
+__device__ __forceinline__ bool claim_last_piece(unsigned long long* c, unsigned int epoch, int n) {
+  const uint32_t cnt = counter_add(c, epoch);
+  if (cnt == kCounterError || (int)cnt + 1 != n) return false;
+  st_relaxed_u64(c, (unsigned long long)(epoch + 1u) << 32);
+  return true;
+}
+
+// Log-sum-exp merge of `count` (<= kFusedMergeMax) partial slots slot0, slot0 +
+// sstride, ... of the nrows rows row0 .. row0 + nrows - 1 of sequence b, in
+// ascending slot order, by the W consumer warps.  to_partial: the merged
+// unnormalised partial (acc, m, l) of the slots' joint token range replaces slot
+// slot0; else the bf16 output rows are written.  Partials written by other CTAs
+// are read through L2 (ld.global.cg).  First each warp turns the (m, l) of its
+// rows into weights in shared memory (wsm: 10 floats per row, the 8 weights, M
+// and the denominator), then every thread merges (row, 4-column) items with all
+// of an item's slot loads in flight at once.
 template <int D, int W>
-__device__ __forceinline__ void merge_segment(const SplitParams& p, int b, int first_head, int nrows, int n,
-                                              float* rowM) {
+__device__ __forceinline__ void merge_slots(const SplitParams& p, float* wsm, int b, int row0, int nrows, int slot0,
+                                            int sstride, int count, bool to_partial) {
+  constexpr int C4 = D / 4;  // float4 columns per row
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float kNegInf = -__int_as_float(0x7f800000);
   for (int r = warp; r < nrows; r += W) {
-    const float* ml = p.part_ml + ((size_t)b * p.Hq + first_head + r) * p.S * 2;
-    float M = kNegInf;  // over the slots that saw a token (l > 0)
-    for (int j = lane; j < n; j += 32) {
-      const float2 v = __ldcg(reinterpret_cast<const float2*>(ml) + j);
-      if (v.y > 0.f) M = fmaxf(M, v.x);
-    }
+    const size_t row = (size_t)b * p.Hq + row0 + r;
+    float2 v = make_float2(kNegInf, 0.f);
+    if (lane < count) v = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + row * p.S + slot0 + (size_t)lane * sstride);
+    float M = v.y > 0.f ? v.x : kNegInf;  // over the slots that saw a token
+    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
+    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
+    const float w = v.y > 0.f ? exp2_approx((v.x - M) * 1.4426950408889634f) : 0.f;
+    float den = 0.f;  // ascending slot order, the same in every lane
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if (lane == 0) rowM[r] = M;
+    for (int i = 0; i < kFusedMergeMax; ++i) den += __shfl_sync(0xffffffffu, w * v.y, i);
+    if (lane < kFusedMergeMax) wsm[r * 10 + lane] = w;
+    if (lane == 0) {
+      wsm[r * 10 + 8] = M;
+      wsm[r * 10 + 9] = den;
+    }
   }
-  named_bar_sync(1, W * 32);
-  for (int e = tid; e < nrows * (D / 4); e += W * 32) {
-    const int r = e / (D / 4), c4 = e % (D / 4);
-    const size_t row = (size_t)b * p.Hq + first_head + r;
-    const float2* ml = reinterpret_cast<const float2*>(p.part_ml + row * p.S * 2);
-    const float4* acc = reinterpret_cast<const float4*>(p.part_acc + row * p.S * D) + c4;
-    const float M = rowM[r];
-    // n <= kFusedMergeMax: a column's loads are issued 4 at a time
+  named_bar_sync(1, W * 32);  // weights ready; every (m, l) of slot0 has been read
+  if (to_partial && tid < nrows) {
+    const size_t row = (size_t)b * p.Hq + row0 + tid;
+    reinterpret_cast<float2*>(p.part_ml)[row * p.S + slot0] = make_float2(wsm[tid * 10 + 8], wsm[tid * 10 + 9]);
+  }
+  for (int e = tid; e < nrows * C4; e += W * 32) {
+    const int r = e / C4;
+    const size_t row = (size_t)b * p.Hq + row0 + r;
+    float4* acc = reinterpret_cast<float4*>(p.part_acc + (row * p.S + slot0) * D) + e % C4;
+    float4 a[kFusedMergeMax];
+#pragma unroll
+    for (int i = 0; i < kFusedMergeMax; ++i)
+      if (i < count) a[i] = __ldcg(acc + (size_t)i * sstride * C4);
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-    float den = 0.f;
 #pragma unroll
-    for (int j0 = 0; j0 < kFusedMergeMax; j0 += 4) {
-      float2 v[4];
-      float4 a[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (j0 + u < n) {
-          v[u] = __ldcg(ml + j0 + u);
-          a[u] = __ldcg(acc + (size_t)(j0 + u) * (D / 4));
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (j0 + u < n) {
-          const float w = v[u].y > 0.f ? exp2_approx((v[u].x - M) * 1.4426950408889634f) : 0.f;
-          num.x += w * a[u].x;
-          num.y += w * a[u].y;
-          num.z += w * a[u].z;
-          num.w += w * a[u].w;
-          den += w * v[u].y;
-        }
+    for (int i = 0; i < kFusedMergeMax; ++i) {
+      if (i < count) {
+        const float wi = wsm[r * 10 + i];
+        num.x += wi * a[i].x;
+        num.y += wi * a[i].y;
+        num.z += wi * a[i].z;
+        num.w += wi * a[i].w;
       }
     }
-    const float inv = den > 0.f ? 1.f / den : 0.f;  // a row that saw no token: zeros
-    uint2 o;
-    o.x = pack_bf16x2(num.x * inv, num.y * inv);
-    o.y = pack_bf16x2(num.z * inv, num.w * inv);
-    *reinterpret_cast<uint2*>(p.out + row * D + 4 * c4) = o;
+    if (to_partial) {
+      *acc = num;
+    } else {
+      const float den = wsm[r * 10 + 9];
+      const float inv = den > 0.f ? 1.f / den : 0.f;  // a row that saw no token: zeros
+      uint2 o;
+      o.x = pack_bf16x2(num.x * inv, num.y * inv);
+      o.y = pack_bf16x2(num.z * inv, num.w * inv);
+      *reinterpret_cast<uint2*>(p.out + row * D + 4 * (e % C4)) = o;
+    }
   }
 }
 
@@ -478,7 +561,8 @@ __device__ __forceinline__ void lds_words(const uint8_t* p, uint32_t* w) {
 
 template <int D, bool PAGED, int NGP, bool KV8>
 __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan& pl, const int* lens, const int* P,
-                                               uint8_t* smem, uint32_t sbase, volatile int* abort_flag) {
+                                               uint8_t* smem, uint32_t sbase, volatile int* abort_flag,
+                                               const Piece& guess, int k_spec) {
   using Gm = SplitGeo<D, NGP, KV8, PAGED>;
   constexpr int KCH = D / 16;  // k-chunks of the QK^T product
   constexpr int NB8 = D / 8;   // 8-column blocks of the PV product
@@ -563,10 +647,14 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
   }
 
   PieceWalker walk;
-  walk.init();
+  walk.init(blockIdx.x, gridDim.x);
   Piece pc;
   int stage = 0;  // ring position of the next tile to consume
   uint32_t parity = 0;
+  if (k_spec > 0 && !guess_hit(pl, lens, P, p.B, guess)) {  // the producer drains the guessed stages
+    stage = k_spec % Gm::STAGES;
+    parity = (uint32_t)(k_spec / Gm::STAGES);
+  }
   while (walk.next(pl, lens, P, p.B, false, pc)) {
     uint32_t qa[KCH][2];
     float acc[NB8][4];
@@ -922,17 +1010,13 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
     }
     if (!direct && pc.npieces <= kFusedMergeMax) {
       // publish this piece; the CTA that completes the segment merges it.  The
-      // barrier orders every consumer's partial stores before thread 0's gpu-scope
-      // fence, which releases them before the counter update.
+      // barrier orders every consumer's partial stores before thread 0's
+      // acquire-release counter update, which releases them.
       named_bar_sync(1, Gm::W * 32);
       volatile int* last = reinterpret_cast<volatile int*>(smem + Gm::OFF_MISC) + 1;
-      if (tid == 0) {
-        __threadfence();
-        *last = claim_last_piece(p.seg_counters + (size_t)pc.b * p.U + pc.u, p.epoch, pc.npieces);
-        if (*last) __threadfence();  // acquire: the other pieces' partials are read next
-      }
+      if (tid == 0) *last = claim_last_piece(p.seg_counters + (size_t)pc.b * p.U + pc.u, p.epoch, pc.npieces);
       named_bar_sync(1, Gm::W * 32);
-      if (*last) merge_segment<D, Gm::W>(p, pc.b, row0, nrows_pass, pc.npieces, fsc);
+      if (*last) merge_slots<D, Gm::W>(p, facc, pc.b, row0, nrows_pass, 0, 1, pc.npieces, false);
     }
     named_bar_sync(1, Gm::W * 32);
   }
@@ -951,34 +1035,57 @@ __global__ void __launch_bounds__(SplitGeo<D, NGP, KV8, PAGED>::NTHREADS, 1) spl
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Gm::OFF_MISC);
   const int warp = threadIdx.x >> 5;
 
-  if (threadIdx.x == 0) {
+  // Contiguous caches of small batches: the first tiles of the piece this CTA gets
+  // if every sequence holds max_len tokens (the usual case there) are requested
+  // before seq_lens is read; the plan then confirms or drains them.
+  Piece guess{};
+  int k_spec = 0;
+  if (!PAGED && p.spec_first && guess_first_piece(p.B, p.U, p.S, plan_gap_blocks(D), p.max_len, blockIdx.x, guess))
+    k_spec = min(Gm::STAGES, (guess.t1 - guess.t0 + Gm::T - 1) / Gm::T);
+  // Barriers 2 (consumers) and 3, 4 (everyone) order the start.  The consumers
+  // read seq_lens first (so the guessed copies do not queue ahead of it) and build
+  // the plan on barrier 2; then they wait on barrier 3 for the mbarriers, which the
+  // producer lane initialises before its warp arrives there, and arrive on barrier
+  // 4, where the producer waits for the plan after issuing the guessed tiles.
+  constexpr int kAll = Gm::NTHREADS, kCons = Gm::W * 32;
+  if (warp == Gm::W) {
+    if ((threadIdx.x & 31) == 0) {
 #pragma unroll
-    for (int s = 0; s < Gm::STAGES; ++s) {
-      mbar_init(sbase + Gm::OFF_BAR + s * 8, 1);
-      mbar_init(sbase + Gm::OFF_BAR + (Gm::STAGES + s) * 8, Gm::W);
+      for (int s = 0; s < Gm::STAGES; ++s) {
+        mbar_init(sbase + Gm::OFF_BAR + s * 8, 1);
+        mbar_init(sbase + Gm::OFF_BAR + (Gm::STAGES + s) * 8, Gm::W);
+      }
+      *abort_flag = 0;
+      fence_mbar_init();
+      prefetch_tensormap(&p.tm_k);
+      prefetch_tensormap(&p.tm_v);
+      prefetch_tensormap(&p.tm_q);
+      if (KV8) {
+        prefetch_tensormap(&p.tm_ks);
+        prefetch_tensormap(&p.tm_vs);
+      }
     }
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == Gm::W && (threadIdx.x & 31) == 0) {
-    prefetch_tensormap(&p.tm_k);
-    prefetch_tensormap(&p.tm_v);
-    prefetch_tensormap(&p.tm_q);
-    if (KV8) {
-      prefetch_tensormap(&p.tm_ks);
-      prefetch_tensormap(&p.tm_vs);
+    __syncwarp();
+    named_bar_arrive(3, kAll);
+    if constexpr (!PAGED) {
+      if ((threadIdx.x & 31) == 0)
+        for (int k = 0; k < k_spec; ++k) issue_contig_tile<D, NGP, KV8>(p, sbase, k, guess, guess.t0 + k * Gm::T);
     }
+    // The combine kernel (launched only when a segment can have more than 8
+    // pieces) may start now; it waits on the device for this grid to finish.
+    pdl_launch_dependents();
+    named_bar_sync(4, kAll);
+  } else {
+    build_plan_arrays(p.seq_lens, p.B, p.max_len, plan_gap_blocks(D), lens, P, 2, kCons);
+    pdl_launch_dependents();
+    named_bar_sync(3, kAll);
+    named_bar_arrive(4, kAll);
   }
-
-  // The combine kernel (launched only when a segment can have more than 8 pieces)
-  // may start now; it waits on the device for this grid to finish.
-  pdl_launch_dependents();
-  build_plan_arrays(p.seq_lens, p.B, p.max_len, plan_gap_blocks(D), lens, P);
   const Plan pl = make_plan(p.B, p.U, p.S, plan_gap_blocks(D), P);
   if (warp == Gm::W)
-    split_producer<D, PAGED, NGP, KV8>(p, pl, lens, P, smem, sbase, abort_flag);
+    split_producer<D, PAGED, NGP, KV8>(p, pl, lens, P, smem, sbase, abort_flag, guess, k_spec);
   else
-    split_consumer<D, PAGED, NGP, KV8>(p, pl, lens, P, smem, sbase, abort_flag);
+    split_consumer<D, PAGED, NGP, KV8>(p, pl, lens, P, smem, sbase, abort_flag, guess, k_spec);
 }
 
 }  // namespace da

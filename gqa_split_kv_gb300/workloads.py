@@ -123,6 +123,9 @@ WORKLOADS = {
     "sweep_paged_b64_hq64_hkv8_d64_ctx2048_ps16": Workload(
         "sweep_paged_b64_hq64_hkv8_d64_ctx2048_ps16", B=64, Hq=64, Hkv=8, D=64, max_ctx=2048,
         layout="paged", page_size=16, seed=1242),
+    "sweep_paged_b64_hq64_hkv8_d32_ctx2048_ps16": Workload(
+        "sweep_paged_b64_hq64_hkv8_d32_ctx2048_ps16", B=64, Hq=64, Hkv=8, D=32, max_ctx=2048,
+        layout="paged", page_size=16, seed=1250),
     # multi-query decode (speculative verification of a draft block)
     "verify_contig_b1_hq24_hkv4_d256_ctx4096_q7": Workload(
         "verify_contig_b1_hq24_hkv4_d256_ctx4096_q7", B=1, Hq=24, Hkv=4, D=256, max_ctx=4096, q_len=7,
@@ -160,6 +163,11 @@ def draw_seq_lens(wl: Workload, rng: np.random.Generator) -> np.ndarray:
         u = rng.uniform(0.0, math.log(wl.lens_hi), size=wl.B)
         return np.clip(np.floor(np.exp(u)), 1, wl.lens_hi).astype(np.int32)
     raise ValueError(f"unknown length distribution {wl.lens!r}")
+
+
+def workload_lens(wl: Workload) -> np.ndarray:
+    """The sequence lengths make_inputs(wl) draws (its first draw from the seed)."""
+    return draw_seq_lens(wl, np.random.default_rng(wl.seed))
 
 
 def _normal_bf16(rng: np.random.Generator, shape, chunk: int = 1 << 24) -> np.ndarray:

@@ -52,8 +52,11 @@
  *     one with several leaves partials in slots j = 0..pieces-1, which are merged
  *     into the output by the CTA that finishes its last piece (found with the
  *     segment's counter) when there are at most 8, else by a combine kernel that
- *     follows as a programmatic dependent launch; an empty sequence (L_b == 0)
- *     gets a zero output.
+ *     follows as a programmatic dependent launch (one CTA alone would need several
+ *     dependent rounds of L2 reads for a long run of partials); an empty sequence
+ *     (L_b == 0) gets a zero output.
+ *   decode_plan_pieces reports this partition, and what every partial slot holds
+ *   when a call returns, for any shape (host only).
  */
 #ifndef DECODE_ATTN_H
 #define DECODE_ATTN_H
@@ -102,15 +105,20 @@ int decode_num_splits(int batch, int num_kv_heads, int max_seq_len, int head_dim
  *           (may be NULL) when num_splits == 1.  Slots the plan does not use are not
  *           written.
  *  seg_counters  uint64 [batch * num_kv_heads * ceil(G / 8)] (at least batch * U entries are
- *           used): caller-owned, zeroed
- *           once before the first call and then reusable by every later call
- *           (each call tags its updates, so no reset is needed, even after a
- *           failed call); unused (may be NULL) when num_splits == 1.  Calls that
- *           share partial buffers or counters must not overlap on the GPU.
- *           A call may be captured in a CUDA graph and replayed: every call
- *           leaves the counters it used at zero.  Only after a call that ended in
- *           DA_ERR_TIMEOUT must the counters be zeroed again before a captured
- *           graph that uses them is replayed.
+ *           used): caller-owned, zeroed once before the first call and then
+ *           reusable by every later call (each call tags its updates with its own
+ *           epoch, and a value left by another call counts as zero, so no reset is
+ *           needed, even after a failed call); unused (may be NULL) when
+ *           num_splits == 1.  Calls that share partial buffers or counters must
+ *           not overlap on the GPU.  A call may be captured in a CUDA graph and
+ *           replayed: a completed call leaves each counter it used holding a value
+ *           that every later call, replays included, counts as zero.  Only after a
+ *           call that ended in DA_ERR_TIMEOUT must the counters be zeroed again
+ *           before a captured graph that uses them is replayed.
+ *  Batch limit: the split kernel keeps 8 bytes of plan per sequence in shared
+ *           memory, so batch is at most decode_max_batch(...) for the shape
+ *           (1159 for bf16 head_dim 128 with G <= 8); a larger batch returns
+ *           DA_ERR_UNSUPPORTED and launches nothing.
  *  out      bf16 [batch, num_q_heads, head_dim]
  *  stream   cudaStream_t
  * Enqueues the split kernel, and the combine kernel when num_splits > 8.
@@ -158,19 +166,23 @@ int decode_combine(const float* part_acc, const float* part_ml, int batch, int n
 /*
  * decode_attn_contig_noalloc — decode_attn_contig for callers that cannot allocate.
  *
- * The paper has no counterpart: this entry point exists for callers that may not
- * allocate device memory or hold any workspace (a runtime with a fixed device
- * budget that gives its plugins only input and output buffers, or a serving loop
- * that must not call cudaMalloc between steps).  Arguments are those of
- * decode_attn_contig without num_splits, part_acc and part_ml: the split count is
- * decode_num_splits(batch, num_kv_heads, max_ctx, head_dim, <SMs of the device>)
- * and the partials and segment counters live in an 8 MiB array inside the library
- * (every GPU that loads the library holds it until exit).  Shapes that need more
- * than 8 MiB (batch * num_q_heads * S * (head_dim + 2) * 4 bytes of partials plus
- * 8 bytes per segment, plus alignment) return DA_ERR_WORKSPACE and launch nothing.  The first call on a device looks
- * up the array's device address (no allocation); make that first call before any
- * stream capture.  Calls share the array: calls that overlap on the GPU race.
- * Calls no cudaMalloc, cudaFree or allocating library routine.
+ * For callers that may not allocate device memory or hold any workspace of
+ * their own: a runtime with a fixed device-memory budget that hands its plugins
+ * only input and output buffers, or a serving loop that must not call cudaMalloc
+ * (which can synchronise the device) between steps.  The source pages have no
+ * such entry point; it is specific to this library.  Arguments are those of
+ * decode_attn_contig without num_splits, part_acc, part_ml and seg_counters: the
+ * split count is decode_num_splits(batch, num_kv_heads, max_ctx, head_dim, <SMs of
+ * the device>), and the segment counters and partials live in an 8 MiB array
+ * inside the library (every GPU that loads the library holds it until exit).
+ * The array holds at most 16384 segments (batch * num_kv_heads * ceil(G / 8)) and
+ * batch * num_q_heads * S * head_dim * 4 bytes of partial values (rounded up to
+ * 256) plus batch * num_q_heads * S * 8 bytes of (m, l) in 8 MiB - 128 KiB;
+ * larger shapes return DA_ERR_WORKSPACE and launch nothing.  Argument errors
+ * return the status decode_attn_contig returns for them.  The first call on a
+ * device looks up the array's device address (no allocation); make that first
+ * call before any stream capture.  Calls share the array: calls that overlap on
+ * the GPU race.  Calls no cudaMalloc, cudaFree or allocating library routine.
  */
 int decode_attn_contig_noalloc(const void* q, const void* k, const void* v, const int* seq_lens,
                                int batch, int num_q_heads, int num_kv_heads, int head_dim, int max_ctx,
@@ -188,6 +200,47 @@ int decode_attn_contig_noalloc(const void* q, const void* k, const void* v, cons
  */
 int decode_num_splits_multi(int batch, int q_len, int num_q_heads, int num_kv_heads, int max_seq_len,
                             int head_dim, int num_sms);
+
+/*
+ * decode_plan_pieces — the partition of a decode call into pieces (host only, pure).
+ *
+ * Reports, for a call with these sizes, host copies of its sequence lengths and
+ * num_splits, every piece the split kernel computes: the same plan code runs
+ * here on the host.  The pages fix only caps on the split count (AstrAI commit
+ * 988e013 "csrc", split-KV items: at most the tile count and 32 splits); the
+ * partition itself is this library's (see "The split plan" above), and any
+ * partition of each segment into at most num_splits pieces gives the same
+ * attention output.
+ *  seq_lens   int32 [batch] on the HOST, or NULL (every sequence max_len tokens);
+ *             clamped to [0, max_len]
+ *  q_len      query tokens per sequence (1 for decode_attn_contig / _paged);
+ *             rows of a sequence are num_q_heads * q_len (head-major)
+ *  max_len    the call's length cap: max_ctx (contiguous) or
+ *             min(max_pages_per_seq * page_size, max_seq_len) (paged)
+ *  records    int32 [capacity][9], one record per piece in CTA walk order:
+ *             (b, row0, nrows, j, npieces, t0, t1, held_t0, held_t1): sequence b,
+ *             rows row0 .. row0 + nrows - 1 of the pass (query heads x q_len
+ *             rows, head-major), partial slot j of npieces, tokens [t0, t1), and
+ *             the token range whose partial slot j holds when the call returns
+ *             ([t0, t1); held_t0 == held_t1 == 0 when the segment has one piece,
+ *             which is written straight to the output).  Empty sequences
+ *             have no pieces.
+ * *count receives the number of pieces; at most capacity records are written.
+ * Returns DA_OK, DA_ERR_WORKSPACE (capacity < *count; *count is still set),
+ * DA_ERR_INVALID_ARG or DA_ERR_UNSUPPORTED.
+ */
+int decode_plan_pieces(const int* seq_lens, int batch, int q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                       int max_len, int num_splits, int* records, int capacity, int* count);
+
+/*
+ * decode_max_batch — the largest batch the decode kernels accept for a shape
+ * (host only, pure): the split kernel keeps two ints of plan per sequence in
+ * shared memory beside its K/V stages.  q_len and the heads are as for
+ * decode_num_splits_multi; kv_int8 != 0 for the int8 cache entry points, paged
+ * != 0 for paged caches.  Returns the limit, or -DA_ERR_INVALID_ARG /
+ * -DA_ERR_UNSUPPORTED.
+ */
+int decode_max_batch(int q_len, int num_q_heads, int num_kv_heads, int head_dim, int kv_int8, int paged);
 
 /*
  * decode_attn_multi_contig / decode_attn_multi_paged — multi-query decode, the

@@ -21,9 +21,11 @@ Split-KV (AstrAI commit 988e013 "csrc", split-KV items; "perf(qwen3.8):
 split the flash-decode KV range across warp-groups", section "Mechanism"):
 a piece of the token range yields unnormalised partials (acc, m, l) with
 m = max over the piece, acc = sum exp(s - m) v, l = sum exp(s - m); pieces
-are merged by the log-sum-exp rescale in ascending piece order.  The
-partition of the token range into pieces is this library's own rule (the
-pages only give caps on the split count); ``split_pieces`` states it.
+are merged by the log-sum-exp rescale in ascending piece order.  Which
+partition of the token range a GPU call uses is not the oracle's business
+(the pages fix only caps on the split count, and any partition merges to the
+same result): ``range_partials`` computes the partials of whatever token
+ranges it is given.
 
 Paged caches (AstrAI commit 69fecaf "csrc/tests", paged decode items): token
 t of sequence b is row t % page_size of physical page page_table[b, t // page_size].
@@ -48,28 +50,13 @@ __all__ = [
     "decode_contig",
     "decode_paged",
     "decode_rows",
-    "head_groups",
-    "piece_gap_blocks",
-    "groups_per_pass",
-    "split_pieces",
-    "decode_partials",
+    "range_partials",
     "combine_partials",
     "visible_tokens",
     "decode_multi",
-    "decode_multi_partials",
     "dequant_rows",
     "decode_int8",
-    "decode_int8_partials",
-    "BLOCK_TOKENS",
-    "MAX_GROUP_ROWS",
 ]
-
-# Token granularity of the split rule: piece boundaries fall on multiples of
-# 16 tokens of a sequence.
-BLOCK_TOKENS = 16
-# At most 8 query heads share one pass over a KV head's tokens; larger groups
-# are cut into ceil(G / 8) equal-sized sub-groups, each a separate pass.
-MAX_GROUP_ROWS = 8
 
 
 # ---------------------------------------------------------------- bf16 bits
@@ -170,16 +157,6 @@ def merge_partials(parts: Sequence[Tuple[np.ndarray, np.ndarray, np.ndarray]]) -
 
 # --------------------------------------------------------------- KV access
 
-def head_groups(G: int) -> List[Tuple[int, int]]:
-    """Sub-groups of the G query heads of one KV head: [(first, count)].
-
-    ceil(G / 8) groups of ceil(G / ngroups) heads; the last may be shorter.
-    """
-    ng = -(-G // MAX_GROUP_ROWS)
-    gr = -(-G // ng)
-    return [(j * gr, min(gr, G - j * gr)) for j in range(ng) if j * gr < G]
-
-
 def gather_paged(pool: np.ndarray, page_table: np.ndarray, b: int, L: int, page_size: int) -> np.ndarray:
     """Logical token rows [L, Hkv, D] of sequence b from a paged pool, one token at a time."""
     rows = [pool[page_table[b, t // page_size], t % page_size] for t in range(L)]
@@ -244,118 +221,52 @@ def _decode_all(inp: dict) -> np.ndarray:
     return out
 
 
-# ------------------------------------------------------------ split rule
+# ------------------------------------------------------------ partials of given ranges
 
-def piece_gap_blocks(head_dim: int) -> int:
-    """Line positions charged to each segment for the fixed cost of one piece
-    (a multiple of 4)."""
-    return (2816 // head_dim + 3) // 4 * 4
+def range_partials(inp: dict, ranges: Iterable[Tuple[int, int, int, int, int, int]], num_splits: int):
+    """fp64 unnormalised partials of given query rows over given token ranges,
+    laid out as a GPU call's partial buffers.
 
+    inp is a decode input (q [B, Hq, D]), a multi-query input (q [B, Hq, q_len, D])
+    or an int8-cache input, with a contiguous or paged cache.  The rows of a
+    sequence are its Hq * q_len (query head h, query token i) pairs, head-major
+    (row r = h * q_len + i; q_len = 1 for single-token decode); query token i sees
+    visible_tokens(L_b, q_len, i) tokens.  Each range (b, row0, nrows, slot, t0, t1)
+    asks for the partials of rows row0 .. row0 + nrows - 1 of sequence b over
+    tokens [t0, t1), cut at what each row sees, stored in partial slot `slot`:
+    attend_partial of that row and token range (an empty range gives (0, -inf, 0)).
 
-def groups_per_pass(G: int, head_dim: int) -> int:
-    """Sub-groups of head_groups(G) that one pass over a KV head runs together: the
-    largest power of two that divides their number, at most 2 for head_dim 128 and
-    4 otherwise."""
-    ng, per, cap = len(head_groups(G)), 1, (2 if head_dim == 128 else 4)
-    while per * 2 <= cap and ng % (per * 2) == 0:
-        per *= 2
-    return per
-
-
-def split_pieces(seq_lens: Sequence[int], Hkv: int, G: int, num_splits: int, gap: int = 0, per_pass: int = 1):
-    """The partition of every (sequence, KV head, pass) token range into pieces.
-
-    Work units are 16-token blocks; sequence b has n_b = ceil(L_b / 16) of them.
-    The G rows of a KV head form the sub-groups head_groups(G); a pass runs
-    per_pass consecutive sub-groups, npass = ceil(len(head_groups(G)) / per_pass).
-    A segment is one (b, KV head h, pass p), slot u = h * npass + p, U = Hkv * npass
-    slots per sequence.  The segments lie end to end on one line,
-    in (u, b) order (slot-major); segment (b, u) takes w_b = gap + 4 * ceil(n_b / 4) positions
-    (none when the sequence is empty): first `gap` positions that hold no block,
-    then its n_b blocks, then empty positions up to the width.  NB = U * (w_0 +
-    ... + w_{B-1}) positions in total.  With gap a multiple of 4, every piece
-    starts on a 64-token boundary of its sequence.
-
-    num_splits == 1: every segment is one piece.
-    num_splits >= 2: the line is cut into ranges of q positions, q = ceil(NB / R)
-    with R = (num_splits - 1) * U, rounded up to a multiple of 4, at least 4;
-    range r = [r q, (r + 1) q).  A segment's pieces are the non-empty sets of its
-    blocks that share a range, in order; piece index j = r - (range of its first
-    block).  This never gives a segment more than num_splits pieces.
-
-    Returns a list of dicts {b, u, h, group (first row, row count), piece, t0, t1, npieces}.
-    """
-    subs = head_groups(G)
-    npass = -(-len(subs) // per_pass)
-    groups = []
-    for j in range(npass):
-        part = subs[j * per_pass:(j + 1) * per_pass]
-        groups.append((part[0][0], sum(c for _, c in part)))
-    ng = npass
-    U = Hkv * ng
-    lens = [int(x) for x in seq_lens]
-    nblk = [-(-L // BLOCK_TOKENS) for L in lens]
-    out = []
-    if num_splits == 1:
-        for b, L in enumerate(lens):
-            for u in range(U):
-                if L > 0:
-                    out.append(dict(b=b, u=u, h=u // ng, group=groups[u % ng], piece=0,
-                                    t0=0, t1=L, npieces=1))
-        return out
-    w = [gap + -(-n // 4) * 4 if n > 0 else 0 for n in nblk]
-    P = [0]
-    for x in w:
-        P.append(P[-1] + x)
-    NB = U * P[-1]
-    R = (num_splits - 1) * U
-    q = max(4, -(-max(1, -(-NB // R)) // 4) * 4)
-    for b, L in enumerate(lens):
-        for u in range(U):
-            if nblk[b] == 0:
-                continue
-            start = u * P[-1] + P[b] + gap  # first block
-            end = start + nblk[b]
-            r_first, r_last = start // q, (end - 1) // q
-            for r in range(r_first, r_last + 1):
-                x0, x1 = max(start, r * q), min(end, (r + 1) * q)
-                out.append(dict(b=b, u=u, h=u // ng, group=groups[u % ng], piece=r - r_first,
-                                t0=(x0 - start) * BLOCK_TOKENS,
-                                t1=min((x1 - start) * BLOCK_TOKENS, L),
-                                npieces=r_last - r_first + 1))
-    return out
-
-
-def decode_partials(inp: dict, num_splits: int):
-    """fp64 partials of every piece, laid out as the library's partial buffers.
-
-    Returns (part_acc [B, Hq, S, D], part_ml [B, Hq, S, 2], npieces [B, Hq]).
-    Slots that no piece fills are NaN.
+    Returns (acc [B, R, S, D], ml [B, R, S, 2]) with R = Hq * q_len; slots that no
+    range fills are NaN.
     """
     q = inp["q"]
-    B, Hq, D = q.shape
-    Hkv = (inp["k"] if "k" in inp else inp["k_pool"]).shape[2]
+    B, Hq = q.shape[:2]
+    D = q.shape[-1]
+    qlen = q.shape[2] if q.ndim == 4 else 1
+    qrows = q.reshape(B, Hq * qlen, D)
+    kname = next(n for n in ("k", "k_pool", "k_i8", "k_pool_i8") if n in inp)
+    Hkv = inp[kname].shape[2]
     G = Hq // Hkv
-    S = num_splits
-    acc = np.full((B, Hq, S, D), np.nan)
-    ml = np.full((B, Hq, S, 2), np.nan)
-    npieces = np.zeros((B, Hq), dtype=np.int64)
+    acc = np.full((B, Hq * qlen, num_splits, D), np.nan)
+    ml = np.full((B, Hq * qlen, num_splits, 2), np.nan)
     cache = {}
-    for pc in split_pieces(inp["seq_lens"], Hkv, G, S, piece_gap_blocks(D), groups_per_pass(G, D)):
-        b, h = pc["b"], pc["h"]
+    for b, row0, nrows, slot, t0, t1 in ranges:
+        L = int(inp["seq_lens"][b])
         if b not in cache:
-            cache = {b: _kv_rows(inp, b, int(inp["seq_lens"][b]))}
-        Kb, Vb = cache[b]
-        first, count = pc["group"]
-        heads = slice(h * G + first, h * G + first + count)
-        a, m, l = attend_partial(widen_bf16(q[b, heads]),
-                                 widen_bf16(Kb[pc["t0"]:pc["t1"], h]),
-                                 widen_bf16(Vb[pc["t0"]:pc["t1"], h]), inp["scale"])
-        acc[b, heads, pc["piece"]] = a
-        ml[b, heads, pc["piece"], 0] = m
-        ml[b, heads, pc["piece"], 1] = l
-        npieces[b, heads] = pc["npieces"]
-    return acc, ml, npieces
+            if kname in ("k_i8", "k_pool_i8"):
+                cache = {b: dequant_rows(inp, b, L)}
+            else:
+                Kb, Vb = _kv_rows(inp, b, L)
+                cache = {b: (widen_bf16(Kb), widen_bf16(Vb))}
+        K, V = cache[b]
+        for r in range(row0, row0 + nrows):
+            h, i = r // qlen, r % qlen
+            hi = min(t1, visible_tokens(L, qlen, i))
+            lo = min(t0, hi)
+            a, m, l = attend_partial(widen_bf16(qrows[b, r])[None], K[lo:hi, h // G], V[lo:hi, h // G], inp["scale"])
+            acc[b, r, slot] = a[0]
+            ml[b, r, slot] = (m[0], l[0])
+    return acc, ml
 
 
 def combine_partials(part_acc: np.ndarray, part_ml: np.ndarray) -> np.ndarray:
@@ -414,41 +325,6 @@ def decode_multi(inp: dict, rows: Optional[Iterable[Tuple[int, int, int]]] = Non
     return res.reshape(B, Hq, qlen, D) if rows is None else res
 
 
-def decode_multi_partials(inp: dict, num_splits: int):
-    """fp64 partials of every piece for multi-query decode, laid out as the library's
-    buffers: (part_acc [B, Hq, q_len, S, D], part_ml [B, Hq, q_len, S, 2], npieces
-    [B, Hq, q_len]).  The split rule is split_pieces with G * q_len rows per KV head
-    (rows ordered head-major: row r is head r // q_len, query token r % q_len); a
-    row's piece covers its tokens [t0, min(t1, visible)), and a piece in which the
-    row sees no token gives (0, -inf, 0).  Unfilled slots are NaN."""
-    q = inp["q"]
-    B, Hq, qlen, D = q.shape
-    Hkv = (inp["k"] if "k" in inp else inp["k_pool"]).shape[2]
-    G = Hq // Hkv
-    S = num_splits
-    acc = np.full((B, Hq, qlen, S, D), np.nan)
-    ml = np.full((B, Hq, qlen, S, 2), np.nan)
-    npieces = np.zeros((B, Hq, qlen), dtype=np.int64)
-    cache = {}
-    for pc in split_pieces(inp["seq_lens"], Hkv, G * qlen, S, piece_gap_blocks(D), groups_per_pass(G * qlen, D)):
-        b, kv = pc["b"], pc["h"]
-        L = int(inp["seq_lens"][b])
-        if b not in cache:
-            cache = {b: _kv_rows(inp, b, L)}
-        Kb, Vb = cache[b]
-        first, count = pc["group"]
-        for r in range(first, first + count):
-            h, i = kv * G + r // qlen, r % qlen
-            t1 = min(pc["t1"], visible_tokens(L, qlen, i))
-            t0 = min(pc["t0"], t1)
-            a, m, l = attend_partial(widen_bf16(q[b, h, i])[None], widen_bf16(Kb[t0:t1, kv]),
-                                     widen_bf16(Vb[t0:t1, kv]), inp["scale"])
-            acc[b, h, i, pc["piece"]] = a[0]
-            ml[b, h, i, pc["piece"]] = (m[0], l[0])
-            npieces[b, h, i] = pc["npieces"]
-    return acc, ml, npieces
-
-
 # ------------------------------------------------------------ int8 KV cache
 #
 # "perf(dspark): overlap KV staging with compute via cp.async", section "Cost and
@@ -496,32 +372,3 @@ def decode_int8(inp: dict, rows: Optional[Iterable[Tuple[int, int]]] = None) -> 
         K, V = cache[b]
         res[n] = attend(widen_bf16(q[b, h])[None], K[:, h // G], V[:, h // G], inp["scale"])[0]
     return res.reshape(B, Hq, D) if rows is None else res
-
-
-def decode_int8_partials(inp: dict, num_splits: int):
-    """fp64 partials of every piece over an int8 cache, laid out as the library's
-    buffers (part_acc [B, Hq, S, D], part_ml [B, Hq, S, 2], npieces [B, Hq]); the
-    split rule is the one of decode_partials."""
-    q = inp["q"]
-    B, Hq, D = q.shape
-    Hkv = (inp["k_i8"] if "k_i8" in inp else inp["k_pool_i8"]).shape[2]
-    G = Hq // Hkv
-    S = num_splits
-    acc = np.full((B, Hq, S, D), np.nan)
-    ml = np.full((B, Hq, S, 2), np.nan)
-    npieces = np.zeros((B, Hq), dtype=np.int64)
-    cache = {}
-    for pc in split_pieces(inp["seq_lens"], Hkv, G, S, piece_gap_blocks(D), groups_per_pass(G, D)):
-        b, h = pc["b"], pc["h"]
-        if b not in cache:
-            cache = {b: dequant_rows(inp, b, int(inp["seq_lens"][b]))}
-        K, V = cache[b]
-        first, count = pc["group"]
-        heads = slice(h * G + first, h * G + first + count)
-        a, m, l = attend_partial(widen_bf16(q[b, heads]), K[pc["t0"]:pc["t1"], h], V[pc["t0"]:pc["t1"], h],
-                                 inp["scale"])
-        acc[b, heads, pc["piece"]] = a
-        ml[b, heads, pc["piece"], 0] = m
-        ml[b, heads, pc["piece"], 1] = l
-        npieces[b, heads] = pc["npieces"]
-    return acc, ml, npieces

@@ -84,24 +84,51 @@ def check_out(out_bits: np.ndarray, ref: np.ndarray, what: str = ""):
     return float(err.max())
 
 
-def check_partials(acc: np.ndarray, ml: np.ndarray, ref_acc: np.ndarray, ref_ml: np.ndarray, npieces: np.ndarray,
-                   what: str = ""):
-    """Compare every slot j < npieces of rows that have >= 2 pieces."""
-    B, Hq, S, D = ref_acc.shape
+def plan_max_len(inp: dict, max_seq_len: int = None) -> int:
+    """The length cap a call on inp uses: max_ctx, or min(max_pages * page_size, max_seq_len)."""
+    for name in ("k", "k_i8"):
+        if name in inp:
+            return int(inp[name].shape[1])
+    cap = int(inp["page_table"].shape[1]) * int(inp["page_size"])
+    return cap if max_seq_len is None else min(cap, int(max_seq_len))
+
+
+def check_plan_partials(acc: np.ndarray, ml: np.ndarray, inp: dict, S: int, max_seq_len: int = None,
+                        segments: int = None, rng=None, what: str = ""):
+    """Every partial slot a call leaves filled, against the oracle's partials of the
+    token range the slot holds.  The pieces come from the library's planner
+    (decode_plan_pieces): any partition is correct, so the oracle is not told which
+    one the library uses.  acc/ml are the call's buffers ([B, Hq(, q_len), S, ...]);
+    segments: check only this many randomly chosen multi-piece segments."""
+    q = inp["q"]
+    B, Hq = q.shape[:2]
+    qlen = q.shape[2] if q.ndim == 4 else 1
+    D = q.shape[-1]
+    Hkv = next(inp[n] for n in ("k", "k_pool", "k_i8", "k_pool_i8") if n in inp).shape[2]
+    rec = binding.plan_pieces(inp["seq_lens"], Hq, Hkv, D, plan_max_len(inp, max_seq_len), S, q_len=qlen)
+    rec = rec[rec[:, 8] > rec[:, 7]]  # slots that hold a partial when the call returns
+    if segments is not None and len(rec):
+        segs = sorted({(int(r[0]), int(r[1])) for r in rec})
+        rng = rng if rng is not None else np.random.default_rng(0)
+        keep = {segs[i] for i in rng.choice(len(segs), size=min(segments, len(segs)), replace=False)}
+        rec = np.array([r for r in rec if (int(r[0]), int(r[1])) in keep]).reshape(-1, rec.shape[1])
+    ranges = [(int(r[0]), int(r[1]), int(r[2]), int(r[3]), int(r[7]), int(r[8])) for r in rec]
+    ref_acc, ref_ml = oracle.range_partials(inp, ranges, S)
+    acc = acc.reshape(B, Hq * qlen, S, D)
+    ml = ml.reshape(B, Hq * qlen, S, 2)
     checked = 0
-    for b in range(B):
-        for h in range(Hq):
-            n = int(npieces[b, h])
-            if n < 2:
+    for b, row0, nrows, j, t0, t1 in ranges:
+        for r in range(row0, row0 + nrows):
+            m_ref, l_ref = ref_ml[b, r, j]
+            m_got, l_got = ml[b, r, j]
+            if l_ref == 0:  # a row that sees no token of this range
+                assert m_got == -np.inf and l_got == 0 and np.all(acc[b, r, j] == 0), (what, b, r, j)
                 continue
-            for j in range(n):
-                m_ref, l_ref = ref_ml[b, h, j]
-                m_got, l_got = ml[b, h, j]
-                assert abs(m_got - m_ref) <= PART_RTOL * max(1.0, abs(m_ref)), (what, b, h, j, m_got, m_ref)
-                assert abs(l_got - l_ref) <= PART_RTOL * l_ref, (what, b, h, j, l_got, l_ref)
-                da = np.abs(acc[b, h, j].astype(np.float64) - ref_acc[b, h, j]).max()
-                assert da <= PART_RTOL * np.abs(ref_acc[b, h, j]).max(), (what, b, h, j, da)
-                checked += 1
+            assert abs(m_got - m_ref) <= PART_RTOL * max(1.0, abs(m_ref)), (what, b, r, j, m_got, m_ref)
+            assert abs(l_got - l_ref) <= PART_RTOL * l_ref, (what, b, r, j, l_got, l_ref)
+            da = np.abs(acc[b, r, j].astype(np.float64) - ref_acc[b, r, j]).max()
+            assert da <= PART_RTOL * np.abs(ref_acc[b, r, j]).max(), (what, b, r, j, da)
+            checked += 1
     return checked
 
 
@@ -130,26 +157,6 @@ def run_multi(inp, S=None, max_seq_len=None, dev_inputs=None):
     torch.cuda.synchronize()
     assert binding.device_error() == 0
     return host_bits(out), acc.cpu().numpy(), ml.cpu().numpy(), S
-
-
-def check_multi_partials(acc, ml, inp, S):
-    """Slots of rows whose segment has >= 2 pieces; a piece in which the row sees no
-    token must be (0, -inf, 0)."""
-    ra, rm, npc = oracle.decode_multi_partials(inp, S)
-    checked = 0
-    for idx in zip(*np.nonzero(npc >= 2)):
-        for j in range(npc[idx]):
-            m_ref, l_ref = rm[idx + (j,)]
-            m_got, l_got = ml[idx + (j,)]
-            if l_ref == 0:
-                assert m_got == -np.inf and l_got == 0 and np.all(acc[idx + (j,)] == 0), (idx, j)
-                continue
-            assert abs(m_got - m_ref) <= PART_RTOL * max(1.0, abs(m_ref)), (idx, j, m_got, m_ref)
-            assert abs(l_got - l_ref) <= PART_RTOL * l_ref, (idx, j, l_got, l_ref)
-            da = np.abs(acc[idx + (j,)].astype(np.float64) - ra[idx + (j,)]).max()
-            assert da <= PART_RTOL * np.abs(ra[idx + (j,)]).max(), (idx, j, da)
-            checked += 1
-    return checked
 
 
 def dev(x):

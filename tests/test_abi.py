@@ -218,3 +218,109 @@ def test_binding_rejects_host_and_mistyped_tensors(clib):
         binding.decode_attn_int8_contig(q, k, k, q, q)
     with pytest.raises(ValueError, match="q"):
         binding.prefill_attn_paged(q.float().unsqueeze(0), k, k, None, None, 32)
+
+
+# ---------------------------------------------------- the library's split plan
+#
+# The pages fix only caps on the split count (AstrAI commit 988e013 "csrc",
+# split-KV items: at most the tile count and 32 splits), and any partition of a
+# row's tokens gives the same output.  So the partition the library uses is not
+# restated anywhere; decode_plan_pieces reports it from the planner code the
+# kernels run, and these checks hold it to the properties every valid partition
+# must have.
+
+def check_library_plan(lens, Hq, Hkv, D, S, q_len=1):
+    from gqa_split_kv_gb300 import binding
+    max_len = max(lens) if len(lens) else 0
+    rec = binding.plan_pieces(list(lens), Hq, Hkv, D, max_len, S, q_len=q_len)
+    R, G = Hq * q_len, Hq // Hkv * q_len
+    segs = {}
+    for r in rec:
+        segs.setdefault((int(r[0]), int(r[1])), []).append([int(x) for x in r])
+    for b, L in enumerate(lens):
+        mine = sorted(k for k in segs if k[0] == b)
+        if L == 0:
+            assert not mine, (b, "an empty sequence has no pieces")
+            continue
+        rows = sorted(r for (bb, row0) in mine for r in range(row0, row0 + segs[(bb, row0)][0][2]))
+        assert rows == list(range(R)), (b, "every row in exactly one pass")
+    for (b, row0), ps in segs.items():
+        ps.sort(key=lambda p: p[3])
+        n, L = len(ps), int(lens[b])
+        nrows = ps[0][2]
+        assert 1 <= nrows <= 32 and row0 // G == (row0 + nrows - 1) // G, "a pass stays within one KV head"
+        assert [p[3] for p in ps] == list(range(n)) and all(p[4] == n for p in ps)
+        assert 1 <= n <= S
+        assert all(p[2] == nrows for p in ps)
+        assert ps[0][5] == 0 and ps[-1][6] == L, "the pieces cover [0, L)"
+        for a, c in zip(ps, ps[1:]):
+            assert a[6] == c[5], "in order, no gap, no overlap"
+        assert all(p[5] < p[6] for p in ps), "no empty piece"
+        assert all(p[5] % 64 == 0 for p in ps), "pieces start on 64-token boundaries"
+        for p in ps:  # what slot j holds when the call returns
+            t0, t1, h0, h1 = p[5], p[6], p[7], p[8]
+            assert (h0, h1) == ((0, 0) if n == 1 else (t0, t1))
+    return rec
+
+
+def test_library_plan_is_a_valid_partition_random_shapes():
+    import numpy as np
+    rng = np.random.default_rng(41)
+    for trial in range(300):
+        B = int(rng.integers(1, 7))
+        lens = rng.integers(0, 3000, size=B)
+        lens[rng.random(B) < 0.2] = 0
+        Hkv = int(rng.integers(1, 9))
+        G = int(rng.choice([1, 2, 4, 6, 8, 9, 12, 16, 24, 32, 64]))
+        D = int(rng.choice([32, 64, 128, 256]))
+        S = int(rng.integers(1, 80))
+        check_library_plan(lens.tolist(), G * Hkv, Hkv, D, S)
+
+
+def test_library_plan_is_a_valid_partition_multi_query():
+    import numpy as np
+    rng = np.random.default_rng(42)
+    for trial in range(100):
+        B = int(rng.integers(1, 5))
+        lens = rng.integers(0, 2000, size=B).tolist()
+        Hkv, G, q_len = int(rng.integers(1, 5)), int(rng.choice([1, 4, 6, 8])), int(rng.integers(1, 9))
+        if G * q_len > 64:
+            continue
+        D = int(rng.choice([64, 128, 256]))
+        check_library_plan(lens, G * Hkv, Hkv, D, int(rng.integers(2, 40)), q_len=q_len)
+
+
+@pytest.mark.parametrize("name", ["gqa6_contig_b1_hq24_hkv4_d256_ctx4096", "gqa6_contig_b1_hq24_hkv4_d256_ctx16384",
+                                  "paged_b16_hq32_hkv8_d128_u256_8192_ps32",
+                                  "long_contig_b1_hq32_hkv8_d128_ctx65536_outliers",
+                                  "mixed_paged_b64_hq64_hkv8_d128_log1_32768_ps16"])
+def test_library_plan_on_the_workloads(name):
+    from gqa_split_kv_gb300 import binding
+    from gqa_split_kv_gb300.workloads import WORKLOADS, workload_lens
+    wl = WORKLOADS[name]
+    lens = workload_lens(wl)
+    S = binding.num_splits(wl.B, wl.Hkv, wl.max_ctx, wl.D, 152)
+    rec = check_library_plan(lens.tolist(), wl.Hq, wl.Hkv, wl.D, S)
+    assert rec[:, 4].max() <= S
+
+
+def test_gqa6_pieces():
+    """GQA-6 at ctx 4096 with the planner's 39 slots: 32 or 33 pieces per KV head, every
+    slot holding its own piece's partial."""
+    rec = check_library_plan([4096], 24, 4, 256, 39)
+    for h in range(4):
+        seg = rec[rec[:, 1] == 6 * h]
+        assert 32 <= len(seg) <= 39 and set(seg[:, 2].tolist()) == {6}
+
+
+def test_max_batch_values(clib):
+    from gqa_split_kv_gb300 import binding
+    assert binding.max_batch(32, 8, 128) == 1159
+    for D in (32, 64, 128, 256):
+        for paged in (False, True):
+            for kv8 in (False, True):
+                m = binding.max_batch(8 * 4, 8, D, kv_int8=kv8, paged=paged)
+                assert 500 <= m <= 20000, (D, paged, kv8, m)
+    assert clib.decode_max_batch(1, 8, 2, 48, 0, 0) == -2
+    assert clib.decode_max_batch(0, 8, 2, 64, 0, 0) == -1
+    assert clib.decode_max_batch(2, 8, 2, 64, 1, 0) == -2  # int8 caches take one query token

@@ -1,7 +1,9 @@
 """Full-size parity: every benchmark workload at its full size, in the launch
 configuration bench.py times (the planner's split count), checked on sampled
-outputs the oracle computes one by one, on the partials of sampled
-multi-piece segments, and for bitwise run-to-run determinism."""
+outputs the oracle computes one by one (whole KV-head groups), on every output
+against a property that holds at any size (a softmax-weighted mean of V rows
+lies between their smallest and largest value, per column), on the partials of
+sampled multi-piece segments, and for bitwise run-to-run determinism."""
 import numpy as np
 import pytest
 
@@ -14,11 +16,41 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
-from gpu_helpers import OUT_ATOL, OUT_RTOL, PART_RTOL, run, run_int8, run_multi, to_device  # noqa: E402
+from gpu_helpers import (OUT_ATOL, OUT_RTOL, check_plan_partials, run, run_int8, run_multi,  # noqa: E402
+                         to_device)
 from gqa_split_kv_gb300.workloads import bf16_bits_to_f32  # noqa: E402
 
-N_ROWS = 24       # sampled (b, query head) outputs per workload
+N_ROWS = 24       # sampled (b, query head) outputs per workload (multi-query, int8)
+N_GROUPS = 24     # sampled (b, KV head) groups, all G query heads each (decode)
 N_SEGMENTS = 3    # sampled multi-piece segments whose partials are checked
+
+
+def _v_rows(inp, b):
+    """V rows [L, Hkv, D] of sequence b as float32."""
+    L = int(inp["seq_lens"][b])
+    if "v" in inp:
+        bits = inp["v"][b, :L]
+    else:
+        ps = int(inp["page_size"])
+        pages = inp["page_table"][b, :(L + ps - 1) // ps]
+        bits = inp["v_pool"][pages].reshape(-1, *inp["v_pool"].shape[2:])[:L]
+    return bf16_bits_to_f32(bits)
+
+
+def _check_convex_bounds(inp, out_bits, G, name):
+    """Every output row is a convex combination of its V rows: per column it lies
+    between their smallest and largest value (an empty sequence gives zeros)."""
+    out = bf16_bits_to_f32(out_bits).astype(np.float64)
+    B, Hq, D = out.shape
+    for b in range(B):
+        if int(inp["seq_lens"][b]) == 0:
+            assert np.all(out[b] == 0), (name, b)
+            continue
+        V = _v_rows(inp, b)
+        lo = np.repeat(V.min(axis=0), G, axis=0).astype(np.float64)  # [Hq, D]
+        hi = np.repeat(V.max(axis=0), G, axis=0).astype(np.float64)
+        tol = OUT_ATOL + OUT_RTOL * np.maximum(np.abs(lo), np.abs(hi))
+        assert np.all(out[b] >= lo - tol) and np.all(out[b] <= hi + tol), (name, b)
 
 
 def _sample_rows(inp, rng):
@@ -48,6 +80,8 @@ def _full_size_multi(wl, inp, d):
     got = np.stack([bf16_bits_to_f32(out[b, h, i]).astype(np.float64) for b, h, i in rows])
     err = np.abs(got - ref)
     assert np.all(err <= OUT_ATOL + OUT_RTOL * np.abs(ref)), f"{wl.name}: max abs err {err.max():.3e}"
+    if S >= 2:
+        check_plan_partials(acc, ml, inp, S, max_seq_len=max_len, segments=2, rng=rng, what=wl.name)
     out2, *_ = run_multi(inp, S, max_seq_len=max_len, dev_inputs=d)
     assert np.array_equal(out, out2)
 
@@ -63,6 +97,9 @@ def _full_size_int8(wl, inp):
     got = np.stack([bf16_bits_to_f32(out[b, h]).astype(np.float64) for b, h in pairs])
     err = np.abs(got - ref)
     assert np.all(err <= OUT_ATOL + OUT_RTOL * np.abs(ref)), f"{wl.name}: max abs err {err.max():.3e}"
+    if S >= 2:
+        check_plan_partials(acc, ml, inp, S, max_seq_len=max_len, segments=2, rng=np.random.default_rng(4445),
+                            what=wl.name)
     out2, *_ = run_int8(inp, S, max_seq_len=max_len)
     assert np.array_equal(out, out2)
 
@@ -111,40 +148,24 @@ def test_full_size_workload(name):
     max_len = wl.max_ctx
     out, acc, ml, S = run(inp, None, dev_inputs=d, max_seq_len=max_len if "k_pool" in inp else None)
     assert np.all(np.isfinite(bf16_bits_to_f32(out)))
-    # sampled outputs, one by one against the oracle
+    # sampled whole KV-head groups, row by row against the oracle
     rng = np.random.default_rng(4242)
-    pairs = _sample_rows(inp, rng)
+    G = wl.Hq // wl.Hkv
+    lens = inp["seq_lens"]
+    groups = {(int(np.argmax(lens)), 0), (int(np.argmin(lens)), wl.Hkv - 1)}
+    while len(groups) < min(N_GROUPS, wl.B * wl.Hkv):
+        groups.add((int(rng.integers(wl.B)), int(rng.integers(wl.Hkv))))
+    pairs = [(b, g * G + i) for b, g in sorted(groups) for i in range(G)]
     ref = oracle.decode_rows(inp, pairs)
     got = np.stack([bf16_bits_to_f32(out[b, h]).astype(np.float64) for b, h in pairs])
     err = np.abs(got - ref)
     assert np.all(err <= OUT_ATOL + OUT_RTOL * np.abs(ref)), f"{name}: max abs err {err.max():.3e}"
+    # every output row, against the convex-combination bounds
+    _check_convex_bounds(inp, out, G, name)
     # partials of sampled segments cut into several pieces, at the same plan
     if S >= 2:
-        G = wl.Hq // wl.Hkv
-        pieces = [pc for pc in oracle.split_pieces(inp["seq_lens"], wl.Hkv, G, S, oracle.piece_gap_blocks(wl.D),
-                                                    oracle.groups_per_pass(G, wl.D)) if pc["npieces"] >= 2]
-        if pieces:
-            segs = sorted({(pc["b"], pc["u"]) for pc in pieces})
-            chosen = [segs[i] for i in rng.choice(len(segs), size=min(N_SEGMENTS, len(segs)), replace=False)]
-            for pc in pieces:
-                if (pc["b"], pc["u"]) not in chosen:
-                    continue
-                b, h = pc["b"], pc["h"]
-                first, count = pc["group"]
-                heads = list(range(h * G + first, h * G + first + count))
-                L = int(inp["seq_lens"][b])
-                if "k" in inp:
-                    K, V = inp["k"][b, pc["t0"]:pc["t1"], h], inp["v"][b, pc["t0"]:pc["t1"], h]
-                else:
-                    K = oracle.gather_paged(inp["k_pool"], inp["page_table"], b, L, inp["page_size"])[pc["t0"]:pc["t1"], h]
-                    V = oracle.gather_paged(inp["v_pool"], inp["page_table"], b, L, inp["page_size"])[pc["t0"]:pc["t1"], h]
-                a, m, l = oracle.attend_partial(oracle.widen_bf16(inp["q"][b, heads]), oracle.widen_bf16(K),
-                                                oracle.widen_bf16(V), inp["scale"])
-                for r, hq in enumerate(heads):
-                    j = pc["piece"]
-                    assert abs(ml[b, hq, j, 0] - m[r]) <= PART_RTOL * max(1.0, abs(m[r]))
-                    assert abs(ml[b, hq, j, 1] - l[r]) <= PART_RTOL * l[r]
-                    assert np.abs(acc[b, hq, j].astype(np.float64) - a[r]).max() <= PART_RTOL * np.abs(a[r]).max()
+        check_plan_partials(acc, ml, inp, S, max_seq_len=max_len if "k_pool" in inp else None,
+                            segments=N_SEGMENTS, rng=rng, what=name)
     # the same launch again: identical bits
     out2, *_ = run(inp, S, dev_inputs=d, max_seq_len=max_len if "k_pool" in inp else None)
     assert np.array_equal(out, out2)

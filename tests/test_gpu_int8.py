@@ -14,7 +14,7 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
-from gpu_helpers import check_out, check_partials, run_int8  # noqa: E402
+from gpu_helpers import check_out, check_plan_partials, run_int8  # noqa: E402
 
 RAGGED = [1, 15, 16, 17, 100, 300, 777]
 
@@ -37,8 +37,7 @@ def test_int8_contig_matches_oracle(D, Hq, Hkv):
         out, acc, ml, S_used = run_int8(inp, S)
         check_out(out, ref, f"int8 D={D} G={Hq // Hkv} S={S_used}")
         if S_used >= 2:
-            ra, rm, npc = oracle.decode_int8_partials(inp, S_used)
-            checked += check_partials(acc, ml, ra, rm, npc, f"int8 D={D} S={S_used}")
+            checked += check_plan_partials(acc, ml, inp, S_used, what=f"int8 D={D} S={S_used}")
     assert checked > 0
 
 
@@ -66,3 +65,16 @@ def test_int8_deterministic_and_edge_lengths():
     assert np.all(first[0][1] == 0)
     for _ in range(2):
         assert np.array_equal(run_int8(inp)[0], first[0])
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("lens", [[512], [500, 512], [0, 9]])
+def test_int8_small_batches_whose_lengths_differ_from_the_cache(D, lens):
+    """The guessed first tiles of small contiguous batches (kept or drained) with an int8 cache."""
+    inp = int8_case(41 + D + sum(lens), len(lens), 16, 4, D, ctx=512, lens=lens)
+    ref = oracle.decode_int8(inp)
+    for S in (None, 1, 5):
+        out, acc, ml, S_used = run_int8(inp, S)
+        check_out(out, ref, f"int8 D={D} lens={lens} S={S_used}")
+        if S_used >= 2:
+            check_plan_partials(acc, ml, inp, S_used, what=f"int8 D={D} lens={lens}")

@@ -14,7 +14,7 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
-from gpu_helpers import check_multi_partials, check_out, run_multi  # noqa: E402
+from gpu_helpers import check_out, check_plan_partials, run_multi  # noqa: E402
 
 RAGGED = [1, 7, 15, 16, 17, 100, 300, 777]
 
@@ -27,7 +27,7 @@ def multi_case(seed, B, Hq, Hkv, D, qlen, ctx, lens):
                 seq_lens=np.asarray(lens, np.int32), scale=float(np.float32(1 / math.sqrt(D))))
 
 
-@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
 @pytest.mark.parametrize("Hq,Hkv,qlen", [(8, 2, 2), (24, 4, 7), (16, 2, 4), (16, 2, 8), (4, 4, 8), (24, 4, 1)])
 def test_multi_contig_matches_oracle(D, Hq, Hkv, qlen):
     inp = multi_case(D + 10 * qlen + Hq, len(RAGGED), Hq, Hkv, D, qlen, ctx=max(RAGGED), lens=RAGGED)
@@ -42,7 +42,7 @@ def test_multi_contig_matches_oracle(D, Hq, Hkv, qlen):
                 if oracle.visible_tokens(L, qlen, i) == 0:
                     assert np.all(out[b, :, i] == 0)
         if S_used >= 2:
-            checked += check_multi_partials(acc, ml, inp, S_used)
+            checked += check_plan_partials(acc, ml, inp, S_used, what=f"multi D={D} q_len={qlen}")
     assert checked > 0
 
 
@@ -56,9 +56,10 @@ def test_multi_with_one_query_token_is_plain_decode_bitwise():
         assert np.array_equal(m_out, s_out)
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("ps", [16, 32, 64])
-def test_multi_paged_matches_contiguous_bitwise(ps):
-    inp = multi_case(ps, len(RAGGED), 32, 8, 128, 4, ctx=max(RAGGED), lens=RAGGED)
+def test_multi_paged_matches_contiguous_bitwise(D, ps):
+    inp = multi_case(ps + D, len(RAGGED), 32, 8, D, 4, ctx=max(RAGGED), lens=RAGGED)
     rng = np.random.default_rng(ps + 1)
     kp, vp, table = contig_to_paged(inp["k"], inp["v"], inp["seq_lens"], ps, rng, spare_pages=2)
     pin = dict(q=inp["q"], k_pool=kp, v_pool=vp, page_table=table, seq_lens=inp["seq_lens"], page_size=ps,
@@ -67,8 +68,10 @@ def test_multi_paged_matches_contiguous_bitwise(ps):
     for S in (None, 1, 7):
         out_c, acc_c, ml_c, S_used = run_multi(inp, S)
         out_p, acc_p, ml_p, _ = run_multi(pin, S_used, max_seq_len=max(RAGGED))
-        check_out(out_p, ref, f"paged ps={ps} S={S_used}")
+        check_out(out_p, ref, f"paged D={D} ps={ps} S={S_used}")
         assert np.array_equal(out_p, out_c)
+        if S_used >= 2:
+            check_plan_partials(acc_p, ml_p, pin, S_used, max_seq_len=max(RAGGED), what=f"multi paged D={D}")
         used = ~np.isnan(ml_c[..., 1])
         assert np.array_equal(acc_p[used], acc_c[used]) and np.array_equal(ml_p[used], ml_c[used])
 

@@ -16,7 +16,7 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
-from gpu_helpers import check_out, check_partials, run, to_device  # noqa: E402
+from gpu_helpers import check_out, check_plan_partials, run, to_device  # noqa: E402
 
 RAGGED = [1, 15, 16, 17, 100, 300, 777]
 
@@ -40,8 +40,7 @@ def test_contig_matches_oracle(D, Hq, Hkv):
         out, acc, ml, S_used = run(inp, S)
         check_out(out, ref, f"D={D} G={Hq // Hkv} S={S_used}")
         if S_used >= 2:
-            ra, rm, npc = oracle.decode_partials(inp, S_used)
-            checked += check_partials(acc, ml, ra, rm, npc, f"D={D} S={S_used}")
+            checked += check_plan_partials(acc, ml, inp, S_used, what=f"D={D} S={S_used}")
     assert checked > 0  # some segment was cut into several pieces
 
 
@@ -61,8 +60,7 @@ def test_paged_matches_oracle_and_contiguous_bitwise(D, ps):
         # same tokens, same plan, same order: identical bits
         assert np.array_equal(out_p, out_c)
         if S_used >= 2:
-            ra, rm, npc = oracle.decode_partials(pin, S_used)
-            check_partials(acc_p, ml_p, ra, rm, npc, "paged")
+            check_plan_partials(acc_p, ml_p, pin, S_used, max_seq_len=max(RAGGED), what="paged")
             used = ~np.isnan(ml_c[..., 1])
             assert np.array_equal(acc_p[used], acc_c[used]) and np.array_equal(ml_p[used], ml_c[used])
 
@@ -87,8 +85,7 @@ def test_large_groups(G):
         out, acc, ml, S_used = run(inp, S)
         check_out(out, ref, f"G={G}")
         if S_used >= 2:
-            ra, rm, npc = oracle.decode_partials(inp, S_used)
-            check_partials(acc, ml, ra, rm, npc, f"G={G}")
+            check_plan_partials(acc, ml, inp, S_used, what=f"G={G}")
 
 
 def test_deterministic_across_runs():
@@ -133,15 +130,19 @@ def test_outlier_keys_small():
     ref = oracle.decode_contig(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["scale"])
     out, acc, ml, S = run(inp, None)
     check_out(out, ref, "outliers")
-    ra, rm, npc = oracle.decode_partials(inp, S)
-    assert check_partials(acc, ml, ra, rm, npc, "outliers") > 0
+    assert check_plan_partials(acc, ml, inp, S, what="outliers") > 0
 
 
 def test_combine_alone_matches_oracle_merge():
     rng = np.random.default_rng(13)
     inp = contig_case(13, 3, 8, 2, 64, ctx=900, lens=[900, 40, 0])
     S = 6
-    ra, rm, npc = oracle.decode_partials(inp, S)
+    # partials of arbitrary pieces (any partition merges to the same output)
+    ranges = []
+    for b, L in enumerate([900, 40, 0]):
+        cuts = [0, *sorted(rng.integers(0, L + 1, size=S - 1).tolist()), L]
+        ranges += [(b, 0, 8, j, cuts[j], cuts[j + 1]) for j in range(S)]
+    ra, rm = oracle.range_partials(inp, ranges, S)
     acc = np.nan_to_num(ra, nan=0.0).astype(np.float32)
     ml = rm.copy()
     ml[..., 0] = np.where(np.isnan(ml[..., 0]), -np.inf, ml[..., 0])
@@ -279,3 +280,44 @@ def test_cuda_graph_replays_are_exact(S):
         assert binding.device_error() == 0
         ref = oracle.decode_contig(qbits, inp["k"], inp["v"], inp["seq_lens"], inp["scale"])
         check_out(host_bits(out), ref, f"graph replay {rep} S={S}")
+
+
+@pytest.mark.parametrize("D,paged", [(128, False), (64, True)])
+def test_batch_at_the_limit_and_past_it(D, paged):
+    """The plan keeps 8 bytes per sequence in shared memory: decode_max_batch
+    sequences run and match the oracle; one more returns DA_ERR_UNSUPPORTED and
+    launches nothing (the output stays untouched)."""
+    from gqa_split_kv_gb300 import binding
+    Bmax = binding.max_batch(8, 2, D, paged=paged)
+    rng = np.random.default_rng(D + paged)
+    lens = rng.integers(0, 33, size=Bmax + 1).astype(np.int32)
+    inp = contig_case(21 + D, Bmax + 1, 8, 2, D, ctx=32, lens=lens)
+    if paged:
+        kp, vp, table = contig_to_paged(inp["k"], inp["v"], inp["seq_lens"], 16, rng, spare_pages=1)
+        inp = dict(q=inp["q"], k_pool=kp, v_pool=vp, page_table=table, seq_lens=inp["seq_lens"], page_size=16,
+                   scale=inp["scale"])
+    cut = {k: (v[:Bmax] if k in ("q", "k", "v", "seq_lens", "page_table") else v) for k, v in inp.items()}
+    ref = oracle.decode_paged(cut["q"], kp, vp, cut["page_table"], cut["seq_lens"], 16, inp["scale"]) if paged \
+        else oracle.decode_contig(cut["q"], cut["k"], cut["v"], cut["seq_lens"], cut["scale"])
+    out, *_ = run(cut, None, max_seq_len=32 if paged else None)
+    check_out(out, ref, f"B={Bmax}")
+    with pytest.raises(binding.DecodeAttnError) as e:
+        run(inp, None, max_seq_len=32 if paged else None)
+    assert e.value.status == 2
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("lens", [[700], [699, 700], [640, 1], [0, 700, 33, 700], [5]])
+def test_small_batches_whose_lengths_differ_from_the_cache(D, lens):
+    """Small contiguous batches start their first tiles from a guess (every sequence
+    max_ctx tokens) before seq_lens is read; the plan then keeps or drains them.
+    Lengths that match the guess, and lengths that do not, against the oracle."""
+    inp = contig_case(31 + D + sum(lens), len(lens), 24, 4, D, ctx=700, lens=lens)
+    ref = oracle.decode_contig(inp["q"], inp["k"], inp["v"], inp["seq_lens"], inp["scale"])
+    d = to_device(inp)
+    for S in (None, 1, 3, 9):
+        out, acc, ml, S_used = run(inp, S, dev_inputs=d)
+        check_out(out, ref, f"D={D} lens={lens} S={S_used}")
+        if S_used >= 2:
+            check_plan_partials(acc, ml, inp, S_used, what=f"D={D} lens={lens}")
+        assert np.array_equal(run(inp, S_used, dev_inputs=d)[0], out)

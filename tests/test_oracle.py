@@ -241,142 +241,94 @@ def test_single_group_is_per_head_attention():
         assert np.array_equal(out[0, h], ref)
 
 
-# ------------------------------------------------------------ split rule
+# ------------------------------------------- partials of arbitrary ranges
+#
+# The pages fix only caps on the split count; any partition of a row's tokens
+# into pieces must merge back to the unsplit result.  These pins cut the token
+# ranges at random places (pieces of any length, empty ones included), so they
+# do not depend on the partition the library happens to use.
 
-def _check_plan(lens, Hkv, G, S, gap=0, per=1):
-    pieces = od.split_pieces(lens, Hkv, G, S, gap, per)
-    ng = -(-len(od.head_groups(G)) // per)
-    by_seg = {}
-    for p in pieces:
-        by_seg.setdefault((p["b"], p["u"]), []).append(p)
+def _random_ranges(rng, lens, rows, S, group=1):
+    """Random partitions of every (sequence, row group) token range into at most S
+    pieces: [(b, row0, nrows, slot, t0, t1)], slots 0.. in token order."""
+    out = []
     for b, L in enumerate(lens):
-        for u in range(Hkv * ng):
-            ps = by_seg.get((b, u), [])
-            if L == 0:
-                assert not ps
-                continue
-            assert 1 <= len(ps) <= S
-            assert [p["piece"] for p in ps] == list(range(len(ps)))
-            assert all(p["npieces"] == len(ps) for p in ps)
-            assert ps[0]["t0"] == 0 and ps[-1]["t1"] == L
-            for a, c in zip(ps, ps[1:]):
-                assert a["t1"] == c["t0"] and a["t1"] % 16 == 0
-            assert all(p["t0"] < p["t1"] for p in ps)
-    return pieces
+        for row0 in range(0, rows, group):
+            n = int(rng.integers(1, S + 1))
+            cuts = np.sort(rng.integers(0, L + 1, size=n - 1)) if L > 0 else np.zeros(n - 1, np.int64)
+            edges = [0, *cuts.tolist(), L]
+            for j in range(n):
+                out.append((b, row0, min(group, rows - row0), j, edges[j], edges[j + 1]))
+    return out
 
 
-def test_split_rule_partitions_every_segment():
-    rng = np.random.default_rng(31)
-    for trial in range(300):
-        B = int(rng.integers(1, 6))
-        lens = rng.integers(0, 300, size=B).tolist()
-        Hkv = int(rng.integers(1, 5))
-        G = int(rng.integers(1, 18))
-        S = int(rng.integers(1, 12))
-        gap = int(rng.choice([0, 1, 6, 12, 24, 48]))
-        per = int(rng.choice([1, 2, 4]))
-        pieces = _check_plan(lens, Hkv, G, S, gap, per)
-        # every row of every KV head is in exactly one slot's group
-        for b, L in enumerate(lens):
-            if L == 0:
-                continue
-            for h in range(Hkv):
-                rows = sorted(r for p in pieces if p["b"] == b and p["h"] == h and p["piece"] == 0
-                              for r in range(p["group"][0], p["group"][0] + p["group"][1]))
-                assert rows == list(range(G))
-        if gap % 4 == 0:  # segments padded to 64-token units: pieces start on 64-token boundaries
-            assert all(p["t0"] % 64 == 0 for p in pieces)
+def _merge_rows(acc, ml, n_of):
+    """Merge slots 0 .. n - 1 of every (b, r) with merge_partials."""
+    B, R, S, D = acc.shape
+    out = np.zeros((B, R, D))
+    for b in range(B):
+        for r in range(R):
+            n = n_of[b, r]
+            parts = [(acc[b, r, j][None], ml[b, r, j, :1], ml[b, r, j, 1:]) for j in range(n)]
+            out[b, r] = od.merge_partials(parts)[0]
+    return out
 
 
-def test_split_rule_matches_block_by_block_brute_force():
-    """Re-derive the pieces by walking every line position (gap or block) through its range."""
-    rng = np.random.default_rng(32)
-    for trial in range(150):
-        B = int(rng.integers(1, 5))
-        lens = rng.integers(0, 200, size=B).tolist()
-        Hkv, G, S = int(rng.integers(1, 4)), int(rng.integers(1, 10)), int(rng.integers(2, 9))
-        gap = int(rng.choice([0, 1, 3, 6, 12, 24]))
-        per = int(rng.choice([1, 2, 4]))
-        ng = -(-(-(-G // 8)) // per)  # passes of `per` sub-groups of <= 8 rows
-        U = Hkv * ng
-        line = []  # one entry per position: None (gap or padding) or (b, u, block index in segment)
-        for u in range(U):
-            for b, L in enumerate(lens):
-                n = -(-L // 16)
-                if n:
-                    line += [None] * gap + [(b, u, i) for i in range(n)] + [None] * (-n % 4)
-        R = (S - 1) * U
-        q = max(4, -(-max(1, -(-len(line) // R)) // 4) * 4)
-        want = {}
-        for x, e in enumerate(line):
-            if e is not None:
-                want.setdefault((e[0], e[1], x // q), []).append(e[2])
-        got = {}
-        for p in od.split_pieces(lens, Hkv, G, S, gap, per):
-            got[(p["b"], p["u"], p["t0"], p["t1"])] = True
-        want_pieces = set()
-        for (b, u, r), blocks in want.items():
-            want_pieces.add((b, u, blocks[0] * 16, min((blocks[-1] + 1) * 16, lens[b])))
-        assert set(got) == want_pieces
+def _slot_counts(ranges, B, R):
+    n = np.zeros((B, R), np.int64)
+    for b, row0, nrows, j, t0, t1 in ranges:
+        n[b, row0:row0 + nrows] = np.maximum(n[b, row0:row0 + nrows], j + 1)
+    return n
 
 
-def test_merge_of_partials_equals_unsplit():
+def test_merge_of_partials_over_any_partition_equals_unsplit():
     rng = np.random.default_rng(33)
-    lens = [5, 130, 64, 1000]
-    inp = _contig_case(rng, 4, 12, 2, 64, ctx=1000, lens=lens)
+    lens = [5, 130, 64, 1000, 0]
+    inp = _contig_case(rng, 5, 12, 2, 64, ctx=1000, lens=lens)
     ref = od.decode_contig(**inp)
-    for S in (1, 2, 3, 5, 17, 39):
-        acc, ml, npc = od.decode_partials(inp, S)
-        assert npc.max() <= S
-        for b in range(4):
-            for h in range(12):
-                n = npc[b, h]
-                parts = [(acc[b, h, j][None], ml[b, h, j, :1], ml[b, h, j, 1:]) for j in range(n)]
-                got = od.merge_partials(parts)[0]
-                assert np.allclose(got, ref[b, h], rtol=0, atol=1e-12), (S, b, h)
+    kp, vp, table = contig_to_paged(inp["k"], inp["v"], inp["seq_lens"], 32, rng, 2)
+    pin = dict(q=inp["q"], k_pool=kp, v_pool=vp, page_table=table, seq_lens=inp["seq_lens"], scale=inp["scale"],
+               page_size=32)
+    for trial, S in enumerate((1, 2, 3, 5, 17, 39)):
+        ranges = _random_ranges(rng, lens, 12, S, group=int(rng.choice([1, 3, 6])))
+        for case in (inp, pin):
+            acc, ml = od.range_partials(case, ranges, S)
+            got = _merge_rows(acc, ml, _slot_counts(ranges, 5, 12))
+            assert np.allclose(got, ref, rtol=0, atol=1e-12), (S, trial)
 
 
-def test_partials_follow_their_definition():
-    """acc / l of one piece is attention over that piece alone; m is the piece's max score."""
+def test_range_partials_follow_their_definition():
+    """acc / l of a range is attention over that range alone; m is its largest
+    score; an empty range gives (0, -inf, 0)."""
     rng = np.random.default_rng(34)
     inp = _contig_case(rng, 1, 4, 1, 32, ctx=200)
-    acc, ml, npc = od.decode_partials(inp, 4)
-    pieces = od.split_pieces([200], 1, 4, 4, od.piece_gap_blocks(32), od.groups_per_pass(4, 32))
+    ranges = [(0, 0, 4, 0, 0, 64), (0, 1, 2, 1, 64, 77), (0, 3, 1, 2, 77, 200), (0, 0, 1, 3, 50, 50)]
+    acc, ml = od.range_partials(inp, ranges, 4)
     qf, kf, vf = (od.widen_bf16(inp[n]) for n in ("q", "k", "v"))
-    for p in pieces:
-        for h in range(4):
-            K, V = kf[0, p["t0"]:p["t1"], 0], vf[0, p["t0"]:p["t1"], 0]
-            s = K @ qf[0, h] * inp["scale"]
-            assert ml[0, h, p["piece"], 0] == s.max()
-            assert np.allclose(acc[0, h, p["piece"]] / ml[0, h, p["piece"], 1],
-                               od.attend(qf[0, h][None], K, V, inp["scale"])[0], atol=1e-13)
+    for b, row0, nrows, j, t0, t1 in ranges:
+        for h in range(row0, row0 + nrows):
+            if t1 == t0:
+                assert ml[0, h, j, 0] == -np.inf and ml[0, h, j, 1] == 0 and np.all(acc[0, h, j] == 0)
+                continue
+            K, V = kf[0, t0:t1, 0], vf[0, t0:t1, 0]
+            sc = K @ qf[0, h] * inp["scale"]
+            assert ml[0, h, j, 0] == sc.max()
+            assert np.allclose(ml[0, h, j, 1], np.exp(sc - sc.max()).sum(), rtol=1e-14)
+            assert np.allclose(acc[0, h, j] / ml[0, h, j, 1], od.attend(qf[0, h][None], K, V, inp["scale"])[0],
+                               atol=1e-13)
+    assert np.isnan(acc[0, 2, 2]).all()  # slot 2 of row 2 was not asked for
 
 
 def test_combine_skips_empty_slots():
     rng = np.random.default_rng(35)
     inp = _contig_case(rng, 2, 4, 1, 32, ctx=300, lens=[300, 40])
-    acc, ml, npc = od.decode_partials(inp, 6)
+    ranges = _random_ranges(rng, [300, 40], 4, 6)
+    acc, ml = od.range_partials(inp, ranges, 6)
     acc = np.nan_to_num(acc, nan=0.0)
     ml[..., 0] = np.where(np.isnan(ml[..., 0]), -np.inf, ml[..., 0])
     ml[..., 1] = np.nan_to_num(ml[..., 1], nan=0.0)
     out = od.combine_partials(acc, ml)
     assert np.allclose(out, od.decode_contig(**inp), rtol=0, atol=1e-12)
-
-
-def test_groups_per_pass():
-    # sub-group counts 1, 1, 2, 2, 3, 3, 6, 8
-    assert [od.groups_per_pass(G, 64) for G in (1, 8, 9, 16, 17, 24, 42, 64)] == [1, 1, 2, 2, 1, 1, 2, 4]
-    assert [od.groups_per_pass(G, 128) for G in (8, 9, 42, 64)] == [1, 2, 2, 2]
-    groups = {p["u"]: p["group"] for p in od.split_pieces([40], 2, 42, 1, 0, 2)}
-    # 42 rows = 6 sub-groups of 7; three passes of 2 sub-groups per KV head
-    assert groups == {0: (0, 14), 1: (14, 14), 2: (28, 14), 3: (0, 14), 4: (14, 14), 5: (28, 14)}
-
-
-def test_groups_larger_than_eight_are_split_evenly():
-    assert od.head_groups(8) == [(0, 8)]
-    assert od.head_groups(12) == [(0, 6), (6, 6)]
-    assert od.head_groups(9) == [(0, 5), (5, 4)]
-    assert od.head_groups(17) == [(0, 6), (6, 6), (12, 5)]
 
 
 # --------------------------------------------------- planted mistakes
@@ -394,7 +346,9 @@ def _pins(monkey_od):
         ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, scale=inp["scale"])[0, :, 0].numpy()
         if not np.allclose(out[b], ref, rtol=0, atol=1e-12):
             return False
-    acc, ml, npc = monkey_od.decode_partials(inp, 40)
+    ranges = _random_ranges(np.random.default_rng(98), [200, 11], 6, 40, group=3)
+    acc, ml = monkey_od.range_partials(inp, ranges, 40)
+    npc = _slot_counts(ranges, 2, 6)
     assert npc.max() >= 2  # the merge must be exercised
     for b in range(2):
         for h in range(6):
@@ -546,23 +500,16 @@ def test_multi_query_edge_lengths():
 
 
 def test_multi_query_merge_of_partials_equals_unsplit():
+    """Rows are (head, query token) pairs, head-major; a row's range is cut at what
+    its query token sees, so pieces past it are empty and merge to nothing."""
     rng = np.random.default_rng(63)
     inp = _multi_case(rng, 3, 4, 1, 32, 6, ctx=400, lens=[400, 5, 130])
-    ref = od.decode_multi(inp)
-    cut = 0
+    ref = od.decode_multi(inp).reshape(3, 24, 32)
     for S in (1, 3, 9, 40):
-        acc, ml, npc = od.decode_multi_partials(inp, S)
-        assert npc.max() <= S
-        cut += int((npc >= 2).sum())
-        for b in range(3):
-            for h in range(4):
-                for i in range(6):
-                    n = npc[b, h, i]
-                    parts = [(acc[b, h, i, j][None], ml[b, h, i, j, :1], ml[b, h, i, j, 1:]) for j in range(n)
-                             if ml[b, h, i, j, 1] > 0]
-                    got = od.merge_partials(parts)[0] if parts else np.zeros(32)
-                    assert np.allclose(got, ref[b, h, i], rtol=0, atol=1e-12), (S, b, h, i)
-    assert cut > 0
+        ranges = _random_ranges(rng, [400, 5, 130], 24, S, group=int(rng.choice([1, 6, 8])))
+        acc, ml = od.range_partials(inp, ranges, S)
+        got = _merge_rows(acc, ml, _slot_counts(ranges, 3, 24))
+        assert np.allclose(got, ref, rtol=0, atol=1e-12), S
 
 
 def test_multi_query_planted_off_by_one_is_caught(monkeypatch):
@@ -635,17 +582,12 @@ def test_int8_brute_force_and_paged():
 def test_int8_merge_of_partials_equals_unsplit():
     inp = _int8_case(73, 3, 8, 2, 64, 600, [600, 70, 0])
     ref = od.decode_int8(inp)
-    cut = 0
+    rng = np.random.default_rng(75)
     for S in (1, 4, 40):
-        acc, ml, npc = od.decode_int8_partials(inp, S)
-        cut += int((npc >= 2).sum())
-        for b in range(3):
-            for h in range(8):
-                n = npc[b, h]
-                parts = [(acc[b, h, j][None], ml[b, h, j, :1], ml[b, h, j, 1:]) for j in range(n)]
-                got = od.merge_partials(parts)[0] if parts else np.zeros(64)
-                assert np.allclose(got, ref[b, h], rtol=0, atol=1e-12)
-    assert cut > 0
+        ranges = _random_ranges(rng, [600, 70, 0], 8, S, group=4)
+        acc, ml = od.range_partials(inp, ranges, S)
+        got = _merge_rows(acc, ml, _slot_counts(ranges, 3, 8))
+        assert np.allclose(got, ref, rtol=0, atol=1e-12), S
 
 
 def test_int8_planted_mistakes_are_caught(monkeypatch):
