@@ -60,6 +60,7 @@ def parse_args():
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--suite", action="store_true", help="also measure every other workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-gates", action="store_true", help="skip the gated configurations (profiling runs)")
     ap.add_argument("--cpu-child", default=None, help=argparse.SUPPRESS)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -67,12 +68,18 @@ def parse_args():
 
 # ------------------------------------------------------------------ helpers
 
-def kernel_source_hash() -> str:
+# The sources each kind of workload runs (the ncu figures in profiles/ are tied to them).
+KERNEL_SOURCES = {
+    "decode": ("decode_attn.cu", "plan.cuh", "ptx.cuh", "split_kernel.cuh", "combine_kernel.cuh"),
+    "prefill": ("prefill_host.cuh", "prefill_kernel.cuh", "ptx.cuh"),
+}
+
+
+def kernel_source_hash(kind: str = "decode") -> str:
     csrc = os.path.join(ROOT, "gqa_split_kv_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in KERNEL_SOURCES[kind]:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -89,7 +96,7 @@ def ncu_traffic(workload: str):
     p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash("prefill" if workload.startswith("prefill_") else "decode")
     for line in open(p):
         parts = line.split()
         if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload and parts[1] == want:
@@ -563,7 +570,7 @@ def ours(args):
     }
     if wl.name in PAGES_US_PER_CALL:
         line["vs_baseline_basis"] = "pages' fa_split_gqa_kernel 1.11 ms/call on RTX 5090, same workload (µs ratio)"
-    if wl.name == HEADLINE and rank == 0:
+    if wl.name == HEADLINE and rank == 0 and not args.no_gates:
         line["gates"] = measure_gates(peaks, flush_bytes, max(20, min(args.steps, 200)), max(3, args.warmup))
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = run_cpu_baseline(wl.name, args.cpu_seconds)

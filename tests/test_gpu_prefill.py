@@ -126,3 +126,19 @@ def test_prefill_bad_page_entry_is_flagged():
     got = bf16_bits_to_f32(host_bits(out)[1]).astype(np.float64).reshape(-1, 64)
     err = np.abs(got - ref)
     assert np.all(err <= OUT_ATOL + OUT_RTOL * np.abs(ref))
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_prefill_ignores_cache_rows_past_the_sequence(D):
+    """Cache rows at or past a sequence's length may hold anything, NaN included:
+    they are masked out of the scores and their V rows never reach the output."""
+    lens = [300, 129, 64]
+    inp = prefill_case(8 + D, 3, 64, 16, 4, D, 384, lens)
+    ref = oracle.prefill(inp)
+    for b, L in enumerate(lens):
+        inp["k"][b, L:] = 0x7FC0  # bf16 quiet NaN
+        inp["v"][b, L:] = 0x7FC0
+    check(run_prefill(inp), ref, f"NaN past the sequence, D={D}")
+    kp, vp, table = contig_to_paged(inp["k"], inp["v"], np.full(3, 384, np.int32), 32, np.random.default_rng(D))
+    paged = dict(inp, k_pool=kp, v_pool=vp, page_table=table, page_size=32)
+    check(run_prefill(paged, max_seq_len=384), ref, f"paged, NaN past the sequence, D={D}")
