@@ -71,7 +71,7 @@ def parse_args():
 # The sources each kind of workload runs (the ncu figures in profiles/ are tied to them).
 KERNEL_SOURCES = {
     "decode": ("decode_attn.cu", "plan.cuh", "ptx.cuh", "split_kernel.cuh", "combine_kernel.cuh"),
-    "prefill": ("prefill_host.cuh", "prefill_kernel.cuh", "ptx.cuh"),
+    "prefill": ("prefill_host.cuh", "prefill_kernel.cuh", "prefill_tc.cuh", "tc05.cuh", "ptx.cuh"),
 }
 
 
@@ -334,7 +334,7 @@ def measure(wl, inp, steps: int, warmup: int, flush_bytes: int, dist=None, sampl
     tb = traffic_bytes(wl.B, wl.Hq, wl.Hkv, wl.D, inp["seq_lens"], S, wl.page_size if paged else None, wl.q_len,
                        wl.kv_dtype)
     # the split kernel, plus the combine kernel when a segment can have more than 56 pieces
-    res = {"S": S, "times_ms": times, "bytes": tb, "clocks": clocks, "launches_per_step": 1 if S <= 56 else 2}
+    res = {"S": S, "times_ms": times, "bytes": tb, "clocks": clocks, "launches_per_step": 1 if S <= 8 else 2}
 
     if e2e_steps > 0:
         # end to end through the public call: pinned host inputs -> device, call, output -> host
@@ -469,7 +469,8 @@ def prefill_line(wl, r, ws, K, W, total_ms, e2e_ms, peaks) -> dict:
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "us_per_call": {"mean": round(1e3 * total_ms / K, 3), "median": round(1e3 * per[len(per) // 2], 3)},
         "work_per_call": r["work"],
-        "roofline": {"bound": "tensor", "kernel": "prefill_kernel (mma.sync bf16), events around the call",
+        "roofline": {"bound": "tensor", "kernel": ("prefill_kernel (mma.sync bf16)" if wl.D == 32 else
+                                                   "prefill_tc_kernel (tcgen05 bf16)") + ", events around the call",
                      "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(achieved / peaks["bf16_tflops"], 4),
                      "peak_source": f"{peaks['source']} cuBLAS bf16 burst", "traffic": ncu_traffic(wl.name)},
@@ -559,7 +560,7 @@ def ours(args):
         "us_per_call": {"mean": round(1e3 * total_ms / K, 3), "median": round(us_med, 3),
                         "p10": round(1e3 * per[len(per) // 10], 3), "p90": round(1e3 * per[9 * len(per) // 10], 3)},
         "bytes_per_call": r["bytes"],
-        "roofline": {"bound": "hbm", "kernel": "split_kernel (+ combine_kernel when S > 56), events around the call",
+        "roofline": {"bound": "hbm", "kernel": "split_kernel (+ combine_kernel when S > 8), events around the call",
                      "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
                      "traffic": ncu_traffic(wl.name)},

@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             tc_mma_ts(tmem + Gm::TCOL_O, aP + 8 * kk,
-                      tc_sdesc(vst + kk * 16 * 128, BK * 128, 1024, kTcSwizzle128B), id_o, j > 0);
+                      tc_sdesc(vst + kk * 16 * 128, BK * 128, 1024, kTcSwizzle128B), id_o, j > 0 || kk > 0);
           tc_commit(bar(Gm::BAR_O + (j & 1)));
           tc_commit(bar(Gm::BAR_KV_EMPTY + st));
         }
