@@ -21,8 +21,8 @@
 // O and cancels in O / l.  While the softmax works on tile j the tensor cores
 // compute S for tile j + 1 into the other buffer.
 //
-// Warp roles: warp 0 one lane issues the K/V tile copies (TMA) into a ring of
-// STAGES stages; warp 1 allocates tensor memory and one lane issues every MMA and
+// Warp roles: warp 0 one lane issues the K and V tile copies (TMA) into two rings
+// (K of tile j + 1 can land while tile j's P V still holds its V); warp 1 allocates tensor memory and one lane issues every MMA and
 // commits it to an mbarrier; warps 4-7 run the softmax and the epilogue; all
 // warps stage the query rows first.  Every wait is bounded: after the limit the
 // kernel sets the device error word, lets the work it issued finish, frees its
@@ -41,17 +41,22 @@ struct PrefillTcGeo {
   static constexpr int M = 128;                      // query rows per CTA (tensor memory lanes)
   static constexpr int BK = D == 256 ? 64 : 128;     // keys per tile (N of Q K^T)
   static constexpr int NSUB = D / 64;                // 64-element swizzle columns
-  static constexpr int STAGES = D == 64 ? 4 : 2;
+  // K and V have rings of their own: a K stage frees once its Q K^T is done, a V
+  // stage once its P V is
+  static constexpr int KST = D == 64 ? 4 : 3;
+  static constexpr int VST = D == 64 ? 4 : D == 128 ? 3 : 2;
   static constexpr int KV_BYTES = BK * D * 2;        // one tensor, one stage: [NSUB][BK][64]
   static constexpr int Q_BYTES = M * D * 2;          // [NSUB][M][64]
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
-  // barriers: kv_full[STAGES], kv_empty[STAGES], s_full[2], p_full[2], o_done[2]
-  // (P V of even / odd tiles, so every wait knows its phase), fin (the last MMA)
-  static constexpr int BAR_KV_FULL = 0, BAR_KV_EMPTY = STAGES, BAR_S = 2 * STAGES, BAR_P = 2 * STAGES + 2,
-                       BAR_O = 2 * STAGES + 4, BAR_FIN = 2 * STAGES + 6, NBAR = 2 * STAGES + 7;
+  static constexpr int OFF_V = OFF_K + KST * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_V + VST * KV_BYTES;
+  // barriers: k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], s_full[2],
+  // p_full[2], o_done[2] (P V of even / odd tiles, so every wait knows its phase),
+  // fin (the last MMA)
+  static constexpr int BAR_K_FULL = 0, BAR_K_EMPTY = KST, BAR_V_FULL = 2 * KST, BAR_V_EMPTY = 2 * KST + VST,
+                       BAR_S = 2 * KST + 2 * VST, BAR_P = BAR_S + 2, BAR_O = BAR_S + 4, BAR_FIN = BAR_S + 6,
+                       NBAR = BAR_S + 7;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] tensor memory base, [1] abort flag
   static constexpr int SMEM = OFF_MISC + 16 + 1024;    // + alignment slack
   static constexpr int TCOL_S0 = 0, TCOL_S1 = BK, TCOL_O = 2 * BK;
@@ -101,9 +106,13 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
   const int nrows = nq * p.G;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < Gm::STAGES; ++i) {
-      mbar_init(bar(Gm::BAR_KV_FULL + i), 1);
-      mbar_init(bar(Gm::BAR_KV_EMPTY + i), 1);
+    for (int i = 0; i < Gm::KST; ++i) {
+      mbar_init(bar(Gm::BAR_K_FULL + i), 1);
+      mbar_init(bar(Gm::BAR_K_EMPTY + i), 1);
+    }
+    for (int i = 0; i < Gm::VST; ++i) {
+      mbar_init(bar(Gm::BAR_V_FULL + i), 1);
+      mbar_init(bar(Gm::BAR_V_EMPTY + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(Gm::BAR_S + i), 1);
@@ -140,27 +149,21 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ---- producer: tile j of K and V into stage j % STAGES once it is free
-    int issued = 0;
+    // ---- producer: K of tile j, then V of tile j - 1 (the order the tensor cores
+    // free their stages in), each once its stage is free
+    int k_issued = 0, v_issued = 0;
     if (lane == 0) {
-      for (int j = 0; j < ntiles; ++j) {
-        const int st = j % Gm::STAGES;
-        if (j >= Gm::STAGES &&
-            !tc_wait(bar(Gm::BAR_KV_EMPTY + st), (uint32_t)(((j / Gm::STAGES) & 1) ^ 1), abort_flag, p.timeout_ns))
-          break;
+      // one tensor's tile j into dst, counted on the mbarrier full
+      auto load = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int j) {
         const int t = j * BK;
-        const uint32_t full = bar(Gm::BAR_KV_FULL + st);
-        const uint32_t kdst = sbase + Gm::OFF_K + st * Gm::KV_BYTES;
-        const uint32_t vdst = sbase + Gm::OFF_V + st * Gm::KV_BYTES;
         if (!PAGED) {
-          mbar_arrive_expect_tx(full, 2u * Gm::KV_BYTES);
-          tma_load_5d(kdst, &p.tm_k, full, 0, t, 0, h, b);  // box [64][BK][NSUB]
-          tma_load_5d(vdst, &p.tm_v, full, 0, t, 0, h, b);
+          mbar_arrive_expect_tx(full, (uint32_t)Gm::KV_BYTES);
+          tma_load_5d(dst, map, full, 0, t, 0, h, b);  // box [64][BK][NSUB]
         } else {
           // boxes of R rows of one page and one swizzle column: [NSUB][BK][64]
           const int R = 16 << p.box_shift;
           const int nbox = (min(BK, kv_end - t) + R - 1) / R;
-          mbar_arrive_expect_tx(full, (uint32_t)(2 * nbox * R * 128 * Gm::NSUB));
+          mbar_arrive_expect_tx(full, (uint32_t)(nbox * R * 128 * Gm::NSUB));
           for (int bx = 0; bx < nbox; ++bx) {
             const int tok = t + bx * R;
             const int col = p.page_shift >= 0 ? tok >> p.page_shift : tok / p.page_size;
@@ -170,31 +173,56 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
               page = 0;
             }
             const int row0 = tok - col * p.page_size;
-            for (int sub = 0; sub < Gm::NSUB; ++sub) {
-              const uint32_t off = (uint32_t)(sub * BK * 128 + bx * R * 128);
-              tma_load_5d(kdst + off, &p.tm_k, full, 0, row0, sub, h, page);
-              tma_load_5d(vdst + off, &p.tm_v, full, 0, row0, sub, h, page);
-            }
+#pragma unroll
+            for (int sub = 0; sub < Gm::NSUB; ++sub)
+              tma_load_5d(dst + (uint32_t)(sub * BK * 128 + bx * R * 128), map, full, 0, row0, sub, h, page);
           }
         }
-        ++issued;
+      };
+      for (int j = 0; j <= ntiles; ++j) {
+        if (j < ntiles) {
+          const int st = j % Gm::KST;
+          if (j >= Gm::KST &&
+              !tc_wait(bar(Gm::BAR_K_EMPTY + st), (uint32_t)(((j / Gm::KST) & 1) ^ 1), abort_flag, p.timeout_ns))
+            break;
+          load(&p.tm_k, sbase + Gm::OFF_K + st * Gm::KV_BYTES, bar(Gm::BAR_K_FULL + st), j);
+          ++k_issued;
+        }
+        if (j >= 1) {
+          const int jv = j - 1, st = jv % Gm::VST;
+          if (jv >= Gm::VST &&
+              !tc_wait(bar(Gm::BAR_V_EMPTY + st), (uint32_t)(((jv / Gm::VST) & 1) ^ 1), abort_flag, p.timeout_ns))
+            break;
+          load(&p.tm_v, sbase + Gm::OFF_V + st * Gm::KV_BYTES, bar(Gm::BAR_V_FULL + st), jv);
+          ++v_issued;
+        }
       }
       // after an abort, let the copies already issued land before the CTA exits
       if (*abort_flag) {
-        for (int k = issued > Gm::STAGES ? issued - Gm::STAGES : 0; k < issued; ++k) {
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(bar(Gm::BAR_KV_FULL + k % Gm::STAGES), (uint32_t)((k / Gm::STAGES) & 1)) &&
-                 globaltimer_ns() - t0 < p.timeout_ns) {
+        auto drain = [&](int base_bar, int nst, int issued) {
+          for (int k = issued > nst ? issued - nst : 0; k < issued; ++k) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(bar(base_bar + k % nst), (uint32_t)((k / nst) & 1)) &&
+                   globaltimer_ns() - t0 < p.timeout_ns) {
+            }
           }
-        }
+        };
+        drain(Gm::BAR_K_FULL, Gm::KST, k_issued);
+        drain(Gm::BAR_V_FULL, Gm::VST, v_issued);
       }
     }
   } else if (warp == 1) {
     // ---- MMA issue (lane 0); the warp zeroes V rows past the keys of the last tile
     const uint32_t id_s = tc_idesc_bf16(Gm::M, BK, false, false);
     const uint32_t id_o = tc_idesc_bf16(Gm::M, D, false, true);
-    auto issue_qk = [&](int j) {  // S[j & 1] = Q K_j^T over D in steps of 16
-      const int st = j % Gm::STAGES;
+    // the whole warp waits (the tail zeroing writes what the copy wrote)
+    auto wait_all = [&](uint32_t b_, uint32_t par) {
+      const bool w = tc_wait(b_, par, abort_flag, p.timeout_ns);
+      return __all_sync(0xffffffffu, w);
+    };
+    // S[j & 1] = Q K_j^T over D in steps of 16; the K stage frees when it is done
+    auto issue_qk = [&](int j) {
+      const int st = j % Gm::KST;
       const uint32_t kst = sbase + Gm::OFF_K + st * Gm::KV_BYTES;
       const uint32_t dS = tmem + (j & 1 ? Gm::TCOL_S1 : Gm::TCOL_S0);
 #pragma unroll
@@ -205,64 +233,61 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
                   tc_sdesc(kst + ko, 16, 1024, kTcSwizzle128B), id_s, kk > 0);
       }
       tc_commit(bar(Gm::BAR_S + (j & 1)));
+      tc_commit(bar(Gm::BAR_K_EMPTY + st));
     };
     int done_o = -1;  // last tile whose P V was issued
-    bool ok = true;
-    if (ntiles > 0) {
-      if (lane == 0) {
-        ok = tc_wait(bar(Gm::BAR_KV_FULL), 0, abort_flag, p.timeout_ns);
-        if (ok) {
+    bool ok = ntiles > 0 && wait_all(bar(Gm::BAR_K_FULL), 0);
+    if (ok && lane == 0) {
+      tc_fence_after();
+      issue_qk(0);
+    }
+    for (int j = 0; j < ntiles && ok; ++j) {
+      // Q K^T of the next tile goes ahead of this tile's P V, so the softmax of
+      // tile j + 1 can start as soon as that of tile j ends
+      if (j + 1 < ntiles) {
+        const int st1 = (j + 1) % Gm::KST;
+        ok = wait_all(bar(Gm::BAR_K_FULL + st1), (uint32_t)(((j + 1) / Gm::KST) & 1));
+        if (!ok) break;
+        if (lane == 0) {
           tc_fence_after();
-          issue_qk(0);
+          issue_qk(j + 1);
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      for (int j = 0; j < ntiles && ok; ++j) {
-        const int st = j % Gm::STAGES;
-        if (lane == 0) {
-          if (j + 1 < ntiles) {
-            const int st1 = (j + 1) % Gm::STAGES;
-            ok = tc_wait(bar(Gm::BAR_KV_FULL + st1), (uint32_t)(((j + 1) / Gm::STAGES) & 1), abort_flag, p.timeout_ns);
-            if (ok) {
-              tc_fence_after();
-              issue_qk(j + 1);
-            }
-          }
-          if (ok) ok = tc_wait(bar(Gm::BAR_P + (j & 1)), (uint32_t)((j >> 1) & 1), abort_flag, p.timeout_ns);
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        const int t = j * BK;
-        const uint32_t vst = sbase + Gm::OFF_V + st * Gm::KV_BYTES;
-        if (t + BK > kv_end) {
-          // V rows at or past kv_end may hold anything (0 * NaN would poison O): zero them
-          const int r0 = kv_end - t;
-          for (int e = r0 * 8 + lane; e < BK * 8; e += 32) {
-            const int r = e / 8, ch = e % 8;
+      const int st = j % Gm::VST;
+      ok = wait_all(bar(Gm::BAR_V_FULL + st), (uint32_t)((j / Gm::VST) & 1));
+      if (!ok) break;
+      const int t = j * BK;
+      const uint32_t vst = sbase + Gm::OFF_V + st * Gm::KV_BYTES;
+      if (t + BK > kv_end) {
+        // V rows at or past kv_end may hold anything (0 * NaN would poison O): zero them
+        const int r0 = kv_end - t;
+        for (int e = r0 * 8 + lane; e < BK * 8; e += 32) {
+          const int r = e / 8, ch = e % 8;
 #pragma unroll
-            for (int sub = 0; sub < Gm::NSUB; ++sub)
-              *reinterpret_cast<uint4*>(smem + Gm::OFF_V + st * Gm::KV_BYTES + sub * (BK * 128) + swz<128>(r, ch)) =
-                  make_uint4(0u, 0u, 0u, 0u);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
+          for (int sub = 0; sub < Gm::NSUB; ++sub)
+            *reinterpret_cast<uint4*>(smem + Gm::OFF_V + st * Gm::KV_BYTES + sub * (BK * 128) + swz<128>(r, ch)) =
+                make_uint4(0u, 0u, 0u, 0u);
         }
-        if (lane == 0) {
-          tc_fence_after();
-          const uint32_t aP = tmem + (j & 1 ? Gm::TCOL_S1 : Gm::TCOL_S0);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            tc_mma_ts(tmem + Gm::TCOL_O, aP + 8 * kk,
-                      tc_sdesc(vst + kk * 16 * 128, BK * 128, 1024, kTcSwizzle128B), id_o, j > 0 || kk > 0);
-          tc_commit(bar(Gm::BAR_O + (j & 1)));
-          tc_commit(bar(Gm::BAR_KV_EMPTY + st));
-        }
-        done_o = j;
+        fence_proxy_async_smem();
         __syncwarp();
       }
+      ok = wait_all(bar(Gm::BAR_P + (j & 1)), (uint32_t)((j >> 1) & 1));
+      if (!ok) break;
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t aP = tmem + (j & 1 ? Gm::TCOL_S1 : Gm::TCOL_S0);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          tc_mma_ts(tmem + Gm::TCOL_O, aP + 8 * kk, tc_sdesc(vst + kk * 16 * 128, BK * 128, 1024, kTcSwizzle128B),
+                    id_o, j > 0 || kk > 0);
+        tc_commit(bar(Gm::BAR_O + (j & 1)));
+        tc_commit(bar(Gm::BAR_V_EMPTY + st));
+      }
+      done_o = j;
+      __syncwarp();
     }
     // before the tensor memory is freed, every MMA issued must have completed
-    if (lane == 0 && done_o >= 0) {
+    if (lane == 0 && (done_o >= 0 || ntiles > 0)) {
       tc_commit(bar(Gm::BAR_FIN));
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(bar(Gm::BAR_FIN), 0) && globaltimer_ns() - t0 < p.timeout_ns) {
