@@ -125,6 +125,13 @@ class ClockSampler:
                  "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+        # the tool's start-up stalls the GPU for up to seconds: let it reach its
+        # first sample before the timed region begins
+        t0 = time.time()
+        while self.proc is not None and time.time() - t0 < 15.0 and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.05)
         time.sleep(0.15)
 
     def stop(self) -> dict:

@@ -43,7 +43,8 @@ template <int D, bool PAGED>
 int launch_prefill_tc(const PrefillParams& prm, unsigned grid, int dev, cudaStream_t st) {
   static bool attr_done[kMaxDevices] = {false};
   auto kern = prefill_tc_kernel<D, PAGED>;
-  const int smem = PrefillTcGeo<D>::SMEM;
+  using Gm = PrefillTcGeo<D>;
+  const int smem = Gm::SMEM;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!attr_done[dev]) {
@@ -52,6 +53,17 @@ int launch_prefill_tc(const PrefillParams& prm, unsigned grid, int dev, cudaStre
                                cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
         cudaGetLastError();
         return DA_ERR_UNSUPPORTED;
+      }
+      if (Gm::NQT == 2) {
+        // the softmax warpgroups raise their registers (setmaxnreg.inc) out of what
+        // the launch gave the CTA; a build whose per-thread count is below the
+        // split would wait there for ever, so it is refused instead
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) {
+          cudaGetLastError();
+          return DA_ERR_CUDA;
+        }
+        if (fa.numRegs * Gm::NTHREADS < Gm::REG_POOL_NEEDED) return DA_ERR_UNSUPPORTED;
       }
       attr_done[dev] = true;
     }
@@ -73,6 +85,9 @@ int launch_prefill_tc(const PrefillParams& prm, unsigned grid, int dev, cudaStre
 int tc_tile_keys(int D) {
   return D == 64 ? PrefillTcGeo<64>::BK : D == 128 ? PrefillTcGeo<128>::BK : D == 256 ? PrefillTcGeo<256>::BK : 0;
 }
+int tc_query_tiles(int D) {
+  return D == 64 ? PrefillTcGeo<64>::NQT : D == 128 ? PrefillTcGeo<128>::NQT : PrefillTcGeo<256>::NQT;
+}
 
 // Shared by the contiguous and paged calls.  max_len: lengths are clamped to it
 // (max_ctx, or min(max_pages * page_size, max_seq_len)).
@@ -87,8 +102,9 @@ int prefill_call(bool paged, const void* q, const void* k, const void* v, const 
   if (B == 0 || q_len == 0) return DA_OK;
   if (!q || !out || !aligned(q, 16) || !aligned(out, 16)) return DA_ERR_INVALID_ARG;
   const int tcbk = tc_tile_keys(D);
-  const int rows = tcbk ? PrefillTcGeo<128>::M : PrefillGeo<32>::ROWS;  // query rows per CTA
-  const int BQ = rows / G;  // query tokens per CTA
+  // query tokens per CTA: a whole number of tokens per 128-row query tile (the
+  // tensor-core kernel has one or two such tiles), or per the warp-MMA kernel's rows
+  const int BQ = tcbk ? tc_query_tiles(D) * (PrefillTcGeo<128>::M / G) : PrefillGeo<32>::ROWS / G;
   const long long nqb = (q_len + BQ - 1) / BQ;
   if (nqb * B * Hkv > 0x7fffffffLL) return DA_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -6,27 +6,40 @@
 // token i of a chunk of q_len (position L - q_len + i) attends to cached
 // positions 0 .. L - q_len + i.  Only the engine differs.
 //
-// One CTA owns 128 query rows: a block of BQ = 128 / G query tokens x the G query
-// heads of one KV head (token-major, as prefill_kernel).  The rows live in the
-// 128 lanes of tensor memory:
+// A CTA owns NQT query tiles of 128 rows (NQT = 2 up to head_dim 128, 1 at 256).
+// A tile is a block of 128 / G query tokens x the G query heads of one KV head
+// (token-major, as prefill_kernel), and its rows live in the 128 lanes of tensor
+// memory:
 //   S = Q K^T   tcgen05.mma, Q and the K tile K-major in shared memory (128-byte
-//               swizzle), fp32 into one of two S buffers of BK columns;
-//   softmax     one thread per row (warps 4-7, TMEM lane = row) loads its row of S,
-//               masks, and writes P = exp2(s - m) as bf16 pairs over the first
-//               BK / 2 columns of the same S buffer;
+//               swizzle), fp32 into an S buffer of BK columns;
+//   softmax     one thread per row (TMEM lane = row) loads its row of S, masks,
+//               and writes P = exp2(s - m) as bf16 pairs over the first BK / 2
+//               columns of the same S buffer;
 //   O += P V    tcgen05.mma with P from tensor memory and the V tile MN-major in
 //               shared memory, fp32 into D columns of tensor memory.
 // The running maximum m is only raised (and O, l rescaled) when a row's maximum
 // grows by more than 8 in log2 units; otherwise the stale m stays in both l and
-// O and cancels in O / l.  While the softmax works on tile j the tensor cores
-// compute S for tile j + 1 into the other buffer.
+// O and cancels in O / l.
+//
+// Overlap.  With two query tiles (A, B) each has one S buffer and its own
+// softmax warpgroup, and the tensor cores alternate between them: while the
+// softmax of A works on key tile j + 1, the tensor cores run P_B V_j and
+// S_B = Q_B K_{j+1}^T, and the other way round.  Tensor memory: S_A, S_B (BK
+// columns each), O_A, O_B (D each), 512 columns at D = 128.  With one query tile
+// (head_dim 256: two O of 256 columns would not fit) S is double-buffered
+// instead and S of tile j + 1 is computed while the softmax works on tile j.
+// The MMAs of one thread run in issue order, so an S buffer can be overwritten
+// by the next Q K^T as soon as the P V that reads its P has been issued.
 //
 // Warp roles: warp 0 one lane issues the K and V tile copies (TMA) into two rings
-// (K of tile j + 1 can land while tile j's P V still holds its V); warp 1 allocates tensor memory and one lane issues every MMA and
-// commits it to an mbarrier; warps 4-7 run the softmax and the epilogue; all
-// warps stage the query rows first.  Every wait is bounded: after the limit the
-// kernel sets the device error word, lets the work it issued finish, frees its
-// tensor memory and exits.
+// (K of tile j + 1 can land while tile j's P V still holds its V); warp 1
+// allocates tensor memory and one lane issues every MMA and commits it to an
+// mbarrier; the last NQT warpgroups run the softmax and the epilogue, one query
+// tile each; all warps stage the query rows first.  With two query tiles the
+// first warpgroup gives registers up (setmaxnreg) to the softmax warpgroups; the
+// host launches that form only when the kernel's register budget covers the
+// split.  Every wait is bounded: after the limit the kernel sets the device error
+// word, lets the work it issued finish, frees its tensor memory and exits.
 #pragma once
 
 #include <cstdint>
@@ -38,32 +51,43 @@ namespace da {
 
 template <int D>
 struct PrefillTcGeo {
-  static constexpr int M = 128;                      // query rows per CTA (tensor memory lanes)
-  static constexpr int BK = D == 256 ? 64 : 128;     // keys per tile (N of Q K^T)
-  static constexpr int NSUB = D / 64;                // 64-element swizzle columns
+  static constexpr int NQT = D <= 128 ? 2 : 1;     // query tiles per CTA
+  static constexpr int M = 128;                    // rows per query tile (tensor memory lanes)
+  static constexpr int ROWS = NQT * M;             // query rows per CTA
+  static constexpr int BK = D == 256 ? 64 : 128;   // keys per tile (N of Q K^T)
+  static constexpr int NSUB = D / 64;              // 64-element swizzle columns
   // K and V have rings of their own: a K stage frees once its Q K^T is done, a V
   // stage once its P V is
   static constexpr int KST = D == 64 ? 4 : 3;
-  static constexpr int VST = D == 64 ? 4 : D == 128 ? 3 : 2;
-  static constexpr int KV_BYTES = BK * D * 2;        // one tensor, one stage: [NSUB][BK][64]
-  static constexpr int Q_BYTES = M * D * 2;          // [NSUB][M][64]
+  static constexpr int VST = D == 64 ? 4 : 2;
+  static constexpr int KV_BYTES = BK * D * 2;      // one tensor, one stage: [NSUB][BK][64]
+  static constexpr int QT_BYTES = M * D * 2;       // one query tile: [NSUB][M][64]
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_K = OFF_Q + NQT * QT_BYTES;
   static constexpr int OFF_V = OFF_K + KST * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + VST * KV_BYTES;
-  // barriers: k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], s_full[2],
-  // p_full[2], o_done[2] (P V of even / odd tiles, so every wait knows its phase),
-  // fin (the last MMA)
+  // barriers: k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], then s[2],
+  // p[2], o[2] (two query tiles: one each per tile, o completing once after the
+  // last P V; one query tile: by key-tile parity), fin (the last MMA)
   static constexpr int BAR_K_FULL = 0, BAR_K_EMPTY = KST, BAR_V_FULL = 2 * KST, BAR_V_EMPTY = 2 * KST + VST,
                        BAR_S = 2 * KST + 2 * VST, BAR_P = BAR_S + 2, BAR_O = BAR_S + 4, BAR_FIN = BAR_S + 6,
                        NBAR = BAR_S + 7;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] tensor memory base, [1] abort flag
   static constexpr int SMEM = OFF_MISC + 16 + 1024;    // + alignment slack
-  static constexpr int TCOL_S0 = 0, TCOL_S1 = BK, TCOL_O = 2 * BK;
-  static constexpr uint32_t TMEM_COLS = 2 * BK + D <= 256 ? 256u : 512u;
-  static constexpr int NTHREADS = 256;
+  // tensor memory columns: S buffer i at i * BK (two of them either way), O of
+  // query tile t at 2 * BK + t * D
+  static constexpr int TCOL_O = 2 * BK;
+  static constexpr int TCOLS_USED = 2 * BK + NQT * D;
+  static constexpr uint32_t TMEM_COLS = TCOLS_USED <= 256 ? 256u : 512u;
+  static constexpr int NTHREADS = 128 * (1 + NQT);
+  // registers per thread after the split (two query tiles): the first warpgroup
+  // (producer, MMA issue, two idle warps) drops to REG_LOW, the softmax
+  // warpgroups rise to REG_HIGH; the launch must provide
+  // 128 * REG_LOW + 256 * REG_HIGH registers
+  static constexpr int REG_LOW = 56, REG_HIGH = 216;
+  static constexpr int REG_POOL_NEEDED = 128 * REG_LOW + 256 * REG_HIGH;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
-  static_assert(2 * BK + D <= 512, "tensor memory budget");
+  static_assert(TCOLS_USED <= 512, "tensor memory budget");
 };
 
 __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -71,10 +95,21 @@ __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, volatile 
   return wait_bounded(bar, parity, abort_flag, timeout_ns);
 }
 
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 template <int D, bool PAGED>
-__global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
+    prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
   using Gm = PrefillTcGeo<D>;
   constexpr int BK = Gm::BK;
+  constexpr int NQT = Gm::NQT;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
@@ -97,13 +132,12 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
   const int b = bh / p.Hkv, h = bh % p.Hkv;
   int L = p.seq_lens ? __ldg(p.seq_lens + b) : p.max_len;
   L = L < 0 ? 0 : (L > p.max_len ? p.max_len : L);
+  const int BQT = p.BQ / NQT;  // query tokens per query tile
   const int q0 = qb * p.BQ;
   const int nq = min(p.BQ, p.q_len - q0);
   const int base = L - p.q_len;  // position of query token 0
-  const int kv_end = max(0, min(L, base + q0 + nq));   // keys some row sees
-  const int lim_first = max(0, min(L, base + q0 + 1)); // keys every row sees
+  const int kv_end = max(0, min(L, base + q0 + nq));  // keys some row sees
   const int ntiles = (kv_end + BK - 1) / BK;
-  const int nrows = nq * p.G;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < Gm::KST; ++i) {
@@ -131,16 +165,20 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
     tmem_alloc(sbase + Gm::OFF_MISC, Gm::TMEM_COLS);
     tmem_relinquish();
   }
-  // query rows: row r = (token r / G, head r % G) of the block, zero past it;
-  // [NSUB][M][64] with the 128-byte swizzle (the K-major layout the MMA reads)
-  for (int e = threadIdx.x; e < Gm::M * (D / 8); e += Gm::NTHREADS) {
-    const int r = e / (D / 8), ch = e % (D / 8);
+  // query rows: row r of tile t = (token t * BQT + r / G, head r % G) of the block,
+  // zero past it; [NSUB][M][64] per tile with the 128-byte swizzle (the K-major
+  // layout the MMA reads)
+  for (int e = threadIdx.x; e < Gm::ROWS * (D / 8); e += Gm::NTHREADS) {
+    const int rr = e / (D / 8), ch = e % (D / 8);
+    const int t = rr / Gm::M, r = rr % Gm::M;
+    const int tok = t * BQT + r / p.G;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (r < nrows) {
-      const int i = q0 + r / p.G, hq = h * p.G + r % p.G;
+    if (r < BQT * p.G && tok < nq) {
+      const int i = q0 + tok, hq = h * p.G + r % p.G;
       v = __ldg(reinterpret_cast<const uint4*>(p.q + (((size_t)b * p.q_len + i) * p.Hq + hq) * D) + ch);
     }
-    *reinterpret_cast<uint4*>(smem + Gm::OFF_Q + (ch / 8) * (Gm::M * 128) + swz<128>(r, ch % 8)) = v;
+    *reinterpret_cast<uint4*>(smem + Gm::OFF_Q + t * Gm::QT_BYTES + (ch / 8) * (Gm::M * 128) + swz<128>(r, ch % 8)) =
+        v;
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -148,247 +186,312 @@ __global__ void __launch_bounds__(256, 1) prefill_tc_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ---- producer: K of tile j, then V of tile j - 1 (the order the tensor cores
-    // free their stages in), each once its stage is free
-    int k_issued = 0, v_issued = 0;
-    if (lane == 0) {
-      // one tensor's tile j into dst, counted on the mbarrier full
-      auto load = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int j) {
-        const int t = j * BK;
-        if (!PAGED) {
-          mbar_arrive_expect_tx(full, (uint32_t)Gm::KV_BYTES);
-          tma_load_5d(dst, map, full, 0, t, 0, h, b);  // box [64][BK][NSUB]
-        } else {
-          // boxes of R rows of one page and one swizzle column: [NSUB][BK][64]
-          const int R = 16 << p.box_shift;
-          const int nbox = (min(BK, kv_end - t) + R - 1) / R;
-          mbar_arrive_expect_tx(full, (uint32_t)(nbox * R * 128 * Gm::NSUB));
-          for (int bx = 0; bx < nbox; ++bx) {
-            const int tok = t + bx * R;
-            const int col = p.page_shift >= 0 ? tok >> p.page_shift : tok / p.page_size;
-            int page = __ldg(p.page_table + (size_t)b * p.max_pages + col);
-            if ((unsigned)page >= (unsigned)p.num_pages) {  // a bad entry: flag it, read page 0 instead
-              atomicOr(&g_error_word, 4u);
-              page = 0;
-            }
-            const int row0 = tok - col * p.page_size;
+  if (warp < 4) {
+    // ---- first warpgroup: every warp gives registers up at the same instruction
+    if constexpr (NQT == 2) setmaxnreg_dec<Gm::REG_LOW>();
+    if (warp == 0) {
+      // ---- producer: K of tile j, then V of tile j - 1 (the order the tensor cores
+      // free their stages in), each once its stage is free
+      int k_issued = 0, v_issued = 0;
+      if (lane == 0) {
+        // one tensor's tile j into dst, counted on the mbarrier full
+        auto load = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int j) {
+          const int t = j * BK;
+          if (!PAGED) {
+            mbar_arrive_expect_tx(full, (uint32_t)Gm::KV_BYTES);
+            tma_load_5d(dst, map, full, 0, t, 0, h, b);  // box [64][BK][NSUB]
+          } else {
+            // boxes of R rows of one page and one swizzle column: [NSUB][BK][64]
+            const int R = 16 << p.box_shift;
+            const int nbox = (min(BK, kv_end - t) + R - 1) / R;
+            mbar_arrive_expect_tx(full, (uint32_t)(nbox * R * 128 * Gm::NSUB));
+            for (int bx = 0; bx < nbox; ++bx) {
+              const int tok = t + bx * R;
+              const int col = p.page_shift >= 0 ? tok >> p.page_shift : tok / p.page_size;
+              int page = __ldg(p.page_table + (size_t)b * p.max_pages + col);
+              if ((unsigned)page >= (unsigned)p.num_pages) {  // a bad entry: flag it, read page 0 instead
+                atomicOr(&g_error_word, 4u);
+                page = 0;
+              }
+              const int row0 = tok - col * p.page_size;
 #pragma unroll
-            for (int sub = 0; sub < Gm::NSUB; ++sub)
-              tma_load_5d(dst + (uint32_t)(sub * BK * 128 + bx * R * 128), map, full, 0, row0, sub, h, page);
-          }
-        }
-      };
-      for (int j = 0; j <= ntiles; ++j) {
-        if (j < ntiles) {
-          const int st = j % Gm::KST;
-          if (j >= Gm::KST &&
-              !tc_wait(bar(Gm::BAR_K_EMPTY + st), (uint32_t)(((j / Gm::KST) & 1) ^ 1), abort_flag, p.timeout_ns))
-            break;
-          load(&p.tm_k, sbase + Gm::OFF_K + st * Gm::KV_BYTES, bar(Gm::BAR_K_FULL + st), j);
-          ++k_issued;
-        }
-        if (j >= 1) {
-          const int jv = j - 1, st = jv % Gm::VST;
-          if (jv >= Gm::VST &&
-              !tc_wait(bar(Gm::BAR_V_EMPTY + st), (uint32_t)(((jv / Gm::VST) & 1) ^ 1), abort_flag, p.timeout_ns))
-            break;
-          load(&p.tm_v, sbase + Gm::OFF_V + st * Gm::KV_BYTES, bar(Gm::BAR_V_FULL + st), jv);
-          ++v_issued;
-        }
-      }
-      // after an abort, let the copies already issued land before the CTA exits
-      if (*abort_flag) {
-        auto drain = [&](int base_bar, int nst, int issued) {
-          for (int k = issued > nst ? issued - nst : 0; k < issued; ++k) {
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(bar(base_bar + k % nst), (uint32_t)((k / nst) & 1)) &&
-                   globaltimer_ns() - t0 < p.timeout_ns) {
+              for (int sub = 0; sub < Gm::NSUB; ++sub)
+                tma_load_5d(dst + (uint32_t)(sub * BK * 128 + bx * R * 128), map, full, 0, row0, sub, h, page);
             }
           }
         };
-        drain(Gm::BAR_K_FULL, Gm::KST, k_issued);
-        drain(Gm::BAR_V_FULL, Gm::VST, v_issued);
-      }
-    }
-  } else if (warp == 1) {
-    // ---- MMA issue (lane 0); the warp zeroes V rows past the keys of the last tile
-    const uint32_t id_s = tc_idesc_bf16(Gm::M, BK, false, false);
-    const uint32_t id_o = tc_idesc_bf16(Gm::M, D, false, true);
-    // the whole warp waits (the tail zeroing writes what the copy wrote)
-    auto wait_all = [&](uint32_t b_, uint32_t par) {
-      const bool w = tc_wait(b_, par, abort_flag, p.timeout_ns);
-      return __all_sync(0xffffffffu, w);
-    };
-    // S[j & 1] = Q K_j^T over D in steps of 16; the K stage frees when it is done
-    auto issue_qk = [&](int j) {
-      const int st = j % Gm::KST;
-      const uint32_t kst = sbase + Gm::OFF_K + st * Gm::KV_BYTES;
-      const uint32_t dS = tmem + (j & 1 ? Gm::TCOL_S1 : Gm::TCOL_S0);
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t qo = (kk / 4) * (Gm::M * 128) + (kk % 4) * 32;
-        const uint32_t ko = (kk / 4) * (BK * 128) + (kk % 4) * 32;
-        tc_mma_ss(dS, tc_sdesc(sbase + Gm::OFF_Q + qo, 16, 1024, kTcSwizzle128B),
-                  tc_sdesc(kst + ko, 16, 1024, kTcSwizzle128B), id_s, kk > 0);
-      }
-      tc_commit(bar(Gm::BAR_S + (j & 1)));
-      tc_commit(bar(Gm::BAR_K_EMPTY + st));
-    };
-    int done_o = -1;  // last tile whose P V was issued
-    bool ok = ntiles > 0 && wait_all(bar(Gm::BAR_K_FULL), 0);
-    if (ok && lane == 0) {
-      tc_fence_after();
-      issue_qk(0);
-    }
-    for (int j = 0; j < ntiles && ok; ++j) {
-      // Q K^T of the next tile goes ahead of this tile's P V, so the softmax of
-      // tile j + 1 can start as soon as that of tile j ends
-      if (j + 1 < ntiles) {
-        const int st1 = (j + 1) % Gm::KST;
-        ok = wait_all(bar(Gm::BAR_K_FULL + st1), (uint32_t)(((j + 1) / Gm::KST) & 1));
-        if (!ok) break;
-        if (lane == 0) {
-          tc_fence_after();
-          issue_qk(j + 1);
+        for (int j = 0; j <= ntiles; ++j) {
+          if (j < ntiles) {
+            const int st = j % Gm::KST;
+            if (j >= Gm::KST &&
+                !tc_wait(bar(Gm::BAR_K_EMPTY + st), (uint32_t)(((j / Gm::KST) & 1) ^ 1), abort_flag, p.timeout_ns))
+              break;
+            load(&p.tm_k, sbase + Gm::OFF_K + st * Gm::KV_BYTES, bar(Gm::BAR_K_FULL + st), j);
+            ++k_issued;
+          }
+          if (j >= 1) {
+            const int jv = j - 1, st = jv % Gm::VST;
+            if (jv >= Gm::VST &&
+                !tc_wait(bar(Gm::BAR_V_EMPTY + st), (uint32_t)(((jv / Gm::VST) & 1) ^ 1), abort_flag, p.timeout_ns))
+              break;
+            load(&p.tm_v, sbase + Gm::OFF_V + st * Gm::KV_BYTES, bar(Gm::BAR_V_FULL + st), jv);
+            ++v_issued;
+          }
+        }
+        // after an abort, let the copies already issued land before the CTA exits
+        if (*abort_flag) {
+          auto drain = [&](int base_bar, int nst, int issued) {
+            for (int k = issued > nst ? issued - nst : 0; k < issued; ++k) {
+              const uint64_t t0 = globaltimer_ns();
+              while (!mbar_try_wait(bar(base_bar + k % nst), (uint32_t)((k / nst) & 1)) &&
+                     globaltimer_ns() - t0 < p.timeout_ns) {
+              }
+            }
+          };
+          drain(Gm::BAR_K_FULL, Gm::KST, k_issued);
+          drain(Gm::BAR_V_FULL, Gm::VST, v_issued);
         }
       }
-      const int st = j % Gm::VST;
-      ok = wait_all(bar(Gm::BAR_V_FULL + st), (uint32_t)((j / Gm::VST) & 1));
-      if (!ok) break;
-      const int t = j * BK;
-      const uint32_t vst = sbase + Gm::OFF_V + st * Gm::KV_BYTES;
-      if (t + BK > kv_end) {
-        // V rows at or past kv_end may hold anything (0 * NaN would poison O): zero them
+    } else if (warp == 1) {
+      // ---- MMA issue (lane 0); the warp zeroes V rows past the keys of the last tile
+      const uint32_t id_s = tc_idesc_bf16(Gm::M, BK, false, false);
+      const uint32_t id_o = tc_idesc_bf16(Gm::M, D, false, true);
+      // the whole warp waits (the tail zeroing writes what the copy wrote)
+      auto wait_all = [&](uint32_t b_, uint32_t par) {
+        const bool w = tc_wait(b_, par, abort_flag, p.timeout_ns);
+        return __all_sync(0xffffffffu, w);
+      };
+      // S buffer sb = Q_t K_j^T over D in steps of 16
+      auto issue_qk = [&](int t, int j, int sb) {
+        const uint32_t kst = sbase + Gm::OFF_K + (j % Gm::KST) * Gm::KV_BYTES;
+        const uint32_t qt = sbase + Gm::OFF_Q + t * Gm::QT_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t qo = (kk / 4) * (Gm::M * 128) + (kk % 4) * 32;
+          const uint32_t ko = (kk / 4) * (BK * 128) + (kk % 4) * 32;
+          tc_mma_ss(tmem + sb * BK, tc_sdesc(qt + qo, 16, 1024, kTcSwizzle128B),
+                    tc_sdesc(kst + ko, 16, 1024, kTcSwizzle128B), id_s, kk > 0);
+        }
+      };
+      // O_t += P (S buffer sb) V_j over the tile's keys in steps of 16
+      auto issue_pv = [&](int t, int j, int sb) {
+        const uint32_t vst = sbase + Gm::OFF_V + (j % Gm::VST) * Gm::KV_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          tc_mma_ts(tmem + Gm::TCOL_O + t * D, tmem + sb * BK + 8 * kk,
+                    tc_sdesc(vst + kk * 16 * 128, BK * 128, 1024, kTcSwizzle128B), id_o, j > 0 || kk > 0);
+      };
+      // V rows at or past kv_end may hold anything (0 * NaN would poison O): zero them
+      auto zero_tail = [&](int j) {
+        const int t = j * BK;
+        if (t + BK <= kv_end) return;
         const int r0 = kv_end - t;
+        uint8_t* vs = smem + Gm::OFF_V + (j % Gm::VST) * Gm::KV_BYTES;
         for (int e = r0 * 8 + lane; e < BK * 8; e += 32) {
           const int r = e / 8, ch = e % 8;
 #pragma unroll
           for (int sub = 0; sub < Gm::NSUB; ++sub)
-            *reinterpret_cast<uint4*>(smem + Gm::OFF_V + st * Gm::KV_BYTES + sub * (BK * 128) + swz<128>(r, ch)) =
-                make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(vs + sub * (BK * 128) + swz<128>(r, ch)) = make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
         __syncwarp();
-      }
-      ok = wait_all(bar(Gm::BAR_P + (j & 1)), (uint32_t)((j >> 1) & 1));
-      if (!ok) break;
-      if (lane == 0) {
+      };
+      bool ok = ntiles > 0 && wait_all(bar(Gm::BAR_K_FULL), 0);
+      const bool issued_any = ok;
+      if (ok && lane == 0) {
         tc_fence_after();
-        const uint32_t aP = tmem + (j & 1 ? Gm::TCOL_S1 : Gm::TCOL_S0);
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          tc_mma_ts(tmem + Gm::TCOL_O, aP + 8 * kk, tc_sdesc(vst + kk * 16 * 128, BK * 128, 1024, kTcSwizzle128B),
-                    id_o, j > 0 || kk > 0);
-        tc_commit(bar(Gm::BAR_O + (j & 1)));
-        tc_commit(bar(Gm::BAR_V_EMPTY + st));
+        for (int t = 0; t < NQT; ++t) {
+          issue_qk(t, 0, t);
+          tc_commit(bar(Gm::BAR_S + t));
+        }
+        tc_commit(bar(Gm::BAR_K_EMPTY));
       }
-      done_o = j;
       __syncwarp();
-    }
-    // before the tensor memory is freed, every MMA issued must have completed
-    if (lane == 0 && (done_o >= 0 || ntiles > 0)) {
-      tc_commit(bar(Gm::BAR_FIN));
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(bar(Gm::BAR_FIN), 0) && globaltimer_ns() - t0 < p.timeout_ns) {
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const bool more = j + 1 < ntiles;
+        if constexpr (NQT == 2) {
+          // A: P_A V_j, then S_A of tile j + 1; B: the same, then both free their stages
+          ok = wait_all(bar(Gm::BAR_V_FULL + j % Gm::VST), (uint32_t)((j / Gm::VST) & 1));
+          if (!ok) break;
+          zero_tail(j);
+          for (int t = 0; t < 2 && ok; ++t) {
+            ok = wait_all(bar(Gm::BAR_P + t), (uint32_t)(j & 1));
+            if (ok && more && t == 0)
+              ok = wait_all(bar(Gm::BAR_K_FULL + (j + 1) % Gm::KST), (uint32_t)(((j + 1) / Gm::KST) & 1));
+            if (!ok) break;
+            if (lane == 0) {
+              tc_fence_after();
+              issue_pv(t, j, t);
+              if (t == 1) tc_commit(bar(Gm::BAR_V_EMPTY + j % Gm::VST));
+              if (more) {
+                issue_qk(t, j + 1, t);
+                tc_commit(bar(Gm::BAR_S + t));
+                if (t == 1) tc_commit(bar(Gm::BAR_K_EMPTY + (j + 1) % Gm::KST));
+              } else {
+                tc_commit(bar(Gm::BAR_O + t));
+              }
+            }
+            __syncwarp();
+          }
+        } else {
+          // Q K^T of the next tile goes ahead of this tile's P V, so the softmax of
+          // tile j + 1 can start as soon as that of tile j ends
+          if (more) {
+            ok = wait_all(bar(Gm::BAR_K_FULL + (j + 1) % Gm::KST), (uint32_t)(((j + 1) / Gm::KST) & 1));
+            if (!ok) break;
+            if (lane == 0) {
+              tc_fence_after();
+              issue_qk(0, j + 1, (j + 1) & 1);
+              tc_commit(bar(Gm::BAR_S + ((j + 1) & 1)));
+              tc_commit(bar(Gm::BAR_K_EMPTY + (j + 1) % Gm::KST));
+            }
+            __syncwarp();
+          }
+          ok = wait_all(bar(Gm::BAR_V_FULL + j % Gm::VST), (uint32_t)((j / Gm::VST) & 1));
+          if (!ok) break;
+          zero_tail(j);
+          ok = wait_all(bar(Gm::BAR_P + (j & 1)), (uint32_t)((j >> 1) & 1));
+          if (!ok) break;
+          if (lane == 0) {
+            tc_fence_after();
+            issue_pv(0, j, j & 1);
+            tc_commit(bar(Gm::BAR_O + (j & 1)));
+            tc_commit(bar(Gm::BAR_V_EMPTY + j % Gm::VST));
+          }
+          __syncwarp();
+        }
       }
-    }
-    __syncwarp();
-  } else if (warp >= 4) {
-    // ---- softmax and epilogue: thread = row = tensor memory lane
-    const int row = threadIdx.x - 128;
-    const uint32_t lane_addr = (uint32_t)((warp - 4) * 32) << 16;
-    const int lim = row < nrows ? max(0, min(L, base + q0 + row / p.G + 1)) : 0;  // keys this row sees
+      // before the tensor memory is freed, every MMA issued must have completed
+      if (lane == 0 && issued_any) {
+        tc_commit(bar(Gm::BAR_FIN));
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar(Gm::BAR_FIN), 0) && globaltimer_ns() - t0 < p.timeout_ns) {
+        }
+      }
+      __syncwarp();
+    }  // warps 2 and 3: idle
+  } else {
+    // ---- softmax and epilogue of query tile qt: thread = row = tensor memory lane
+    if constexpr (NQT == 2) setmaxnreg_inc<Gm::REG_HIGH>();
+    const int qt = (warp - 4) >> 2;
+    const int row = (threadIdx.x - 128) & 127;
+    const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+    const int tok = qt * BQT + row / p.G;  // this row's token within the block
+    const bool has_row = row < BQT * p.G && tok < nq;
+    const int lim = has_row ? max(0, min(L, base + q0 + tok + 1)) : 0;  // keys this row sees
+    const int lim_first = max(0, min(L, base + q0 + qt * BQT + 1));      // keys every row of the tile sees
+    const uint32_t o_addr = tmem + lane_addr + Gm::TCOL_O + qt * D;
     float m = kNegInf, l = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
-      ok = tc_wait(bar(Gm::BAR_S + (j & 1)), (uint32_t)((j >> 1) & 1), abort_flag, p.timeout_ns);
+      const int sb = NQT == 2 ? qt : (j & 1);  // S buffer
+      const uint32_t spar = NQT == 2 ? (uint32_t)(j & 1) : (uint32_t)((j >> 1) & 1);
+      ok = tc_wait(bar(Gm::BAR_S + sb), spar, abort_flag, p.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t sAddr = tmem + lane_addr + (j & 1 ? Gm::TCOL_S1 : Gm::TCOL_S0);
+      const uint32_t sAddr = tmem + lane_addr + sb * BK;
       const int t = j * BK;
+      // the row of S: four loads in flight, one wait
+      uint32_t r[BK];
+#pragma unroll
+      for (int c0 = 0; c0 < BK; c0 += 32) tmem_ld32(sAddr + c0, *reinterpret_cast<uint32_t(*)[32]>(r + c0));
+      tmem_ld_wait();
+      // x = s * scale_log2, or (fold: scale_log2 > 0) x = s, with the scale applied
+      // in the exponent's fma and to the maximum; -inf at or past this row's limit
+      // (only tiles that reach past the first row's).  Max and sum run in eight
+      // independent chains.
+      const bool fold = p.scale_log2 > 0.f;  // uniform over the grid
       float x[BK];
 #pragma unroll
-      for (int c0 = 0; c0 < BK; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(sAddr + c0, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[c0 + i] = __uint_as_float(r[i]) * p.scale_log2;
-      }
-      // -inf at or past this row's limit (only tiles that reach past the first row's)
+      for (int i = 0; i < BK; ++i) x[i] = fold ? __uint_as_float(r[i]) : __uint_as_float(r[i]) * p.scale_log2;
       if (t + BK > lim_first) {
 #pragma unroll
         for (int i = 0; i < BK; ++i) x[i] = t + i < lim ? x[i] : kNegInf;
       }
-      float mx = kNegInf;
+      float mk[8];
 #pragma unroll
-      for (int i = 0; i < BK; ++i) mx = fmaxf(mx, x[i]);
+      for (int k = 0; k < 8; ++k) mk[k] = fmaxf(x[k], x[k + 8]);
+#pragma unroll
+      for (int i = 16; i < BK; i += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mk[k] = fmaxf(mk[k], fmaxf(x[i + k], x[i + 8 + k]));
+      float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])), fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
+      if (fold) mx *= p.scale_log2;
       // raise m (and rescale O and l) only when the row's maximum grew by more than 8
       const bool raise = mx > m + 8.f;
       const float m_new = raise ? mx : m;
       const float alpha = raise ? exp2_approx(m - m_new) : 1.f;  // 0 while m is still -inf
       if (__any_sync(0xffffffffu, raise && m != kNegInf) && j > 0) {
-        // O holds the P V of tiles < j: wait for tile j - 1's (tile j - 3's, the previous
-        // completion of that barrier, is done: S of tile j was committed after it),
-        // then scale this warp's rows
-        ok = tc_wait(bar(Gm::BAR_O + ((j - 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1), abort_flag, p.timeout_ns);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after();
+        // O holds the P V of tiles < j.  Two query tiles: S of tile j was issued
+        // after P V of tile j - 1, and its commit covers every MMA before it, so
+        // O is complete.  One query tile: wait for tile j - 1's P V (tile j - 3's,
+        // the previous completion of that barrier, is done: S of tile j was
+        // committed after it).
+        if constexpr (NQT == 1) {
+          ok = tc_wait(bar(Gm::BAR_O + ((j - 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1), abort_flag, p.timeout_ns);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+        }
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_addr + Gm::TCOL_O + c0, r);
+          uint32_t o[32];
+          tmem_ld32(o_addr + c0, o);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          tmem_st32(tmem + lane_addr + Gm::TCOL_O + c0, r);
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(o_addr + c0, o);
         }
         tmem_st_wait();
       }
       m = m_new;
       const float mu = m == kNegInf ? 0.f : m;  // a row that has seen no key: weights exactly 0
-      float sum = 0.f;
+      const float sc = fold ? p.scale_log2 : 1.f;
+      float sk[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sk[k] = 0.f;
 #pragma unroll
       for (int c0 = 0; c0 < BK; c0 += 64) {
-        uint32_t r[32];
+        uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float a = exp2_approx(x[c0 + 2 * i] - mu), c = exp2_approx(x[c0 + 2 * i + 1] - mu);
-          sum += a + c;
-          r[i] = pack_bf16x2(a, c);
+          const float e0 = exp2_approx(fmaf(x[c0 + 2 * i], sc, -mu));
+          const float e1 = exp2_approx(fmaf(x[c0 + 2 * i + 1], sc, -mu));
+          sk[i & 7] += e0 + e1;
+          pk[i] = pack_bf16x2(e0, e1);
         }
-        tmem_st32(sAddr + c0 / 2, r);
+        tmem_st32(sAddr + c0 / 2, pk);
       }
+      const float sum = ((sk[0] + sk[1]) + (sk[2] + sk[3])) + ((sk[4] + sk[5]) + (sk[6] + sk[7]));
       l = l * alpha + sum;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(Gm::BAR_P + (j & 1)));
+      mbar_arrive(bar(Gm::BAR_P + sb));
     }
-    // ---- normalise and write the block's rows (a row that saw nothing: zeros)
+    // ---- normalise and write the tile's rows (a row that saw nothing: zeros)
     if (ok && ntiles > 0) {
-      // the last tile's P V (it completes after every earlier one)
-      ok = tc_wait(bar(Gm::BAR_O + ((ntiles - 1) & 1)), (uint32_t)(((ntiles - 1) >> 1) & 1), abort_flag,
-                   p.timeout_ns);
+      // the last P V of this tile (it completes after every earlier one)
+      const int ob = NQT == 2 ? qt : ((ntiles - 1) & 1);
+      const uint32_t opar = NQT == 2 ? 0u : (uint32_t)(((ntiles - 1) >> 1) & 1);
+      ok = tc_wait(bar(Gm::BAR_O + ob), opar, abort_flag, p.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* dst = p.out + (((size_t)b * p.q_len + q0 + row / p.G) * p.Hq + h * p.G + row % p.G) * D;
+      __nv_bfloat16* dst = p.out + (((size_t)b * p.q_len + q0 + tok) * p.Hq + h * p.G + row % p.G) * D;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t r[32];
         if (ntiles > 0) {
-          tmem_ld32(tmem + lane_addr + Gm::TCOL_O + c0, r);
+          tmem_ld32(o_addr + c0, r);
           tmem_ld_wait();
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[i] = 0u;
         }
-        if (row < nrows) {
+        if (has_row) {
           uint4* o = reinterpret_cast<uint4*>(dst + c0);
 #pragma unroll
           for (int k = 0; k < 4; ++k)

@@ -65,6 +65,18 @@ def test_prefill_matches_oracle(D, Hq, Hkv):
     check(run_prefill(inp), oracle.prefill(inp), f"D={D} G={Hq // Hkv}")
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("scale", [-0.125, 0.0, 0.5])
+def test_prefill_any_scale(D, scale):
+    # the kernels take a positive scale into the exponent and the row maximum;
+    # a negative or zero one is applied to the scores first: every sign is exact
+    # to the oracle (zero: uniform weights over the visible keys)
+    lens = [75 + 130, 75, 40]
+    inp = prefill_case(7 * D + 3, len(lens), 75, 16, 4, D, 256, lens)
+    inp["scale"] = scale
+    check(run_prefill(inp), oracle.prefill(inp), f"D={D} scale={scale}")
+
+
 @pytest.mark.parametrize("Hq,Hkv,D", [(32, 2, 64), (64, 1, 32), (64, 1, 128)])
 def test_prefill_large_groups(Hq, Hkv, D):
     # G = 16 (4 query tokens per block) and G = 64 (one token per block, all 64 rows)
