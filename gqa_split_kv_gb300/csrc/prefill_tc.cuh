@@ -31,8 +31,8 @@
 // The MMAs of one thread run in issue order, so an S buffer can be overwritten
 // by the next Q K^T as soon as the P V that reads its P has been issued.
 //
-// Warp roles: warp 0 one lane issues the K and V tile copies (TMA) into two rings
-// (K of tile j + 1 can land while tile j's P V still holds its V); warp 1
+// Warp roles: warp 0 one lane issues the K and V tile copies (TMA) into one ring
+// of slots in the order the MMAs use them (K_0, V_0, K_1, V_1, ...); warp 1
 // allocates tensor memory and one lane issues every MMA and commits it to an
 // mbarrier; the last NQT warpgroups run the softmax and the epilogue, one query
 // tile each; all warps stage the query rows first.  With two query tiles the
@@ -56,22 +56,21 @@ struct PrefillTcGeo {
   static constexpr int ROWS = NQT * M;             // query rows per CTA
   static constexpr int BK = D == 256 ? 64 : 128;   // keys per tile (N of Q K^T)
   static constexpr int NSUB = D / 64;              // 64-element swizzle columns
-  // K and V have rings of their own: a K stage frees once its Q K^T is done, a V
-  // stage once its P V is
-  static constexpr int KST = D == 64 ? 4 : 3;
-  static constexpr int VST = D == 64 ? 4 : 2;
-  static constexpr int KV_BYTES = BK * D * 2;      // one tensor, one stage: [NSUB][BK][64]
+  // one ring of NSLOT slots holds K and V tiles in the order the MMAs use and
+  // free them: item 2 j is K_j, item 2 j + 1 is V_j, item n in slot n % NSLOT.  A
+  // slot frees when the last MMA that reads it completes; each load starts as soon
+  // as its slot is free, whatever tensor the slot held before
+  static constexpr int KV_BYTES = BK * D * 2;      // one tile of K or V: [NSUB][BK][64]
   static constexpr int QT_BYTES = M * D * 2;       // one query tile: [NSUB][M][64]
+  static constexpr int NSLOT = D == 64 ? 8 : 5;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + NQT * QT_BYTES;
-  static constexpr int OFF_V = OFF_K + KST * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_V + VST * KV_BYTES;
-  // barriers: k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], then s[2],
-  // p[2], o[2] (two query tiles: one each per tile, o completing once after the
-  // last P V; one query tile: by key-tile parity), fin (the last MMA)
-  static constexpr int BAR_K_FULL = 0, BAR_K_EMPTY = KST, BAR_V_FULL = 2 * KST, BAR_V_EMPTY = 2 * KST + VST,
-                       BAR_S = 2 * KST + 2 * VST, BAR_P = BAR_S + 2, BAR_O = BAR_S + 4, BAR_FIN = BAR_S + 6,
-                       NBAR = BAR_S + 7;
+  static constexpr int OFF_KV = OFF_Q + NQT * QT_BYTES;
+  static constexpr int OFF_BAR = OFF_KV + NSLOT * KV_BYTES;
+  // barriers: full[NSLOT], empty[NSLOT], then s[2], p[2], o[2] (two query tiles:
+  // one each per tile, o completing once after the last P V; one query tile: by
+  // key-tile parity), fin (the last MMA)
+  static constexpr int BAR_FULL = 0, BAR_EMPTY = NSLOT, BAR_S = 2 * NSLOT, BAR_P = BAR_S + 2, BAR_O = BAR_S + 4,
+                       BAR_FIN = BAR_S + 6, NBAR = BAR_S + 7;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] tensor memory base, [1] abort flag
   static constexpr int SMEM = OFF_MISC + 16 + 1024;    // + alignment slack
   // tensor memory columns: S buffer i at i * BK (two of them either way), O of
@@ -140,13 +139,9 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
   const int ntiles = (kv_end + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < Gm::KST; ++i) {
-      mbar_init(bar(Gm::BAR_K_FULL + i), 1);
-      mbar_init(bar(Gm::BAR_K_EMPTY + i), 1);
-    }
-    for (int i = 0; i < Gm::VST; ++i) {
-      mbar_init(bar(Gm::BAR_V_FULL + i), 1);
-      mbar_init(bar(Gm::BAR_V_EMPTY + i), 1);
+    for (int i = 0; i < Gm::NSLOT; ++i) {
+      mbar_init(bar(Gm::BAR_FULL + i), 1);
+      mbar_init(bar(Gm::BAR_EMPTY + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(Gm::BAR_S + i), 1);
@@ -190,9 +185,8 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
     // ---- first warpgroup: every warp gives registers up at the same instruction
     if constexpr (NQT == 2) setmaxnreg_dec<Gm::REG_LOW>();
     if (warp == 0) {
-      // ---- producer: K of tile j, then V of tile j - 1 (the order the tensor cores
-      // free their stages in), each once its stage is free
-      int k_issued = 0, v_issued = 0;
+      // ---- producer: the ring's items in order, each once its slot is free
+      int issued = 0;
       if (lane == 0) {
         // one tensor's tile j into dst, counted on the mbarrier full
         auto load = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int j) {
@@ -220,36 +214,22 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
             }
           }
         };
-        for (int j = 0; j <= ntiles; ++j) {
-          if (j < ntiles) {
-            const int st = j % Gm::KST;
-            if (j >= Gm::KST &&
-                !tc_wait(bar(Gm::BAR_K_EMPTY + st), (uint32_t)(((j / Gm::KST) & 1) ^ 1), abort_flag, p.timeout_ns))
-              break;
-            load(&p.tm_k, sbase + Gm::OFF_K + st * Gm::KV_BYTES, bar(Gm::BAR_K_FULL + st), j);
-            ++k_issued;
-          }
-          if (j >= 1) {
-            const int jv = j - 1, st = jv % Gm::VST;
-            if (jv >= Gm::VST &&
-                !tc_wait(bar(Gm::BAR_V_EMPTY + st), (uint32_t)(((jv / Gm::VST) & 1) ^ 1), abort_flag, p.timeout_ns))
-              break;
-            load(&p.tm_v, sbase + Gm::OFF_V + st * Gm::KV_BYTES, bar(Gm::BAR_V_FULL + st), jv);
-            ++v_issued;
-          }
+        for (int n = 0; n < 2 * ntiles; ++n) {
+          const int slot = n % Gm::NSLOT;
+          if (n >= Gm::NSLOT &&
+              !tc_wait(bar(Gm::BAR_EMPTY + slot), (uint32_t)(((n / Gm::NSLOT) & 1) ^ 1), abort_flag, p.timeout_ns))
+            break;
+          load(n & 1 ? &p.tm_v : &p.tm_k, sbase + Gm::OFF_KV + slot * Gm::KV_BYTES, bar(Gm::BAR_FULL + slot), n >> 1);
+          ++issued;
         }
         // after an abort, let the copies already issued land before the CTA exits
         if (*abort_flag) {
-          auto drain = [&](int base_bar, int nst, int issued) {
-            for (int k = issued > nst ? issued - nst : 0; k < issued; ++k) {
-              const uint64_t t0 = globaltimer_ns();
-              while (!mbar_try_wait(bar(base_bar + k % nst), (uint32_t)((k / nst) & 1)) &&
-                     globaltimer_ns() - t0 < p.timeout_ns) {
-              }
+          for (int k = issued > Gm::NSLOT ? issued - Gm::NSLOT : 0; k < issued; ++k) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(bar(Gm::BAR_FULL + k % Gm::NSLOT), (uint32_t)((k / Gm::NSLOT) & 1)) &&
+                   globaltimer_ns() - t0 < p.timeout_ns) {
             }
-          };
-          drain(Gm::BAR_K_FULL, Gm::KST, k_issued);
-          drain(Gm::BAR_V_FULL, Gm::VST, v_issued);
+          }
         }
       }
     } else if (warp == 1) {
@@ -261,9 +241,15 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
         const bool w = tc_wait(b_, par, abort_flag, p.timeout_ns);
         return __all_sync(0xffffffffu, w);
       };
+      // ring slot (shared-memory address) and mbarrier parity of K_j (item 2 j) and
+      // V_j (item 2 j + 1)
+      auto slot_addr = [&](int n) { return sbase + Gm::OFF_KV + (uint32_t)((n % Gm::NSLOT) * Gm::KV_BYTES); };
+      auto full_bar = [&](int n) { return bar(Gm::BAR_FULL + n % Gm::NSLOT); };
+      auto empty_bar = [&](int n) { return bar(Gm::BAR_EMPTY + n % Gm::NSLOT); };
+      auto full_par = [&](int n) { return (uint32_t)((n / Gm::NSLOT) & 1); };
       // S buffer sb = Q_t K_j^T over D in steps of 16
       auto issue_qk = [&](int t, int j, int sb) {
-        const uint32_t kst = sbase + Gm::OFF_K + (j % Gm::KST) * Gm::KV_BYTES;
+        const uint32_t kst = slot_addr(2 * j);
         const uint32_t qt = sbase + Gm::OFF_Q + t * Gm::QT_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -275,7 +261,7 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
       };
       // O_t += P (S buffer sb) V_j over the tile's keys in steps of 16
       auto issue_pv = [&](int t, int j, int sb) {
-        const uint32_t vst = sbase + Gm::OFF_V + (j % Gm::VST) * Gm::KV_BYTES;
+        const uint32_t vst = slot_addr(2 * j + 1);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
           tc_mma_ts(tmem + Gm::TCOL_O + t * D, tmem + sb * BK + 8 * kk,
@@ -286,7 +272,7 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
         const int t = j * BK;
         if (t + BK <= kv_end) return;
         const int r0 = kv_end - t;
-        uint8_t* vs = smem + Gm::OFF_V + (j % Gm::VST) * Gm::KV_BYTES;
+        uint8_t* vs = smem + Gm::OFF_KV + ((2 * j + 1) % Gm::NSLOT) * Gm::KV_BYTES;
         for (int e = r0 * 8 + lane; e < BK * 8; e += 32) {
           const int r = e / 8, ch = e % 8;
 #pragma unroll
@@ -296,7 +282,7 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
       };
-      bool ok = ntiles > 0 && wait_all(bar(Gm::BAR_K_FULL), 0);
+      bool ok = ntiles > 0 && wait_all(full_bar(0), full_par(0));
       const bool issued_any = ok;
       if (ok && lane == 0) {
         tc_fence_after();
@@ -304,29 +290,30 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
           issue_qk(t, 0, t);
           tc_commit(bar(Gm::BAR_S + t));
         }
-        tc_commit(bar(Gm::BAR_K_EMPTY));
+        tc_commit(empty_bar(0));
       }
       __syncwarp();
       for (int j = 0; j < ntiles && ok; ++j) {
         const bool more = j + 1 < ntiles;
         if constexpr (NQT == 2) {
-          // A: P_A V_j, then S_A of tile j + 1; B: the same, then both free their stages
-          ok = wait_all(bar(Gm::BAR_V_FULL + j % Gm::VST), (uint32_t)((j / Gm::VST) & 1));
+          // A: P_A V_j, then S_A of tile j + 1; B: the same, then V_j and K_{j+1} free
+          // their slots
+          ok = wait_all(full_bar(2 * j + 1), full_par(2 * j + 1));
           if (!ok) break;
           zero_tail(j);
           for (int t = 0; t < 2 && ok; ++t) {
             ok = wait_all(bar(Gm::BAR_P + t), (uint32_t)(j & 1));
             if (ok && more && t == 0)
-              ok = wait_all(bar(Gm::BAR_K_FULL + (j + 1) % Gm::KST), (uint32_t)(((j + 1) / Gm::KST) & 1));
+              ok = wait_all(full_bar(2 * j + 2), full_par(2 * j + 2));
             if (!ok) break;
             if (lane == 0) {
               tc_fence_after();
               issue_pv(t, j, t);
-              if (t == 1) tc_commit(bar(Gm::BAR_V_EMPTY + j % Gm::VST));
+              if (t == 1) tc_commit(empty_bar(2 * j + 1));
               if (more) {
                 issue_qk(t, j + 1, t);
                 tc_commit(bar(Gm::BAR_S + t));
-                if (t == 1) tc_commit(bar(Gm::BAR_K_EMPTY + (j + 1) % Gm::KST));
+                if (t == 1) tc_commit(empty_bar(2 * j + 2));
               } else {
                 tc_commit(bar(Gm::BAR_O + t));
               }
@@ -337,17 +324,17 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
           // Q K^T of the next tile goes ahead of this tile's P V, so the softmax of
           // tile j + 1 can start as soon as that of tile j ends
           if (more) {
-            ok = wait_all(bar(Gm::BAR_K_FULL + (j + 1) % Gm::KST), (uint32_t)(((j + 1) / Gm::KST) & 1));
+            ok = wait_all(full_bar(2 * j + 2), full_par(2 * j + 2));
             if (!ok) break;
             if (lane == 0) {
               tc_fence_after();
               issue_qk(0, j + 1, (j + 1) & 1);
               tc_commit(bar(Gm::BAR_S + ((j + 1) & 1)));
-              tc_commit(bar(Gm::BAR_K_EMPTY + (j + 1) % Gm::KST));
+              tc_commit(empty_bar(2 * j + 2));
             }
             __syncwarp();
           }
-          ok = wait_all(bar(Gm::BAR_V_FULL + j % Gm::VST), (uint32_t)((j / Gm::VST) & 1));
+          ok = wait_all(full_bar(2 * j + 1), full_par(2 * j + 1));
           if (!ok) break;
           zero_tail(j);
           ok = wait_all(bar(Gm::BAR_P + (j & 1)), (uint32_t)((j >> 1) & 1));
@@ -356,7 +343,7 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
             tc_fence_after();
             issue_pv(0, j, j & 1);
             tc_commit(bar(Gm::BAR_O + (j & 1)));
-            tc_commit(bar(Gm::BAR_V_EMPTY + j % Gm::VST));
+            tc_commit(empty_bar(2 * j + 1));
           }
           __syncwarp();
         }
