@@ -316,11 +316,16 @@ int decode_attn_int8_paged(const void* q, const void* k_pool_i8, const void* v_p
  *  seq_lens int32 [batch], clamped to [0, max_ctx] (paged: to
  *           min(max_pages_per_seq * page_size, max_seq_len))
  *  head_dim 32, 64, 128 or 256; G = num_q_heads / num_kv_heads <= 64.
+ *  scale    any finite value (a positive one is applied in the exponent's fma).
  * Softmax in fp32 (log2 units), P rounded to bf16 for the P V product, fp32
- * accumulation, output rounded to bf16.  No workspace; the library allocates
- * nothing.  Argument errors return DA_ERR_INVALID_ARG / DA_ERR_UNSUPPORTED before
- * any launch; page-table entries outside [0, num_pages) set bit 2 of the device
- * error word (decode_device_error) and read page 0 instead.
+ * accumulation, output rounded to bf16.  head_dim 64, 128 and 256 run on the
+ * tcgen05 tensor cores with the S and O accumulators in tensor memory; head_dim
+ * 32 on warp-level MMAs.  No workspace; the library allocates nothing.  Argument
+ * errors return DA_ERR_INVALID_ARG / DA_ERR_UNSUPPORTED before any launch; so
+ * does a build whose tensor-core kernel was compiled with fewer registers per
+ * thread than its warpgroup split needs (DA_ERR_UNSUPPORTED).  Page-table entries
+ * outside [0, num_pages) set bit 2 of the device error word (decode_device_error)
+ * and read page 0 instead.
  */
 int prefill_attn_contig(const void* q, const void* k, const void* v, const int* seq_lens, int batch, int q_len,
                         int num_q_heads, int num_kv_heads, int head_dim, int max_ctx, float scale, void* out,
