@@ -31,8 +31,9 @@
 // The MMAs of one thread run in issue order, so an S buffer can be overwritten
 // by the next Q K^T as soon as the P V that reads its P has been issued.
 //
-// Warp roles: warp 0 one lane issues the K and V tile copies (TMA) into one ring
-// of slots in the order the MMAs use them (K_0, V_0, K_1, V_1, ...); warp 1
+// Warp roles: one lane of warp 0 issues the K tile copies (TMA) and one of warp 2
+// the V tile copies, into one ring of slots in the order the MMAs use them (K_0,
+// V_0, K_1, V_1, ...); warp 1
 // allocates tensor memory and one lane issues every MMA and commits it to an
 // mbarrier; the last NQT warpgroups run the softmax and the epilogue, one query
 // tile each; all warps stage the query rows first.  With two query tiles the
@@ -184,9 +185,16 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
   if (warp < 4) {
     // ---- first warpgroup: every warp gives registers up at the same instruction
     if constexpr (NQT == 2) setmaxnreg_dec<Gm::REG_LOW>();
-    if (warp == 0) {
-      // ---- producer: the ring's items in order, each once its slot is free
-      int issued = 0;
+    if (warp == 0 || warp == 2) {
+      // ---- producers: warp 0 issues the K items (even n), warp 2 the V items (odd
+      // n), each in order and once its slot is free.  One thread issues copies one
+      // after another, so two issuing threads double the rate for the small page
+      // boxes.  A producer waits for the free of item n - NSLOT by phase parity.
+      // Its previous item, n - 2, needed item n - 2 - NSLOT freed, and the MMAs
+      // free items at most one place out of order, so item n - 2 NSLOT is freed by
+      // then: the parity it waits on is never a whole ring cycle stale.
+      const int first = warp == 0 ? 0 : 1;
+      int last = -1;  // last item this producer issued
       if (lane == 0) {
         // one tensor's tile j into dst, counted on the mbarrier full
         auto load = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int j) {
@@ -214,17 +222,18 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
             }
           }
         };
-        for (int n = 0; n < 2 * ntiles; ++n) {
+        for (int n = first; n < 2 * ntiles; n += 2) {
           const int slot = n % Gm::NSLOT;
           if (n >= Gm::NSLOT &&
               !tc_wait(bar(Gm::BAR_EMPTY + slot), (uint32_t)(((n / Gm::NSLOT) & 1) ^ 1), abort_flag, p.timeout_ns))
             break;
           load(n & 1 ? &p.tm_v : &p.tm_k, sbase + Gm::OFF_KV + slot * Gm::KV_BYTES, bar(Gm::BAR_FULL + slot), n >> 1);
-          ++issued;
+          last = n;
         }
-        // after an abort, let the copies already issued land before the CTA exits
+        // after an abort, let this producer's copies still in flight (its items
+        // among the last NSLOT) land before the CTA exits
         if (*abort_flag) {
-          for (int k = issued > Gm::NSLOT ? issued - Gm::NSLOT : 0; k < issued; ++k) {
+          for (int k = last; k >= 0 && k > last - Gm::NSLOT; k -= 2) {
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(bar(Gm::BAR_FULL + k % Gm::NSLOT), (uint32_t)((k / Gm::NSLOT) & 1)) &&
                    globaltimer_ns() - t0 < p.timeout_ns) {
@@ -356,7 +365,7 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
         }
       }
       __syncwarp();
-    }  // warps 2 and 3: idle
+    }  // warp 3: idle
   } else {
     // ---- softmax and epilogue of query tile qt: thread = row = tensor memory lane
     if constexpr (NQT == 2) setmaxnreg_inc<Gm::REG_HIGH>();
