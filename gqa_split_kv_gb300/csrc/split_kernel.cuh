@@ -94,7 +94,11 @@ struct SplitGeo {
   // warps; the warps of a sub-group take the sub-blocks ws, ws + W / ngp, ... of a tile.
   static constexpr int NGP_MAX = D == 128 ? 2 : 4;
   static constexpr int NP = KV8 ? (D <= 64 ? 2 : 1) : (D <= 64 ? 4 : D <= 128 ? 2 : 1);  // sub-blocks per softmax step
-  static constexpr int NTHREADS = (W + 1) * 32;
+  // producer warps: paged tiles are many small page boxes, and one issuing warp
+  // pays its per-tile and per-copy costs in series, so two producer warps take
+  // alternate tiles; a contiguous tile is one or two large copies
+  static constexpr int NPROD = PG ? 2 : 1;
+  static constexpr int NTHREADS = (W + NPROD) * 32;
   static constexpr int SUBW = D >= 64 ? 64 : 32;    // elements per swizzle row
   static constexpr int NSUB = D / SUBW;             // swizzle rows per token
   static constexpr int ROWB = SUBW * 2;             // 128 or 64 bytes
@@ -254,6 +258,12 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
                                                const Piece& guess, int k_spec) {
   using Gm = SplitGeo<D, NGP, KV8, PAGED>;
   const int lane = threadIdx.x & 31;
+  // With two producer warps, warp pw issues the tiles n with n % 2 == pw (with
+  // their page entries and query boxes).  Both walk every tile.  The consumers
+  // release tiles in order, and a producer's previous tile (n - 2) waited for
+  // tile n - 2 - STAGES, so its stage wait on tile n - STAGES cannot see a phase
+  // a whole ring cycle old.
+  const int pw = (threadIdx.x >> 5) - Gm::W;
   const uint32_t bar_full = sbase + Gm::OFF_BAR;
   const uint32_t bar_empty = bar_full + Gm::STAGES * 8;
   const uint32_t pg_ring = sbase + Gm::OFF_PG;
@@ -270,7 +280,7 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
   auto request_pages = [&](int k) {
     if (look.valid) {
       const int nb = (min(Gm::T, look.pc.t1 - look.t) + box_rows - 1) >> (4 + p.box_shift);
-      if (lane < nb) {
+      if (k % Gm::NPROD == pw && lane < nb) {
         const int tok = look.t + lane * box_rows;
         cp_async_4(pg_ring + (uint32_t)((k % Gm::RING) * 32 + lane) * 4,
                    p.page_table + (size_t)look.pc.b * p.max_pages + page_of(p, tok));
@@ -309,6 +319,7 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
     const bool first_tile = cur.t == pc.t0;
     const int ntok = min(Gm::T, pc.t1 - cur.t);
     const int nbox = PAGED ? (ntok + box_rows - 1) >> (4 + p.box_shift) : 1;  // boxes of this tile
+    const bool own = Gm::NPROD == 1 || n % Gm::NPROD == pw;  // this warp issues tile n
 
     int page = 0;
     if (PAGED) {
@@ -319,7 +330,7 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
         cp_async_wait<0>();
       }
       __syncwarp();
-      if (lane < nbox) {
+      if (own && lane < nbox) {
         page = pg_ring_ptr[(n % Gm::RING) * 32 + lane];
         if ((unsigned)page >= (unsigned)p.num_pages) {  // a bad entry: flag it, read page 0 instead
           atomicOr(&g_error_word, 4u);
@@ -328,50 +339,52 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
       }
     }
 
-    // wait until the consumers have released this stage (first pass: free)
-    bool ok = true;
-    if (lane == 0) ok = wait_bounded(bar_empty + stage * 8, parity ^ 1u, abort_flag, p.timeout_ns);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    if (!ok) break;
+    if (own) {
+      // wait until the consumers have released this stage (first pass: free)
+      bool ok = true;
+      if (lane == 0) ok = wait_bounded(bar_empty + stage * 8, parity ^ 1u, abort_flag, p.timeout_ns);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
 
-    const uint32_t full = bar_full + stage * 8;
-    const uint32_t kdst = sbase + Gm::OFF_K + stage * Gm::KV_BYTES;
-    const uint32_t vdst = sbase + Gm::OFF_V + stage * Gm::KV_BYTES;
-    const uint32_t qdst = sbase + Gm::OFF_Q + stage * Gm::Q_BYTES;
-    const uint32_t qbytes = first_tile ? (uint32_t)(nsg * Gm::NSUB * p.gr * Gm::ROWB) : 0u;
-    // K/V boxes (and, for int8 caches, their per-token scales) move whole
-    const uint32_t kvbytes = PAGED ? (uint32_t)(nbox * box_rows * (D * (KV8 ? 1 : 2) + (KV8 ? 4 : 0)))
-                                   : (uint32_t)(Gm::KV_BYTES + (KV8 ? Gm::T * 4 : 0));
-    if (lane == 0) mbar_arrive_expect_tx(full, 2u * kvbytes + qbytes);
-    __syncwarp();
-    if (PAGED) {
-      // tiles start on 64-token boundaries (the plan pads segments to whole
-      // 64-token units) and box_rows divides both 64 and the page size, so a
-      // box never crosses a page
-      if (lane < nbox) {
-        const int tok = cur.t + lane * box_rows;
-        const int row0 = tok - page_of(p, tok) * p.page_size;
-        const uint32_t off = (uint32_t)(lane * box_rows * D * (KV8 ? 1 : 2));
-        tma_load_5d(kdst + off, &p.tm_k, full, 0, row0, 0, h, page);
-        tma_load_5d(vdst + off, &p.tm_v, full, 0, row0, 0, h, page);
-        if constexpr (KV8) {  // [rows] fp32 scale boxes, one 128-byte aligned slot per box
-          const uint32_t soff = (uint32_t)(lane * max(box_rows, 32) * 4);
-          tma_load_3d(sbase + Gm::OFF_KS + stage * Gm::SC_BYTES + soff, &p.tm_ks, full, row0, h, page);
-          tma_load_3d(sbase + Gm::OFF_VS + stage * Gm::SC_BYTES + soff, &p.tm_vs, full, row0, h, page);
+      const uint32_t full = bar_full + stage * 8;
+      const uint32_t kdst = sbase + Gm::OFF_K + stage * Gm::KV_BYTES;
+      const uint32_t vdst = sbase + Gm::OFF_V + stage * Gm::KV_BYTES;
+      const uint32_t qdst = sbase + Gm::OFF_Q + stage * Gm::Q_BYTES;
+      const uint32_t qbytes = first_tile ? (uint32_t)(nsg * Gm::NSUB * p.gr * Gm::ROWB) : 0u;
+      // K/V boxes (and, for int8 caches, their per-token scales) move whole
+      const uint32_t kvbytes = PAGED ? (uint32_t)(nbox * box_rows * (D * (KV8 ? 1 : 2) + (KV8 ? 4 : 0)))
+                                     : (uint32_t)(Gm::KV_BYTES + (KV8 ? Gm::T * 4 : 0));
+      if (lane == 0) mbar_arrive_expect_tx(full, 2u * kvbytes + qbytes);
+      __syncwarp();
+      if (PAGED) {
+        // tiles start on 64-token boundaries (the plan pads segments to whole
+        // 64-token units) and box_rows divides both 64 and the page size, so a
+        // box never crosses a page
+        if (lane < nbox) {
+          const int tok = cur.t + lane * box_rows;
+          const int row0 = tok - page_of(p, tok) * p.page_size;
+          const uint32_t off = (uint32_t)(lane * box_rows * D * (KV8 ? 1 : 2));
+          tma_load_5d(kdst + off, &p.tm_k, full, 0, row0, 0, h, page);
+          tma_load_5d(vdst + off, &p.tm_v, full, 0, row0, 0, h, page);
+          if constexpr (KV8) {  // [rows] fp32 scale boxes, one 128-byte aligned slot per box
+            const uint32_t soff = (uint32_t)(lane * max(box_rows, 32) * 4);
+            tma_load_3d(sbase + Gm::OFF_KS + stage * Gm::SC_BYTES + soff, &p.tm_ks, full, row0, h, page);
+            tma_load_3d(sbase + Gm::OFF_VS + stage * Gm::SC_BYTES + soff, &p.tm_vs, full, row0, h, page);
+          }
+        }
+      } else if (lane == 0) {
+        tma_load_5d(kdst, &p.tm_k, full, 0, cur.t, 0, h, pc.b);
+        tma_load_5d(vdst, &p.tm_v, full, 0, cur.t, 0, h, pc.b);
+        if constexpr (KV8) {
+          tma_load_3d(sbase + Gm::OFF_KS + stage * Gm::SC_BYTES, &p.tm_ks, full, cur.t, h, pc.b);
+          tma_load_3d(sbase + Gm::OFF_VS + stage * Gm::SC_BYTES, &p.tm_vs, full, cur.t, h, pc.b);
         }
       }
-    } else if (lane == 0) {
-      tma_load_5d(kdst, &p.tm_k, full, 0, cur.t, 0, h, pc.b);
-      tma_load_5d(vdst, &p.tm_v, full, 0, cur.t, 0, h, pc.b);
-      if constexpr (KV8) {
-        tma_load_3d(sbase + Gm::OFF_KS + stage * Gm::SC_BYTES, &p.tm_ks, full, cur.t, h, pc.b);
-        tma_load_3d(sbase + Gm::OFF_VS + stage * Gm::SC_BYTES, &p.tm_vs, full, cur.t, h, pc.b);
+      if (first_tile && lane < nsg * Gm::NSUB) {  // one box per (sub-group, swizzle column)
+        const int sg = lane / Gm::NSUB, sub = lane % Gm::NSUB;
+        tma_load_4d(qdst + sg * Gm::Q_SG_BYTES + sub * Gm::Q_SUB_BYTES, &p.tm_q, full, 0, sub,
+                    h * p.G + (g0 + sg) * p.gr, pc.b);
       }
-    }
-    if (first_tile && lane < nsg * Gm::NSUB) {  // one box per (sub-group, swizzle column)
-      const int sg = lane / Gm::NSUB, sub = lane % Gm::NSUB;
-      tma_load_4d(qdst + sg * Gm::Q_SG_BYTES + sub * Gm::Q_SUB_BYTES, &p.tm_q, full, 0, sub,
-                  h * p.G + (g0 + sg) * p.gr, pc.b);
     }
     if (PAGED && n == 0) {
 #pragma unroll 1
@@ -386,9 +399,10 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
   }
   if (PAGED) cp_async_wait<0>();
 
-  // After an abort, let the copies already issued land before the CTA exits.
+  // After an abort, let the copies this warp issued land before the CTA exits.
   if (*abort_flag && lane == 0) {
     for (int k = n > Gm::STAGES ? n - Gm::STAGES : 0; k < n; ++k) {
+      if (k % Gm::NPROD != pw) continue;
       const uint32_t full = bar_full + (uint32_t)(k % Gm::STAGES) * 8;
       const uint32_t par = (uint32_t)((k / Gm::STAGES) & 1);
       const uint64_t t0 = globaltimer_ns();
@@ -1044,12 +1058,13 @@ __global__ void __launch_bounds__(SplitGeo<D, NGP, KV8, PAGED>::NTHREADS, 1) spl
     k_spec = min(Gm::STAGES, (guess.t1 - guess.t0 + Gm::T - 1) / Gm::T);
   // Barriers 2 (consumers) and 3, 4 (everyone) order the start.  The consumers
   // read seq_lens first (so the guessed copies do not queue ahead of it) and build
-  // the plan on barrier 2; then they wait on barrier 3 for the mbarriers, which the
-  // producer lane initialises before its warp arrives there, and arrive on barrier
-  // 4, where the producer waits for the plan after issuing the guessed tiles.
+  // the plan on barrier 2; then they wait on barrier 3 for the mbarriers, which
+  // lane 0 of the first producer warp initialises before the producer warps arrive
+  // there, and arrive on barrier 4, where the producers wait for the plan (after
+  // the guessed tiles are issued).
   constexpr int kAll = Gm::NTHREADS, kCons = Gm::W * 32;
-  if (warp == Gm::W) {
-    if ((threadIdx.x & 31) == 0) {
+  if (warp >= Gm::W) {
+    if (threadIdx.x == Gm::W * 32) {
 #pragma unroll
       for (int s = 0; s < Gm::STAGES; ++s) {
         mbar_init(sbase + Gm::OFF_BAR + s * 8, 1);
@@ -1068,7 +1083,7 @@ __global__ void __launch_bounds__(SplitGeo<D, NGP, KV8, PAGED>::NTHREADS, 1) spl
     __syncwarp();
     named_bar_arrive(3, kAll);
     if constexpr (!PAGED) {
-      if ((threadIdx.x & 31) == 0)
+      if (threadIdx.x == Gm::W * 32)
         for (int k = 0; k < k_spec; ++k) issue_contig_tile<D, NGP, KV8>(p, sbase, k, guess, guess.t0 + k * Gm::T);
     }
     // The combine kernel (launched only when a segment can have more than 8
@@ -1082,7 +1097,7 @@ __global__ void __launch_bounds__(SplitGeo<D, NGP, KV8, PAGED>::NTHREADS, 1) spl
     named_bar_arrive(4, kAll);
   }
   const Plan pl = make_plan(p.B, p.U, p.S, plan_gap_blocks(D), P);
-  if (warp == Gm::W)
+  if (warp >= Gm::W)
     split_producer<D, PAGED, NGP, KV8>(p, pl, lens, P, smem, sbase, abort_flag, guess, k_spec);
   else
     split_consumer<D, PAGED, NGP, KV8>(p, pl, lens, P, smem, sbase, abort_flag, guess, k_spec);
