@@ -95,9 +95,10 @@ struct SplitGeo {
   static constexpr int NGP_MAX = D == 128 ? 2 : 4;
   static constexpr int NP = KV8 ? (D <= 64 ? 2 : 1) : (D <= 64 ? 4 : D <= 128 ? 2 : 1);  // sub-blocks per softmax step
   // producer warps: paged tiles are many small page boxes, and one issuing warp
-  // pays its per-tile and per-copy costs in series, so two producer warps take
-  // alternate tiles; a contiguous tile is one or two large copies
-  static constexpr int NPROD = PG ? 2 : 1;
+  // pays its per-tile and per-copy costs in series, so NPROD producer warps take
+  // tiles in turn (four at D = 32, whose 1 KB boxes are the smallest); a
+  // contiguous tile is one or two large copies
+  static constexpr int NPROD = PG ? (D == 32 ? 4 : 2) : 1;
   static constexpr int NTHREADS = (W + NPROD) * 32;
   static constexpr int SUBW = D >= 64 ? 64 : 32;    // elements per swizzle row
   static constexpr int NSUB = D / SUBW;             // swizzle rows per token
@@ -151,6 +152,10 @@ struct SplitGeo {
   static_assert(NGP <= NGP_MAX && NGP_MAX <= W && W % NGP_MAX == 0 && D % FD == 0,
                 "warp groups and fold passes divide evenly");
   static_assert(RING >= LA + 2, "page ring must hold the prefetch window");
+  // a producer's previous tile (n - NPROD) waited for tile n - NPROD - STAGES, which
+  // must cover tile n - 2 STAGES for its stage wait to be unambiguous; the page
+  // ring must hold every entry a producer can request ahead of the slowest one
+  static_assert(NPROD <= STAGES && NPROD + STAGES + LA <= RING, "producer warps and rings");
   static_assert(smem_bytes(64) <= 227 * 1024, "shared memory budget");
 };
 
@@ -258,11 +263,11 @@ __device__ __forceinline__ void split_producer(const SplitParams& p, const Plan&
                                                const Piece& guess, int k_spec) {
   using Gm = SplitGeo<D, NGP, KV8, PAGED>;
   const int lane = threadIdx.x & 31;
-  // With two producer warps, warp pw issues the tiles n with n % 2 == pw (with
-  // their page entries and query boxes).  Both walk every tile.  The consumers
-  // release tiles in order, and a producer's previous tile (n - 2) waited for
-  // tile n - 2 - STAGES, so its stage wait on tile n - STAGES cannot see a phase
-  // a whole ring cycle old.
+  // With NPROD producer warps, warp pw issues the tiles n with n % NPROD == pw
+  // (with their page entries and query boxes).  All walk every tile.  The
+  // consumers release tiles in order, and a producer's previous tile (n - NPROD)
+  // waited for tile n - NPROD - STAGES, so its stage wait on tile n - STAGES
+  // cannot see a phase a whole ring cycle old (NPROD <= STAGES).
   const int pw = (threadIdx.x >> 5) - Gm::W;
   const uint32_t bar_full = sbase + Gm::OFF_BAR;
   const uint32_t bar_empty = bar_full + Gm::STAGES * 8;
