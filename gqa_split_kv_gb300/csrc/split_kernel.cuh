@@ -83,9 +83,9 @@ template <int D, int NGP = 1, bool KV8 = false, bool PG = false>
 struct SplitGeo {
   // bf16 tiles carry 32 KB (D = 32) or 64 KB of K+V so the per-tile costs (barrier
   // round trip, TMA issue, page lookups) stay small against the bytes moved; int8
-  // tiles carry half as much, except paged at D = 128, where 256-token tiles (two
-  // stages) cut the per-tile cost of the many small page boxes.
-  static constexpr int T = KV8 && PG && D == 128 ? 256 : D <= 64 ? 256 : D <= 128 ? 128 : 64;  // tokens per tile
+  // tiles carry half as much (the many small page boxes of a paged int8 tile are
+  // split over the producer warps, below).
+  static constexpr int T = D <= 64 ? 256 : D <= 128 ? 128 : 64;  // tokens per tile
   // consumer warps: two per scheduler for int8 tiles up to D = 128 (their
   // per-token work is a chain of short-latency integer steps), else one
   static constexpr int W = KV8 && D <= 128 ? 8 : 4;
@@ -94,18 +94,18 @@ struct SplitGeo {
   // warps; the warps of a sub-group take the sub-blocks ws, ws + W / ngp, ... of a tile.
   static constexpr int NGP_MAX = D == 128 ? 2 : 4;
   static constexpr int NP = KV8 ? (D <= 64 ? 2 : 1) : (D <= 64 ? 4 : D <= 128 ? 2 : 1);  // sub-blocks per softmax step
+  static constexpr int SUBW = D >= 64 ? 64 : 32;    // elements per swizzle row
+  static constexpr int NSUB = D / SUBW;             // swizzle rows per token
+  static constexpr int ROWB = SUBW * 2;             // 128 or 64 bytes
+  static constexpr int CPR = SUBW / 8;              // 16-byte chunks per swizzle row
+  static constexpr int STAGES = KV8 ? (D == 256 ? 3 : D == 32 ? 6 : 4)
+                                    : (D == 256 ? 2 : D >= 64 ? 3 : 5);
   // producer warps: paged tiles are many small page boxes, and one issuing warp
   // pays its per-tile and per-copy costs in series, so NPROD producer warps take
   // tiles in turn (four at D = 32, whose 1 KB boxes are the smallest); a
   // contiguous tile is one or two large copies
   static constexpr int NPROD = PG ? (D == 32 ? 4 : 2) : 1;
   static constexpr int NTHREADS = (W + NPROD) * 32;
-  static constexpr int SUBW = D >= 64 ? 64 : 32;    // elements per swizzle row
-  static constexpr int NSUB = D / SUBW;             // swizzle rows per token
-  static constexpr int ROWB = SUBW * 2;             // 128 or 64 bytes
-  static constexpr int CPR = SUBW / 8;              // 16-byte chunks per swizzle row
-  static constexpr int STAGES = KV8 ? (D == 256 ? 3 : D == 32 ? 6 : D == 128 && PG ? 2 : 4)
-                                    : (D == 256 ? 2 : D >= 64 ? 3 : 5);
   // fold scratch columns per fold pass (two passes at D = 128 with extra query rows)
   static constexpr int FD = D == 128 && NGP > 1 ? 64 : D;
   // One TMA box fills all NSUB swizzle columns of its R rows, so a tile is
