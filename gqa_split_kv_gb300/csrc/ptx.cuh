@@ -150,6 +150,16 @@ __device__ __forceinline__ void int8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
 }
 
+// Four signed int8 (bytes of w) -> two f16x2 holding 1152 + x, exactly: the byte
+// x ^ 0x80 = x + 128 becomes the mantissa of 1024 (f16 0x6400).  The caller
+// removes the 1152 offset after a dot product (1152 times the sum of the other
+// operand), which spares the two subtractions of int8x4_to_f16x4.
+__device__ __forceinline__ void int8x4_to_f16x4_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  lo = __byte_perm(u, 0x64646464u, 0x5150);  // bytes 0, 1
+  hi = __byte_perm(u, 0x64646464u, 0x5352);  // bytes 2, 3
+}
+
 // Two fp32 values -> packed bf16x2 (round to nearest even); `lo` in bits 0..15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;

@@ -680,6 +680,9 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
 #pragma unroll
     for (int c = 0; c < NB8; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
     float m_run = kNegInf, l_run = 0.f;
+    // int8: K enters the MMA as 1152 + k (int8x4_to_f16x4_biased), so every score
+    // of row g carries 1152 * (sum of the row's f16 query), removed before scaling
+    float kbias = 0.f;
     const int h = pc.u / p.npass;
     const int pass_u = pc.u % p.npass;
     const int gidx = pass_u * p.ngp + sg;  // this warp's sub-group
@@ -716,6 +719,20 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
             qa[(D >= 64 ? 4 : 2) * j + m][1] = pack_f16x2(bf16lo_to_f32(a2), bf16hi_to_f32(a2));
           }
         }
+        // the row's query sum, from the f16 values the MMA multiplies (each thread
+        // of the quad holds a quarter of the row's d's)
+        float qsum = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KCH; ++kk)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const __half2 hq = *reinterpret_cast<const __half2*>(&qa[kk][e]);
+            const float2 fq = __half22float2(hq);
+            qsum += fq.x + fq.y;
+          }
+        qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+        qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+        kbias = 1152.f * qsum;
         if constexpr (Gm::Q_SMEM) {  // k-chunks 2m, 2m + 1 per 16-byte slot, read back by this lane only
           uint4* qf = reinterpret_cast<uint4*>(smem + Gm::OFF_QF) + warp * (KCH / 2) * 32 + lane;
 #pragma unroll
@@ -784,8 +801,8 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
                 lds_words<4>(sb8 + o, kw[i][0] + kk);
                 lds_words<4>(sb8 + o + 8 * SW8, kw[i][1] + kk);
               }
-              int8x4_to_f16x4(kw[i][0][kk], b0, b1);
-              int8x4_to_f16x4(kw[i][1][kk], b2, b3);
+              int8x4_to_f16x4_biased(kw[i][0][kk], b0, b1);
+              int8x4_to_f16x4_biased(kw[i][1][kk], b2, b3);
               uint32_t a0 = qa[kk][0], a2 = qa[kk][1];
               if constexpr (Gm::Q_SMEM) {
                 const uint4 q4 = reinterpret_cast<const uint4*>(smem + Gm::OFF_QF)[(warp * (KCH / 2) + kk / 2) * 32 + lane];
@@ -807,10 +824,10 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
             s1[0] += s3[0];
             s1[1] += s3[1];
           }
-          x[i][0] = s0[0] * p.scale_log2;
-          x[i][1] = s0[1] * p.scale_log2;
-          x[i][2] = s1[0] * p.scale_log2;
-          x[i][3] = s1[1] * p.scale_log2;
+          x[i][0] = (s0[0] - kbias) * p.scale_log2;
+          x[i][1] = (s0[1] - kbias) * p.scale_log2;
+          x[i][2] = (s1[0] - kbias) * p.scale_log2;
+          x[i][3] = (s1[1] - kbias) * p.scale_log2;
           if constexpr (KV8) {  // K = k_i8 * k_scale: the scale of token t multiplies its score
             const float2 ka = *reinterpret_cast<const float2*>(ksc + kb * sc_blk + 2 * i4);
             const float2 kc = *reinterpret_cast<const float2*>(ksc + kb * sc_blk + 8 + 2 * i4);
