@@ -65,6 +65,27 @@ def test_paged_matches_oracle_and_contiguous_bitwise(D, ps):
             assert np.array_equal(acc_p[used], acc_c[used]) and np.array_equal(ml_p[used], ml_c[used])
 
 
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+@pytest.mark.parametrize("ps", [16, 64])
+def test_paged_long_pieces_cycle_every_producer_warp(D, ps):
+    # paged caches have two producer warps (four at D = 32) that issue the tiles of
+    # a piece in turn; a 3001-token sequence in one piece (S = 1) gives each of them
+    # many tiles and many passes over the stage ring, and the planner's split gives
+    # pieces whose tile counts are not multiples of the producer count
+    lens = [3001, 1, 2048, 700]
+    inp = contig_case(11 * D + ps, len(lens), 16, 4, D, ctx=max(lens), lens=lens)
+    rng = np.random.default_rng(D + ps)
+    kp, vp, table = contig_to_paged(inp["k"], inp["v"], inp["seq_lens"], ps, rng, spare_pages=2)
+    pin = dict(q=inp["q"], k_pool=kp, v_pool=vp, page_table=table, seq_lens=inp["seq_lens"], page_size=ps,
+               scale=inp["scale"])
+    ref = oracle.decode_paged(inp["q"], kp, vp, table, inp["seq_lens"], ps, inp["scale"])
+    for S in (1, None):
+        out_c, _, _, S_used = run(inp, S)
+        out_p, _, _, _ = run(pin, S_used, max_seq_len=max(lens))
+        check_out(out_p, ref, f"paged D={D} ps={ps} S={S_used}")
+        assert np.array_equal(out_p, out_c)
+
+
 def test_page_table_permutation_gives_identical_bits():
     inp = contig_case(5, 5, 16, 2, 128, ctx=700, lens=[700, 333, 64, 1, 519])
     rng = np.random.default_rng(1)
