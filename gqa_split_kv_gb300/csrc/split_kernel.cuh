@@ -87,13 +87,14 @@ struct SplitGeo {
   // split over the producer warps, below).
   static constexpr int T = D <= 64 ? 256 : D <= 128 ? 128 : 64;  // tokens per tile
   // consumer warps: two per scheduler for int8 tiles up to D = 128 (their
-  // per-token work is a chain of short-latency integer steps), else one
-  static constexpr int W = KV8 && D <= 128 ? 8 : 4;
+  // per-token work is a chain of short-latency integer steps) and for bf16 at
+  // D = 32 (256 tokens of softmax per 32 KB tile), else one
+  static constexpr int W = (KV8 && D <= 128) || D == 32 ? 8 : 4;
   static constexpr int SB = T / 16;                 // 16-token sub-blocks per tile
   // A pass runs ngp <= NGP_MAX sub-groups of <= 8 rows, one per group of W / ngp
   // warps; the warps of a sub-group take the sub-blocks ws, ws + W / ngp, ... of a tile.
   static constexpr int NGP_MAX = D == 128 ? 2 : 4;
-  static constexpr int NP = KV8 ? (D <= 64 ? 2 : 1) : (D <= 64 ? 4 : D <= 128 ? 2 : 1);  // sub-blocks per softmax step
+  static constexpr int NP = KV8 ? (D <= 64 ? 2 : 1) : (D == 32 ? 2 : D <= 64 ? 4 : D <= 128 ? 2 : 1);  // sub-blocks per softmax step
   static constexpr int SUBW = D >= 64 ? 64 : 32;    // elements per swizzle row
   static constexpr int NSUB = D / SUBW;             // swizzle rows per token
   static constexpr int ROWB = SUBW * 2;             // 128 or 64 bytes
