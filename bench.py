@@ -4,7 +4,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--suite]
 
 One step = one decode-attention call (the split-KV kernel, which merges every
-segment of up to 56 pieces itself; a combine kernel follows only for longer
+segment of up to 8 pieces itself; a combine kernel follows only for longer
 ones) over the largest decode configuration that fits one GPU, the mixed serving
 batch: B=64, Hq=64, Hkv=8 (G=8), head_dim 128, sequence lengths log-uniform in
 [1, 32768], paged bf16 cache with 16-token pages and a shuffled page table,
@@ -560,7 +560,8 @@ def ours(args):
                         if wl.name in PAGES_US_PER_CALL else None),
         "dtype": "bf16" if wl.kv_dtype == "bf16" else "f16 (int8 KV dequantized exactly)", "data": "synthetic",
         "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "head_dim": wl.D,
-                   "ctx": wl.max_ctx, "q_len": wl.q_len, "layout": wl.layout, "kv_dtype": wl.kv_dtype, "num_splits": r["S"], "accum": "fp32",
+                   "ctx": wl.max_ctx, "q_len": wl.q_len, "layout": wl.layout, "kv_dtype": wl.kv_dtype,
+                   "num_splits": r["S"], "accum": "fp32",
                    "l2": f"flushed before every step ({flush_bytes >> 20} MiB write + {flush_bytes >> 20} MiB read, "
                          "outside the timed pair)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},

@@ -412,7 +412,8 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
       for (int i = 16; i < BK; i += 16)
 #pragma unroll
         for (int k = 0; k < 8; ++k) mk[k] = fmaxf(mk[k], fmaxf(x[i + k], x[i + 8 + k]));
-      float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])), fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
+      float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])),
+                       fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
       if (fold) mx *= p.scale_log2;
       // raise m (and rescale O and l) only when the row's maximum grew by more than 8
       const bool raise = mx > m + 8.f;

@@ -94,7 +94,8 @@ struct SplitGeo {
   // A pass runs ngp <= NGP_MAX sub-groups of <= 8 rows, one per group of W / ngp
   // warps; the warps of a sub-group take the sub-blocks ws, ws + W / ngp, ... of a tile.
   static constexpr int NGP_MAX = D == 128 ? 2 : 4;
-  static constexpr int NP = KV8 ? (D <= 64 ? 2 : 1) : (D == 32 ? 2 : D <= 64 ? 4 : D <= 128 ? 2 : 1);  // sub-blocks per softmax step
+  // sub-blocks per softmax step
+  static constexpr int NP = KV8 ? (D <= 64 ? 2 : 1) : (D == 32 ? 2 : D <= 64 ? 4 : D <= 128 ? 2 : 1);
   static constexpr int SUBW = D >= 64 ? 64 : 32;    // elements per swizzle row
   static constexpr int NSUB = D / SUBW;             // swizzle rows per token
   static constexpr int ROWB = SUBW * 2;             // 128 or 64 bytes
@@ -1060,7 +1061,8 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
 }
 
 template <int D, bool PAGED, int NGP, bool KV8>
-__global__ void __launch_bounds__(SplitGeo<D, NGP, KV8, PAGED>::NTHREADS, 1) split_kernel(const __grid_constant__ SplitParams p) {
+__global__ void __launch_bounds__(SplitGeo<D, NGP, KV8, PAGED>::NTHREADS, 1)
+    split_kernel(const __grid_constant__ SplitParams p) {
   using Gm = SplitGeo<D, NGP, KV8, PAGED>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
