@@ -340,7 +340,7 @@ def measure(wl, inp, steps: int, warmup: int, flush_bytes: int, dist=None, sampl
     assert binding.device_error() == 0
     tb = traffic_bytes(wl.B, wl.Hq, wl.Hkv, wl.D, inp["seq_lens"], S, wl.page_size if paged else None, wl.q_len,
                        wl.kv_dtype)
-    # the split kernel, plus the combine kernel when a segment can have more than 56 pieces
+    # the split kernel, plus the combine kernel when a segment can have more than 8 pieces
     res = {"S": S, "times_ms": times, "bytes": tb, "clocks": clocks, "launches_per_step": 1 if S <= 8 else 2}
 
     if e2e_steps > 0:
