@@ -73,19 +73,27 @@ struct PrefillTcGeo {
   static constexpr int BAR_FULL = 0, BAR_EMPTY = NSLOT, BAR_S = 2 * NSLOT, BAR_P = BAR_S + 2, BAR_O = BAR_S + 4,
                        BAR_FIN = BAR_S + 6, NBAR = BAR_S + 7;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // [0] tensor memory base, [1] abort flag
-  static constexpr int SMEM = OFF_MISC + 16 + 1024;    // + alignment slack
+  // softmax threads per row: two with one query tile (one per half of the keys;
+  // they exchange the row's maximum and sum through one float per (query tile,
+  // row) and read the loop decision of the step from one word per query tile),
+  // one with two query tiles, where four softmax warpgroups would leave too few
+  // registers for each
+  static constexpr int NH = NQT == 1 ? 2 : 1;
+  static constexpr int OFF_XCH = OFF_MISC + 16;
+  static constexpr int OFF_DEC = OFF_XCH + NQT * M * 4;
+  static constexpr int SMEM = OFF_DEC + 16 + 1024;    // + alignment slack
   // tensor memory columns: S buffer i at i * BK (two of them either way), O of
   // query tile t at 2 * BK + t * D
   static constexpr int TCOL_O = 2 * BK;
   static constexpr int TCOLS_USED = 2 * BK + NQT * D;
   static constexpr uint32_t TMEM_COLS = TCOLS_USED <= 256 ? 256u : 512u;
-  static constexpr int NTHREADS = 128 * (1 + NQT);
+  static constexpr int NTHREADS = 128 * (1 + NQT * NH);
   // registers per thread after the split (two query tiles): the first warpgroup
-  // (producer, MMA issue, two idle warps) drops to REG_LOW, the softmax
+  // (producers, MMA issue, an idle warp) drops to REG_LOW, the softmax
   // warpgroups rise to REG_HIGH; the launch must provide
   // 128 * REG_LOW + 256 * REG_HIGH registers
   static constexpr int REG_LOW = 56, REG_HIGH = 216;
-  static constexpr int REG_POOL_NEEDED = 128 * REG_LOW + 256 * REG_HIGH;
+  static constexpr int REG_POOL_NEEDED = 128 * REG_LOW + 128 * NQT * NH * REG_HIGH;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(TCOLS_USED <= 512, "tensor memory budget");
 };
@@ -146,7 +154,7 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(Gm::BAR_S + i), 1);
-      mbar_init(bar(Gm::BAR_P + i), 128);
+      mbar_init(bar(Gm::BAR_P + i), 128 * Gm::NH);  // every softmax thread of the query tile
       mbar_init(bar(Gm::BAR_O + i), 1);
     }
     mbar_init(bar(Gm::BAR_FIN), 1);
@@ -367,54 +375,88 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
       __syncwarp();
     }  // warp 3: idle
   } else {
-    // ---- softmax and epilogue of query tile qt: thread = row = tensor memory lane
+    // ---- softmax and epilogue of query tile qt: NH threads per row, one per part
+    // of the key columns (tensor memory lane = row; warps w and w + 4 reach the
+    // same lanes); two halves exchange the row's maximum every key tile and the
+    // row's sum at the end, and each handles its part of O
     if constexpr (NQT == 2) setmaxnreg_inc<Gm::REG_HIGH>();
-    const int qt = (warp - 4) >> 2;
-    const int row = (threadIdx.x - 128) & 127;
+    constexpr int NH = Gm::NH;
+    constexpr int HK = BK / NH, HD = D / NH;
+    const int sw = warp - 4;
+    const int qt = sw / (4 * NH), hh = NH == 2 ? (sw >> 2) & 1 : 0;
+    const int row = lane + 32 * (warp & 3);
     const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+    volatile float* xch = reinterpret_cast<volatile float*>(smem + Gm::OFF_XCH) + qt * Gm::M + row;
+    volatile int* dec = reinterpret_cast<volatile int*>(smem + Gm::OFF_DEC) + qt;
     const int tok = qt * BQT + row / p.G;  // this row's token within the block
     const bool has_row = row < BQT * p.G && tok < nq;
     const int lim = has_row ? max(0, min(L, base + q0 + tok + 1)) : 0;  // keys this row sees
     const int lim_first = max(0, min(L, base + q0 + qt * BQT + 1));      // keys every row of the tile sees
-    const uint32_t o_addr = tmem + lane_addr + Gm::TCOL_O + qt * D;
+    const uint32_t o_addr = tmem + lane_addr + Gm::TCOL_O + qt * D + hh * HD;
+    // the 256 threads of the query tile meet on named barrier 1 + qt; a step's
+    // decision to stop (the CTA's abort flag, read once by one thread between the
+    // two meetings) is the same for all of them, so none waits for a partner that
+    // left
+    auto meet = [&]() { named_bar_sync(1 + qt, 128 * NH); };
     float m = kNegInf, l = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int sb = NQT == 2 ? qt : (j & 1);  // S buffer
       const uint32_t spar = NQT == 2 ? (uint32_t)(j & 1) : (uint32_t)((j >> 1) & 1);
-      ok = tc_wait(bar(Gm::BAR_S + sb), spar, abort_flag, p.timeout_ns);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
+      bool ok_s = tc_wait(bar(Gm::BAR_S + sb), spar, abort_flag, p.timeout_ns);
+      ok_s = __all_sync(0xffffffffu, ok_s);
       const uint32_t sAddr = tmem + lane_addr + sb * BK;
-      const int t = j * BK;
-      // the row of S: four loads in flight, one wait
-      uint32_t r[BK];
-#pragma unroll
-      for (int c0 = 0; c0 < BK; c0 += 32) tmem_ld32(sAddr + c0, *reinterpret_cast<uint32_t(*)[32]>(r + c0));
-      tmem_ld_wait();
+      const int t = j * BK + hh * HK;  // first key of this half
       // x = s * scale_log2, or (fold: scale_log2 > 0) x = s, with the scale applied
       // in the exponent's fma and to the maximum; -inf at or past this row's limit
       // (only tiles that reach past the first row's).  Max and sum run in eight
       // independent chains.
       const bool fold = p.scale_log2 > 0.f;  // uniform over the grid
-      float x[BK];
+      float x[HK];
+      float mxh = kNegInf;
+      if (ok_s) {
+        tc_fence_after();
+        uint32_t r[HK];
 #pragma unroll
-      for (int i = 0; i < BK; ++i) x[i] = fold ? __uint_as_float(r[i]) : __uint_as_float(r[i]) * p.scale_log2;
-      if (t + BK > lim_first) {
+        for (int c0 = 0; c0 < HK; c0 += 32) tmem_ld32(sAddr + hh * HK + c0, *reinterpret_cast<uint32_t(*)[32]>(r + c0));
+        tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < BK; ++i) x[i] = t + i < lim ? x[i] : kNegInf;
+        for (int i = 0; i < HK; ++i) x[i] = fold ? __uint_as_float(r[i]) : __uint_as_float(r[i]) * p.scale_log2;
+        if (j * BK + BK > lim_first) {
+#pragma unroll
+          for (int i = 0; i < HK; ++i) x[i] = t + i < lim ? x[i] : kNegInf;
+        }
+        float mk[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mk[k] = fmaxf(x[k], x[k + 8]);
+#pragma unroll
+        for (int i = 16; i < HK; i += 16)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mk[k] = fmaxf(mk[k], fmaxf(x[i + k], x[i + 8 + k]));
+        mxh = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])), fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
+        if (fold) mxh *= p.scale_log2;
       }
-      float mk[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mk[k] = fmaxf(x[k], x[k + 8]);
-#pragma unroll
-      for (int i = 16; i < BK; i += 16)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mk[k] = fmaxf(mk[k], fmaxf(x[i + k], x[i + 8 + k]));
-      float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])),
-                       fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
-      if (fold) mx *= p.scale_log2;
+      // the row's maximum: half 0 posts its own, half 1 combines and posts the
+      // row's, half 0 reads it
+      float mx = mxh;
+      if constexpr (NH == 2) {
+        if (hh == 0) *xch = mxh;
+        meet();
+        if (hh == 1) {
+          mx = fmaxf(mx, *xch);
+          *xch = mx;
+          if (row == 0) *dec = *abort_flag;
+        }
+        meet();
+        if (hh == 0) mx = *xch;
+        if (*dec) {
+          ok = false;
+          break;
+        }
+      } else if (!ok_s) {
+        ok = false;
+        break;
+      }
       // raise m (and rescale O and l) only when the row's maximum grew by more than 8
       const bool raise = mx > m + 8.f;
       const float m_new = raise ? mx : m;
@@ -424,23 +466,26 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
         // after P V of tile j - 1, and its commit covers every MMA before it, so
         // O is complete.  One query tile: wait for tile j - 1's P V (tile j - 3's,
         // the previous completion of that barrier, is done: S of tile j was
-        // committed after it).
+        // committed after it).  A wait that gives up leaves O as it is; the
+        // next step's decision stops the loop.
+        bool ok_o = true;
         if constexpr (NQT == 1) {
-          ok = tc_wait(bar(Gm::BAR_O + ((j - 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1), abort_flag, p.timeout_ns);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
+          ok_o = tc_wait(bar(Gm::BAR_O + ((j - 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1), abort_flag, p.timeout_ns);
+          ok_o = __all_sync(0xffffffffu, ok_o);
           tc_fence_after();
         }
+        if (ok_o) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld32(o_addr + c0, o);
-          tmem_ld_wait();
+          for (int c0 = 0; c0 < HD; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(o_addr + c0, o);
+            tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(o_addr + c0, o);
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(o_addr + c0, o);
+          }
+          tmem_st_wait();
         }
-        tmem_st_wait();
       }
       m = m_new;
       const float mu = m == kNegInf ? 0.f : m;  // a row that has seen no key: weights exactly 0
@@ -448,17 +493,24 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
       float sk[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) sk[k] = 0.f;
+      {
+        uint32_t pk[HK / 2];
 #pragma unroll
-      for (int c0 = 0; c0 < BK; c0 += 64) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float e0 = exp2_approx(fmaf(x[c0 + 2 * i], sc, -mu));
-          const float e1 = exp2_approx(fmaf(x[c0 + 2 * i + 1], sc, -mu));
+        for (int i = 0; i < HK / 2; ++i) {
+          const float e0 = exp2_approx(fmaf(x[2 * i], sc, -mu));
+          const float e1 = exp2_approx(fmaf(x[2 * i + 1], sc, -mu));
           sk[i & 7] += e0 + e1;
           pk[i] = pack_bf16x2(e0, e1);
         }
-        tmem_st32(sAddr + c0 / 2, pk);
+        // P of this half's keys: bf16 pairs over columns [hh HK / 2, (hh + 1) HK / 2)
+        if constexpr (HK / 2 >= 32) {
+#pragma unroll
+          for (int c0 = 0; c0 < HK / 2; c0 += 32)
+            tmem_st32(sAddr + hh * (HK / 2) + c0, *reinterpret_cast<uint32_t(*)[32]>(pk + c0));
+        } else {
+          static_assert(HK / 2 == 16, "a half row of P is 16 or a multiple of 32 columns");
+          tmem_st16(sAddr + hh * (HK / 2), *reinterpret_cast<uint32_t(*)[16]>(pk));
+        }
       }
       const float sum = ((sk[0] + sk[1]) + (sk[2] + sk[3])) + ((sk[4] + sk[5]) + (sk[6] + sk[7]));
       l = l * alpha + sum;
@@ -466,7 +518,18 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(Gm::BAR_P + sb));
     }
-    // ---- normalise and write the tile's rows (a row that saw nothing: zeros)
+    // ---- normalise and write the tile's rows (a row that saw nothing: zeros):
+    // the row's sum from both halves, then each half writes its half of O
+    if constexpr (NH == 2) {
+      if (hh == 1) *xch = l;
+      meet();
+      if (hh == 0) {
+        l += *xch;
+        *xch = l;
+      }
+      meet();
+      if (hh == 1) l = *xch;
+    }
     if (ok && ntiles > 0) {
       // the last P V of this tile (it completes after every earlier one)
       const int ob = NQT == 2 ? qt : ((ntiles - 1) & 1);
@@ -477,9 +540,9 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
     if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* dst = p.out + (((size_t)b * p.q_len + q0 + tok) * p.Hq + h * p.G + row % p.G) * D;
+      __nv_bfloat16* dst = p.out + (((size_t)b * p.q_len + q0 + tok) * p.Hq + h * p.G + row % p.G) * D + hh * HD;
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = 0; c0 < HD; c0 += 32) {
         uint32_t r[32];
         if (ntiles > 0) {
           tmem_ld32(o_addr + c0, r);
