@@ -33,14 +33,16 @@
 //
 // Warp roles: one lane of warp 0 issues the K tile copies (TMA) and one of warp 2
 // the V tile copies, into one ring of slots in the order the MMAs use them (K_0,
-// V_0, K_1, V_1, ...); warp 1
-// allocates tensor memory and one lane issues every MMA and commits it to an
-// mbarrier; the last NQT warpgroups run the softmax and the epilogue, one query
-// tile each; all warps stage the query rows first.  With two query tiles the
-// first warpgroup gives registers up (setmaxnreg) to the softmax warpgroups; the
-// host launches that form only when the kernel's register budget covers the
-// split.  Every wait is bounded: after the limit the kernel sets the device error
-// word, lets the work it issued finish, frees its tensor memory and exits.
+// V_0, K_1, V_1, ...); warp 1 allocates tensor memory and one lane issues every
+// MMA and commits it to an mbarrier; the last NQT * NH warpgroups run the softmax
+// and the epilogue (NH = 1 thread per row with two query tiles, 2 with one: each
+// takes half of the row's keys and of its O, and the two exchange the row's
+// maximum through shared memory); all warps stage the query rows first.  With two
+// query tiles the first warpgroup gives registers up (setmaxnreg) to the softmax
+// warpgroups; the host launches that form only when the kernel's register budget
+// covers the split.  Every wait is bounded: after the limit the kernel sets the
+// device error word, lets the work it issued finish, frees its tensor memory and
+// exits.
 #pragma once
 
 #include <cstdint>
