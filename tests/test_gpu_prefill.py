@@ -85,7 +85,10 @@ def test_prefill_large_groups(Hq, Hkv, D):
     check(run_prefill(inp), oracle.prefill(inp), f"G={Hq // Hkv} D={D}")
 
 
-@pytest.mark.parametrize("D,ps", [(64, 16), (128, 32), (256, 64), (32, 48)])
+@pytest.mark.parametrize("D,ps", [(64, 16), (128, 32), (256, 64), (32, 48),
+                                  # many page boxes per key tile, split over the two
+                                  # producer warps; pages that are not powers of two
+                                  (128, 16), (128, 48), (256, 16), (256, 96), (64, 96)])
 def test_prefill_paged_equals_contiguous_bitwise(D, ps):
     lens = [300, 64, 17]
     inp = prefill_case(3 * D + ps, len(lens), 64, 16, 4, D, 320, lens)
