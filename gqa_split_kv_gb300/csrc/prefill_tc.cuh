@@ -414,8 +414,8 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
       // (only tiles that reach past the first row's).  Max and sum run in eight
       // independent chains.
       const bool fold = p.scale_log2 > 0.f;  // uniform over the grid
+      const float sc = fold ? p.scale_log2 : 1.f;
       float x[HK];
-      float mxh = kNegInf;
       if (ok_s) {
         tc_fence_after();
         uint32_t r[HK];
@@ -428,6 +428,8 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
 #pragma unroll
           for (int i = 0; i < HK; ++i) x[i] = t + i < lim ? x[i] : kNegInf;
         }
+      }
+      auto tile_max = [&]() {  // this thread's maximum of x, scaled
         float mk[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) mk[k] = fmaxf(x[k], x[k + 8]);
@@ -435,13 +437,49 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
         for (int i = 16; i < HK; i += 16)
 #pragma unroll
           for (int k = 0; k < 8; ++k) mk[k] = fmaxf(mk[k], fmaxf(x[i + k], x[i + 8 + k]));
-        mxh = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])), fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
-        if (fold) mxh *= p.scale_log2;
-      }
-      // the row's maximum: half 0 posts its own, half 1 combines and posts the
-      // row's, half 0 reads it
-      float mx = mxh;
+        const float mxh =
+            fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])), fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
+        return fold ? mxh * p.scale_log2 : mxh;
+      };
+      // P = exp2(x sc - mu) as bf16 pairs, stored over this part's columns of the S
+      // buffer, [hh HK / 2, (hh + 1) HK / 2); returns the sum of the weights
+      auto weights = [&](float mu_) {
+        float sk[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) sk[k] = 0.f;
+        constexpr int CH = HK / 2 >= 32 ? 32 : HK / 2;  // columns per store
+#pragma unroll
+        for (int c0 = 0; c0 < HK / 2; c0 += CH) {
+          uint32_t pk[CH];
+#pragma unroll
+          for (int i = 0; i < CH; ++i) {
+            const float e0 = exp2_approx(fmaf(x[2 * (c0 + i)], sc, -mu_));
+            const float e1 = exp2_approx(fmaf(x[2 * (c0 + i) + 1], sc, -mu_));
+            sk[i & 7] += e0 + e1;
+            pk[i] = pack_bf16x2(e0, e1);
+          }
+          if constexpr (CH == 32) {
+            tmem_st32(sAddr + hh * (HK / 2) + c0, pk);
+          } else {
+            static_assert(CH == 16, "a part of P is 16 or a multiple of 32 columns");
+            tmem_st16(sAddr + hh * (HK / 2) + c0, pk);
+          }
+        }
+        return ((sk[0] + sk[1]) + (sk[2] + sk[3])) + ((sk[4] + sk[5]) + (sk[6] + sk[7]));
+      };
+      // The running maximum m is raised (and O, l rescaled) only when needed.  Two
+      // threads per row: when the row's maximum, exchanged every step, exceeds m
+      // by more than 8.  One thread per row: the weights are first taken against
+      // the current m, and only a row that has seen no key yet or whose weights
+      // sum past 2^14 takes its maximum and raises m to it; every weight then
+      // stays below 2^14.
+      float mx = kNegInf, sum = 0.f;
+      bool need_max = true, have_weights = false;
       if constexpr (NH == 2) {
+        const float mxh = ok_s ? tile_max() : kNegInf;
+        // the row's maximum: half 0 posts its own, half 1 combines and posts the
+        // row's, half 0 reads it
+        mx = mxh;
         if (hh == 0) *xch = mxh;
         meet();
         if (hh == 1) {
@@ -455,12 +493,20 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
           ok = false;
           break;
         }
-      } else if (!ok_s) {
-        ok = false;
-        break;
+      } else {
+        if (!ok_s) {
+          ok = false;
+          break;
+        }
+        // weights() ends in a tensor-memory store that the whole warp executes:
+        // every call is warp-uniform, each lane with its own m (a warp none of
+        // whose rows has seen a key skips this pass: they all take the maximum)
+        have_weights = __any_sync(0xffffffffu, m != kNegInf);
+        if (have_weights) sum = weights(m == kNegInf ? 0.f : m);
+        need_max = m == kNegInf || !(sum <= 16384.f);
+        if (need_max) mx = tile_max();
       }
-      // raise m (and rescale O and l) only when the row's maximum grew by more than 8
-      const bool raise = mx > m + 8.f;
+      const bool raise = need_max && (NH == 2 ? mx > m + 8.f : mx > m);
       const float m_new = raise ? mx : m;
       const float alpha = raise ? exp2_approx(m - m_new) : 1.f;  // 0 while m is still -inf
       if (__any_sync(0xffffffffu, raise && m != kNegInf) && j > 0) {
@@ -490,31 +536,10 @@ __global__ void __launch_bounds__(PrefillTcGeo<D>::NTHREADS, 1)
         }
       }
       m = m_new;
-      const float mu = m == kNegInf ? 0.f : m;  // a row that has seen no key: weights exactly 0
-      const float sc = fold ? p.scale_log2 : 1.f;
-      float sk[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) sk[k] = 0.f;
-      {
-        uint32_t pk[HK / 2];
-#pragma unroll
-        for (int i = 0; i < HK / 2; ++i) {
-          const float e0 = exp2_approx(fmaf(x[2 * i], sc, -mu));
-          const float e1 = exp2_approx(fmaf(x[2 * i + 1], sc, -mu));
-          sk[i & 7] += e0 + e1;
-          pk[i] = pack_bf16x2(e0, e1);
-        }
-        // P of this half's keys: bf16 pairs over columns [hh HK / 2, (hh + 1) HK / 2)
-        if constexpr (HK / 2 >= 32) {
-#pragma unroll
-          for (int c0 = 0; c0 < HK / 2; c0 += 32)
-            tmem_st32(sAddr + hh * (HK / 2) + c0, *reinterpret_cast<uint32_t(*)[32]>(pk + c0));
-        } else {
-          static_assert(HK / 2 == 16, "a half row of P is 16 or a multiple of 32 columns");
-          tmem_st16(sAddr + hh * (HK / 2), *reinterpret_cast<uint32_t(*)[16]>(pk));
-        }
-      }
-      const float sum = ((sk[0] + sk[1]) + (sk[2] + sk[3])) + ((sk[4] + sk[5]) + (sk[6] + sk[7]));
+      // weights against the new m (replacing those taken against the old one; a
+      // lane that did not raise writes the same values again); a row that has seen
+      // no key yet takes 0, so its weights are exactly 0
+      if (!have_weights || __any_sync(0xffffffffu, raise)) sum = weights(m == kNegInf ? 0.f : m);
       l = l * alpha + sum;
       tmem_st_wait();
       tc_fence_before();
