@@ -1074,13 +1074,16 @@ __global__ void __launch_bounds__(SplitGeo<D, NGP, KV8, PAGED>::NTHREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Gm::OFF_MISC);
   const int warp = threadIdx.x >> 5;
 
-  // Contiguous caches of small batches: the first tiles of the piece this CTA gets
-  // if every sequence holds max_len tokens (the usual case there) are requested
-  // before seq_lens is read; the plan then confirms or drains them.
+  // Contiguous caches of small batches: the first tile of the piece this CTA gets
+  // if every sequence holds max_len tokens (the usual case there) is requested
+  // before seq_lens is read; the plan then confirms or drains it.  One tile only:
+  // DRAM serves the requests of all CTAs side by side, so a whole ring per CTA
+  // requested at once would land no tile early; the rest follow once the plan
+  // is built.
   Piece guess{};
   int k_spec = 0;
   if (!PAGED && p.spec_first && guess_first_piece(p.B, p.U, p.S, plan_gap_blocks(D), p.max_len, blockIdx.x, guess))
-    k_spec = min(Gm::STAGES, (guess.t1 - guess.t0 + Gm::T - 1) / Gm::T);
+    k_spec = min(1, (guess.t1 - guess.t0 + Gm::T - 1) / Gm::T);
   // Barriers 2 (consumers) and 3, 4 (everyone) order the start.  The consumers
   // read seq_lens first (so the guessed copies do not queue ahead of it) and build
   // the plan on barrier 2; then they wait on barrier 3 for the mbarriers, which
