@@ -461,16 +461,38 @@ __device__ __forceinline__ bool claim_last_piece(unsigned long long* c, unsigned
 // ascending slot order, by the W consumer warps.  to_partial: the merged
 // unnormalised partial (acc, m, l) of the slots' joint token range replaces slot
 // slot0; else the bf16 output rows are written.  Partials written by other CTAs
-// are read through L2 (ld.global.cg).  First each warp turns the (m, l) of its
-// rows into weights in shared memory (wsm: 10 floats per row, the 8 weights, M
-// and the denominator), then every thread merges (row, 4-column) items with all
-// of an item's slot loads in flight at once.
-template <int D, int W>
+// are read through L2 (ld.global.cg).  Every thread merges (row, 4-column)
+// items, MI at a time with all of their slot loads in flight; the first items'
+// loads go out before anything else, and each warp meanwhile turns the (m, l) of
+// its rows into weights in shared memory (wsm: 10 floats per row, the 8 weights,
+// M and the denominator), so the weights cost no L2 round trip of their own.
+template <int D, int W, int MI>
 __device__ __forceinline__ void merge_slots(const SplitParams& p, float* wsm, int b, int row0, int nrows, int slot0,
                                             int sstride, int count, bool to_partial) {
   constexpr int C4 = D / 4;  // float4 columns per row
+  constexpr int NT = W * 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float kNegInf = -__int_as_float(0x7f800000);
+  const int nitems = nrows * C4;
+  // item e: row e / C4, float4 column e % C4; slot i of it at acc_of(e) + i * sstride * C4
+  auto acc_of = [&](int e) {
+    const size_t row = (size_t)b * p.Hq + row0 + e / C4;
+    return reinterpret_cast<float4*>(p.part_acc + (row * p.S + slot0) * D) + e % C4;
+  };
+  float4 a[MI][kFusedMergeMax];
+  auto load_items = [&](int e0) {
+#pragma unroll
+    for (int k = 0; k < MI; ++k) {
+      const int e = e0 + k * NT + tid;
+      if (e < nitems) {
+        const float4* acc = acc_of(e);
+#pragma unroll
+        for (int i = 0; i < kFusedMergeMax; ++i)
+          if (i < count) a[k][i] = __ldcg(acc + (size_t)i * sstride * C4);
+      }
+    }
+  };
+  load_items(0);
   for (int r = warp; r < nrows; r += W) {
     const size_t row = (size_t)b * p.Hq + row0 + r;
     float2 v = make_float2(kNegInf, 0.f);
@@ -489,39 +511,40 @@ __device__ __forceinline__ void merge_slots(const SplitParams& p, float* wsm, in
       wsm[r * 10 + 9] = den;
     }
   }
-  named_bar_sync(1, W * 32);  // weights ready; every (m, l) of slot0 has been read
+  named_bar_sync(1, NT);  // weights ready; every (m, l) of slot0 has been read
   if (to_partial && tid < nrows) {
     const size_t row = (size_t)b * p.Hq + row0 + tid;
     reinterpret_cast<float2*>(p.part_ml)[row * p.S + slot0] = make_float2(wsm[tid * 10 + 8], wsm[tid * 10 + 9]);
   }
-  for (int e = tid; e < nrows * C4; e += W * 32) {
-    const int r = e / C4;
-    const size_t row = (size_t)b * p.Hq + row0 + r;
-    float4* acc = reinterpret_cast<float4*>(p.part_acc + (row * p.S + slot0) * D) + e % C4;
-    float4 a[kFusedMergeMax];
+  for (int e0 = 0; e0 < nitems; e0 += MI * NT) {
+    if (e0 > 0) load_items(e0);
 #pragma unroll
-    for (int i = 0; i < kFusedMergeMax; ++i)
-      if (i < count) a[i] = __ldcg(acc + (size_t)i * sstride * C4);
-    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < MI; ++k) {
+      const int e = e0 + k * NT + tid;
+      if (e >= nitems) continue;
+      const int r = e / C4;
+      float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < kFusedMergeMax; ++i) {
-      if (i < count) {
-        const float wi = wsm[r * 10 + i];
-        num.x += wi * a[i].x;
-        num.y += wi * a[i].y;
-        num.z += wi * a[i].z;
-        num.w += wi * a[i].w;
+      for (int i = 0; i < kFusedMergeMax; ++i) {
+        if (i < count) {
+          const float wi = wsm[r * 10 + i];
+          num.x += wi * a[k][i].x;
+          num.y += wi * a[k][i].y;
+          num.z += wi * a[k][i].z;
+          num.w += wi * a[k][i].w;
+        }
       }
-    }
-    if (to_partial) {
-      *acc = num;
-    } else {
-      const float den = wsm[r * 10 + 9];
-      const float inv = den > 0.f ? 1.f / den : 0.f;  // a row that saw no token: zeros
-      uint2 o;
-      o.x = pack_bf16x2(num.x * inv, num.y * inv);
-      o.y = pack_bf16x2(num.z * inv, num.w * inv);
-      *reinterpret_cast<uint2*>(p.out + row * D + 4 * (e % C4)) = o;
+      if (to_partial) {
+        *acc_of(e) = num;  // this thread read every slot of item e above
+      } else {
+        const float den = wsm[r * 10 + 9];
+        const float inv = den > 0.f ? 1.f / den : 0.f;  // a row that saw no token: zeros
+        uint2 o;
+        o.x = pack_bf16x2(num.x * inv, num.y * inv);
+        o.y = pack_bf16x2(num.z * inv, num.w * inv);
+        const size_t row = (size_t)b * p.Hq + row0 + r;
+        *reinterpret_cast<uint2*>(p.out + row * D + 4 * (e % C4)) = o;
+      }
     }
   }
 }
@@ -1054,7 +1077,10 @@ __device__ __forceinline__ void split_consumer(const SplitParams& p, const Plan&
       volatile int* last = reinterpret_cast<volatile int*>(smem + Gm::OFF_MISC) + 1;
       if (tid == 0) *last = claim_last_piece(p.seg_counters + (size_t)pc.b * p.U + pc.u, p.epoch, pc.npieces);
       named_bar_sync(1, Gm::W * 32);
-      if (*last) merge_slots<D, Gm::W>(p, facc, pc.b, row0, nrows_pass, 0, 1, pc.npieces, false);
+      // one item per thread in flight: two raise the bf16 D = 128 kernel from 216
+      // to 248 registers, and a 192-thread paged CTA then leaves no room beside it
+      // for a combine CTA (512 threads x 40 registers)
+      if (*last) merge_slots<D, Gm::W, 1>(p, facc, pc.b, row0, nrows_pass, 0, 1, pc.npieces, false);
     }
     named_bar_sync(1, Gm::W * 32);
   }
